@@ -1,0 +1,158 @@
+/*
+ * nystrom.h - C ABI of the Nyström self-attention forward library
+ * (libnystrom.so, CUDA, sm_103a).
+ *
+ * What it computes, per head (b, h) of q, k, v in [B, H, n, d]:
+ *
+ *   Q~, K~ = segment means of Q and K over m contiguous segments of n/m rows
+ *            ("Nyströmformer" review page, Proposed method, bullet 4)
+ *   A_S    = softmax(Q~ K~^T / sqrt(d))                       (bullet 2)
+ *   Z      = iterative Moore-Penrose inverse of A_S, `iters` updates of
+ *            Z <- 1/4 Z (13I - A_S Z (15I - A_S Z (7I - A_S Z)))
+ *            from Z_0 = A_S^T / (||A_S||_1 ||A_S||_inf)       (bullet 5)
+ *   out    = softmax(Q K~^T / sqrt(d)) Z softmax(Q~ K^T / sqrt(d)) V
+ *            + DWConv(V)                                      (bullets 3, 6)
+ *
+ * DWConv is a depthwise convolution along the sequence: one odd-width filter
+ * of conv_ks taps per head, shared by the d channels, cross-correlation with
+ * (conv_ks-1)/2 zero rows of padding on each side, no bias:
+ *   conv[t] = sum_{j<conv_ks} conv_w[h][j] * V[t + j - (conv_ks-1)/2].
+ * conv_ks = 0 drops the term (the output is then the attention alone).
+ *
+ * Conventions shared by every entry point below:
+ *  - Device pointers unless a name says "host". The caller owns every
+ *    buffer; the library never frees or keeps a caller pointer.
+ *  - q, k, v, out: [B][H][n][d] contiguous, d innermost, element type
+ *    `dtype` (NYS_FP32: float; NYS_BF16: bfloat16 bit patterns). Each base
+ *    address 16-byte aligned. out is fully overwritten; it may not alias
+ *    q, k or v.
+ *  - conv_w: [H][conv_ks] float32 (for both dtypes); may be NULL when
+ *    conv_ks == 0.
+ *  - Shape rules (else NYS_ERR_SHAPE, nothing launched): B, H, n, d, m >= 1;
+ *    n % m == 0; m <= 256; d % 8 == 0 and d <= 128; for NYS_BF16 also
+ *    d in {32, 64, 128}; 0 <= iters <= 64; conv_ks == 0 or odd and <= 127;
+ *    B*H*n*d < 2^40.
+ *  - Scale: every softmax uses 1/sqrt(d).
+ *  - Asynchrony: compute entry points enqueue work on `stream` (0 = the
+ *    legacy default stream) and return without waiting. A negative return
+ *    means nothing was enqueued (argument errors) or that a launch failed
+ *    (NYS_ERR_CUDA; see nystrom_last_error_string). Device-side failures
+ *    (a bounded wait that ran out) are reported by nystrom_get_status after
+ *    the stream has finished.
+ *  - Thread safety: calls may come from several host threads; the cached
+ *    workspace of nystrom_attn_fwd is shared per device, so concurrent calls
+ *    on different streams of one device must use nystrom_attn_fwd_ws with
+ *    their own workspaces.
+ */
+#ifndef NYSTROM_H_
+#define NYSTROM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st* nys_stream_t;
+
+typedef enum { NYS_FP32 = 0, NYS_BF16 = 1 } nys_dtype_t;
+
+typedef enum {
+  NYS_OK = 0,
+  NYS_ERR_ARG = -1,         /* NULL pointer, bad dtype, negative size      */
+  NYS_ERR_SHAPE = -2,       /* shape outside the rules above               */
+  NYS_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned            */
+  NYS_ERR_UNSUPPORTED = -4, /* no GPU of compute capability 10.3 current   */
+  NYS_ERR_NOMEM = -5,       /* workspace allocation failed / too small     */
+  NYS_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed        */
+  NYS_ERR_TIMEOUT = -7      /* a device-side bounded wait ran out          */
+} nys_status_t;
+
+/*
+ * nystrom_attn_fwd - the forward pass (see the top of this file).
+ * Uses a workspace the library allocates and caches per device (grown with
+ * cudaMalloc when a call needs more; growing synchronises the device).
+ * iters: number of pseudo-inverse updates ("about 6", Proposed method,
+ * bullet 5); run exactly, no early exit.
+ * Returns NYS_OK or a negative nys_status_t.
+ */
+int nystrom_attn_fwd(const void* q, const void* k, const void* v,
+                     const float* conv_w, void* out, int B, int H, int n,
+                     int d, int m, int iters, int conv_ks, int dtype,
+                     nys_stream_t stream);
+
+/*
+ * nystrom_attn_workspace_bytes - bytes of device workspace that
+ * nystrom_attn_fwd_ws needs for this shape (0 if the shape is invalid).
+ * Pure host arithmetic; touches no GPU.
+ */
+size_t nystrom_attn_workspace_bytes(int B, int H, int n, int d, int m,
+                                    int dtype);
+
+/*
+ * nystrom_attn_fwd_ws - as nystrom_attn_fwd, with a caller-owned device
+ * workspace of ws_bytes >= nystrom_attn_workspace_bytes(...) bytes,
+ * 256-byte aligned. The library allocates nothing. The workspace must stay
+ * valid and unused by others until the stream has finished the call.
+ * Returns NYS_ERR_NOMEM if ws_bytes is too small.
+ */
+int nystrom_attn_fwd_ws(const void* q, const void* k, const void* v,
+                        const float* conv_w, void* out, int B, int H, int n,
+                        int d, int m, int iters, int conv_ks, int dtype,
+                        void* workspace, size_t ws_bytes, nys_stream_t stream);
+
+/*
+ * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
+ * copies q, k, v, conv_w to the device, runs nystrom_attn_fwd on `stream`,
+ * copies out back and waits for the stream. Host buffers should be pinned
+ * (page-locked) for full copy speed; pageable memory works but is slower.
+ * Device staging buffers are allocated and cached per device (grown with
+ * cudaMalloc when needed). Synchronous: out_host is complete on return.
+ */
+int nystrom_attn_fwd_host(const void* q_host, const void* k_host,
+                          const void* v_host, const float* conv_w_host,
+                          void* out_host, int B, int H, int n, int d, int m,
+                          int iters, int conv_ks, int dtype,
+                          nys_stream_t stream);
+
+/*
+ * Stage export, for testing the intermediate results against a reference.
+ * After a nystrom_attn_fwd_ws call has finished, the workspace holds, as
+ * float32 arrays per head (b*H + h major):
+ *   NYS_STAGE_Q_TILDE [m][d], NYS_STAGE_K_TILDE [m][d], NYS_STAGE_G [m][d]
+ *   (= softmax(Q~ K^T/sqrt d) V), NYS_STAGE_A_S [m][m], NYS_STAGE_W [m][d]
+ *   (= Z G).
+ * nystrom_attn_stage_offset returns the byte offset of `stage` in the
+ * workspace for this shape, or -1 for an invalid shape or stage.
+ */
+typedef enum {
+  NYS_STAGE_Q_TILDE = 0,
+  NYS_STAGE_K_TILDE = 1,
+  NYS_STAGE_G = 2,
+  NYS_STAGE_A_S = 3,
+  NYS_STAGE_W = 4
+} nys_stage_t;
+long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m,
+                                    int dtype, int stage);
+
+/*
+ * nystrom_get_status - waits for `stream`, then returns and clears the
+ * device-side status word of the most recent call on the current device
+ * (NYS_OK, or NYS_ERR_TIMEOUT if a bounded wait inside a kernel ran out).
+ * Returns NYS_ERR_CUDA if the stream reports an error.
+ */
+int nystrom_get_status(nys_stream_t stream);
+
+/* Static description of a status code. Never NULL. */
+const char* nystrom_strerror(int code);
+
+/* Text of the last CUDA error seen by this host thread ("" if none). */
+const char* nystrom_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NYSTROM_H_ */
