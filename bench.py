@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the Nyström self-attention forward pass on GB300.
+
+Metric: tokens/s = B*H*n / time of one forward pass over one batch, with the
+inputs resident in HBM (``value``), and end to end through the host-buffer
+C ABI call with the host<->device copies inside the timed region (``e2e``).
+
+One step = one full forward pass (landmarks, landmark rows, pseudo-inverse,
+token rows + conv + store) over the workload's whole batch. Between timed
+steps the inputs rotate over several copies whose total exceeds L2, so no
+step starts with its inputs in L2.
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+the host cores, on a bounded sample of the same workload per step.
+Under torchrun every rank runs its own full replica of the workload (heads
+are independent, no data-path collective: weak scaling); the time is the
+max over ranks and ``value`` counts the tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "Nyström attn fwd tokens/s (B·H·n per s) at 1 GB300; % of HBM/tensor roofline"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: enough for about 3 s)")
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="c2", choices=workloads.ORDER,
+                   help="workload (default c2: B=32 H=12 n=512 d=64 m=64, bf16)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU work budget of the oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms."""
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        mine = [p for (t, p) in self.samples if p[1] == str(self.gpu_index)] or \
+               [p for (t, p) in self.samples]
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1 and p in mine]
+        use = inside if inside else mine
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in use if num(p[2]) is not None]
+        smax = [num(p[3]) for p in use if num(p[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in use:
+            for nm, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------- CPU oracle ----
+
+def oracle_sample(inp, budget_s: float, max_heads: int | None = None):
+    """Run the fp64 oracle head by head until ``budget_s`` is spent (at least
+    one head). Returns (tokens, seconds, heads)."""
+    from oracle import nystrom_ref as R
+    wl = inp.wl
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    if max_heads is not None:
+        heads = heads[:max_heads]
+    done = 0
+    t0 = time.perf_counter()
+    for b, h in heads:
+        R.nystrom_head(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.conv_w[h], wl.m, wl.iters)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done * wl.n, dt, done
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------- reference ----
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(wl)
+    # per-step sample: whole heads, sized so warmup + steps stay within ~150 s
+    _, t_head, _ = oracle_sample(inp, 0.0, max_heads=1)
+    steps = args.steps if args.steps is not None else 10
+    per_step_budget = max(t_head, min(3.0, 150.0 / max(1, steps + args.warmup)))
+    heads_per_step = max(1, min(wl.heads, int(per_step_budget / max(t_head, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(inp, 1e9, max_heads=heads_per_step)
+    tokens = 0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        tk, _, _ = oracle_sample(inp, 1e9, max_heads=heads_per_step)
+        tokens += tk
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    sample = (f"{heads_per_step} of {wl.heads} heads (n={wl.n}) per step; "
+              f"fp64 numpy oracle, BLAS threads = library default")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normal draws)",
+        "config": {"workload": wl.describe()},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours ----
+
+KERNEL_BYTES = {
+    # algorithmic HBM bytes per launch, in units of T*e (T = B*H*n*d, e = element bytes)
+    "landmarks_simt": 2.0,   # read Q, K
+    "rows_simt": 2.0,        # read K, V
+    "tokens_simt": 3.0,      # read Q, V; write out
+}
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    from nystr_self_attention_gb300 import build as nbuild
+    nbuild.build()
+    import nystr_self_attention_gb300 as N
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    inp = workloads.make_inputs(wl)
+    dt_code = N.NYS_BF16 if wl.dtype == "bf16" else N.NYS_FP32
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+    def upload(x, bits):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    q0, k0, v0 = upload(inp.q, inp.q_bits), upload(inp.k, inp.k_bits), upload(inp.v, inp.v_bits)
+    w = torch.from_numpy(inp.conv_w).to(dev)
+    set_bytes = 4 * q0.numel() * q0.element_size()
+    nsets = max(1, min(8, -(-2 * L2_BYTES // set_bytes)))
+    sets = [(q0, k0, v0, torch.empty_like(q0))]
+    for _ in range(nsets - 1):
+        sets.append((q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)))
+    B, H, n, d, m = wl.B, wl.H, wl.n, wl.d, wl.m
+
+    def step(i):
+        q, k, v, out = sets[i % nsets]
+        N.nystrom_attn_fwd(q, k, v, w, out, B, H, n, d, m, wl.iters, wl.ks, dt_code, stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    # default step count: about 3 s of timed work
+    steps = args.steps
+    if steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(10):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / 10 / 1e3
+        steps = int(max(20, min(200000, 3.0 / max(per, 1e-7))))
+        if world > 1:
+            t = torch.tensor([steps], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MIN)
+            steps = int(t.item())
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = N.nystrom_launch_count()
+    barrier()
+    t_wall0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    launches = N.nystrom_launch_count() - launches0
+    elapsed_ms = ev0.elapsed_time(ev1)
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert N.nystrom_get_status(stream) == N.NYS_OK
+
+    tokens_step = wl.tokens
+    value = tokens_step * world * steps / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / steps
+
+    # per-kernel times (CUDA events on the launch stream) over a second pass of
+    # the same steps (capped), for the roofline of the dominant kernel
+    prof_steps = min(steps, 500)
+    N.nystrom_profile_read()
+    N.nystrom_profile_enable(True)
+    for i in range(prof_steps):
+        step(i)
+    torch.cuda.synchronize()
+    N.nystrom_profile_enable(False)
+    prof = N.nystrom_profile_read()
+    peaks, peak_src = load_peaks()
+    roofline = None
+    kernels = {}
+    if prof:
+        tot = sum(ms for ms, _ in prof.values())
+        for name, (ms, cnt) in prof.items():
+            kernels[name] = {"launches_per_step": cnt / prof_steps, "us_per_launch": ms / cnt * 1e3,
+                             "share": ms / tot}
+        dom = max(prof, key=lambda k: prof[k][0])
+        ms, cnt = prof[dom]
+        t_launch = ms / cnt / 1e3
+        te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
+        if dom in KERNEL_BYTES:
+            achieved = KERNEL_BYTES[dom] * te / t_launch / 1e9
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                        "peak_source": f"hbm_gbs of {peak_src}"}
+        else:
+            # pseudo-inverse on CUDA cores: fp32 FMA arithmetic
+            flops = wl.heads * (8.0 * wl.iters * wl.m ** 3 + 2.0 * wl.m ** 2 * wl.d * 2)
+            achieved = flops / t_launch / 1e12
+            peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
+            roofline = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": peak,
+                        "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                        "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
+
+    # end to end through the host-buffer C ABI call, pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        esz = 2 if wl.dtype == "bf16" else 4
+        shape = (B, H, n, d)
+        hq = torch.empty(shape, dtype=tdt, pin_memory=True)
+        hk = torch.empty_like(hq, pin_memory=True)
+        hv = torch.empty_like(hq, pin_memory=True)
+        hout = torch.empty_like(hq, pin_memory=True)
+        hw = torch.from_numpy(inp.conv_w).pin_memory()
+        hq.copy_(q0.cpu())
+        hk.copy_(k0.cpu())
+        hv.copy_(v0.cpu())
+        e2e_steps = max(3, min(steps, 50))
+        for _ in range(2):
+            N.nystrom_attn_fwd_host(hq, hk, hv, hw, hout, B, H, n, d, m, wl.iters, wl.ks, dt_code,
+                                    stream)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            N.nystrom_attn_fwd_host(hq, hk, hv, hw, hout, B, H, n, d, m, wl.iters, wl.ks, dt_code,
+                                    stream)
+        t1 = time.perf_counter()
+        dt_e2e = t1 - t0
+        if world > 1:
+            t = torch.tensor([dt_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt_e2e = float(t.item())
+        e2e = {"value": tokens_step * world * e2e_steps / dt_e2e, "unit": "tokens/s",
+               "h2d_bytes_per_step": 3 * wl.tokens * d * esz + wl.H * wl.ks * 4,
+               "d2h_bytes_per_step": wl.tokens * d * esz, "steps": e2e_steps,
+               "api": "nystrom_attn_fwd_host"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tk, secs, heads = oracle_sample(inp, args.cpu_seconds)
+        cpu = {"value": tk / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{heads} of {wl.heads} heads (n={wl.n} tokens each), fp64 numpy, "
+                         f"{secs:.1f} s"}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded normal draws, bf16-rounded where bf16)",
+        "config": {"workload": wl.describe(), "tokens_per_step": tokens_step,
+                   "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
+                   "parallelism": f"replicas x{world} (independent heads, no collective)"},
+        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks, "gpu_launches": launches,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    wl = workloads.WORKLOADS[args.config]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -145,6 +145,25 @@ long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m,
  */
 int nystrom_get_status(nys_stream_t stream);
 
+/*
+ * Launch accounting and per-kernel timing, for benchmarks.
+ * nystrom_launch_count: kernels this library has launched in this process
+ * (all devices, all threads).
+ * nystrom_profile_enable(1): from now on every kernel launch is bracketed
+ * by two CUDA events recorded on the launch's own stream (adds two event
+ * records per launch). nystrom_profile_enable(0) stops recording.
+ * nystrom_profile_read: waits for the recorded events, returns the number of
+ * distinct kernels seen since the last read (at most max_kernels are
+ * written), and for kernel i writes its name to names + i*name_len
+ * (NUL-terminated, truncated), its summed duration in ms to total_ms[i] and
+ * its launch count to launches[i]; then forgets the records. Returns
+ * NYS_ERR_CUDA if an event query fails.
+ */
+unsigned long long nystrom_launch_count(void);
+int nystrom_profile_enable(int on);
+int nystrom_profile_read(int max_kernels, char* names, int name_len,
+                         double* total_ms, long long* launches);
+
 /* Static description of a status code. Never NULL. */
 const char* nystrom_strerror(int code);
 

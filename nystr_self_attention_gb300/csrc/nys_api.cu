@@ -1,0 +1,286 @@
+// C ABI of libnystrom.so: argument checks, workspace layout and caching,
+// status word, host-buffer entry point. Declared in include/nystrom.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "nys_internal.h"
+
+namespace nys {
+
+int launch_forward_simt(const Shape& s, const void* q, const void* k, const void* v,
+                        const float* conv_w, void* out, char* ws, const Layout& L,
+                        cudaStream_t stream);
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local std::string g_last_error;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int set_cuda_error(cudaError_t e) {
+  g_last_error = cudaGetErrorString(e);
+  return NYS_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape rules of include/nystrom.h. Pure host arithmetic.
+int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype) {
+  if (dtype != NYS_FP32 && dtype != NYS_BF16) return NYS_ERR_ARG;
+  if (B < 1 || H < 1 || n < 1 || d < 1 || m < 1) return NYS_ERR_SHAPE;
+  if (n % m != 0 || m > 256) return NYS_ERR_SHAPE;
+  if (d % 8 != 0 || d > 128) return NYS_ERR_SHAPE;
+  if (dtype == NYS_BF16 && d != 32 && d != 64 && d != 128) return NYS_ERR_SHAPE;
+  if (iters < 0 || iters > 64) return NYS_ERR_SHAPE;
+  if (ks < 0 || ks > 127 || (ks > 0 && ks % 2 == 0)) return NYS_ERR_SHAPE;
+  const long long total = (long long)B * H * (long long)n * d;
+  if (total >= (1ll << 40)) return NYS_ERR_SHAPE;
+  return NYS_OK;
+}
+
+int check_args(const void* q, const void* k, const void* v, const float* conv_w, const void* out,
+               int B, int H, int n, int d, int m, int iters, int ks, int dtype) {
+  if (!q || !k || !v || !out) return NYS_ERR_ARG;
+  if (ks > 0 && !conv_w) return NYS_ERR_ARG;
+  const int rc = check_shape(B, H, n, d, m, iters, ks, dtype);
+  if (rc != NYS_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NYS_ERR_ALIGN;
+  if (ks > 0 && (reinterpret_cast<uintptr_t>(conv_w) & 3u)) return NYS_ERR_ALIGN;
+  return NYS_OK;
+}
+
+// The current device must be compute capability 10.3 (GB300).
+int check_device(int* dev_out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { set_cuda_error(e); return NYS_ERR_UNSUPPORTED; }
+  static int cc_cache[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return NYS_ERR_UNSUPPORTED;
+  if (cc_cache[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NYS_ERR_UNSUPPORTED;
+    cc_cache[dev] = major * 10 + minor;
+  }
+  if (cc_cache[dev] != 103) return NYS_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  return NYS_OK;
+}
+
+struct DeviceCache {
+  std::mutex mu;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* last_ws = nullptr;  // status word of the most recent call
+  void* stage = nullptr;    // host-entry staging buffers
+  size_t stage_bytes = 0;
+};
+DeviceCache g_dev[kMaxDevices];
+
+// Grow-only device buffer. cudaFree synchronises the device.
+int ensure_buffer(void** ptr, size_t* have, size_t need) {
+  if (*have >= need) return NYS_OK;
+  if (*ptr) {
+    cudaFree(*ptr);
+    *ptr = nullptr;
+    *have = 0;
+  }
+  cudaError_t e = cudaMalloc(ptr, need);
+  if (e != cudaSuccess) {
+    *ptr = nullptr;
+    g_last_error = cudaGetErrorString(e);
+    cudaGetLastError();
+    return NYS_ERR_NOMEM;
+  }
+  e = cudaMemset(*ptr, 0, need);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  *have = need;
+  return NYS_OK;
+}
+
+int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
+        void* out, char* ws, cudaStream_t stream, int dev) {
+  const Layout L = make_layout(s);
+  {
+    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+    g_dev[dev].last_ws = ws;
+  }
+  const int rc = launch_forward_simt(s, q, k, v, conv_w, out, ws, L, stream);
+  if (rc == NYS_ERR_CUDA) g_last_error = cudaGetErrorString(cudaGetLastError());
+  return rc;
+}
+
+}  // namespace
+
+Layout make_layout(const Shape& s) {
+  Layout L{};
+  const size_t bh = (size_t)s.bh(), md = (size_t)s.m * s.d, mm = (size_t)s.m * s.m;
+  // Key splits of the landmark-row pass: enough CTAs to fill the GPU a few
+  // times over, at least 32 keys per split.
+  const long long rb = (s.m + 7) / 8;
+  long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);
+  long long cap = s.n / 32 > 0 ? s.n / 32 : 1;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  if (want > 1024) want = 1024;
+  L.splits = (int)want;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  L.status = take(256);
+  L.q_tilde = take(bh * md * 4);
+  L.k_tilde = take(bh * md * 4);
+  L.g_part = take(bh * L.splits * md * 4);
+  L.g_ml = take(bh * L.splits * s.m * 2 * 4);
+  L.g = take(bh * md * 4);
+  L.a_s = take(bh * mm * 4);
+  L.z = take(bh * mm * 4);
+  L.w = take(bh * md * 4);
+  L.scratch = take(bh * 3 * mm * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace nys
+
+using namespace nys;
+
+extern "C" {
+
+size_t nystrom_attn_workspace_bytes(int B, int H, int n, int d, int m, int dtype) {
+  if (check_shape(B, H, n, d, m, 0, 0, dtype) != NYS_OK) return 0;
+  Shape s{B, H, n, d, m, 0, 0, dtype};
+  return make_layout(s).total;
+}
+
+long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m, int dtype, int stage) {
+  if (check_shape(B, H, n, d, m, 0, 0, dtype) != NYS_OK) return -1;
+  Shape s{B, H, n, d, m, 0, 0, dtype};
+  const Layout L = make_layout(s);
+  switch (stage) {
+    case NYS_STAGE_Q_TILDE: return (long long)L.q_tilde;
+    case NYS_STAGE_K_TILDE: return (long long)L.k_tilde;
+    case NYS_STAGE_G: return (long long)L.g;
+    case NYS_STAGE_A_S: return (long long)L.a_s;
+    case NYS_STAGE_W: return (long long)L.w;
+    default: return -1;
+  }
+}
+
+int nystrom_attn_fwd_ws(const void* q, const void* k, const void* v, const float* conv_w,
+                        void* out, int B, int H, int n, int d, int m, int iters, int conv_ks,
+                        int dtype, void* workspace, size_t ws_bytes, nys_stream_t stream) {
+  int rc = check_args(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype);
+  if (rc != NYS_OK) return rc;
+  if (!workspace) return NYS_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NYS_ERR_ALIGN;
+  Shape s{B, H, n, d, m, iters, conv_ks, dtype};
+  if (ws_bytes < make_layout(s).total) return NYS_ERR_NOMEM;
+  int dev = 0;
+  rc = check_device(&dev);
+  if (rc != NYS_OK) return rc;
+  return run(s, q, k, v, conv_w, out, static_cast<char*>(workspace), stream, dev);
+}
+
+int nystrom_attn_fwd(const void* q, const void* k, const void* v, const float* conv_w, void* out,
+                     int B, int H, int n, int d, int m, int iters, int conv_ks, int dtype,
+                     nys_stream_t stream) {
+  int rc = check_args(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype);
+  if (rc != NYS_OK) return rc;
+  int dev = 0;
+  rc = check_device(&dev);
+  if (rc != NYS_OK) return rc;
+  Shape s{B, H, n, d, m, iters, conv_ks, dtype};
+  const Layout L = make_layout(s);
+  char* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+    rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, L.total);
+    if (rc != NYS_OK) return rc;
+    ws = static_cast<char*>(g_dev[dev].ws);
+  }
+  return run(s, q, k, v, conv_w, out, ws, stream, dev);
+}
+
+int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                          const float* conv_w_host, void* out_host, int B, int H, int n, int d,
+                          int m, int iters, int conv_ks, int dtype, nys_stream_t stream) {
+  if (!q_host || !k_host || !v_host || !out_host || (conv_ks > 0 && !conv_w_host))
+    return NYS_ERR_ARG;
+  int rc = check_shape(B, H, n, d, m, iters, conv_ks, dtype);
+  if (rc != NYS_OK) return rc;
+  int dev = 0;
+  rc = check_device(&dev);
+  if (rc != NYS_OK) return rc;
+  const size_t elems = (size_t)B * H * n * d;
+  const size_t tb = align256(elems * (dtype == NYS_FP32 ? 4 : 2));
+  const size_t wb = align256((size_t)H * (conv_ks > 0 ? conv_ks : 1) * 4);
+  char* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+    rc = ensure_buffer(&g_dev[dev].stage, &g_dev[dev].stage_bytes, 4 * tb + wb);
+    if (rc != NYS_OK) return rc;
+    base = static_cast<char*>(g_dev[dev].stage);
+  }
+  char *dq = base, *dk = base + tb, *dv = base + 2 * tb, *dout = base + 3 * tb;
+  float* dw = reinterpret_cast<float*>(base + 4 * tb);
+  const size_t bytes = elems * (dtype == NYS_FP32 ? 4 : 2);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(dq, q_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dk, k_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(dv, v_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return set_cuda_error(e);
+  if (conv_ks > 0 &&
+      (e = cudaMemcpyAsync(dw, conv_w_host, (size_t)H * conv_ks * 4, cudaMemcpyHostToDevice,
+                           stream)) != cudaSuccess)
+    return set_cuda_error(e);
+  rc = nystrom_attn_fwd(dq, dk, dv, conv_ks > 0 ? dw : nullptr, dout, B, H, n, d, m, iters,
+                        conv_ks, dtype, stream);
+  if (rc != NYS_OK) return rc;
+  if ((e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return set_cuda_error(e);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return set_cuda_error(e);
+  return NYS_OK;
+}
+
+int nystrom_get_status(nys_stream_t stream) {
+  int dev = 0;
+  int rc = check_device(&dev);
+  if (rc != NYS_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+    ws = g_dev[dev].last_ws;
+  }
+  if (!ws) return NYS_OK;
+  int status = 0;
+  if ((e = cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return set_cuda_error(e);
+  if (status != 0 && (e = cudaMemset(ws, 0, sizeof(int))) != cudaSuccess) return set_cuda_error(e);
+  return status;
+}
+
+const char* nystrom_strerror(int code) {
+  switch (code) {
+    case NYS_OK: return "ok";
+    case NYS_ERR_ARG: return "invalid argument (NULL pointer, bad dtype)";
+    case NYS_ERR_SHAPE: return "shape outside the supported set";
+    case NYS_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case NYS_ERR_UNSUPPORTED: return "no compute capability 10.3 GPU is current";
+    case NYS_ERR_NOMEM: return "workspace allocation failed or too small";
+    case NYS_ERR_CUDA: return "CUDA runtime error";
+    case NYS_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    default: return "unknown status code";
+  }
+}
+
+const char* nystrom_last_error_string(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

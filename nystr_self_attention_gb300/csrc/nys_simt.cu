@@ -1,0 +1,485 @@
+// Plain CUDA-core (SIMT) kernels for every step of the forward pass, fp32
+// arithmetic throughout. They are the path for float32 inputs, where the
+// output must stay within 1e-4 of an fp64 result and tensor-core rounding
+// (bf16 / tf32 operands) would not do.
+//
+// Steps (the "Nyströmformer" review page, Proposed method, bullets 2-6):
+//   landmarks   Q~, K~ = segment means                          (bullet 4)
+//   rows        G = softmax(Q~ K^T s) V, split over keys with an
+//               online softmax; partial (sum, max, sum-of-exp)  (bullets 3, 6)
+//   pinv        merge partials; A_S = softmax(Q~ K~^T s); Z_0 = A_S^T /
+//               (||A_S||_1 ||A_S||_inf); iters x cubic update; W = Z G
+//                                                               (bullets 2, 5)
+//   tokens      out = softmax(Q K~^T s) W + DWConv(V)           (bullets 3, 6)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "nys_internal.h"
+
+namespace nys {
+namespace {
+
+__device__ __forceinline__ float ld(const float* p) { return *p; }
+__device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st(float* p, float x) { *p = x; }
+__device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// ---------------------------------------------------------------- landmarks
+// grid (ceil(m*d/256), B*H), block 256: one thread per landmark element.
+template <typename T>
+__global__ void __launch_bounds__(256)
+landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
+               float* __restrict__ kt, int n, int d, int m) {
+  const long long bh = blockIdx.y;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= m * d) return;
+  const int i = idx / d, c = idx % d, seg = n / m;
+  const size_t base = ((size_t)bh * n + (size_t)i * seg) * d + c;
+  float sq = 0.f, sk = 0.f;
+  for (int t = 0; t < seg; ++t) {
+    sq += ld(q + base + (size_t)t * d);
+    sk += ld(k + base + (size_t)t * d);
+  }
+  qt[(size_t)bh * m * d + idx] = sq / (float)seg;
+  kt[(size_t)bh * m * d + idx] = sk / (float)seg;
+}
+
+// -------------------------------------------------------------------- rows
+// grid (ceil(m/8), splits, B*H), block 128. CTA: 8 landmark rows x one key
+// range, keys in chunks of 32. Writes unnormalised partial O, and (max, sum).
+constexpr int RW_ROWS = 8, RW_KEYS = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __restrict__ v,
+          float* __restrict__ gpart, float* __restrict__ gml, int n, int d, int m, int splits,
+          int keys_per_split, float scale) {
+  extern __shared__ float sm[];
+  float* sq = sm;                          // [8][d]
+  float* sk = sq + RW_ROWS * d;            // [32][d+1]
+  float* sv = sk + RW_KEYS * (d + 1);      // [32][d]
+  float* sp = sv + RW_KEYS * d;            // [8][32]
+  float* salpha = sp + RW_ROWS * RW_KEYS;  // [8]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r0 = blockIdx.x * RW_ROWS, split = blockIdx.y;
+  const long long bh = blockIdx.z;
+  for (int e = tid; e < RW_ROWS * d; e += 128) {
+    const int r = e / d, c = e % d;
+    sq[e] = (r0 + r < m) ? qt[((size_t)bh * m + r0 + r) * d + c] * scale : 0.f;
+  }
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+  const int key0 = split * keys_per_split;
+  const int key1 = min(n, key0 + keys_per_split);
+  const T* kb = k + (size_t)bh * n * d;
+  const T* vb = v + (size_t)bh * n * d;
+  for (int kc = key0; kc < key1; kc += RW_KEYS) {
+    const int nk = min(RW_KEYS, key1 - kc);
+    __syncthreads();
+    for (int e = tid; e < RW_KEYS * d; e += 128) {
+      const int j = e / d, c = e % d;
+      float kv = 0.f, vv = 0.f;
+      if (j < nk) {
+        kv = ld(kb + (size_t)(kc + j) * d + c);
+        vv = ld(vb + (size_t)(kc + j) * d + c);
+      }
+      sk[j * (d + 1) + c] = kv;
+      sv[j * d + c] = vv;
+    }
+    __syncthreads();
+    for (int p = tid; p < RW_ROWS * RW_KEYS; p += 128) {
+      const int r = p / RW_KEYS, j = p % RW_KEYS;
+      float s = 0.f;
+      for (int c = 0; c < d; ++c) s += sq[r * d + c] * sk[j * (d + 1) + c];
+      sp[p] = (j < nk) ? s : -INFINITY;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = warp * 2 + rr;
+      const float s = sp[r * RW_KEYS + lane];
+      const float mnew = fmaxf(mrun[rr], warp_max(s));
+      const float p = (lane < nk) ? expf(s - mnew) : 0.f;
+      const float alpha = expf(mrun[rr] - mnew);
+      lrun[rr] = lrun[rr] * alpha + warp_sum(p);
+      mrun[rr] = mnew;
+      sp[r * RW_KEYS + lane] = p;
+      if (lane == 0) salpha[r] = alpha;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int e = tid + 128 * jj;
+      if (e < RW_ROWS * d) {
+        const int r = e / d, c = e % d;
+        float a = acc[jj] * salpha[r];
+        for (int j = 0; j < nk; ++j) a += sp[r * RW_KEYS + j] * sv[j * d + c];
+        acc[jj] = a;
+      }
+    }
+  }
+  const size_t pbase = ((size_t)bh * splits + split) * m;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    const int e = tid + 128 * jj;
+    if (e < RW_ROWS * d) {
+      const int r = e / d, c = e % d;
+      if (r0 + r < m) gpart[(pbase + r0 + r) * d + c] = acc[jj];
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = r0 + warp * 2 + rr;
+      if (r < m) {
+        gml[(pbase + r) * 2 + 0] = mrun[rr];
+        gml[(pbase + r) * 2 + 1] = lrun[rr];
+      }
+    }
+  }
+}
+
+// -------------------------------------------------------------------- pinv
+// Block-wide C = diag * I + alpha * A B on float matrices in global memory
+// (the head's workspace, L2-resident). B is [K][N] row-major, or [N][K]
+// row-major when b_trans. 256 threads, 64x64 output tiles, 4x4 per thread.
+// C must not alias A or B.
+constexpr int GT = 64, GK = 16, GP = GT + 4;
+
+__device__ void block_gemm(const float* A, int lda, const float* Bm, int ldb, bool b_trans,
+                           float* C, int ldc, int M, int N, int K, float alpha, float diag,
+                           float* smem) {
+  float* As = smem;            // [GK][GP]: As[kk][row]
+  float* Bs = smem + GK * GP;  // [GK][GP]: Bs[kk][col]
+  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+  for (int m0 = 0; m0 < M; m0 += GT) {
+    for (int n0 = 0; n0 < N; n0 += GT) {
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      for (int k0 = 0; k0 < K; k0 += GK) {
+        __syncthreads();
+        for (int e = tid; e < GT * GK; e += 256) {
+          const int r = e / GK, kk = e % GK, gr = m0 + r, gk = k0 + kk;
+          As[kk * GP + r] = (gr < M && gk < K) ? A[(size_t)gr * lda + gk] : 0.f;
+        }
+        for (int e = tid; e < GT * GK; e += 256) {
+          int kk, c;
+          if (b_trans) { c = e / GK; kk = e % GK; } else { kk = e / GT; c = e % GT; }
+          const int gk = k0 + kk, gc = n0 + c;
+          float x = 0.f;
+          if (gk < K && gc < N) x = b_trans ? Bm[(size_t)gc * ldb + gk] : Bm[(size_t)gk * ldb + gc];
+          Bs[kk * GP + c] = x;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < GK; ++kk) {
+          float a[4], b[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[i] = As[kk * GP + tr * 4 + i];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) b[j] = Bs[kk * GP + tc * 4 + j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] += a[i] * b[j];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int gr = m0 + tr * 4 + i, gc = n0 + tc * 4 + j;
+          if (gr < M && gc < N) C[(size_t)gr * ldc + gc] = alpha * acc[i][j] + (gr == gc ? diag : 0.f);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// grid (B*H), block 256. Everything for one head: merge the key-split
+// partials into G, form A_S, run the iteration, write W = Z G.
+__global__ void __launch_bounds__(256)
+pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
+          const float* __restrict__ gpart, const float* __restrict__ gml, float* __restrict__ g_all,
+          float* __restrict__ a_all, float* __restrict__ z_all, float* __restrict__ w_all,
+          float* __restrict__ scratch_all, int d, int m, int splits, int iters, float scale) {
+  __shared__ float smem[2 * GK * GP];
+  __shared__ float red[2][8];
+  const long long bh = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t md = (size_t)m * d, mm = (size_t)m * m;
+  const float* qt = qt_all + bh * md;
+  const float* kt = kt_all + bh * md;
+  float* g = g_all + bh * md;
+  float* A = a_all + bh * mm;
+  float* Z = z_all + bh * mm;
+  float* W = w_all + bh * md;
+  float* X = scratch_all + bh * 3 * mm;
+  float* U = X + mm;
+  float* V = U + mm;
+
+  // 1) G = merge over splits of (O_s, max_s, sum_s)
+  for (size_t e = tid; e < md; e += 256) {
+    const int i = (int)(e / d);
+    float mx = -INFINITY;
+    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, gml[(((size_t)bh * splits + s) * m + i) * 2]);
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const size_t row = ((size_t)bh * splits + s) * m + i;
+      const float f = expf(gml[row * 2] - mx);
+      num += gpart[row * d + (e % d)] * f;
+      den += gml[row * 2 + 1] * f;
+    }
+    g[e] = num / den;
+  }
+  // 2) A_S = softmax(Q~ K~^T s), rows by warps
+  block_gemm(qt, d, kt, d, true, A, m, m, m, d, scale, 0.f, smem);
+  for (int i = warp; i < m; i += 8) {
+    float mx = -INFINITY;
+    for (int j = lane; j < m; j += 32) mx = fmaxf(mx, A[(size_t)i * m + j]);
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int j = lane; j < m; j += 32) {
+      const float p = expf(A[(size_t)i * m + j] - mx);
+      A[(size_t)i * m + j] = p;
+      sum += p;
+    }
+    sum = warp_sum(sum);
+    const float inv = 1.f / sum;
+    for (int j = lane; j < m; j += 32) A[(size_t)i * m + j] *= inv;
+  }
+  __syncthreads();
+  // 3) Z_0 = A^T / (max column abs-sum * max row abs-sum)
+  float cmax = 0.f, rmax = 0.f;
+  for (int j = tid; j < m; j += 256) {
+    float cs = 0.f, rs = 0.f;
+    for (int i = 0; i < m; ++i) {
+      cs += fabsf(A[(size_t)i * m + j]);
+      rs += fabsf(A[(size_t)j * m + i]);
+    }
+    cmax = fmaxf(cmax, cs);
+    rmax = fmaxf(rmax, rs);
+  }
+  cmax = warp_max(cmax);
+  rmax = warp_max(rmax);
+  if (lane == 0) { red[0][warp] = cmax; red[1][warp] = rmax; }
+  __syncthreads();
+  if (tid == 0) {
+    float c = 0.f, r = 0.f;
+    for (int w = 0; w < 8; ++w) { c = fmaxf(c, red[0][w]); r = fmaxf(r, red[1][w]); }
+    red[0][0] = 1.f / (c * r);
+  }
+  __syncthreads();
+  const float alpha0 = red[0][0];
+  for (size_t e = tid; e < mm; e += 256) {
+    const int i = (int)(e / m), j = (int)(e % m);
+    Z[e] = A[(size_t)j * m + i] * alpha0;
+  }
+  __syncthreads();
+  // 4) Z <- 1/4 Z (13I - X (15I - X (7I - X))), X = A Z
+  float* zc = Z;
+  float* zn = V;
+  for (int it = 0; it < iters; ++it) {
+    block_gemm(A, m, zc, m, false, X, m, m, m, m, 1.f, 0.f, smem);            // X = A Z
+    for (size_t e = tid; e < mm; e += 256)                                       // U = 7I - X
+      U[e] = ((e / m) == (e % m) ? 7.f : 0.f) - X[e];
+    __syncthreads();
+    block_gemm(X, m, U, m, false, zn, m, m, m, m, -1.f, 15.f, smem);            // zn = 15I - X U
+    block_gemm(X, m, zn, m, false, U, m, m, m, m, -1.f, 13.f, smem);            // U = 13I - X zn
+    block_gemm(zc, m, U, m, false, zn, m, m, m, m, 0.25f, 0.f, smem);           // zn = Z U / 4
+    float* t = zc; zc = zn; zn = t;
+  }
+  if (zc != Z) {
+    for (size_t e = tid; e < mm; e += 256) Z[e] = zc[e];
+    __syncthreads();
+  }
+  // 5) W = Z G
+  block_gemm(Z, m, g, d, false, W, d, m, d, m, 1.f, 0.f, smem);
+}
+
+// ------------------------------------------------------------------ tokens
+// grid (ceil(n/32), B*H), block 256. CTA: 32 tokens; online softmax over
+// landmark chunks of 32, then the depthwise conv of V and the store.
+constexpr int TK_ROWS = 32, TK_LM = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __restrict__ kt_all,
+            const float* __restrict__ w_all, const float* __restrict__ conv_w, T* __restrict__ out,
+            int H, int n, int d, int m, int ks, float scale) {
+  extern __shared__ float sm[];
+  float* sq = sm;                            // [32][d]
+  float* sk = sq + TK_ROWS * d;              // [32][d+1]
+  float* sw = sk + TK_LM * (d + 1);          // [32][d]
+  float* sp = sw + TK_LM * d;                // [32][33]
+  float* salpha = sp + TK_ROWS * 33;         // [32]
+  float* sl = salpha + TK_ROWS;              // [32]
+  float* svh = sl + TK_ROWS;                 // [32 + ks - 1][d]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * TK_ROWS;
+  const long long bh = blockIdx.y;
+  const int h = (int)(bh % H);
+  const T* qb = q + (size_t)bh * n * d;
+  const T* vb = v + (size_t)bh * n * d;
+  const float* kt = kt_all + (size_t)bh * m * d;
+  const float* W = w_all + (size_t)bh * m * d;
+  for (int e = tid; e < TK_ROWS * d; e += 256) {
+    const int r = e / d, c = e % d;
+    sq[e] = (t0 + r < n) ? ld(qb + (size_t)(t0 + r) * d + c) * scale : 0.f;
+  }
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  float mrun[4], lrun[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) { mrun[j] = -INFINITY; lrun[j] = 0.f; }
+  for (int l0 = 0; l0 < m; l0 += TK_LM) {
+    const int nl = min(TK_LM, m - l0);
+    __syncthreads();
+    for (int e = tid; e < TK_LM * d; e += 256) {
+      const int i = e / d, c = e % d;
+      sk[i * (d + 1) + c] = (i < nl) ? kt[(size_t)(l0 + i) * d + c] : 0.f;
+      sw[i * d + c] = (i < nl) ? W[(size_t)(l0 + i) * d + c] : 0.f;
+    }
+    __syncthreads();
+    for (int p = tid; p < TK_ROWS * TK_LM; p += 256) {
+      const int r = p / TK_LM, i = p % TK_LM;
+      float s = 0.f;
+      for (int c = 0; c < d; ++c) s += sq[r * d + c] * sk[i * (d + 1) + c];
+      sp[r * 33 + i] = (i < nl) ? s : -INFINITY;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = warp * 4 + rr;
+      const float s = sp[r * 33 + lane];
+      const float mnew = fmaxf(mrun[rr], warp_max(s));
+      const float p = (lane < nl) ? expf(s - mnew) : 0.f;
+      const float alpha = expf(mrun[rr] - mnew);
+      lrun[rr] = lrun[rr] * alpha + warp_sum(p);
+      mrun[rr] = mnew;
+      sp[r * 33 + lane] = p;
+      if (lane == 0) salpha[r] = alpha;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int e = tid + 256 * jj;
+      if (e < TK_ROWS * d) {
+        const int r = e / d, c = e % d;
+        float a = acc[jj] * salpha[r];
+        for (int i = 0; i < nl; ++i) a += sp[r * 33 + i] * sw[i * d + c];
+        acc[jj] = a;
+      }
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) sl[warp * 4 + rr] = lrun[rr];
+  }
+  // V rows t0 - r .. t0 + 31 + r (zero outside [0, n)) for the conv
+  const int rad = ks > 0 ? (ks - 1) / 2 : 0;
+  const int vrows = TK_ROWS + 2 * rad;
+  for (int e = tid; e < vrows * d; e += 256) {
+    const int u = t0 - rad + e / d, c = e % d;
+    svh[e] = (ks > 0 && u >= 0 && u < n) ? ld(vb + (size_t)u * d + c) : 0.f;
+  }
+  __syncthreads();
+  const float* wh = conv_w ? conv_w + (size_t)h * ks : nullptr;
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const int e = tid + 256 * jj;
+    if (e < TK_ROWS * d) {
+      const int r = e / d, c = e % d;
+      if (t0 + r < n) {
+        float o = acc[jj] / sl[r];
+        float cv = 0.f;
+        for (int j = 0; j < ks; ++j) cv += wh[j] * svh[(r + j) * d + c];
+        st(out + (size_t)bh * n * d + (size_t)(t0 + r) * d + c, o + cv);
+      }
+    }
+  }
+}
+
+template <typename T>
+int launch_simt(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
+                void* out, char* ws, const Layout& L, cudaStream_t stream) {
+  const T* qq = static_cast<const T*>(q);
+  const T* kk = static_cast<const T*>(k);
+  const T* vv = static_cast<const T*>(v);
+  float* qt = reinterpret_cast<float*>(ws + L.q_tilde);
+  float* kt = reinterpret_cast<float*>(ws + L.k_tilde);
+  float* gp = reinterpret_cast<float*>(ws + L.g_part);
+  float* gml = reinterpret_cast<float*>(ws + L.g_ml);
+  float* g = reinterpret_cast<float*>(ws + L.g);
+  float* a = reinterpret_cast<float*>(ws + L.a_s);
+  float* z = reinterpret_cast<float*>(ws + L.z);
+  float* w = reinterpret_cast<float*>(ws + L.w);
+  float* scr = reinterpret_cast<float*>(ws + L.scratch);
+  const float scale = 1.0f / sqrtf((float)s.d);
+  const unsigned bh = (unsigned)s.bh();
+
+  {
+    KernelScope ks_("landmarks_simt", stream);
+    landmarks_simt<T><<<dim3((s.m * s.d + 255) / 256, bh), 256, 0, stream>>>(qq, kk, qt, kt, s.n, s.d, s.m);
+  }
+
+  const int kps = (s.n + L.splits - 1) / L.splits;
+  const size_t rows_smem = sizeof(float) * (RW_ROWS * s.d + RW_KEYS * (s.d + 1) + RW_KEYS * s.d +
+                                            RW_ROWS * RW_KEYS + RW_ROWS);
+  {
+    KernelScope ks_("rows_simt", stream);
+    rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, L.splits, bh), 128, rows_smem, stream>>>(
+      qt, kk, vv, gp, gml, s.n, s.d, s.m, L.splits, kps, scale);
+  }
+
+  {
+    KernelScope ks_("pinv_simt", stream);
+    pinv_simt<<<bh, 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scr, s.d, s.m, L.splits, s.iters,
+                                    scale);
+  }
+
+  const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
+  const size_t tok_smem = sizeof(float) * (TK_ROWS * s.d + TK_LM * (s.d + 1) + TK_LM * s.d +
+                                           TK_ROWS * 33 + 2 * TK_ROWS + (TK_ROWS + 2 * rad) * s.d);
+  if (tok_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(tokens_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tok_smem) != cudaSuccess)
+    return NYS_ERR_CUDA;
+  {
+    KernelScope ks_("tokens_simt", stream);
+    tokens_simt<T><<<dim3((s.n + TK_ROWS - 1) / TK_ROWS, bh), 256, tok_smem, stream>>>(
+      qq, vv, kt, w, conv_w, static_cast<T*>(out), s.H, s.n, s.d, s.m, s.ks, scale);
+  }
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_forward_simt(const Shape& s, const void* q, const void* k, const void* v,
+                        const float* conv_w, void* out, char* ws, const Layout& L,
+                        cudaStream_t stream) {
+  if (s.dtype == NYS_FP32) return launch_simt<float>(s, q, k, v, conv_w, out, ws, L, stream);
+  return launch_simt<__nv_bfloat16>(s, q, k, v, conv_w, out, ws, L, stream);
+}
+
+}  // namespace nys

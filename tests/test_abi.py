@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/nystrom.h declares, and rejects bad arguments with the
+documented codes before touching CUDA. No compute call runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nystrom.h")
+
+
+@pytest.fixture(scope="module")
+def N():
+    from nystr_self_attention_gb300 import build
+    build.build()
+    import nystr_self_attention_gb300 as pkg
+    pkg.load_library()
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nystrom_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for required in ("nystrom_attn_fwd", "nystrom_attn_fwd_ws", "nystrom_attn_workspace_bytes",
+                     "nystrom_attn_fwd_host", "nystrom_get_status", "nystrom_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(N):
+    lib = ctypes.CDLL(N.LIB_PATH)
+    missing = [name for name in declared_functions() if not hasattr(lib, name)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_binding_wraps_every_declared_symbol(N):
+    for name in declared_functions():
+        assert hasattr(N, name), f"binding lacks {name}"
+
+
+def test_strerror_covers_codes(N):
+    for code in range(0, -8, -1):
+        assert N.nystrom_strerror(code) not in ("", "unknown status code")
+    assert N.nystrom_strerror(5) == "unknown status code"
+
+
+GOOD = dict(B=2, H=3, n=64, d=64, m=8, iters=6, ks=5, dtype=1)
+
+
+def call(N, q=16, k=16, v=16, w=16, out=16, **kw):
+    a = dict(GOOD, **kw)
+    lib = N.load_library()
+    return lib.nystrom_attn_fwd(q, k, v, w, out, a["B"], a["H"], a["n"], a["d"], a["m"], a["iters"],
+                                a["ks"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(out=None), -1), (dict(w=None), -1), (dict(dtype=2), -1),
+    (dict(B=0), -2), (dict(n=65), -2), (dict(m=512, n=512), -2), (dict(d=48), -2),
+    (dict(d=12, dtype=0), -2), (dict(d=256), -2), (dict(iters=-1), -2), (dict(iters=65), -2),
+    (dict(ks=4), -2), (dict(ks=129), -2), (dict(ks=-1), -2),
+    (dict(q=24), -3), (dict(out=8), -3), (dict(w=18), -3),
+])
+def test_argument_errors_before_any_launch(N, kw, code):
+    assert call(N, **kw) == code
+
+
+def test_conv_weights_may_be_null_without_conv(N):
+    # with ks = 0 a NULL conv_w is accepted by the checks; the call then
+    # needs a GPU, which this machine may lack (NYS_ERR_UNSUPPORTED)
+    assert call(N, w=None, ks=0, q=24) == -3
+
+
+def test_workspace_sizes(N):
+    assert N.nystrom_attn_workspace_bytes(32, 12, 512, 64, 64, 1) > 0
+    assert N.nystrom_attn_workspace_bytes(1, 1, 100, 64, 64, 1) == 0
+    assert N.nystrom_attn_workspace_bytes(1, 1, 512, 64, 64, 1) % 256 == 0
+    a = N.nystrom_attn_workspace_bytes(2, 16, 32768, 128, 256, 1)
+    b = N.nystrom_attn_workspace_bytes(4, 16, 32768, 128, 256, 1)
+    assert b > a
+    for stage in range(5):
+        off = N.nystrom_attn_stage_offset(2, 3, 64, 64, 8, 1, stage)
+        assert 0 <= off < N.nystrom_attn_workspace_bytes(2, 3, 64, 64, 8, 1) and off % 256 == 0
+    assert N.nystrom_attn_stage_offset(2, 3, 64, 64, 8, 1, 9) == -1
+
+
+def test_workspace_entry_checks(N):
+    lib = N.load_library()
+    ws_need = N.nystrom_attn_workspace_bytes(2, 3, 64, 64, 8, 1)
+    args = (16, 16, 16, 16, 16, 2, 3, 64, 64, 8, 6, 5, 1)
+    assert lib.nystrom_attn_fwd_ws(*args, None, ws_need, None) == -1
+    assert lib.nystrom_attn_fwd_ws(*args, 128, ws_need, None) == -3
+    assert lib.nystrom_attn_fwd_ws(*args, 256, ws_need - 1, None) == -5
+
+
+def test_host_entry_checks(N):
+    lib = N.load_library()
+    assert lib.nystrom_attn_fwd_host(None, 16, 16, 16, 16, 2, 3, 64, 64, 8, 6, 5, 1, None) == -1
+    assert lib.nystrom_attn_fwd_host(16, 16, 16, 16, 16, 2, 3, 65, 64, 8, 6, 5, 1, None) == -2
+
+
+def test_binding_raises_on_error(N):
+    with pytest.raises(N.NystromError) as e:
+        N.nystrom_attn_fwd(16, 16, 16, 16, 16, 2, 3, 65, 64, 8, 6, 5, 1, stream=0)
+    assert e.value.code == -2

@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs. Bar: max|out - ref| / max|ref| <= 2e-2 for bf16 inputs,
+<= 1e-4 for float32, on the full output AND on the attention term alone
+(conv_ks = 0), since the convolution term would otherwise dominate max|ref|.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import nystrom_ref as R
+from tests.gpu_helpers import TOL, dtype_code, rel_err, run_gpu, stage, to_device
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_n4_m2.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    import torch
+    from nystr_self_attention_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    torch.cuda.set_device(0)
+
+
+def oracle_heads(inp, heads, ks=None):
+    """Oracle intermediates for the listed (b, h) heads."""
+    wl = inp.wl
+    res = {}
+    for b, h in heads:
+        w = inp.conv_w[h] if (ks is None or ks > 0) else np.zeros(0)
+        res[(b, h)] = R.nystrom_head(inp.q[b, h], inp.k[b, h], inp.v[b, h], w, wl.m, wl.iters)
+    return res
+
+
+# ------------------------------------------------------------------ golden ----
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_golden_closed_form(dtype):
+    f = json.load(open(GOLDEN))
+    n, d, m = f["n"], f["d"], f["m"]
+    for case in f["cases"]:
+        wl = workloads.custom(1, 1, n, d, m, case["iters"], 3, dtype)
+        q = np.array(f["q"], np.float32)[None, None]
+        v = np.array(f["v"], np.float32)[None, None]
+        inp = workloads.Inputs(wl, q, q.copy(), v, np.array([f["conv_w"]], np.float32))
+        if dtype == "bf16":
+            for name in ("q", "k", "v"):
+                vals, bits = workloads.round_to_bf16(getattr(inp, name))
+                assert (vals == getattr(inp, name)).all()  # exactly representable
+                setattr(inp, name + "_bits", bits)
+        got, _ = run_gpu(inp)
+        err = rel_err(got[0, 0], np.array(case["out"]))
+        assert err <= TOL[dtype], (case["iters"], err)
+
+
+# ------------------------------------------------------------- small shapes ----
+
+SMALL = [
+    # B, H, n, d, m, iters, ks
+    (1, 2, 256, 64, 32, 6, 9),
+    (2, 1, 200, 32, 8, 6, 5),      # n not a multiple of any tile
+    (1, 1, 64, 64, 64, 6, 3),      # m = n (segments of one row)
+    (1, 2, 96, 128, 1, 6, 7),      # one landmark
+    (1, 1, 512, 128, 256, 8, 65),  # largest m
+    (1, 3, 1000, 64, 40, 4, 0),    # m not a power of two, no conv
+    (1, 1, 8, 32, 2, 0, 1),        # no pinv update, 1-tap conv
+    (1, 1, 1, 32, 1, 6, 3),        # a single token
+    (1, 1, 384, 64, 128, 6, 127),  # widest conv
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SMALL, ids=[f"B{s[0]}H{s[1]}n{s[2]}d{s[3]}m{s[4]}i{s[5]}k{s[6]}" for s in SMALL])
+def test_small_shapes(shape, dtype):
+    B, H, n, d, m, iters, ks = shape
+    wl = workloads.custom(B, H, n, d, m, iters, ks, dtype)
+    inp = workloads.make_inputs(wl, seed=hash(shape) % 1000)
+    ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, m, iters)
+    got, _ = run_gpu(inp)
+    assert rel_err(got, ref) <= TOL[dtype]
+    if ks > 0:  # the attention term on its own
+        att_ref = R.nystrom_attention(inp.q, inp.k, inp.v, np.zeros((H, 0)), m, iters)
+        got_att, _ = run_gpu(inp, ks=0)
+        assert rel_err(got_att, att_ref) <= TOL[dtype]
+
+
+# ------------------------------------------------------------------ stages ----
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_stage_intermediates(dtype):
+    import nystr_self_attention_gb300 as N
+    wl = workloads.custom(2, 2, 512, 64, 64, 6, 33, dtype)
+    inp = workloads.make_inputs(wl, seed=3)
+    _, ws = run_gpu(inp, workspace=True)
+    heads = [(0, 0), (1, 1)]
+    ref = oracle_heads(inp, heads)
+    st = {name: stage(ws, wl, code, rows, cols) for name, code, rows, cols in (
+        ("q_tilde", N.NYS_STAGE_Q_TILDE, wl.m, wl.d), ("k_tilde", N.NYS_STAGE_K_TILDE, wl.m, wl.d),
+        ("g", N.NYS_STAGE_G, wl.m, wl.d), ("a_s", N.NYS_STAGE_A_S, wl.m, wl.m),
+        ("w", N.NYS_STAGE_W, wl.m, wl.d))}
+    tol = {"q_tilde": 1e-6, "k_tilde": 1e-6, "a_s": 1e-5,
+           "g": 1e-5 if dtype == "f32" else 1e-2, "w": 1e-4 if dtype == "f32" else 2e-2}
+    for (b, h) in heads:
+        i = b * wl.H + h
+        for name in st:
+            assert rel_err(st[name][i], ref[(b, h)][name]) <= tol[name], name
+        np.testing.assert_allclose(st["a_s"][i].sum(axis=1), 1.0, atol=1e-5)
+
+
+# ----------------------------------------------------------- full workloads ----
+
+FULL = ["c1", "c2", "c3", "c4", "c5"]
+_cache = {}
+
+
+def full_inputs(name):
+    if name not in _cache:
+        _cache.clear()
+        _cache[name] = workloads.make_inputs(workloads.WORKLOADS[name])
+    return _cache[name]
+
+
+def sampled_heads(wl):
+    heads = {(0, 0), (wl.B - 1, wl.H - 1)}
+    g = np.random.default_rng(99)
+    heads.add((int(g.integers(wl.B)), int(g.integers(wl.H))))
+    return sorted(heads)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_workload(name):
+    """Every configuration at its full size, in the launch configuration the
+    benchmark times; the oracle checks sampled heads (heads are independent),
+    full output and attention alone."""
+    inp = full_inputs(name)
+    wl = inp.wl
+    heads = sampled_heads(wl)
+    ref = oracle_heads(inp, heads)
+    got, _ = run_gpu(inp)
+    got_att, _ = run_gpu(inp, ks=0)
+    assert np.isfinite(got).all() and np.isfinite(got_att).all()
+    for b, h in heads:
+        e_out = rel_err(got[b, h], ref[(b, h)]["out"])
+        e_att = rel_err(got_att[b, h], ref[(b, h)]["att"])
+        print(f"{name} head ({b},{h}): out {e_out:.2e}  attention {e_att:.2e}")
+        assert e_out <= TOL[wl.dtype] and e_att <= TOL[wl.dtype]
+
+
+# ------------------------------------------------------------ entry points ----
+
+def test_host_entry_matches_device_entry():
+    import torch
+    import nystr_self_attention_gb300 as N
+    wl = workloads.custom(2, 3, 512, 64, 64, 6, 33, "bf16")
+    inp = workloads.make_inputs(wl, seed=11)
+    dev_out, _ = run_gpu(inp)
+    out_bits = np.zeros(inp.q_bits.shape, np.uint16)
+    N.nystrom_attn_fwd_host(inp.q_bits, inp.k_bits, inp.v_bits, inp.conv_w, out_bits, wl.B, wl.H,
+                            wl.n, wl.d, wl.m, wl.iters, wl.ks, N.NYS_BF16)
+    host_out = (out_bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(host_out, dev_out)
+
+
+def test_repeatable_and_workspace_entry_agrees():
+    wl = workloads.custom(1, 4, 1024, 64, 64, 6, 33, "bf16")
+    inp = workloads.make_inputs(wl, seed=12)
+    a, _ = run_gpu(inp)
+    b, _ = run_gpu(inp)
+    c, _ = run_gpu(inp, workspace=True)
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def test_output_not_written_outside_bounds():
+    import torch
+    import nystr_self_attention_gb300 as N
+    wl = workloads.custom(1, 2, 200, 64, 8, 6, 5, "bf16")
+    inp = workloads.make_inputs(wl, seed=13)
+    q, k, v, w = to_device(inp)
+    total = q.numel()
+    canary = torch.full((total + 4096,), 12345, dtype=torch.int16, device="cuda")
+    out = canary[2048:2048 + total].view(torch.bfloat16).view(q.shape)
+    N.nystrom_attn_fwd(q, k, v, w, out, wl.B, wl.H, wl.n, wl.d, wl.m, wl.iters, wl.ks, N.NYS_BF16)
+    torch.cuda.synchronize()
+    c = canary.cpu().numpy()
+    assert (c[:2048] == 12345).all() and (c[2048 + total:] == 12345).all()
