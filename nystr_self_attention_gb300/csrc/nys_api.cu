@@ -111,6 +111,9 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
     std::lock_guard<std::mutex> lk(g_dev[dev].mu);
     g_dev[dev].last_ws = ws;
   }
+  // each call starts with a clear status word (kernels only ever set it)
+  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return set_cuda_error(e);
   const int rc = launch_forward_simt(s, q, k, v, conv_w, out, ws, L, stream);
   if (rc == NYS_ERR_CUDA) g_last_error = cudaGetErrorString(cudaGetLastError());
   return rc;
