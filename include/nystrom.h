@@ -104,6 +104,29 @@ int nystrom_attn_fwd_ws(const void* q, const void* k, const void* v,
                         void* workspace, size_t ws_bytes, nys_stream_t stream);
 
 /*
+ * nystrom_attn_fwd_noalloc - as nystrom_attn_fwd, but allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library call. The paper has no
+ * counterpart; this entry point exists for callers that cannot allocate
+ * device memory at call time, such as plugins inside a host application that
+ * owns all device memory through its own allocator, or latency-critical
+ * loops where a cudaMalloc/cudaFree would synchronise the device.
+ * Its scratch is a fixed 32 MiB device array inside the library, reserved on
+ * every GPU that loads the library until the process exits. Shapes whose
+ * workspace (nystrom_attn_workspace_bytes) exceeds 32 MiB are rejected with
+ * NYS_ERR_NOMEM before anything is enqueued.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the one array and it keeps the previous call's
+ * contents; the library clears what must start at zero on every call. Calls
+ * that overlap on the GPU (different streams, or different host threads,
+ * same device) race on the array: serialise them.
+ */
+int nystrom_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                             const float* conv_w, void* out, int B, int H,
+                             int n, int d, int m, int iters, int conv_ks,
+                             int dtype, nys_stream_t stream);
+
+/*
  * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
  * copies q, k, v, conv_w to the device, runs nystrom_attn_fwd on `stream`,
  * copies out back and waits for the stream. Host buffers should be pinned

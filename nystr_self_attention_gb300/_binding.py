@@ -22,6 +22,7 @@ _SIG = {
     "nystrom_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "nystrom_attn_fwd_ws": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P,
                                  ctypes.c_size_t, _P]),
+    "nystrom_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "nystrom_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "nystrom_attn_stage_offset": (ctypes.c_longlong, [_I, _I, _I, _I, _I, _I, _I]),
     "nystrom_get_status": (_I, [_P]),
@@ -107,6 +108,17 @@ def nystrom_attn_fwd_ws(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dty
                                           B, H, n, d, m, iters, conv_ks, dtype, _ptr(workspace),
                                           ws_bytes, _stream(stream)),
                   "nystrom_attn_fwd_ws")
+
+
+def nystrom_attn_fwd_noalloc(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype,
+                             stream=None):
+    """The forward pass with no device allocation: scratch is a fixed 32 MiB
+    array inside the library (see include/nystrom.h)."""
+    lib = load_library()
+    return _check(lib.nystrom_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(conv_w), _ptr(out),
+                                               B, H, n, d, m, iters, conv_ks, dtype,
+                                               _stream(stream)),
+                  "nystrom_attn_fwd_noalloc")
 
 
 def nystrom_attn_fwd_host(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype, stream=None):

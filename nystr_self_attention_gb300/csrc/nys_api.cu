@@ -22,12 +22,16 @@ thread_local std::string g_last_error;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+}  // namespace
+
 int set_cuda_error(cudaError_t e) {
   g_last_error = cudaGetErrorString(e);
   return NYS_ERR_CUDA;
 }
 
+namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
 
 // Shape rules of include/nystrom.h. Pure host arithmetic.
 int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype) {
@@ -73,6 +77,7 @@ int check_device(int* dev_out) {
   return NYS_OK;
 }
 
+namespace {
 struct DeviceCache {
   std::mutex mu;
   void* ws = nullptr;
@@ -104,6 +109,8 @@ int ensure_buffer(void** ptr, size_t* have, size_t need) {
   return NYS_OK;
 }
 
+}  // namespace
+
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
         void* out, char* ws, cudaStream_t stream, int dev) {
   const Layout L = make_layout(s);
@@ -118,8 +125,6 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
   if (rc == NYS_ERR_CUDA) g_last_error = cudaGetErrorString(cudaGetLastError());
   return rc;
 }
-
-}  // namespace
 
 Layout make_layout(const Shape& s) {
   Layout L{};

@@ -50,6 +50,16 @@ class KernelScope {
   cudaEvent_t begin_ = nullptr;
 };
 
+// Host helpers of the C ABI (nys_api.cu).
+int set_cuda_error(cudaError_t e);  // remembers the message, returns NYS_ERR_CUDA
+int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype);
+int check_args(const void* q, const void* k, const void* v, const float* conv_w, const void* out,
+               int B, int H, int n, int d, int m, int iters, int ks, int dtype);
+int check_device(int* dev_out);  // current device, must be compute capability 10.3
+// Clears the status word and enqueues the forward pass with workspace `ws`.
+int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
+        void* out, char* ws, cudaStream_t stream, int dev);
+
 // Enqueue the whole forward pass. Pointers are device pointers; ws has
 // Layout::total bytes. Returns NYS_OK or NYS_ERR_CUDA (launch failure).
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,

@@ -1,0 +1,57 @@
+"""nystrom_attn_fwd_noalloc: the entry point for callers that cannot
+allocate device memory (for example a plugin whose host application owns all
+device memory, or a loop where cudaMalloc would stall the device). Its scratch
+is a fixed array inside the library. Checked through the C ABI against the
+allocating entry point, on two calls in a row (the array keeps the previous
+call's contents, so the second call must not depend on them)."""
+import numpy as np
+import pytest
+
+import workloads
+from tests.gpu_helpers import TOL, dtype_code, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    import torch
+    from nystr_self_attention_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_noalloc_matches_allocating_entry_point(dtype):
+    import torch
+    import nystr_self_attention_gb300 as N
+    wl = workloads.custom(2, 4, 1024, 64, 64, 6, 33, dtype)
+    assert N.nystrom_attn_workspace_bytes(wl.B, wl.H, wl.n, wl.d, wl.m, dtype_code(dtype)) <= 32 << 20
+    outs = []
+    for seed in (21, 22):  # two calls in a row, different inputs
+        inp = workloads.make_inputs(wl, seed=seed)
+        q, k, v, w = to_device(inp)
+        ref = torch.empty_like(q)
+        got = torch.full_like(q, float("nan"))
+        args = (wl.B, wl.H, wl.n, wl.d, wl.m, wl.iters, wl.ks, dtype_code(dtype))
+        N.nystrom_attn_fwd(q, k, v, w, ref, *args)
+        torch.cuda.synchronize()
+        N.nystrom_attn_fwd_noalloc(q, k, v, w, got, *args)
+        torch.cuda.synchronize()
+        assert N.nystrom_get_status() == N.NYS_OK
+        r, g = ref.float().cpu().numpy(), got.float().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert rel_err(g, r) <= TOL[dtype]
+        outs.append(g)
+    assert not np.array_equal(outs[0], outs[1])
+
+
+def test_noalloc_rejects_shapes_over_its_scratch():
+    import nystr_self_attention_gb300 as N
+    wl = workloads.WORKLOADS["c5"]
+    assert N.nystrom_attn_workspace_bytes(wl.B, wl.H, wl.n, wl.d, wl.m, N.NYS_BF16) > 32 << 20
+    lib = N.load_library()
+    rc = lib.nystrom_attn_fwd_noalloc(256, 256, 256, 256, 256, wl.B, wl.H, wl.n, wl.d, wl.m,
+                                      wl.iters, wl.ks, N.NYS_BF16, None)
+    assert rc == N.NYS_ERR_NOMEM
