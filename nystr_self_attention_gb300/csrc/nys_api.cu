@@ -58,6 +58,19 @@ int check_args(const void* q, const void* k, const void* v, const float* conv_w,
   return NYS_OK;
 }
 
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
 // The current device must be compute capability 10.3 (GB300).
 int check_device(int* dev_out) {
   int dev = -1;
@@ -150,6 +163,9 @@ Layout make_layout(const Shape& s) {
   L.z = take(bh * mm * 4);
   L.w = take(bh * md * 4);
   L.scratch = take(bh * 3 * mm * 4);
+  const size_t pad_bf16 = s.dtype == NYS_BF16 ? bh * (size_t)s.m64() * s.dpad() * 2 : 0;
+  L.kt_bf16 = take(pad_bf16);
+  L.wt_bf16 = take(pad_bf16);
   L.total = off;
   return L;
 }

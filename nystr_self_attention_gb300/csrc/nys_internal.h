@@ -14,6 +14,8 @@ struct Shape {
   int B, H, n, d, m, iters, ks, dtype;
   long long bh() const { return (long long)B * H; }
   int seg() const { return n / m; }
+  int m64() const { return ((m + 63) / 64) * 64; }  // m rounded up to 64
+  int dpad() const { return d <= 64 ? 64 : 128; }   // d rounded up to a 64-column chunk
 };
 
 // Byte offsets of the workspace regions (all 256-byte aligned). Every
@@ -29,6 +31,8 @@ struct Layout {
   size_t z;        // f32 [m][m]
   size_t w;        // f32 [m][d]          Z G
   size_t scratch;  // f32 [3][m][m]       pseudo-inverse temporaries
+  size_t kt_bf16;  // bf16 [m64][dpad]    K~, zero padded (tensor-core operand)
+  size_t wt_bf16;  // bf16 [dpad][m64]    W^T, zero padded (tensor-core operand)
   size_t total;
   int splits;      // key splits of the landmark-row pass
 };
@@ -59,6 +63,16 @@ int check_device(int* dev_out);  // current device, must be compute capability 1
 // Clears the status word and enqueues the forward pass with workspace `ws`.
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
         void* out, char* ws, cudaStream_t stream, int dev);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Tensor-core token kernel (nys_tokens_tc.cu): shared memory it needs for
+// this shape, 0 if the shape is outside what it handles.
+size_t tokens_tc_smem(const Shape& s);
+int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* kt_bf16,
+                     const void* wt_bf16, const float* conv_w, void* out, int* status,
+                     int num_sms, cudaStream_t stream);
 
 // Enqueue the whole forward pass. Pointers are device pointers; ws has
 // Layout::total bytes. Returns NYS_OK or NYS_ERR_CUDA (launch failure).

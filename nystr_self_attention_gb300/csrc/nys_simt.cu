@@ -38,23 +38,32 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // ---------------------------------------------------------------- landmarks
-// grid (ceil(m*d/256), B*H), block 256: one thread per landmark element.
+// grid (ceil(m64*dpad/256), B*H), block 256: one thread per landmark element
+// of the padded [m64][dpad] grid. Writes Q~, K~ (fp32, [m][d]) and, when
+// kt_b is given, K~ as bf16 [m64][dpad] with zeros in the padding.
 template <typename T>
 __global__ void __launch_bounds__(256)
 landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
-               float* __restrict__ kt, int n, int d, int m) {
+               float* __restrict__ kt, __nv_bfloat16* __restrict__ kt_b, int n, int d, int m,
+               int m64, int dpad) {
   const long long bh = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= m * d) return;
-  const int i = idx / d, c = idx % d, seg = n / m;
+  if (idx >= m64 * dpad) return;
+  const int i = idx / dpad, c = idx % dpad, seg = n / m;
+  if (i >= m || c >= d) {
+    if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(0.f);
+    return;
+  }
   const size_t base = ((size_t)bh * n + (size_t)i * seg) * d + c;
   float sq = 0.f, sk = 0.f;
   for (int t = 0; t < seg; ++t) {
     sq += ld(q + base + (size_t)t * d);
     sk += ld(k + base + (size_t)t * d);
   }
-  qt[(size_t)bh * m * d + idx] = sq / (float)seg;
-  kt[(size_t)bh * m * d + idx] = sk / (float)seg;
+  const float mq = sq / (float)seg, mk = sk / (float)seg;
+  qt[((size_t)bh * m + i) * d + c] = mq;
+  kt[((size_t)bh * m + i) * d + c] = mk;
+  if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mk);
 }
 
 // -------------------------------------------------------------------- rows
@@ -221,7 +230,8 @@ __global__ void __launch_bounds__(256)
 pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
           const float* __restrict__ gpart, const float* __restrict__ gml, float* __restrict__ g_all,
           float* __restrict__ a_all, float* __restrict__ z_all, float* __restrict__ w_all,
-          float* __restrict__ scratch_all, int d, int m, int splits, int iters, float scale) {
+          float* __restrict__ scratch_all, __nv_bfloat16* __restrict__ wt_b, int d, int m,
+          int splits, int iters, float scale, int m64, int dpad) {
   __shared__ float smem[2 * GK * GP];
   __shared__ float red[2][8];
   const long long bh = blockIdx.x;
@@ -314,6 +324,14 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
   }
   // 5) W = Z G
   block_gemm(Z, m, g, d, false, W, d, m, d, m, 1.f, 0.f, smem);
+  // 6) W^T as bf16 [dpad][m64], zero padded, for the tensor-core token kernel
+  if (wt_b) {
+    __nv_bfloat16* wt = wt_b + (size_t)bh * dpad * m64;
+    for (int e = tid; e < dpad * m64; e += 256) {
+      const int c = e / m64, i = e % m64;
+      wt[e] = __float2bfloat16_rn((c < d && i < m) ? W[(size_t)i * d + c] : 0.f);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ tokens
@@ -435,12 +453,17 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
   float* z = reinterpret_cast<float*>(ws + L.z);
   float* w = reinterpret_cast<float*>(ws + L.w);
   float* scr = reinterpret_cast<float*>(ws + L.scratch);
+  const bool tc_tokens = tokens_tc_smem(s) > 0;
+  __nv_bfloat16* kt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.kt_bf16) : nullptr;
+  __nv_bfloat16* wt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.wt_bf16) : nullptr;
+  int* status = reinterpret_cast<int*>(ws + L.status);
   const float scale = 1.0f / sqrtf((float)s.d);
   const unsigned bh = (unsigned)s.bh();
 
   {
     KernelScope ks_("landmarks_simt", stream);
-    landmarks_simt<T><<<dim3((s.m * s.d + 255) / 256, bh), 256, 0, stream>>>(qq, kk, qt, kt, s.n, s.d, s.m);
+    landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, bh), 256, 0, stream>>>(
+        qq, kk, qt, kt, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
   }
 
   const int kps = (s.n + L.splits - 1) / L.splits;
@@ -454,10 +477,13 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
 
   {
     KernelScope ks_("pinv_simt", stream);
-    pinv_simt<<<bh, 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scr, s.d, s.m, L.splits, s.iters,
-                                    scale);
+    pinv_simt<<<bh, 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scr, wt_b, s.d, s.m, L.splits,
+                                      s.iters, scale, s.m64(), s.dpad());
   }
 
+  if (tc_tokens) {
+    return launch_tokens_tc(s, q, v, kt_b, wt_b, conv_w, out, status, num_sms(), stream);
+  }
   const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
   const size_t tok_smem = sizeof(float) * (TK_ROWS * s.d + TK_LM * (s.d + 1) + TK_LM * s.d +
                                            TK_ROWS * 33 + 2 * TK_ROWS + (TK_ROWS + 2 * rad) * s.d);
