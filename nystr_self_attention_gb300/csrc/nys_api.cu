@@ -143,14 +143,20 @@ Layout make_layout(const Shape& s) {
   Layout L{};
   const size_t bh = (size_t)s.bh(), md = (size_t)s.m * s.d, mm = (size_t)s.m * s.m;
   // Key splits of the landmark-row pass: enough CTAs to fill the GPU a few
-  // times over, at least 32 keys per split.
-  const long long rb = (s.m + 7) / 8;
-  long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);
-  long long cap = s.n / 32 > 0 ? s.n / 32 : 1;
-  if (want > cap) want = cap;
-  if (want < 1) want = 1;
-  if (want > 1024) want = 1024;
-  L.splits = (int)want;
+  // times over (CUDA-core path: at least 32 keys per split; tensor-core
+  // path: whole 128-key tiles).
+  if (s.dtype == NYS_BF16) {
+    int tps = 0;
+    rows_tc_split(s, &L.splits, &tps);
+  } else {
+    const long long rb = (s.m + 7) / 8;
+    long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);
+    long long cap = s.n / 32 > 0 ? s.n / 32 : 1;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    if (want > 1024) want = 1024;
+    L.splits = (int)want;
+  }
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
   L.status = take(256);
@@ -164,6 +170,7 @@ Layout make_layout(const Shape& s) {
   L.w = take(bh * md * 4);
   L.scratch = take(bh * 3 * mm * 4);
   const size_t pad_bf16 = s.dtype == NYS_BF16 ? bh * (size_t)s.m64() * s.dpad() * 2 : 0;
+  L.qt_bf16 = take(pad_bf16);
   L.kt_bf16 = take(pad_bf16);
   L.wt_bf16 = take(pad_bf16);
   L.total = off;

@@ -31,6 +31,7 @@ struct Layout {
   size_t z;        // f32 [m][m]
   size_t w;        // f32 [m][d]          Z G
   size_t scratch;  // f32 [3][m][m]       pseudo-inverse temporaries
+  size_t qt_bf16;  // bf16 [m64][dpad]    Q~, zero padded (tensor-core operand)
   size_t kt_bf16;  // bf16 [m64][dpad]    K~, zero padded (tensor-core operand)
   size_t wt_bf16;  // bf16 [dpad][m64]    W^T, zero padded (tensor-core operand)
   size_t total;
@@ -73,6 +74,11 @@ size_t tokens_tc_smem(const Shape& s);
 int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* kt_bf16,
                      const void* wt_bf16, const float* conv_w, void* out, int* status,
                      int num_sms, cudaStream_t stream);
+
+// Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs.
+void rows_tc_split(const Shape& s, int* splits, int* tiles_per_split);
+int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
+                   float* gml, int splits, int* status, cudaStream_t stream);
 
 // Enqueue the whole forward pass. Pointers are device pointers; ws has
 // Layout::total bytes. Returns NYS_OK or NYS_ERR_CUDA (launch failure).

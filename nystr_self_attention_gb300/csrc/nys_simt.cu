@@ -44,14 +44,15 @@ __device__ __forceinline__ float warp_sum(float x) {
 template <typename T>
 __global__ void __launch_bounds__(256)
 landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
-               float* __restrict__ kt, __nv_bfloat16* __restrict__ kt_b, int n, int d, int m,
-               int m64, int dpad) {
+               float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
+               __nv_bfloat16* __restrict__ kt_b, int n, int d, int m, int m64, int dpad) {
   const long long bh = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= m64 * dpad) return;
   const int i = idx / dpad, c = idx % dpad, seg = n / m;
   if (i >= m || c >= d) {
     if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(0.f);
+    if (qt_b) qt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(0.f);
     return;
   }
   const size_t base = ((size_t)bh * n + (size_t)i * seg) * d + c;
@@ -64,6 +65,7 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
   qt[((size_t)bh * m + i) * d + c] = mq;
   kt[((size_t)bh * m + i) * d + c] = mk;
   if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mk);
+  if (qt_b) qt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mq);
 }
 
 // -------------------------------------------------------------------- rows
@@ -456,6 +458,8 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
   const bool tc_tokens = tokens_tc_smem(s) > 0;
   __nv_bfloat16* kt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.kt_bf16) : nullptr;
   __nv_bfloat16* wt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.wt_bf16) : nullptr;
+  const bool tc_rows = s.dtype == NYS_BF16;
+  __nv_bfloat16* qt_b = tc_rows ? reinterpret_cast<__nv_bfloat16*>(ws + L.qt_bf16) : nullptr;
   int* status = reinterpret_cast<int*>(ws + L.status);
   const float scale = 1.0f / sqrtf((float)s.d);
   const unsigned bh = (unsigned)s.bh();
@@ -463,9 +467,13 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
   {
     KernelScope ks_("landmarks_simt", stream);
     landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, bh), 256, 0, stream>>>(
-        qq, kk, qt, kt, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
+        qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
   }
 
+  if (tc_rows) {
+    const int rc = launch_rows_tc(s, qt_b, k, v, gp, gml, L.splits, status, stream);
+    if (rc != NYS_OK) return rc;
+  } else {
   const int kps = (s.n + L.splits - 1) / L.splits;
   const size_t rows_smem = sizeof(float) * (RW_ROWS * s.d + RW_KEYS * (s.d + 1) + RW_KEYS * s.d +
                                             RW_ROWS * RW_KEYS + RW_ROWS);
@@ -473,6 +481,7 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
     KernelScope ks_("rows_simt", stream);
     rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, L.splits, bh), 128, rows_smem, stream>>>(
       qt, kk, vv, gp, gml, s.n, s.d, s.m, L.splits, kps, scale);
+  }
   }
 
   {

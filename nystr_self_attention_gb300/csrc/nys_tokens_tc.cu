@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokM
   const int g0 = blockIdx.x * p.tiles_per_cta;
   const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
 
-  bool pending[2] = {false, false};  // a load into the stage not yet waited on
-  uint32_t n_loads[2] = {0, 0};       // loads issued into each stage
+  uint32_t pend = 0;                  // bit s: a load into stage s not yet waited on
+  uint32_t nload0 = 0, nload1 = 0;    // loads issued into stage 0 / 1
   bool kw_pending = false;
   auto issue_load = [&](int stage, int g) {
     const int bh = g / p.tiles_per_head, t0 = (g % p.tiles_per_head) * 128;
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokM
       for (int dc = 0; dc < DC; ++dc)
         tma_load_3d(vs + dc * (p.kc * 128), &maps.v, &bar_full[stage], dc * 64, t0 - rad, bh);
     }
-    pending[stage] = true;
-    ++n_loads[stage];
+    pend |= 1u << stage;
+    if (stage) ++nload1; else ++nload0;
   };
   auto issue_f = [&](int stage) {
     const uint32_t qs = smem_u32(sm + p.off_q + stage * p.q_stage);
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokM
       if (!mbar_wait(&bar_full[s], (j >> 1) & 1, abort_flag, kWaitNs)) {
         fail(p.status, abort_flag);
       } else {
-        pending[s] = false;
+        pend &= ~(1u << s);
         tc_fence_after_sync();
         issue_f(s);
       }
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokM
         if (!mbar_wait(&bar_full[s1], ((j + 1) >> 1) & 1, abort_flag, kWaitNs)) {
           fail(p.status, abort_flag);
         } else {
-          pending[s1] = false;
+          pend &= ~(1u << s1);
           tc_fence_after_sync();
           issue_f(s1);
         }
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokM
   }
   // wind down: after an abort, wait (bounded) for copies still in flight
   if (tid == 0 && *abort_flag) {
-    for (int s = 0; s < 2; ++s)
-      if (pending[s]) mbar_wait(&bar_full[s], (n_loads[s] - 1) & 1, nullptr, kWaitNs);
+    if (pend & 1u) mbar_wait(&bar_full[0], (nload0 - 1) & 1, nullptr, kWaitNs);
+    if (pend & 2u) mbar_wait(&bar_full[1], (nload1 - 1) & 1, nullptr, kWaitNs);
     if (kw_pending) mbar_wait(&bar_kw, kw_phase ^ 1, nullptr, kWaitNs);
   }
   tc_fence_before_sync();
