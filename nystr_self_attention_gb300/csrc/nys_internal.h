@@ -80,6 +80,12 @@ void rows_tc_split(const Shape& s, int* splits, int* tiles_per_split);
 int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
                    float* gml, int splits, int* status, cudaStream_t stream);
 
+// Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
+bool pinv_tc_supported(const Shape& s);
+int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,
+                   const float* gml, float* g, float* a_s, float* w, void* wt_bf16, int splits,
+                   int* status, cudaStream_t stream);
+
 // Enqueue the whole forward pass. Pointers are device pointers; ws has
 // Layout::total bytes. Returns NYS_OK or NYS_ERR_CUDA (launch failure).
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,

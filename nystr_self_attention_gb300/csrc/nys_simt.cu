@@ -484,7 +484,11 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
   }
   }
 
-  {
+  if (pinv_tc_supported(s)) {
+    const int rc = launch_pinv_tc(s, qt, kt, gp, gml, g, a, w, ws + L.wt_bf16, L.splits, status,
+                                  stream);
+    if (rc != NYS_OK) return rc;
+  } else {
     KernelScope ks_("pinv_simt", stream);
     pinv_simt<<<bh, 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scr, wt_b, s.d, s.m, L.splits,
                                       s.iters, scale, s.m64(), s.dpad());
