@@ -1,6 +1,7 @@
 // Landmark kernel, iterative pseudo-inverse and W = Z G on the tensor cores
 // ("Nyströmformer" review page, Proposed method, bullets 2, 3 and 5), for
-// m <= 128 landmarks, one CTA of 128 threads per head, thread i = row i:
+// m <= 128 landmarks, one CTA of 256 threads per head (row i of every
+// m x m matrix in TMEM lane i):
 //   G   = merge of the key-split partials of softmax(Q~ K^T s) V
 //   A_S = softmax(Q~ K~^T s)   scores as three tf32 products of the hi/lo
 //                              split of Q~ and K~ (hi*hi + hi*lo + lo*hi,
@@ -74,7 +75,12 @@ __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-__global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
+// 256 threads: warp w works on TMEM lane quarter w % 4 (rows 32 (w % 4) ..
+// + 31); the two warps of a quarter split each row's 32-column chunks
+// (half h = w / 4 takes the chunks with index % 2 == h).
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* bbuf = sm;               // B operand [MP rows x MP] fp32
@@ -84,12 +90,16 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float red[2][4];
+  __shared__ float red_row[4], red_col[kThreads];
   volatile int* abort_flag = &abort_sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane;
   const int bh = blockIdx.x;
   const int m = p.m, d = p.d, MP = p.m_pad;
-  const bool live = tid < m;
+  const bool live = row < m;
+  const bool in_mp = row < MP;
+  const int nch = MP >> 5;  // 32-column chunks of an m x m matrix
 
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
@@ -101,19 +111,22 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lo = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t COL_A = 0, COL_Z = MP, COL_X = 2 * MP, COL_Y = 3 * MP;
   const uint32_t COL_QH = 0, COL_QL = d, COL_S = 2 * d;  // prologue only
 
   uint32_t phase = 0;
-  // one tf32 product D = A(TMEM) * B(smem, `b_rows` rows = N), K = k_dim
+  // tf32 product D = A (TMEM columns a_col..) x B (smem, b_rows rows = N),
+  // K = k_dim. Descriptors: one base, then start-address increments.
   auto issue = [&](uint32_t d_col, uint32_t a_col, const uint8_t* b, int b_rows, int k_dim,
-                   bool accumulate_first) {
-    const uint32_t bb = smem_u32(b);
+                   bool acc_first) {
+    const uint64_t d0 = smem_desc(smem_u32(b), 16, 1024, SW_128B);
     const uint32_t id = idesc_tf32(128, b_rows);
+    const uint32_t chunk16 = (uint32_t)b_rows * 8u;  // (b_rows * 128 B) >> 4
+#pragma unroll 4
     for (int kk = 0; kk < k_dim / 8; ++kk) {
-      const uint64_t bd = smem_desc(bb + (kk >> 2) * (b_rows * 128) + (kk & 3) * 32, 16, 1024, SW_128B);
-      mma_tf32_tA(tmem + d_col, tmem + a_col + kk * 8, bd, id, (kk > 0 || accumulate_first) ? 1u : 0u);
+      const uint64_t bd = d0 + (uint64_t)((uint32_t)(kk >> 2) * chunk16 + (uint32_t)(kk & 3) * 2u);
+      mma_tf32_tA(tmem + d_col, tmem + a_col + kk * 8, bd, id, (kk > 0 || acc_first) ? 1u : 0u);
     }
   };
   auto wait_mma = [&]() {
@@ -127,26 +140,26 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
 
   // ---- 1) A_S scores S = Q~ K~^T in 3xTF32 on the tensor cores
   {
-    const float* krow = p.kt + ((size_t)bh * m + (live ? tid : 0)) * d;
-    const float* qrow = p.qt + ((size_t)bh * m + (live ? tid : 0)) * d;
-    for (int c0 = 0; c0 < d; c0 += 32) {
+    const float* krow = p.kt + ((size_t)bh * m + (live ? row : 0)) * d;
+    const float* qrow = p.qt + ((size_t)bh * m + (live ? row : 0)) * d;
+    for (int c0 = half * 32; c0 < d; c0 += 64) {
       uint32_t qh[32], ql[32];
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        float4 kv = live ? *reinterpret_cast<const float4*>(krow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 qv = live ? *reinterpret_cast<const float4*>(qrow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 kv = live ? *reinterpret_cast<const float4*>(krow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 qv = live ? *reinterpret_cast<const float4*>(qrow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 kh = make_float4(tf32_hi(kv.x), tf32_hi(kv.y), tf32_hi(kv.z), tf32_hi(kv.w));
         const float4 kl = make_float4(kv.x - kh.x, kv.y - kh.y, kv.z - kh.z, kv.w - kh.w);
-        if (tid < MP) {
-          store_row4(khi, MP, tid, c0 + e, kh);
-          store_row4(klo, MP, tid, c0 + e, kl);
+        if (in_mp) {
+          store_row4(khi, MP, row, c0 + e, kh);
+          store_row4(klo, MP, row, c0 + e, kl);
         }
         const float q4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const float h = tf32_hi(q4[t]);
-          qh[e + t] = __float_as_uint(h);
-          ql[e + t] = __float_as_uint(q4[t] - h);
+          const float hh = tf32_hi(q4[t]);
+          qh[e + t] = __float_as_uint(hh);
+          ql[e + t] = __float_as_uint(q4[t] - hh);
         }
       }
       tmem_st32(tmem + lo + COL_QH + c0, qh);
@@ -166,8 +179,9 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
   }
   wait_mma();
   __syncthreads();
-  // row softmax of the scores (scale 1/sqrt(d)); A_S -> TMEM, bbuf, stage
-  {
+  // row softmax of the scores (scale 1/sqrt(d)) by the first half of the
+  // CTA; A_S -> TMEM (A operand) and -> bbuf rows
+  if (half == 0) {
     float rmax = -INFINITY;
     for (int j0 = 0; j0 < MP; j0 += 32) {
       uint32_t r[32];
@@ -193,7 +207,6 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
     tmem_st_wait();
     const float inv = live ? 1.f / sum : 0.f;
     float rs = 0.f;
-    float* arow = p.a_s + ((size_t)bh * m + (live ? tid : 0)) * m;
     for (int j0 = 0; j0 < MP; j0 += 32) {
       uint32_t r[32];
       tmem_ld32(tmem + lo + COL_S + j0, r);
@@ -204,73 +217,94 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
         r[e] = __float_as_uint(x);
         rs += fabsf(x);
       }
-      // A_S row -> A operand (its columns only overwrite dead Q~ / score columns)
+      // A_S row -> A operand (only dead Q~ / score columns are overwritten)
       tmem_st32(tmem + lo + COL_A + j0, r);
-      if (tid < MP) {
+      if (in_mp) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
-          store_row4(bbuf, MP, tid, j0 + e,
+          store_row4(bbuf, MP, row, j0 + e,
                      make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
                                  __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
       }
-      if (live) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (j0 + e < m) arow[j0 + e] = __uint_as_float(r[e]);
-      }
     }
+    // ||A_S||_inf: largest row abs-sum
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) rs = fmaxf(rs, __shfl_xor_sync(0xffffffffu, rs, o));
-    if (lane == 0) red[0][warp] = rs;
+    if (lane == 0) red_row[quarter] = rs;
+    tmem_st_wait();
   }
-  tmem_st_wait();
   __syncthreads();
-  // ||A_S||_1: largest column abs-sum (thread j sums column j)
+  // ||A_S||_1: largest column abs-sum. Thread (row j, half h) sums column j
+  // over half of the rows with four independent partial sums.
   {
+    float c4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (in_mp) {
+      const int i0 = half * (MP >> 1), i1 = i0 + (MP >> 1);
+      for (int i = i0; i < i1; i += 4) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          c4[t] += fabsf(*reinterpret_cast<const float*>(bbuf + kmaj_off(i + t, row, MP)));
+      }
+    }
+    red_col[tid] = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+  }
+  // stage export of A_S: coalesced copy of the bbuf rows
+  {
+    float* a_out = p.a_s + (size_t)bh * m * m;
+    for (int e = tid; e < m * m; e += kThreads)
+      a_out[e] = *reinterpret_cast<const float*>(bbuf + kmaj_off(e / m, e % m, MP));
+  }
+  __syncthreads();
+  if (warp == 0) {
     float cs = 0.f;
-    if (tid < MP)
-      for (int i = 0; i < MP; ++i) cs += fabsf(*reinterpret_cast<const float*>(bbuf + kmaj_off(i, tid, MP)));
+    for (int j = lane; j < 128; j += 32) cs = fmaxf(cs, red_col[j] + red_col[j + 128]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cs = fmaxf(cs, __shfl_xor_sync(0xffffffffu, cs, o));
-    if (lane == 0) red[1][warp] = cs;
+    if (lane == 0) red_col[0] = cs;
   }
   __syncthreads();
-  const float alpha = 1.f / (fmaxf(fmaxf(red[1][0], red[1][1]), fmaxf(red[1][2], red[1][3])) *
-                             fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3])));
-  // Z_0 = alpha A_S^T: row i of Z_0 is alpha * column i of A_S -> TMEM.
-  for (int j0 = 0; j0 < MP; j0 += 32) {
+  const float alpha = 1.f / (red_col[0] * fmaxf(fmaxf(red_row[0], red_row[1]), fmaxf(red_row[2], red_row[3])));
+  // Z_0 = alpha A_S^T: row i of Z_0 is alpha * column i of A_S -> TMEM
+  for (int c = half; c < nch; c += 2) {
     uint32_t r[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-      r[e] = __float_as_uint(tid < MP ? alpha * *reinterpret_cast<const float*>(bbuf + kmaj_off(j0 + e, tid, MP)) : 0.f);
-    tmem_st32(tmem + lo + COL_Z + j0, r);
+      r[e] = __float_as_uint(in_mp ? alpha * *reinterpret_cast<const float*>(bbuf + kmaj_off(c * 32 + e, row, MP)) : 0.f);
+    tmem_st32(tmem + lo + COL_Z + c * 32, r);
   }
   __syncthreads();  // every column read done before the rows are rescaled
   // B operand of X = A_S Z_0: Z_0 stored by columns = alpha * A_S rows
-  if (tid < MP)
-    for (int j = 0; j < MP; j += 4) {
-      float4* e4 = reinterpret_cast<float4*>(bbuf + kmaj_off(tid, j, MP));
-      float4 v = *e4;
-      v.x *= alpha; v.y *= alpha; v.z *= alpha; v.w *= alpha;
-      *e4 = v;
-    }
+  if (in_mp)
+    for (int c = half; c < nch; c += 2)
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        float4* e4 = reinterpret_cast<float4*>(bbuf + kmaj_off(row, c * 32 + e, MP));
+        float4 v = *e4;
+        v.x *= alpha; v.y *= alpha; v.z *= alpha; v.w *= alpha;
+        *e4 = v;
+      }
   // ---- 2) G = merge of the key-split partials; G^T into gbuf (B of W = Z G)
   {
     float gm = -INFINITY;
     if (live)
       for (int sp = 0; sp < p.splits; ++sp)
-        gm = fmaxf(gm, p.gml[(((size_t)bh * p.splits + sp) * m + tid) * 2]);
-    float* grow_out = p.g + ((size_t)bh * m + (live ? tid : 0)) * d;
-    for (int c0 = 0; c0 < d; c0 += 32) {
+        gm = fmaxf(gm, p.gml[(((size_t)bh * p.splits + sp) * m + row) * 2]);
+    float den = 0.f;
+    if (live)
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
+        den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
+      }
+    const float inv = live ? 1.f / den : 0.f;
+    float* grow_out = p.g + ((size_t)bh * m + (live ? row : 0)) * d;
+    for (int c0 = half * 32; c0 < d; c0 += 64) {
       float acc[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) acc[e] = 0.f;
       if (live) {
-        float den = 0.f;
         for (int sp = 0; sp < p.splits; ++sp) {
-          const size_t prow = ((size_t)bh * p.splits + sp) * m + tid;
+          const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
           const float f = expf(p.gml[prow * 2] - gm);
-          den += p.gml[prow * 2 + 1] * f;
           const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + c0);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -281,14 +315,13 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
             acc[4 * e + 3] += v.w * f;
           }
         }
-        const float inv = 1.f / den;
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] *= inv;
         float4* go = reinterpret_cast<float4*>(grow_out + c0);
 #pragma unroll
         for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
       }
-      if (tid < MP) store_col32(gbuf, d, tid, c0, acc);
+      if (in_mp) store_col32(gbuf, d, row, c0, acc);
     }
   }
   fence_async_smem();
@@ -305,11 +338,12 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
     }
     wait_mma();
   };
-  // epilogue: this row of D (MP columns) -> sign * scale * D + diag * I,
-  // written transposed as the next product's B operand (element (i, j) ->
-  // storage row j, column i); optionally also Z <- scale * D in TMEM.
+  // epilogue: this row of D -> sign * scale * D + diag * I, written
+  // transposed as the next product's B operand (element (i, j) -> storage
+  // row j, column i); optionally also Z <- scale * D in TMEM.
   auto store_bt = [&](float diag, float sign, float scale_, uint32_t col, bool to_z) {
-    for (int j0 = 0; j0 < MP; j0 += 32) {
+    for (int c = half; c < nch; c += 2) {
+      const int j0 = c * 32;
       uint32_t r[32];
       tmem_ld32(tmem + lo + col + j0, r);
       tmem_ld_wait();
@@ -318,9 +352,9 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
       for (int e = 0; e < 32; ++e) {
         const float x = scale_ * __uint_as_float(r[e]);
         r[e] = __float_as_uint(x);
-        v[e] = fmaf(sign, x, (j0 + e == tid) ? diag : 0.f);
+        v[e] = fmaf(sign, x, (j0 + e == row) ? diag : 0.f);
       }
-      if (tid < MP) store_col32(bbuf, MP, tid, j0, v);
+      if (in_mp) store_col32(bbuf, MP, row, j0, v);
       if (to_z) tmem_st32(tmem + lo + COL_Z + j0, r);
     }
     fence_async_smem();
@@ -346,9 +380,9 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
   if (!*abort_flag) {
     gemm(COL_Y, COL_Z, gbuf, d);
     if (!*abort_flag) {
-      float* wrow = p.w + ((size_t)bh * m + (live ? tid : 0)) * d;
+      float* wrow = p.w + ((size_t)bh * m + (live ? row : 0)) * d;
       __nv_bfloat16* wt = p.wt + (size_t)bh * p.dpad * p.m64;
-      for (int c0 = 0; c0 < d; c0 += 32) {
+      for (int c0 = half * 32; c0 < d; c0 += 64) {
         uint32_t r[32];
         tmem_ld32(tmem + lo + COL_Y + c0, r);
         tmem_ld_wait();
@@ -359,14 +393,14 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
             wo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
         }
-        if (tid < p.m64) {
+        if (row < p.m64) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            wt[(size_t)(c0 + e) * p.m64 + tid] = __float2bfloat16_rn(live ? __uint_as_float(r[e]) : 0.f);
+            wt[(size_t)(c0 + e) * p.m64 + row] = __float2bfloat16_rn(live ? __uint_as_float(r[e]) : 0.f);
         }
       }
-      if (tid < p.m64)
-        for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + tid] = __float2bfloat16_rn(0.f);
+      if (half == 0 && row < p.m64)
+        for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + row] = __float2bfloat16_rn(0.f);
     }
   }
   tc_fence_before_sync();
@@ -374,7 +408,9 @@ __global__ void __launch_bounds__(128, 1) pinv_tc(const PinvParams p) {
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 }
 
-int mpad_of(int m) { return ((m + 31) / 32) * 32; }
+// m rounded up to 32, 64 or 128 (zero padding of A_S is exact: the
+// padded block of every iterate stays zero)
+int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 
 }  // namespace
 
@@ -418,7 +454,7 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
       cudaSuccess)
     return NYS_ERR_CUDA;
   KernelScope scope("pinv_tc", stream);
-  pinv_tc<<<(unsigned)s.bh(), 128, smem, stream>>>(p);
+  pinv_tc<<<(unsigned)s.bh(), kThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
 }
 
