@@ -68,6 +68,65 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
   if (qt_b) qt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mq);
 }
 
+// Segment means with one warp per (tensor, head, segment). A segment is
+// seg consecutive rows, i.e. one contiguous block of seg*d elements; lanes
+// stream it with 16-byte loads. With V elements per load and VPR = d / V
+// loads per row dividing 32, lane l always sees column group l % VPR, so
+// the per-column sums finish with shuffles over lanes l, l+VPR, ... .
+// Warps for padding rows (m <= i < m64) write zeros to the bf16 copies.
+// grid: (ceil(2 * B*H * m64 / 8)), block 256.
+template <typename T>
+__global__ void __launch_bounds__(256)
+landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
+              float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
+              __nv_bfloat16* __restrict__ kt_b, long long n_heads, int n, int d, int m, int m64,
+              int dpad) {
+  constexpr int V = 16 / sizeof(T);
+  const long long job = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (job >= 2 * n_heads * m64) return;
+  const int tensor = (int)(job / (n_heads * m64));
+  const long long rest = job - (long long)tensor * n_heads * m64;
+  const long long bh = rest / m64;
+  const int i = (int)(rest % m64);
+  __nv_bfloat16* outb = tensor == 0 ? qt_b : kt_b;
+  if (i >= m) {
+    if (outb)
+      for (int c = lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int seg = n / m, vpr = d / V;
+  const T* src = (tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)i * seg) * d;
+  const uint4* src4 = reinterpret_cast<const uint4*>(src);
+  const int nvec = seg * vpr;
+  float acc[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 u = __ldg(src4 + v);
+    const T* x = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] += ld(x + e);
+  }
+  for (int o = vpr; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  if (lane < vpr) {
+    const float inv = 1.f / (float)seg;
+    float* out = (tensor == 0 ? qt : kt) + ((size_t)bh * m + i) * d + lane * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) out[e] = acc[e] * inv;
+    if (outb) {
+      __nv_bfloat16* ob = outb + ((size_t)bh * m64 + i) * dpad + lane * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+    }
+  }
+  if (outb)
+    for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
+}
+
 // -------------------------------------------------------------------- rows
 // grid (ceil(m/8), splits, B*H), block 128. CTA: 8 landmark rows x one key
 // range, keys in chunks of 32. Writes unnormalised partial O, and (max, sum).
@@ -464,7 +523,12 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
   const float scale = 1.0f / sqrtf((float)s.d);
   const unsigned bh = (unsigned)s.bh();
 
-  {
+  if (32 % (s.d / (16 / (int)sizeof(T))) == 0) {
+    const long long jobs = 2ll * s.bh() * s.m64();
+    KernelScope ks_("landmarks_vec", stream);
+    landmarks_vec<T><<<(unsigned)((jobs + 7) / 8), 256, 0, stream>>>(
+        qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+  } else {
     KernelScope ks_("landmarks_simt", stream);
     landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, bh), 256, 0, stream>>>(
         qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
