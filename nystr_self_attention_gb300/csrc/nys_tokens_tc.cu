@@ -2,18 +2,25 @@
 //   out[t] = softmax(Q[t] K~^T / sqrt(d)) W + sum_j w[h][j] V[t + j - (ks-1)/2]
 // ("Nyströmformer" review page, Proposed method, bullets 3 and 6).
 //
-// One CTA of 128 threads walks a contiguous range of 128-token tiles
-// (persistent over the whole batch). Per tile:
-//   F   = Q_tile K~^T            tcgen05, A = Q (smem, TMA), B = K~ (smem)
-//   P   = exp(F - rowmax)        thread = row, read from TMEM, written back
-//                                into the same TMEM columns as packed bf16
-//   PW  = P W                    tcgen05, A = P (TMEM), B = W^T (smem)
-//   CV  = T V_halo               tcgen05, A = banded Toeplitz of the conv
-//                                taps (smem), B = V rows t0-r .. (MN-major)
-//   out = PW / rowsum + CV       thread = row, bf16 store
-// Q and the V halo come in by TMA through a two-stage ring; K~, W^T and the
-// Toeplitz block are reloaded only when the head changes. Every wait is
-// bounded; a wait that runs out sets the status word and the CTA winds down.
+// Persistent CTAs walk contiguous ranges of 128-token tiles. Warp roles:
+//   warp 0       TMA producer: Q tiles (ring of 2-3 stages, freed once F is
+//                done), V halos (ring of 2, freed once the conv is done), and
+//                per head K~ and W^T (1-2 buffers); Q and V streams advance
+//                independently
+//   warp 1       tcgen05 issuer, two independent streams:
+//                  F  = Q_tile K~^T          A = Q (smem), B = K~ (smem)
+//                  PW = P W                  A = P (TMEM), B = W^T (smem)
+//                  CV = T V_halo             A = banded Toeplitz of the conv
+//                                            taps (smem), B = V (MN-major)
+//   warps 2-3    build the Toeplitz block of the next head's taps (the first
+//                head's block is built by the whole CTA up front)
+//   warps 4-7    softmax of even tiles, warps 8-11 softmax of odd tiles:
+//                thread = row, reads F from TMEM, writes P (bf16) back over
+//                it, row sum to shared memory
+//   warps 12-15  epilogue: out = PW / rowsum + CV, bf16 store
+// F/P and the PW/CV accumulators are double-buffered in TMEM. Every wait is
+// bounded; a wait that runs out sets the status word, every role winds down,
+// copies in flight are awaited and TMEM is freed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -37,301 +44,462 @@ struct TokParams {
   int* status;
   int H, n, d, m, m_pad, ks, kc;  // m_pad: multiple of 32; kc: conv K extent (0: no conv)
   int tiles_per_head, total_tiles, tiles_per_cta;
-  float c;  // softmax scale * log2(e)
+  int nq, nkw, nt;  // Q stages; buffers of the per-head K~/W^T and Toeplitz blocks
+  float c;          // softmax scale * log2(e)
   uint32_t tmem_cols;
-  uint32_t off_q, off_v, off_kt, off_wt, off_t;  // smem offsets from the 1024-aligned base
-  uint32_t q_stage, v_stage, kt_bytes, wt_bytes;
+  uint32_t off_q, off_v, off_kt, off_t, off_l;  // smem offsets from the aligned base
+  uint32_t q_stage, v_stage, kt_bytes, wt_bytes, t_bytes;
 };
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+constexpr int kThreads = 512;
+constexpr int kNV = 2;  // V halo stages
+// dynamic shared memory budget: the 227 KB per-block opt-in limit less the
+// kernel's static shared memory (barriers) and a margin
+constexpr size_t kSmemBudget = 227 * 1024 - 1024;
 
-__device__ __forceinline__ void fail(int* status, volatile int* abort_flag) {
-  *abort_flag = 1;
-  atomicExch(status, (int)NYS_ERR_TIMEOUT);
+struct Bars {
+  uint64_t qfull[3], qempty[3];      // Q tile ring
+  uint64_t vfull[2], vempty[2];      // V halo ring
+  uint64_t kw_full[2], kw_empty[2];  // per-head K~ / W^T
+  uint64_t t_ready[2], t_empty[2];   // per-head Toeplitz block
+  uint64_t f_full[2], p_full[2], pw_done[2];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t l_full[4];
+};
+
+__device__ __forceinline__ void set_fail(int* status, volatile int* abort_flag) {
+  if (!*abort_flag) {
+    *abort_flag = 1;
+    atomicExch(status, (int)NYS_ERR_TIMEOUT);
+  }
+}
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, int* status,
+                                             volatile int* abort_flag) {
+  if (mbar_wait(bar, parity, abort_flag, kWaitNs)) return true;
+  set_fail(status, abort_flag);
+  return false;
+}
+
+// One 16-byte chunk (8 taps) of row t of the Toeplitz block: column u holds
+// w[u - t] for 0 <= u - t < ks and u < kc, else 0.
+__device__ __forceinline__ void toeplitz_chunk(uint8_t* tbuf, const float* wh, int ks, int kc,
+                                               int t, int u0) {
+  uint32_t wv[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int ua = u0 + 2 * e - t, ub = ua + 1;
+    const float fa = (ua >= 0 && ua < ks && u0 + 2 * e < kc) ? __ldg(wh + ua) : 0.f;
+    const float fb = (ub >= 0 && ub < ks && u0 + 2 * e + 1 < kc) ? __ldg(wh + ub) : 0.f;
+    wv[e] = pack_bf16x2(fa, fb);
+  }
+  *reinterpret_cast<uint4*>(tbuf + (u0 >> 6) * 16384 + sw128_offset(t, (u0 & 63) * 2)) =
+      make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
 template <int DP>
-__global__ void __launch_bounds__(128, 1) tokens_tc(const __grid_constant__ TokMaps maps,
-                                                    const TokParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__ TokMaps maps,
+                                                         const TokParams p) {
   constexpr int DC = DP / 64;  // 64-column chunks of d
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_full[2], bar_kw, bar_mma;
+  __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
+  float* lbuf = reinterpret_cast<float*>(sm + p.off_l);  // [4][128] row sums
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g0 = blockIdx.x * p.tiles_per_cta;
+  const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
+  const int ntiles = g1 - g0;
+  const int rad = p.ks > 0 ? (p.ks - 1) / 2 : 0;
+  const int kc64 = (p.kc + 63) & ~63;
+  auto head_of = [&](int g) { return g / p.tiles_per_head; };
+
   if (tid == 0) {
-    mbar_init(&bar_full[0], 1);
-    mbar_init(&bar_full[1], 1);
-    mbar_init(&bar_kw, 1);
-    mbar_init(&bar_mma, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&bars.qfull[i], 1);
+      mbar_init(&bars.qempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.vfull[i], 1);
+      mbar_init(&bars.vempty[i], 1);
+      mbar_init(&bars.kw_full[i], 1);
+      mbar_init(&bars.kw_empty[i], 1);
+      mbar_init(&bars.t_ready[i], 64);
+      mbar_init(&bars.t_empty[i], 1);
+      mbar_init(&bars.f_full[i], 1);
+      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.pw_done[i], 1);
+      mbar_init(&bars.acc_full[i], 1);
+      mbar_init(&bars.acc_empty[i], 128);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.l_full[i], 128);
     abort_sh = 0;
     fence_barrier_init();
-    tma_prefetch(&maps.q);
-    tma_prefetch(&maps.v);
-    tma_prefetch(&maps.kt);
-    tma_prefetch(&maps.wt);
   }
-  if (warp == 0) tmem_alloc(&tmem_base_sh, p.tmem_cols);
+  if (warp == 1) tmem_alloc(&tmem_base_sh, p.tmem_cols);
+  // the first head's Toeplitz block, by the whole CTA
+  if (p.kc > 0 && ntiles > 0) {
+    const float* wh = p.conv_w + (size_t)(head_of(g0) % p.H) * p.ks;
+    const int nch = kc64 >> 3;
+    for (int task = tid; task < 128 * nch; task += kThreads)
+      toeplitz_chunk(sm + p.off_t, wh, p.ks, p.kc, task / nch, (task % nch) * 8);
+    fence_async_smem();
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (p.kc > 0 && ntiles > 0 && (warp == 2 || warp == 3)) mbar_arrive(&bars.t_ready[0]);
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t COL_F = 0, COL_PW = p.m_pad, COL_CV = p.m_pad + DP;
-  const int rad = p.ks > 0 ? (p.ks - 1) / 2 : 0;
+  // TMEM columns: F/P buffers [2][m_pad], then accumulators [2][PW | CV]
+  const uint32_t COL_F0 = 0, COL_ACC0 = 2 * p.m_pad;
+  const uint32_t ACC_W = 2 * DP;
+  const uint32_t kw_bytes = p.kt_bytes + p.wt_bytes;
 
-  const int g0 = blockIdx.x * p.tiles_per_cta;
-  const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
-
-  uint32_t pend = 0;                  // bit s: a load into stage s not yet waited on
-  uint32_t nload0 = 0, nload1 = 0;    // loads issued into stage 0 / 1
-  bool kw_pending = false;
-  auto issue_load = [&](int stage, int g) {
-    const int bh = g / p.tiles_per_head, t0 = (g % p.tiles_per_head) * 128;
-    uint8_t* qs = sm + p.off_q + stage * p.q_stage;
-    uint8_t* vs = sm + p.off_v + stage * p.v_stage;
-    mbar_arrive_expect_tx(&bar_full[stage], p.q_stage + (p.kc > 0 ? p.v_stage : 0));
-#pragma unroll
-    for (int dc = 0; dc < DC; ++dc) tma_load_3d(qs + dc * 16384, &maps.q, &bar_full[stage], dc * 64, t0, bh);
-    if (p.kc > 0) {
-#pragma unroll
-      for (int dc = 0; dc < DC; ++dc)
-        tma_load_3d(vs + dc * (p.kc * 128), &maps.v, &bar_full[stage], dc * 64, t0 - rad, bh);
-    }
-    pend |= 1u << stage;
-    if (stage) ++nload1; else ++nload0;
-  };
-  auto issue_f = [&](int stage) {
-    const uint32_t qs = smem_u32(sm + p.off_q + stage * p.q_stage);
-    const uint32_t ks_ = smem_u32(sm + p.off_kt);
-    const uint32_t id = idesc_bf16(128, p.m_pad, false, false);
-#pragma unroll
-    for (int kk = 0; kk < DP / 16; ++kk) {
-      const uint64_t a = smem_desc(qs + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, SW_128B);
-      const uint64_t b = smem_desc(ks_ + (kk >> 2) * (p.m_pad * 128) + (kk & 3) * 32, 16, 1024, SW_128B);
-      mma_bf16(tmem + COL_F, a, b, id, kk > 0);
-    }
-    mma_commit(&bar_mma);
-  };
-
-  if (tid == 0) {
-    if (g0 < g1) issue_load(0, g0);
-    if (g0 + 1 < g1) issue_load(1, g0 + 1);
-  }
-
-  uint32_t mma_phase = 0, kw_phase = 0;
-  int cur_bh = -1, cur_h = -1;
-  bool f_issued = false;  // F of the current tile already in flight
-  for (int g = g0; g < g1; ++g) {
-    const int j = g - g0, s = j & 1;
-    const int bh = g / p.tiles_per_head, t0 = (g % p.tiles_per_head) * 128;
-    const int h = bh % p.H;
-    // (A) head change: K~, W^T by TMA; the conv's Toeplitz block by threads
-    if (bh != cur_bh) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_kw, p.kt_bytes + p.wt_bytes);
-        for (int dc = 0; dc < DC; ++dc)
-          tma_load_3d(sm + p.off_kt + dc * (p.m_pad * 128), &maps.kt, &bar_kw, dc * 64, 0, bh);
-        for (int mc = 0; mc < p.m_pad / 64 + ((p.m_pad & 63) ? 1 : 0); ++mc)
-          tma_load_3d(sm + p.off_wt + mc * (DP * 128), &maps.wt, &bar_kw, mc * 64, 0, bh);
-        kw_pending = true;
-      }
-      if (p.kc > 0 && h != cur_h) {
-        // row t of the Toeplitz block: column u holds w[u - t] for 0 <= u - t < ks
-        const int t = tid;
-        const float* wh = p.conv_w + (size_t)h * p.ks;
-        uint8_t* tb = sm + p.off_t;
-        const int kc64 = (p.kc + 63) & ~63;
-        for (int u0 = 0; u0 < kc64; u0 += 8) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ua = u0 + 2 * e - t, ub = ua + 1;
-            const float fa = (ua >= 0 && ua < p.ks && u0 + 2 * e < p.kc) ? wh[ua] : 0.f;
-            const float fb = (ub >= 0 && ub < p.ks && u0 + 2 * e + 1 < p.kc) ? wh[ub] : 0.f;
-            wv[e] = pack_bf16x2(fa, fb);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch(&maps.q);
+      tma_prefetch(&maps.v);
+      tma_prefetch(&maps.kt);
+      tma_prefetch(&maps.wt);
+      int jq = 0, jv = p.kc > 0 ? 0 : ntiles, hi = -1, cur_bh = -1;
+      uint32_t nq_issued[3] = {0, 0, 0}, nv_issued[2] = {0, 0}, nkw_issued[2] = {0, 0};
+      uint64_t t_last = globaltimer_ns();
+      while (jq < ntiles || jv < ntiles) {
+        bool prog = false;
+        if (jq < ntiles) {
+          const int g = g0 + jq, bh = head_of(g), sq = jq % p.nq;
+          const bool new_head = bh != cur_bh;
+          const int kb = (hi + 1) % p.nkw;
+          const bool kw_ok = !new_head || hi + 1 < p.nkw ||
+                             mbar_test(&bars.kw_empty[kb], (((hi + 1) / p.nkw) - 1) & 1);
+          const bool q_ok = jq < p.nq || mbar_test(&bars.qempty[sq], ((jq / p.nq) - 1) & 1);
+          if (kw_ok && q_ok) {
+            if (new_head) {
+              cur_bh = bh;
+              ++hi;
+              uint8_t* kts = sm + p.off_kt + kb * kw_bytes;
+              uint8_t* wts = kts + p.kt_bytes;
+              mbar_arrive_expect_tx(&bars.kw_full[kb], kw_bytes);
+              for (int dc = 0; dc < DC; ++dc)
+                tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bars.kw_full[kb], dc * 64, 0, bh);
+              for (int mc = 0; mc * 64 < p.m_pad; ++mc)
+                tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bars.kw_full[kb], mc * 64, 0, bh);
+              ++nkw_issued[kb];
+            }
+            uint8_t* qs = sm + p.off_q + sq * p.q_stage;
+            mbar_arrive_expect_tx(&bars.qfull[sq], p.q_stage);
+            for (int dc = 0; dc < DC; ++dc)
+              tma_load_3d(qs + dc * 16384, &maps.q, &bars.qfull[sq], dc * 64, (g % p.tiles_per_head) * 128, bh);
+            ++nq_issued[sq];
+            ++jq;
+            prog = true;
           }
-          uint8_t* dst = tb + (u0 >> 6) * 16384 + sw128_offset(t, (u0 & 63) * 2);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
-        fence_async_smem();
-        cur_h = h;
-      }
-      if (tid == 0) {
-        if (!mbar_wait(&bar_kw, kw_phase, abort_flag, kWaitNs)) fail(p.status, abort_flag);
-        else kw_pending = false;
-      }
-      kw_phase ^= 1;
-      cur_bh = bh;
-      f_issued = false;
-      __syncthreads();
-      if (*abort_flag) break;
-    }
-    // (B) F = Q K~^T
-    if (tid == 0 && !f_issued) {
-      if (!mbar_wait(&bar_full[s], (j >> 1) & 1, abort_flag, kWaitNs)) {
-        fail(p.status, abort_flag);
-      } else {
-        pend &= ~(1u << s);
-        tc_fence_after_sync();
-        issue_f(s);
-      }
-    }
-    if (!mbar_wait(&bar_mma, mma_phase, abort_flag, kWaitNs)) fail(p.status, abort_flag);
-    mma_phase ^= 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-    // (C) softmax over the m landmarks of row `tid`; P (bf16) overwrites F
-    float mx = -INFINITY;
-    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_off + COL_F + c0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
-    }
-    const float mc = mx * p.c;
-    float l = 0.f;
-    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_off + COL_F + c0, r);
-      tmem_ld_wait();
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
-        const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
-        l += a + b;
-        pk[e] = pack_bf16x2(a, b);
-      }
-      tmem_st16(tmem + lane_off + COL_F + (c0 >> 1), pk);
-    }
-    tmem_st_wait();
-    tc_fence_before_sync();
-    __syncthreads();
-    // (D) PW = P W ; CV = T V_halo
-    if (tid == 0) {
-      tc_fence_after_sync();
-      const uint32_t ws_ = smem_u32(sm + p.off_wt);
-      const uint32_t idw = idesc_bf16(128, DP, false, false);
-      for (int kk = 0; kk < p.m_pad / 16; ++kk) {
-        const uint64_t b = smem_desc(ws_ + (kk >> 2) * (DP * 128) + (kk & 3) * 32, 16, 1024, SW_128B);
-        mma_bf16_tA(tmem + COL_PW, tmem + COL_F + kk * 8, b, idw, kk > 0);
-      }
-      if (p.kc > 0) {
-        const uint32_t ts = smem_u32(sm + p.off_t);
-        const uint32_t vs = smem_u32(sm + p.off_v + s * p.v_stage);
-        const uint32_t idc = idesc_bf16(128, DP, false, true);
-        for (int kk = 0; kk < p.kc / 16; ++kk) {
-          const uint64_t a = smem_desc(ts + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, SW_128B);
-          const uint64_t b = smem_desc(vs + kk * 2048, p.kc * 128, 1024, SW_128B);
-          mma_bf16(tmem + COL_CV, a, b, idc, kk > 0);
+        if (jv < jq) {
+          const int g = g0 + jv, sv = jv % kNV;
+          if (jv < kNV || mbar_test(&bars.vempty[sv], ((jv / kNV) - 1) & 1)) {
+            uint8_t* vs = sm + p.off_v + sv * p.v_stage;
+            mbar_arrive_expect_tx(&bars.vfull[sv], p.v_stage);
+            for (int dc = 0; dc < DC; ++dc)
+              tma_load_3d(vs + dc * (p.kc * 128), &maps.v, &bars.vfull[sv], dc * 64,
+                          (g % p.tiles_per_head) * 128 - rad, head_of(g));
+            ++nv_issued[sv];
+            ++jv;
+            prog = true;
+          }
         }
-      }
-      mma_commit(&bar_mma);
-    }
-    if (!mbar_wait(&bar_mma, mma_phase, abort_flag, kWaitNs)) fail(p.status, abort_flag);
-    mma_phase ^= 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-    // (E) stage s is free: prefetch tile g+2; start F of tile g+1 (same head)
-    f_issued = false;
-    if (tid == 0) {
-      if (g + 2 < g1) issue_load(s, g + 2);
-      if (g + 1 < g1 && (g + 1) / p.tiles_per_head == bh) {
-        const int s1 = (j + 1) & 1;
-        if (!mbar_wait(&bar_full[s1], ((j + 1) >> 1) & 1, abort_flag, kWaitNs)) {
-          fail(p.status, abort_flag);
+        if (prog) {
+          t_last = globaltimer_ns();
         } else {
-          pend &= ~(1u << s1);
-          tc_fence_after_sync();
-          issue_f(s1);
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitNs) {
+            set_fail(p.status, abort_flag);
+            break;
+          }
+          __nanosleep(64);  // back off: leave issue slots to the working warps
+        }
+      }
+      if (*abort_flag) {
+        // wait (bounded) for this warp's copies still in flight
+        for (int i = 0; i < 3; ++i)
+          if (nq_issued[i]) mbar_wait(&bars.qfull[i], (nq_issued[i] - 1) & 1, nullptr, kWaitNs);
+        for (int i = 0; i < 2; ++i) {
+          if (nv_issued[i]) mbar_wait(&bars.vfull[i], (nv_issued[i] - 1) & 1, nullptr, kWaitNs);
+          if (nkw_issued[i]) mbar_wait(&bars.kw_full[i], (nkw_issued[i] - 1) & 1, nullptr, kWaitNs);
         }
       }
     }
-    if (g + 1 < g1 && (g + 1) / p.tiles_per_head == bh) f_issued = true;
-    // (F) out = PW / l + CV, bf16
-    const int t = t0 + tid;
-    const float inv_l = 1.f / l;
-    __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + t) * p.d;
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t idf = idesc_bf16(128, p.m_pad, false, false);
+      const uint32_t idw = idesc_bf16(128, DP, false, false);
+      const uint32_t idc = idesc_bf16(128, DP, false, true);
+      int jf = 0, jp = 0;
+      int hi_f = -1, bh_f = -1, hi_p = -1, bh_p = -1;
+      uint64_t t_last = globaltimer_ns();
+      while (jp < ntiles) {
+        bool prog = false;
+        // F stream: F(jf) = Q K~^T into F buffer jf & 1
+        if (jf < ntiles && jf < jp + 2) {
+          const int g = g0 + jf, bh = head_of(g);
+          const bool new_head = bh != bh_f;
+          const int kb = (new_head ? hi_f + 1 : hi_f) % p.nkw;
+          const bool ok = (!new_head || mbar_test(&bars.kw_full[kb], ((hi_f + 1) / p.nkw) & 1)) &&
+                          mbar_test(&bars.qfull[jf % p.nq], (jf / p.nq) & 1) &&
+                          (jf < 2 || mbar_test(&bars.pw_done[jf & 1], ((jf >> 1) - 1) & 1));
+          if (ok) {
+            if (new_head) {
+              bh_f = bh;
+              ++hi_f;
+            }
+            tc_fence_after_sync();
+            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_q + (jf % p.nq) * p.q_stage), 16, 1024, SW_128B);
+            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + kb * kw_bytes), 16, 1024, SW_128B);
+            const uint32_t dcol = tmem + COL_F0 + (jf & 1) * p.m_pad;
 #pragma unroll
-    for (int c0 = 0; c0 < DP; c0 += 32) {
-      uint32_t a[32], b[32];
-      tmem_ld32(tmem + lane_off + COL_PW + c0, a);
-      if (p.kc > 0) tmem_ld32(tmem + lane_off + COL_CV + c0, b);
-      tmem_ld_wait();
-      if (t < p.n && c0 < p.d) {
-        uint32_t o[16];
+            for (int kk = 0; kk < DP / 16; ++kk)
+              mma_bf16(dcol, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                       b0 + (uint64_t)((kk >> 2) * (p.m_pad * 8) + (kk & 3) * 2), idf, kk > 0);
+            mma_commit(&bars.f_full[jf & 1]);
+            mma_commit(&bars.qempty[jf % p.nq]);
+            ++jf;
+            prog = true;
+          }
+        }
+        // PW stream: PW(jp) = P W and CV(jp) = T V into accumulator jp & 1
+        if (jp < jf) {
+          const int g = g0 + jp, bh = head_of(g);
+          const bool new_head = bh != bh_p;
+          const int hin = new_head ? hi_p + 1 : hi_p;
+          const bool ok = (p.kc == 0 || !new_head || mbar_test(&bars.t_ready[hin % p.nt], (hin / p.nt) & 1)) &&
+                          mbar_test(&bars.p_full[jp & 1], (jp >> 1) & 1) &&
+                          (jp < 2 || mbar_test(&bars.acc_empty[jp & 1], ((jp >> 1) - 1) & 1)) &&
+                          (p.kc == 0 || mbar_test(&bars.vfull[jp % kNV], (jp / kNV) & 1));
+          if (ok) {
+            if (new_head) {
+              bh_p = bh;
+              hi_p = hin;
+            }
+            tc_fence_after_sync();
+            const uint32_t acc = tmem + COL_ACC0 + (jp & 1) * ACC_W;
+            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + (hi_p % p.nkw) * kw_bytes + p.kt_bytes), 16, 1024, SW_128B);
+            const uint32_t pcol = tmem + COL_F0 + (jp & 1) * p.m_pad;
+            for (int kk = 0; kk < p.m_pad / 16; ++kk)
+              mma_bf16_tA(acc, pcol + kk * 8, b0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
+            if (p.kc > 0) {
+              const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + (hi_p % p.nt) * p.t_bytes), 16, 1024, SW_128B);
+              const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + (jp % kNV) * p.v_stage), p.kc * 128, 1024, SW_128B);
+              for (int kk = 0; kk < p.kc / 16; ++kk)
+                mma_bf16(acc + DP, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2), v0 + (uint64_t)(kk * 128), idc, kk > 0);
+              mma_commit(&bars.vempty[jp % kNV]);
+            }
+            mma_commit(&bars.acc_full[jp & 1]);
+            mma_commit(&bars.pw_done[jp & 1]);
+            if (jp + 1 == ntiles || head_of(g + 1) != bh) {
+              mma_commit(&bars.kw_empty[hi_p % p.nkw]);
+              if (p.kc > 0) mma_commit(&bars.t_empty[hi_p % p.nt]);
+            }
+            ++jp;
+            prog = true;
+          }
+        }
+        if (prog) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitNs) {
+            set_fail(p.status, abort_flag);
+            break;
+          }
+          __nanosleep(64);  // back off: leave issue slots to the working warps
+        }
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------- Toeplitz builders
+    if (p.kc > 0 && ntiles > 0) {
+      const int lt = tid - 64;  // rows lt and lt + 64
+      int hi = 0, cur_bh = head_of(g0);
+      for (int j = 1; j < ntiles; ++j) {
+        const int bh = head_of(g0 + j);
+        if (bh == cur_bh) continue;
+        cur_bh = bh;
+        ++hi;
+        const int tb = hi % p.nt;
+        if (hi >= p.nt && !wait_or_fail(&bars.t_empty[tb], ((hi / p.nt) - 1) & 1, p.status, abort_flag)) break;
+        const float* wh = p.conv_w + (size_t)(bh % p.H) * p.ks;
+        uint8_t* tbuf = sm + p.off_t + tb * p.t_bytes;
+        for (int rr = 0; rr < 2; ++rr)
+          for (int u0 = 0; u0 < kc64; u0 += 8) toeplitz_chunk(tbuf, wh, p.ks, p.kc, lt + rr * 64, u0);
+        fence_async_smem();
+        mbar_arrive(&bars.t_ready[tb]);
+      }
+    }
+  } else if (warp < 12) {
+    // ------------------------------------- softmax: warps 4-7 even tiles,
+    // warps 8-11 odd tiles (F buffer = tile parity)
+    const int grp = (warp - 4) >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t fcol = tmem + lo + COL_F0 + grp * p.m_pad;
+    for (int j = grp; j < ntiles; j += 2) {
+      if (!__all_sync(0xffffffffu, wait_or_fail(&bars.f_full[grp], (j >> 1) & 1, p.status, abort_flag))) break;
+      tc_fence_after_sync();
+      float mx = -INFINITY;
+      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(fcol + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
+      }
+      const float mc = mx * p.c;
+      float l = 0.f;
+      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(fcol + c0, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
-          if (p.kc > 0) {
-            x0 += __uint_as_float(b[2 * e]);
-            x1 += __uint_as_float(b[2 * e + 1]);
-          }
-          o[e] = pack_bf16x2(x0, x1);
+          const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
+          const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
+          l += a + b;
+          pk[e] = pack_bf16x2(a, b);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        tmem_st16(fcol + (c0 >> 1), pk);
+      }
+      tmem_st_wait();
+      lbuf[(j & 3) * 128 + row] = l;
+      tc_fence_before_sync();
+      mbar_arrive(&bars.p_full[grp]);
+      mbar_arrive(&bars.l_full[j & 3]);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int j = 0; j < ntiles; ++j) {
+      const int ab = j & 1;
+      const int g = g0 + j, bh = head_of(g), t = (g % p.tiles_per_head) * 128 + row;
+      bool ok = wait_or_fail(&bars.acc_full[ab], (j >> 1) & 1, p.status, abort_flag);
+      ok = ok && wait_or_fail(&bars.l_full[j & 3], (j >> 2) & 1, p.status, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after_sync();
+      const float inv_l = 1.f / lbuf[(j & 3) * 128 + row];
+      const uint32_t acc = tmem + lo + COL_ACC0 + ab * ACC_W;
+      __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + t) * p.d;
+      uint4 o4[DP / 8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+      for (int c0 = 0; c0 < DP; c0 += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32(acc + c0, a);
+        if (p.kc > 0) tmem_ld32(acc + DP + c0, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const int i0 = 8 * e + 2 * f;
+            float x0 = __uint_as_float(a[i0]) * inv_l, x1 = __uint_as_float(a[i0 + 1]) * inv_l;
+            if (p.kc > 0) {
+              x0 += __uint_as_float(b[i0]);
+              x1 += __uint_as_float(b[i0 + 1]);
+            }
+            w4[f] = pack_bf16x2(x0, x1);
+          }
+          o4[c0 / 8 + e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&bars.acc_empty[ab]);
+      if (t < p.n) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int e = 0; e < DP / 8; ++e)
+          if (e * 8 < p.d) dst[e] = o4[e];
       }
     }
-    tc_fence_before_sync();
-    __syncthreads();
-  }
-  // wind down: after an abort, wait (bounded) for copies still in flight
-  if (tid == 0 && *abort_flag) {
-    if (pend & 1u) mbar_wait(&bar_full[0], (nload0 - 1) & 1, nullptr, kWaitNs);
-    if (pend & 2u) mbar_wait(&bar_full[1], (nload1 - 1) & 1, nullptr, kWaitNs);
-    if (kw_pending) mbar_wait(&bar_kw, kw_phase ^ 1, nullptr, kWaitNs);
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
+  if (warp == 1) tmem_dealloc(tmem, p.tmem_cols);
 }
 
 int dpad_of(int d) { return d <= 64 ? 64 : 128; }
+
+struct TokPlan {
+  int DP, m_pad, m64, kc, nq, nkw, nt;
+  uint32_t q_stage, v_stage, kt_bytes, wt_bytes, t_bytes, tmem_cols;
+  size_t smem;
+};
+
+bool plan_tokens(const Shape& s, TokPlan* pl) {
+  if (s.dtype != NYS_BF16) return false;
+  pl->DP = dpad_of(s.d);
+  pl->m_pad = ((s.m + 31) / 32) * 32;
+  pl->m64 = s.m64();
+  pl->kc = s.ks > 0 ? ((128 + s.ks - 1 + 15) / 16) * 16 : 0;
+  if (pl->kc > 256 || pl->m_pad > 256) return false;
+  pl->q_stage = 128 * pl->DP * 2;
+  pl->v_stage = (uint32_t)pl->kc * pl->DP * 2;
+  pl->kt_bytes = (uint32_t)pl->m_pad * pl->DP * 2;
+  pl->wt_bytes = (uint32_t)((pl->m_pad + 63) / 64) * pl->DP * 128;
+  pl->t_bytes = pl->kc > 0 ? (uint32_t)((pl->kc + 63) / 64) * 16384 : 0;
+  const uint32_t need = 2 * pl->m_pad + 4 * pl->DP;
+  if (need > 512) return false;
+  uint32_t cols = 32;
+  while (cols < need) cols <<= 1;
+  pl->tmem_cols = cols;
+  const size_t fixed = kNV * (size_t)pl->v_stage + 4 * 128 * 4 + 1024;
+  const size_t kw = pl->kt_bytes + pl->wt_bytes;
+  // preferred first: three Q stages and two buffers of each per-head block;
+  // with one buffer the pipeline drains at a head change
+  const int choices[6][3] = {{3, 2, 2}, {3, 2, 1}, {2, 2, 2}, {2, 2, 1}, {3, 1, 1}, {2, 1, 1}};
+  for (const auto& ch : choices) {
+    const size_t total = fixed + ch[0] * (size_t)pl->q_stage + ch[1] * kw + ch[2] * (size_t)pl->t_bytes;
+    if (total <= kSmemBudget) {
+      pl->nq = ch[0];
+      pl->nkw = ch[1];
+      pl->nt = ch[2];
+      pl->smem = total;
+      return true;
+    }
+  }
+  return false;
+}
 
 }  // namespace
 
 // Shared-memory bytes the tensor-core token kernel needs for this shape
 // (0 if the shape is outside what it handles).
 size_t tokens_tc_smem(const Shape& s) {
-  if (s.dtype != NYS_BF16) return 0;
-  const int DP = dpad_of(s.d);
-  const int m_pad = ((s.m + 31) / 32) * 32;
-  const int kc = s.ks > 0 ? ((128 + s.ks - 1 + 15) / 16) * 16 : 0;
-  if (kc > 256 || m_pad > 256) return 0;
-  const size_t q_stage = 128 * DP * 2, v_stage = (size_t)kc * DP * 2;
-  const size_t kt = (size_t)m_pad * DP * 2, wt = (size_t)((m_pad + 63) / 64) * DP * 128;
-  const size_t tb = kc > 0 ? (size_t)((kc + 63) / 64) * 16384 : 0;
-  const size_t total = 2 * q_stage + 2 * v_stage + kt + wt + tb + 1024;
-  return total <= 227 * 1024 ? total : 0;
+  TokPlan pl;
+  return plan_tokens(s, &pl) ? pl.smem : 0;
 }
 
 int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* kt_bf16,
                      const void* wt_bf16, const float* conv_w, void* out, int* status,
                      int num_sms, cudaStream_t stream) {
-  const size_t smem = tokens_tc_smem(s);
-  if (smem == 0) return NYS_ERR_UNSUPPORTED;
-  const int DP = dpad_of(s.d);
-  const int m_pad = ((s.m + 31) / 32) * 32;
-  const int m64 = ((s.m + 63) / 64) * 64;
-  const int kc = s.ks > 0 ? ((128 + s.ks - 1 + 15) / 16) * 16 : 0;
+  TokPlan pl;
+  if (!plan_tokens(s, &pl)) return NYS_ERR_UNSUPPORTED;
   const uint64_t BH = (uint64_t)s.bh();
+  const int DP = pl.DP;
 
   TokMaps maps;
   {
     const uint64_t dims[3] = {(uint64_t)s.d, (uint64_t)s.n, BH};
     const uint64_t strides[2] = {(uint64_t)s.d * 2, (uint64_t)s.n * s.d * 2};
     const uint32_t boxq[3] = {64, 128, 1};
-    const uint32_t boxv[3] = {64, (uint32_t)(kc > 0 ? kc : 16), 1};
+    const uint32_t boxv[3] = {64, (uint32_t)(pl.kc > 0 ? pl.kc : 16), 1};
     if (!make_tensor_map(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, boxq,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, boxv,
@@ -339,16 +507,16 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
       return NYS_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)DP, (uint64_t)m64, BH};
-    const uint64_t strides[2] = {(uint64_t)DP * 2, (uint64_t)m64 * DP * 2};
-    const uint32_t box[3] = {64, (uint32_t)m_pad, 1};
+    const uint64_t dims[3] = {(uint64_t)DP, (uint64_t)pl.m64, BH};
+    const uint64_t strides[2] = {(uint64_t)DP * 2, (uint64_t)pl.m64 * DP * 2};
+    const uint32_t box[3] = {64, (uint32_t)pl.m_pad, 1};
     if (!make_tensor_map(&maps.kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
       return NYS_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)m64, (uint64_t)DP, BH};
-    const uint64_t strides[2] = {(uint64_t)m64 * 2, (uint64_t)m64 * DP * 2};
+    const uint64_t dims[3] = {(uint64_t)pl.m64, (uint64_t)DP, BH};
+    const uint64_t strides[2] = {(uint64_t)pl.m64 * 2, (uint64_t)pl.m64 * DP * 2};
     const uint32_t box[3] = {64, (uint32_t)DP, 1};
     if (!make_tensor_map(&maps.wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, wt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -363,35 +531,36 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
   p.n = s.n;
   p.d = s.d;
   p.m = s.m;
-  p.m_pad = m_pad;
+  p.m_pad = pl.m_pad;
   p.ks = s.ks;
-  p.kc = kc;
+  p.kc = pl.kc;
+  p.nq = pl.nq;
+  p.nkw = pl.nkw;
+  p.nt = pl.nt;
   p.tiles_per_head = (s.n + 127) / 128;
   p.total_tiles = (int)(BH * p.tiles_per_head);
   const int ctas = std::min(p.total_tiles, num_sms);
   p.tiles_per_cta = (p.total_tiles + ctas - 1) / ctas;
   const int grid = (p.total_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
   p.c = (1.0f / sqrtf((float)s.d)) * 1.4426950408889634f;
-  const uint32_t need = (uint32_t)(m_pad + 2 * DP);
-  uint32_t cols = 32;
-  while (cols < need) cols <<= 1;
-  p.tmem_cols = cols;
-  p.q_stage = 128 * DP * 2;
-  p.v_stage = (uint32_t)kc * DP * 2;
-  p.kt_bytes = (uint32_t)m_pad * DP * 2;
-  p.wt_bytes = (uint32_t)((m_pad + 63) / 64) * DP * 128;
+  p.tmem_cols = pl.tmem_cols;
+  p.q_stage = pl.q_stage;
+  p.v_stage = pl.v_stage;
+  p.kt_bytes = pl.kt_bytes;
+  p.wt_bytes = pl.wt_bytes;
+  p.t_bytes = pl.t_bytes;
   p.off_q = 0;
-  p.off_v = 2 * p.q_stage;
-  p.off_kt = p.off_v + 2 * p.v_stage;
-  p.off_wt = p.off_kt + p.kt_bytes;
-  p.off_t = p.off_wt + p.wt_bytes;
+  p.off_v = p.nq * p.q_stage;
+  p.off_kt = p.off_v + kNV * p.v_stage;
+  p.off_t = p.off_kt + p.nkw * (p.kt_bytes + p.wt_bytes);
+  p.off_l = p.off_t + p.nt * p.t_bytes;
 
   auto kern = DP == 64 ? tokens_tc<64> : tokens_tc<128>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
       cudaSuccess)
     return NYS_ERR_CUDA;
   KernelScope scope("tokens_tc", stream);
-  kern<<<grid, 128, smem, stream>>>(maps, p);
+  kern<<<grid, kThreads, pl.smem, stream>>>(maps, p);
   return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
 }
 
