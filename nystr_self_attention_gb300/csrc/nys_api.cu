@@ -11,10 +11,6 @@
 
 namespace nys {
 
-int launch_forward_simt(const Shape& s, const void* q, const void* k, const void* v,
-                        const float* conv_w, void* out, char* ws, const Layout& L,
-                        cudaStream_t stream);
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -134,7 +130,7 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
   // each call starts with a clear status word (kernels only ever set it)
   cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
   if (e != cudaSuccess) return set_cuda_error(e);
-  const int rc = launch_forward_simt(s, q, k, v, conv_w, out, ws, L, stream);
+  const int rc = launch_forward(s, q, k, v, conv_w, out, ws, L, stream, dev);
   if (rc == NYS_ERR_CUDA) g_last_error = cudaGetErrorString(cudaGetLastError());
   return rc;
 }
@@ -145,9 +141,9 @@ Layout make_layout(const Shape& s) {
   // Key splits of the landmark-row pass: enough CTAs to fill the GPU a few
   // times over (CUDA-core path: at least 32 keys per split; tensor-core
   // path: whole 128-key tiles).
+  L.tiles_per_split = 0;
   if (s.dtype == NYS_BF16) {
-    int tps = 0;
-    rows_tc_split(s, &L.splits, &tps);
+    rows_tc_split(s, &L.splits, &L.tiles_per_split);
   } else {
     const long long rb = (s.m + 7) / 8;
     long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);

@@ -1,0 +1,138 @@
+// Forward-pass orchestration: which kernel runs each step, and the split of
+// the batch into head groups that run concurrently on library streams.
+//
+// Per head the steps are landmarks -> landmark rows -> pseudo-inverse ->
+// token rows (each depends on the previous one). The pseudo-inverse is a
+// serial chain of small dependent products and leaves most of the GPU idle,
+// while the other steps stream the inputs. Splitting the batch into groups
+// of whole batch entries and running each group's four steps on its own
+// stream lets one group's pseudo-inverse overlap the other groups' streaming
+// steps. The groups share the workspace arrays (each at its own head
+// offset), so the workspace layout does not depend on the grouping.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "nys_internal.h"
+
+namespace nys {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxGroups = 8;
+
+struct DeviceStreams {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t aux[kMaxGroups] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kMaxGroups] = {};
+};
+DeviceStreams g_streams[kMaxDevices];
+
+int ensure_streams(int dev) {
+  DeviceStreams& d = g_streams[dev];
+  std::lock_guard<std::mutex> lk(d.mu);
+  if (d.ready) return NYS_OK;
+  cudaError_t e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+  for (int i = 1; i < kMaxGroups && e == cudaSuccess; ++i) {
+    e = cudaStreamCreateWithFlags(&d.aux[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return set_cuda_error(e);
+  d.ready = true;
+  return NYS_OK;
+}
+
+// Number of head groups: only for the tensor-core path with short
+// sequences, where the pseudo-inverse dominates; whole batch entries per
+// group. NYS_HEAD_GROUPS overrides the choice (tuning).
+int choose_groups(const Shape& s) {
+  static int override_groups = [] {
+    const char* e = std::getenv("NYS_HEAD_GROUPS");
+    return e ? std::atoi(e) : 0;
+  }();
+  int g = 1;
+  if (s.dtype == NYS_BF16 && s.n <= 2048 && s.bh() >= 256) g = 2;
+  if (override_groups > 0) g = override_groups;
+  if (g > kMaxGroups) g = kMaxGroups;
+  if (g > s.B) g = s.B;
+  while (g > 1 && s.B % g != 0) --g;
+  return g;
+}
+
+template <typename T>
+T* at(char* ws, size_t off) { return reinterpret_cast<T*>(ws + off); }
+
+// The four steps for heads [bh0, bh0 + sg.bh()) of the full problem.
+int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, const void* k,
+              const void* v, const float* conv_w, void* out, char* ws, const Layout& L,
+              cudaStream_t st) {
+  const size_t esz = full.dtype == NYS_FP32 ? 4 : 2;
+  const size_t tok = (size_t)bh0 * full.n * full.d * esz;
+  const void* qg = static_cast<const char*>(q) + tok;
+  const void* kg = static_cast<const char*>(k) + tok;
+  const void* vg = static_cast<const char*>(v) + tok;
+  void* og = static_cast<char*>(out) + tok;
+  const size_t md = (size_t)full.m * full.d, mm = (size_t)full.m * full.m;
+  const size_t pad = (size_t)full.m64() * full.dpad();
+  float* qt = at<float>(ws, L.q_tilde) + bh0 * md;
+  float* kt = at<float>(ws, L.k_tilde) + bh0 * md;
+  float* gp = at<float>(ws, L.g_part) + bh0 * L.splits * md;
+  float* gml = at<float>(ws, L.g_ml) + bh0 * L.splits * full.m * 2;
+  float* g = at<float>(ws, L.g) + bh0 * md;
+  float* a = at<float>(ws, L.a_s) + bh0 * mm;
+  float* z = at<float>(ws, L.z) + bh0 * mm;
+  float* w = at<float>(ws, L.w) + bh0 * md;
+  float* scr = at<float>(ws, L.scratch) + bh0 * 3 * mm;
+  int* status = at<int>(ws, L.status);
+  const bool bf16 = full.dtype == NYS_BF16;
+  const bool tc_tokens = tokens_tc_smem(full) > 0;
+  __nv_bfloat16* qt_b = bf16 ? at<__nv_bfloat16>(ws, L.qt_bf16) + bh0 * pad : nullptr;
+  __nv_bfloat16* kt_b = (bf16 && tc_tokens) ? at<__nv_bfloat16>(ws, L.kt_bf16) + bh0 * pad : nullptr;
+  __nv_bfloat16* wt_b = bf16 ? at<__nv_bfloat16>(ws, L.wt_bf16) + bh0 * pad : nullptr;
+
+  int rc = launch_landmarks(sg, qg, kg, qt, kt, qt_b, kt_b, st);
+  if (rc != NYS_OK) return rc;
+  rc = bf16 ? launch_rows_tc(sg, qt_b, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st)
+            : launch_rows_simt(sg, qt, kg, vg, gp, gml, L.splits, st);
+  if (rc != NYS_OK) return rc;
+  rc = pinv_tc_supported(full)
+           ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, w, wt_b, L.splits, status, st)
+           : launch_pinv_simt(sg, qt, kt, gp, gml, g, a, z, w, scr, tc_tokens ? wt_b : nullptr,
+                              L.splits, st);
+  if (rc != NYS_OK) return rc;
+  return tc_tokens ? launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st)
+                   : launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
+}
+
+}  // namespace
+
+int launch_forward(const Shape& s, const void* q, const void* k, const void* v,
+                   const float* conv_w, void* out, char* ws, const Layout& L,
+                   cudaStream_t stream, int dev) {
+  const int groups = choose_groups(s);
+  if (groups <= 1) return run_group(s, s, 0, q, k, v, conv_w, out, ws, L, stream);
+  int rc = ensure_streams(dev);
+  if (rc != NYS_OK) return rc;
+  DeviceStreams& d = g_streams[dev];
+  cudaError_t e = cudaEventRecord(d.fork, stream);
+  for (int i = 1; i < groups && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(d.aux[i], d.fork, 0);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  Shape sg = s;
+  sg.B = s.B / groups;
+  for (int i = 0; i < groups; ++i) {
+    rc = run_group(s, sg, (long long)i * sg.bh(), q, k, v, conv_w, out, ws, L,
+                   i == 0 ? stream : d.aux[i]);
+    if (rc != NYS_OK) return rc;
+  }
+  for (int i = 1; i < groups && e == cudaSuccess; ++i) {
+    e = cudaEventRecord(d.join[i], d.aux[i]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d.join[i], 0);
+  }
+  return e == cudaSuccess ? NYS_OK : set_cuda_error(e);
+}
+
+}  // namespace nys

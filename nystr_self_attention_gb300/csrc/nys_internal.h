@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -36,6 +37,7 @@ struct Layout {
   size_t wt_bf16;  // bf16 [dpad][m64]    W^T, zero padded (tensor-core operand)
   size_t total;
   int splits;      // key splits of the landmark-row pass
+  int tiles_per_split;  // 128-key tiles per split (tensor-core landmark-row pass)
 };
 
 Layout make_layout(const Shape& s);
@@ -75,10 +77,23 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
                      const void* wt_bf16, const float* conv_w, void* out, int* status,
                      int num_sms, cudaStream_t stream);
 
-// Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs.
+// Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs. `s` may be
+// a group of heads of the full problem: splits / tiles_per_split come from
+// the full problem's layout.
 void rows_tc_split(const Shape& s, int* splits, int* tiles_per_split);
 int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
-                   float* gml, int splits, int* status, cudaStream_t stream);
+                   float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream);
+
+// CUDA-core steps (nys_simt.cu); `s` may be a group of heads.
+int launch_landmarks(const Shape& s, const void* q, const void* k, float* qt, float* kt,
+                     __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream);
+int launch_rows_simt(const Shape& s, const float* qt, const void* k, const void* v, float* gp,
+                     float* gml, int splits, cudaStream_t stream);
+int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const float* gp,
+                     const float* gml, float* g, float* a, float* z, float* w, float* scratch,
+                     __nv_bfloat16* wt_b, int splits, cudaStream_t stream);
+int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,
+                       const float* w, const float* conv_w, void* out, cudaStream_t stream);
 
 // Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
 bool pinv_tc_supported(const Shape& s);
@@ -86,10 +101,11 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
                    const float* gml, float* g, float* a_s, float* w, void* wt_bf16, int splits,
                    int* status, cudaStream_t stream);
 
-// Enqueue the whole forward pass. Pointers are device pointers; ws has
-// Layout::total bytes. Returns NYS_OK or NYS_ERR_CUDA (launch failure).
+// Enqueue the whole forward pass (nys_forward.cu). Pointers are device
+// pointers; ws has Layout::total bytes; dev is the current device. Returns
+// NYS_OK or NYS_ERR_CUDA (a failed launch).
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,
                    const float* conv_w, void* out, char* ws, const Layout& L,
-                   cudaStream_t stream);
+                   cudaStream_t stream, int dev);
 
 }  // namespace nys

@@ -261,7 +261,7 @@ void rows_tc_split(const Shape& s, int* splits, int* tiles_per_split) {
 }
 
 int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
-                   float* gml, int splits, int* status, cudaStream_t stream) {
+                   float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream) {
   const int DP = s.dpad();
   const int m64 = s.m64();
   const uint64_t BH = (uint64_t)s.bh();
@@ -291,9 +291,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
   p.n = s.n;
   p.d = s.d;
   p.m = s.m;
-  int sp = 0, tps = 0;
-  rows_tc_split(s, &sp, &tps);
-  if (sp != splits) return NYS_ERR_CUDA;
+  const int sp = splits, tps = tiles_per_split;
   p.splits = sp;
   p.tiles_per_split = tps;
   p.n_tiles = (s.n + 127) / 128;

@@ -500,29 +500,10 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 }
 
 template <typename T>
-int launch_simt(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
-                void* out, char* ws, const Layout& L, cudaStream_t stream) {
+int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* kt,
+                __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream) {
   const T* qq = static_cast<const T*>(q);
   const T* kk = static_cast<const T*>(k);
-  const T* vv = static_cast<const T*>(v);
-  float* qt = reinterpret_cast<float*>(ws + L.q_tilde);
-  float* kt = reinterpret_cast<float*>(ws + L.k_tilde);
-  float* gp = reinterpret_cast<float*>(ws + L.g_part);
-  float* gml = reinterpret_cast<float*>(ws + L.g_ml);
-  float* g = reinterpret_cast<float*>(ws + L.g);
-  float* a = reinterpret_cast<float*>(ws + L.a_s);
-  float* z = reinterpret_cast<float*>(ws + L.z);
-  float* w = reinterpret_cast<float*>(ws + L.w);
-  float* scr = reinterpret_cast<float*>(ws + L.scratch);
-  const bool tc_tokens = tokens_tc_smem(s) > 0;
-  __nv_bfloat16* kt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.kt_bf16) : nullptr;
-  __nv_bfloat16* wt_b = tc_tokens ? reinterpret_cast<__nv_bfloat16*>(ws + L.wt_bf16) : nullptr;
-  const bool tc_rows = s.dtype == NYS_BF16;
-  __nv_bfloat16* qt_b = tc_rows ? reinterpret_cast<__nv_bfloat16*>(ws + L.qt_bf16) : nullptr;
-  int* status = reinterpret_cast<int*>(ws + L.status);
-  const float scale = 1.0f / sqrtf((float)s.d);
-  const unsigned bh = (unsigned)s.bh();
-
   if (32 % (s.d / (16 / (int)sizeof(T))) == 0) {
     const long long jobs = 2ll * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
@@ -530,59 +511,72 @@ int launch_simt(const Shape& s, const void* q, const void* k, const void* v, con
         qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
   } else {
     KernelScope ks_("landmarks_simt", stream);
-    landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, bh), 256, 0, stream>>>(
+    landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, (unsigned)s.bh()), 256, 0, stream>>>(
         qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
   }
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
 
-  if (tc_rows) {
-    const int rc = launch_rows_tc(s, qt_b, k, v, gp, gml, L.splits, status, stream);
-    if (rc != NYS_OK) return rc;
-  } else {
-  const int kps = (s.n + L.splits - 1) / L.splits;
-  const size_t rows_smem = sizeof(float) * (RW_ROWS * s.d + RW_KEYS * (s.d + 1) + RW_KEYS * s.d +
-                                            RW_ROWS * RW_KEYS + RW_ROWS);
-  {
-    KernelScope ks_("rows_simt", stream);
-    rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, L.splits, bh), 128, rows_smem, stream>>>(
-      qt, kk, vv, gp, gml, s.n, s.d, s.m, L.splits, kps, scale);
-  }
-  }
+template <typename T>
+int rows_t(const Shape& s, const float* qt, const void* k, const void* v, float* gp, float* gml,
+           int splits, cudaStream_t stream) {
+  const float scale = 1.0f / sqrtf((float)s.d);
+  const int kps = (s.n + splits - 1) / splits;
+  const size_t smem = sizeof(float) * (RW_ROWS * s.d + RW_KEYS * (s.d + 1) + RW_KEYS * s.d +
+                                       RW_ROWS * RW_KEYS + RW_ROWS);
+  KernelScope ks_("rows_simt", stream);
+  rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, splits, (unsigned)s.bh()), 128, smem, stream>>>(
+      qt, static_cast<const T*>(k), static_cast<const T*>(v), gp, gml, s.n, s.d, s.m, splits, kps,
+      scale);
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
 
-  if (pinv_tc_supported(s)) {
-    const int rc = launch_pinv_tc(s, qt, kt, gp, gml, g, a, w, ws + L.wt_bf16, L.splits, status,
-                                  stream);
-    if (rc != NYS_OK) return rc;
-  } else {
-    KernelScope ks_("pinv_simt", stream);
-    pinv_simt<<<bh, 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scr, wt_b, s.d, s.m, L.splits,
-                                      s.iters, scale, s.m64(), s.dpad());
-  }
-
-  if (tc_tokens) {
-    return launch_tokens_tc(s, q, v, kt_b, wt_b, conv_w, out, status, num_sms(), stream);
-  }
+template <typename T>
+int tokens_t(const Shape& s, const void* q, const void* v, const float* kt, const float* w,
+             const float* conv_w, void* out, cudaStream_t stream) {
+  const float scale = 1.0f / sqrtf((float)s.d);
   const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
-  const size_t tok_smem = sizeof(float) * (TK_ROWS * s.d + TK_LM * (s.d + 1) + TK_LM * s.d +
-                                           TK_ROWS * 33 + 2 * TK_ROWS + (TK_ROWS + 2 * rad) * s.d);
-  if (tok_smem > 48 * 1024 &&
+  const size_t smem = sizeof(float) * (TK_ROWS * s.d + TK_LM * (s.d + 1) + TK_LM * s.d +
+                                       TK_ROWS * 33 + 2 * TK_ROWS + (TK_ROWS + 2 * rad) * s.d);
+  if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(tokens_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tok_smem) != cudaSuccess)
+                           (int)smem) != cudaSuccess)
     return NYS_ERR_CUDA;
-  {
-    KernelScope ks_("tokens_simt", stream);
-    tokens_simt<T><<<dim3((s.n + TK_ROWS - 1) / TK_ROWS, bh), 256, tok_smem, stream>>>(
-      qq, vv, kt, w, conv_w, static_cast<T*>(out), s.H, s.n, s.d, s.m, s.ks, scale);
-  }
+  KernelScope ks_("tokens_simt", stream);
+  tokens_simt<T><<<dim3((s.n + TK_ROWS - 1) / TK_ROWS, (unsigned)s.bh()), 256, smem, stream>>>(
+      static_cast<const T*>(q), static_cast<const T*>(v), kt, w, conv_w, static_cast<T*>(out), s.H,
+      s.n, s.d, s.m, s.ks, scale);
   return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_forward_simt(const Shape& s, const void* q, const void* k, const void* v,
-                        const float* conv_w, void* out, char* ws, const Layout& L,
-                        cudaStream_t stream) {
-  if (s.dtype == NYS_FP32) return launch_simt<float>(s, q, k, v, conv_w, out, ws, L, stream);
-  return launch_simt<__nv_bfloat16>(s, q, k, v, conv_w, out, ws, L, stream);
+int launch_landmarks(const Shape& s, const void* q, const void* k, float* qt, float* kt,
+                     __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream) {
+  return s.dtype == NYS_FP32 ? landmarks_t<float>(s, q, k, qt, kt, qt_b, kt_b, stream)
+                             : landmarks_t<__nv_bfloat16>(s, q, k, qt, kt, qt_b, kt_b, stream);
+}
+
+int launch_rows_simt(const Shape& s, const float* qt, const void* k, const void* v, float* gp,
+                     float* gml, int splits, cudaStream_t stream) {
+  return s.dtype == NYS_FP32 ? rows_t<float>(s, qt, k, v, gp, gml, splits, stream)
+                             : rows_t<__nv_bfloat16>(s, qt, k, v, gp, gml, splits, stream);
+}
+
+int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const float* gp,
+                     const float* gml, float* g, float* a, float* z, float* w, float* scratch,
+                     __nv_bfloat16* wt_b, int splits, cudaStream_t stream) {
+  KernelScope ks_("pinv_simt", stream);
+  pinv_simt<<<(unsigned)s.bh(), 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scratch, wt_b, s.d,
+                                                  s.m, splits, s.iters,
+                                                  1.0f / sqrtf((float)s.d), s.m64(), s.dpad());
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
+
+int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,
+                       const float* w, const float* conv_w, void* out, cudaStream_t stream) {
+  return s.dtype == NYS_FP32 ? tokens_t<float>(s, q, v, kt, w, conv_w, out, stream)
+                             : tokens_t<__nv_bfloat16>(s, q, v, kt, w, conv_w, out, stream);
 }
 
 }  // namespace nys
