@@ -149,10 +149,13 @@ def oracle_sample(inp, budget_s: float, max_heads: int | None = None):
         heads = heads[:max_heads]
     done = 0
     t0 = time.perf_counter()
-    for b, h in heads:
-        R.nystrom_head(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.conv_w[h], wl.m, wl.iters)
-        done += 1
-        if time.perf_counter() - t0 >= budget_s:
+    while True:  # whole passes over the heads until the budget is spent
+        for b, h in heads:
+            R.nystrom_head(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.conv_w[h], wl.m, wl.iters)
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s or max_heads is not None:
             break
     dt = time.perf_counter() - t0
     return done * wl.n, dt, done
@@ -204,12 +207,76 @@ def run_reference(args, wl):
 
 # --------------------------------------------------------------------- ours ----
 
+# Per-kernel roofline model: algorithmic HBM bytes in units of T*e
+# (T = B*H*n*d elements, e = element bytes), or algorithmic flops.
 KERNEL_BYTES = {
-    # algorithmic HBM bytes per launch, in units of T*e (T = B*H*n*d, e = element bytes)
-    "landmarks_simt": 2.0,   # read Q, K
-    "rows_simt": 2.0,        # read K, V
-    "tokens_simt": 3.0,      # read Q, V; write out
+    "landmarks_vec": 2.0, "landmarks_simt": 2.0,  # read Q, K
+    "rows_tc": 2.0, "rows_simt": 2.0,             # read K, V
+    "tokens_tc": 3.0, "tokens_simt": 3.0,          # read Q, V; write out
 }
+KERNEL_SOURCES = {
+    "landmarks_vec": "nys_simt.cu", "landmarks_simt": "nys_simt.cu", "rows_simt": "nys_simt.cu",
+    "pinv_simt": "nys_simt.cu", "tokens_simt": "nys_simt.cu", "rows_tc": "nys_rows_tc.cu",
+    "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu",
+}
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates
+
+
+def pinv_flops(wl):
+    """Algorithmic flops of the landmark kernel, the iteration and W = Z G."""
+    m, d = wl.m, wl.d
+    return wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + 2.0 * m * m * d)
+
+
+def kernel_source_hash(kernel):
+    import hashlib
+    src = os.path.join(ROOT, "nystr_self_attention_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    if not os.path.isfile(src):
+        return None
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from profiles/dram_traffic.txt (written from an ncu
+    capture), only if the kernel's source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = kernel_source_hash(kernel)
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and \
+                parts[1] == workload and parts[2] == h:
+            return float(parts[3])
+    return None
+
+
+def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
+    """Roofline of one kernel: `launches` launches took `ms` in total, and
+    `per_step` launches make up one forward pass (the batch is split into
+    that many head groups), so one launch covers 1/per_step of the work."""
+    t_launch = ms / launches / 1e3
+    te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes / per_step
+    traffic = measured_traffic(kernel, wl.name)
+    if kernel in KERNEL_BYTES:
+        achieved = KERNEL_BYTES[kernel] * te / t_launch / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes": KERNEL_BYTES[kernel] * te,
+                "peak_source": f"hbm_gbs ({peak_src})"}
+    flops = pinv_flops(wl) / per_step
+    achieved = flops / t_launch / 1e12
+    if kernel == "pinv_tc":
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_flops": flops,
+                "peak_source": f"bf16_tflops_sustained ({peak_src}) x 1.1/2.25 (tf32/bf16 nominal)"}
+    peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
+    return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "algorithmic_flops": flops,
+            "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
 
 
 def run_ours(args, wl):
@@ -319,24 +386,14 @@ def run_ours(args, wl):
         for name, (ms, cnt) in prof.items():
             kernels[name] = {"launches_per_step": cnt / prof_steps, "us_per_launch": ms / cnt * 1e3,
                              "share": ms / tot}
+            per_step = max(1, round(cnt / prof_steps))
+            kernels[name]["roofline"] = roofline_for(name, ms, cnt, per_step, wl, peaks, peak_src)
         dom = max(prof, key=lambda k: prof[k][0])
-        ms, cnt = prof[dom]
-        t_launch = ms / cnt / 1e3
-        te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
-        if dom in KERNEL_BYTES:
-            achieved = KERNEL_BYTES[dom] * te / t_launch / 1e9
-            roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved,
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                        "peak_source": f"hbm_gbs of {peak_src}"}
-        else:
-            # pseudo-inverse on CUDA cores: fp32 FMA arithmetic
-            flops = wl.heads * (8.0 * wl.iters * wl.m ** 3 + 2.0 * wl.m ** 2 * wl.d * 2)
-            achieved = flops / t_launch / 1e12
-            peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
-            roofline = {"kernel": dom, "bound": "alu", "achieved": achieved, "peak": peak,
-                        "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                        "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
+        roofline = dict(kernels[dom]["roofline"])
+        for v in kernels.values():
+            r = v.pop("roofline")
+            v["frac"] = r["frac"]
+            v["bound"] = r["bound"]
 
     # end to end through the host-buffer C ABI call, pinned host memory
     e2e = None
@@ -375,8 +432,8 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tk, secs, heads = oracle_sample(inp, args.cpu_seconds)
         cpu = {"value": tk / secs, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{heads} of {wl.heads} heads (n={wl.n} tokens each), fp64 numpy, "
-                         f"{secs:.1f} s"}
+               "sample": f"{heads} head passes over the {wl.heads} heads (n={wl.n} tokens each), "
+                         f"fp64 numpy, {secs:.1f} s"}
 
     if world > 1:
         dist.destroy_process_group()
