@@ -127,6 +127,76 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
     for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
 }
 
+// Small segments (seg * d / V = 32 * VPL 16-byte vectors, VPL <= 4): one
+// warp takes SPW = 8 / VPL consecutive segments of one (tensor, head) and
+// issues all of its loads before reducing, so each warp keeps 8 vectors per
+// lane in flight. grid: (ceil(2 * B*H * ceil(m64 / SPW) / 8)), block 256.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256)
+landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
+                float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
+                __nv_bfloat16* __restrict__ kt_b, long long n_heads, int n, int d, int m, int m64,
+                int dpad) {
+  constexpr int V = 16 / sizeof(T);
+  constexpr int SPW = 8 / VPL;
+  const int nblk = (m64 + SPW - 1) / SPW;
+  const long long job = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (job >= 2 * n_heads * nblk) return;
+  const int tensor = (int)(job / (n_heads * nblk));
+  const long long rest = job - (long long)tensor * n_heads * nblk;
+  const long long bh = rest / nblk;
+  const int i0 = (int)(rest % nblk) * SPW;
+  const int seg = n / m, vpr = d / V;
+  const T* base = (tensor == 0 ? q : k) + (size_t)bh * n * d;
+  __nv_bfloat16* outb = tensor == 0 ? qt_b : kt_b;
+  float* outf = (tensor == 0 ? qt : kt) + (size_t)bh * m * d;
+  uint4 buf[SPW][VPL];
+#pragma unroll
+  for (int si = 0; si < SPW; ++si) {
+    const int i = i0 + si;
+    const uint4* src4 = reinterpret_cast<const uint4*>(base + (size_t)i * seg * d);
+#pragma unroll
+    for (int u = 0; u < VPL; ++u)
+      buf[si][u] = (i < m) ? __ldg(src4 + lane + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const float inv = 1.f / (float)seg;
+#pragma unroll
+  for (int si = 0; si < SPW; ++si) {
+    const int i = i0 + si;
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const T* x = reinterpret_cast<const T*>(&buf[si][u]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += ld(x + e);
+    }
+    for (int o = vpr; o < 32; o <<= 1)
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    if (i >= m64) continue;
+    if (i >= m) {
+      if (outb)
+        for (int c = lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
+      continue;
+    }
+    if (lane < vpr) {
+      float* out = outf + (size_t)i * d + lane * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) out[e] = acc[e] * inv;
+      if (outb) {
+        __nv_bfloat16* ob = outb + ((size_t)bh * m64 + i) * dpad + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+      }
+    }
+    if (outb)
+      for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
+  }
+}
+
 // -------------------------------------------------------------------- rows
 // grid (ceil(m/8), splits, B*H), block 128. CTA: 8 landmark rows x one key
 // range, keys in chunks of 32. Writes unnormalised partial O, and (max, sum).
@@ -504,7 +574,21 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
                 __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream) {
   const T* qq = static_cast<const T*>(q);
   const T* kk = static_cast<const T*>(k);
-  if (32 % (s.d / (16 / (int)sizeof(T))) == 0) {
+  const int vpr = s.d / (16 / (int)sizeof(T));
+  const long long nvec = (long long)s.seg() * vpr;
+  if (32 % vpr == 0 && (nvec == 32 || nvec == 64 || nvec == 128)) {
+    const int vpl = (int)(nvec / 32);
+    const int spw = 8 / vpl;
+    const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
+    const unsigned grid = (unsigned)((jobs + 7) / 8);
+    KernelScope ks_("landmarks_vec", stream);
+    if (vpl == 1)
+      landmarks_small<T, 1><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+    else if (vpl == 2)
+      landmarks_small<T, 2><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+    else
+      landmarks_small<T, 4><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+  } else if (32 % vpr == 0) {
     const long long jobs = 2ll * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
     landmarks_vec<T><<<(unsigned)((jobs + 7) / 8), 256, 0, stream>>>(

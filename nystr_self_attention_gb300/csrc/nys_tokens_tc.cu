@@ -7,7 +7,9 @@
 //                done), V halos (ring of 2, freed once the conv is done), and
 //                per head K~ and W^T (1-2 buffers); Q and V streams advance
 //                independently
-//   warp 1       tcgen05 issuer, two independent streams:
+//   warp 1       tcgen05 issuer of the F stream; warp 16 issuer of the PW /
+//                conv stream (one issuing thread per stream: each tcgen05.mma
+//                costs its issuing thread tens of cycles):
 //                  F  = Q_tile K~^T          A = Q (smem), B = K~ (smem)
 //                  PW = P W                  A = P (TMEM), B = W^T (smem)
 //                  CV = T V_halo             A = banded Toeplitz of the conv
@@ -52,7 +54,7 @@ struct TokParams {
 };
 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
-constexpr int kThreads = 512;
+constexpr int kThreads = 544;
 constexpr int kNV = 2;  // V halo stages
 // dynamic shared memory budget: the 227 KB per-block opt-in limit less the
 // kernel's static shared memory (barriers) and a margin
@@ -235,18 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------- MMA issuer, F stream
     if (lane == 0 && ntiles > 0) {
       const uint32_t idf = idesc_bf16(128, p.m_pad, false, false);
-      const uint32_t idw = idesc_bf16(128, DP, false, false);
-      const uint32_t idc = idesc_bf16(128, DP, false, true);
-      int jf = 0, jp = 0;
-      int hi_f = -1, bh_f = -1, hi_p = -1, bh_p = -1;
+      int jf = 0;
+      int hi_f = -1, bh_f = -1;
       uint64_t t_last = globaltimer_ns();
-      while (jp < ntiles) {
+      while (jf < ntiles) {
         bool prog = false;
         // F stream: F(jf) = Q K~^T into F buffer jf & 1
-        if (jf < ntiles && jf < jp + 2) {
+        if (jf < ntiles) {
           const int g = g0 + jf, bh = head_of(g);
           const bool new_head = bh != bh_f;
           const int kb = (new_head ? hi_f + 1 : hi_f) % p.nkw;
@@ -272,8 +272,30 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
             prog = true;
           }
         }
+        if (prog) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitNs) {
+            set_fail(p.status, abort_flag);
+            break;
+          }
+          __nanosleep(64);  // back off: leave issue slots to the working warps
+        }
+      }
+    }
+  } else if (warp == 16) {
+    // ---------------------------------------- MMA issuer, PW / conv stream
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t idw = idesc_bf16(128, DP, false, false);
+      const uint32_t idc = idesc_bf16(128, DP, false, true);
+      int jp = 0;
+      int hi_p = -1, bh_p = -1;
+      uint64_t t_last = globaltimer_ns();
+      while (jp < ntiles) {
+        bool prog = false;
         // PW stream: PW(jp) = P W and CV(jp) = T V into accumulator jp & 1
-        if (jp < jf) {
+        {
           const int g = g0 + jp, bh = head_of(g);
           const bool new_head = bh != bh_p;
           const int hin = new_head ? hi_p + 1 : hi_p;
@@ -382,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       mbar_arrive(&bars.p_full[grp]);
       mbar_arrive(&bars.l_full[j & 3]);
     }
-  } else {
+  } else if (warp < 16) {
     // ------------------------------------------------------------ epilogue
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
