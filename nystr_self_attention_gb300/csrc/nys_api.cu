@@ -135,6 +135,8 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
   return rc;
 }
 
+int scratch_mats(const Shape& s) { return pinv_big_supported(s) ? 5 : 3; }
+
 Layout make_layout(const Shape& s) {
   Layout L{};
   const size_t bh = (size_t)s.bh(), md = (size_t)s.m * s.d, mm = (size_t)s.m * s.m;
@@ -164,7 +166,7 @@ Layout make_layout(const Shape& s) {
   L.a_s = take(bh * mm * 4);
   L.z = take(bh * mm * 4);
   L.w = take(bh * md * 4);
-  L.scratch = take(bh * 3 * mm * 4);
+  L.scratch = take(bh * scratch_mats(s) * mm * 4);
   const size_t pad_bf16 = s.dtype == NYS_BF16 ? bh * (size_t)s.m64() * s.dpad() * 2 : 0;
   L.qt_bf16 = take(pad_bf16);
   L.kt_bf16 = take(pad_bf16);

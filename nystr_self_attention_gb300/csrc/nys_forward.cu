@@ -86,12 +86,14 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
   float* a = at<float>(ws, L.a_s) + bh0 * mm;
   float* z = at<float>(ws, L.z) + bh0 * mm;
   float* w = at<float>(ws, L.w) + bh0 * md;
-  float* scr = at<float>(ws, L.scratch) + bh0 * 3 * mm;
+  float* scr = at<float>(ws, L.scratch) + bh0 * scratch_mats(full) * mm;
   int* status = at<int>(ws, L.status);
   const bool bf16 = full.dtype == NYS_BF16;
   const bool tc_tokens = tokens_tc_smem(full) > 0;
+  const bool big_tokens = !tc_tokens && tokens_big_supported(full);
+  const bool bf16_ops = tc_tokens || big_tokens;  // token step reads K~, W^T as bf16
   __nv_bfloat16* qt_b = bf16 ? at<__nv_bfloat16>(ws, L.qt_bf16) + bh0 * pad : nullptr;
-  __nv_bfloat16* kt_b = (bf16 && tc_tokens) ? at<__nv_bfloat16>(ws, L.kt_bf16) + bh0 * pad : nullptr;
+  __nv_bfloat16* kt_b = (bf16 && bf16_ops) ? at<__nv_bfloat16>(ws, L.kt_bf16) + bh0 * pad : nullptr;
   __nv_bfloat16* wt_b = bf16 ? at<__nv_bfloat16>(ws, L.wt_bf16) + bh0 * pad : nullptr;
 
   int rc = launch_landmarks(sg, qg, kg, qt, kt, qt_b, kt_b, st);
@@ -101,11 +103,14 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
   if (rc != NYS_OK) return rc;
   rc = pinv_tc_supported(full)
            ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, w, wt_b, L.splits, status, st)
-           : launch_pinv_simt(sg, qt, kt, gp, gml, g, a, z, w, scr, tc_tokens ? wt_b : nullptr,
+       : pinv_big_supported(full)
+           ? launch_pinv_big(sg, qt, kt, gp, gml, g, a, z, scr, w, wt_b, L.splits, status, st)
+           : launch_pinv_simt(sg, qt, kt, gp, gml, g, a, z, w, scr, bf16_ops ? wt_b : nullptr,
                               L.splits, st);
   if (rc != NYS_OK) return rc;
-  return tc_tokens ? launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st)
-                   : launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
+  if (tc_tokens) return launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+  if (big_tokens) return launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+  return launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
 }
 
 }  // namespace

@@ -31,7 +31,7 @@ struct Layout {
   size_t a_s;      // f32 [m][m]
   size_t z;        // f32 [m][m]
   size_t w;        // f32 [m][d]          Z G
-  size_t scratch;  // f32 [3][m][m]       pseudo-inverse temporaries
+  size_t scratch;  // f32 [scratch_mats][m][m]  pseudo-inverse temporaries
   size_t qt_bf16;  // bf16 [m64][dpad]    Q~, zero padded (tensor-core operand)
   size_t kt_bf16;  // bf16 [m64][dpad]    K~, zero padded (tensor-core operand)
   size_t wt_bf16;  // bf16 [dpad][m64]    W^T, zero padded (tensor-core operand)
@@ -41,6 +41,10 @@ struct Layout {
 };
 
 Layout make_layout(const Shape& s);
+
+// m x m fp32 temporaries per head in Layout::scratch: 5 for the clustered
+// tensor-core pseudo-inverse (m > 128), else 3.
+int scratch_mats(const Shape& s);
 
 // Brackets one kernel launch: counts it and, while profiling is on, records
 // CUDA events before and after it on `stream`.
@@ -77,6 +81,13 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
                      const void* wt_bf16, const float* conv_w, void* out, int* status,
                      int num_sms, cudaStream_t stream);
 
+// Tensor-core token kernel for d = 128 and large m (nys_tokens_big.cu), used
+// where the pipelined token kernel's operands do not fit.
+bool tokens_big_supported(const Shape& s);
+int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* kt_bf16,
+                      const void* wt_bf16, const float* conv_w, void* out, int* status,
+                      int num_sms, cudaStream_t stream);
+
 // Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs. `s` may be
 // a group of heads of the full problem: splits / tiles_per_split come from
 // the full problem's layout.
@@ -100,6 +111,13 @@ bool pinv_tc_supported(const Shape& s);
 int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,
                    const float* gml, float* g, float* a_s, float* w, void* wt_bf16, int splits,
                    int* status, cudaStream_t stream);
+
+// Clustered tensor-core pseudo-inverse (nys_pinv_big.cu), bf16 path,
+// 128 < m <= 256. `scratch` is the group's block of Layout::scratch.
+bool pinv_big_supported(const Shape& s);
+int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const float* gpart,
+                    const float* gml, float* g, float* a_s, float* z, float* scratch, float* w,
+                    void* wt_bf16, int splits, int* status, cudaStream_t stream);
 
 // Enqueue the whole forward pass (nys_forward.cu). Pointers are device
 // pointers; ws has Layout::total bytes; dev is the current device. Returns

@@ -1,0 +1,595 @@
+// Landmark kernel, iterative pseudo-inverse and W = Z G on the tensor cores
+// for 128 < m <= 256 landmarks ("Nyströmformer" review page, Proposed method,
+// bullets 2, 3 and 5). Same arithmetic as the m <= 128 kernel:
+//   A_S = softmax(Q~ K~^T s)    scores in 3xTF32 (hi*hi + hi*lo + lo*hi)
+//   Z_0 = A_S^T / (||A_S||_1 ||A_S||_inf)
+//   iters x:  X = A_S Z;  Y1 = X (7I - X);  Y2 = X (15I - Y1);
+//             Z <- 1/4 Z (13I - Y2)              tcgen05 kind::tf32
+//   W   = Z G
+// An m x m fp32 matrix (256 KB at m = 256) does not fit one SM, so a
+// cluster of four CTAs works on one head: CTA (r, c) owns rows
+// [128 r, 128 r + 128) and columns [128 c, 128 c + 128) of every product
+// (a 128 x 128 accumulator in TMEM). Operands live in global memory (L2
+// resident: a head's matrices total about 1.5 MB) as row-major copies of the
+// left factors and of the TRANSPOSED right factors; TMA streams 32-column
+// K-chunks of both into a six-stage shared-memory ring. Each epilogue writes
+// the next product's operands (row-major and/or transposed, with the 7I /
+// 15I / 13I terms applied exactly as the m <= 128 kernel does), then the
+// cluster synchronises before the next product reads them.
+//
+// Warps 0-3: epilogue / softmax (thread = row, TMEM lane = row); warp 4:
+// TMA producer; warp 5: TMEM owner and tcgen05 issuer. Every mbarrier wait
+// is bounded; after a timeout the CTA skips its remaining work but still
+// takes part in every cluster barrier, so its peers never wait on it.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "nys_internal.h"
+#include "nys_sm100.h"
+#include "nys_tma_host.h"
+
+namespace nys {
+namespace {
+
+using namespace sm100;
+
+enum MapIdx { MAP_A = 0, MAP_Z0 = 1, MAP_Z1 = 2, MAP_ZT = 3, MAP_TA = 4, MAP_TB = 5, MAP_GT = 6 };
+
+struct BigPinvMaps {
+  CUtensorMap m[7];  // fp32 [B*H][rows][m]: A_S, Z (two), Z^T, two transposed temporaries, G^T
+};
+
+struct BigPinvParams {
+  const float* qt;     // [B*H][m][d] fp32
+  const float* kt;     // [B*H][m][d] fp32
+  const float* gpart;  // [B*H][splits][m][d]
+  const float* gml;    // [B*H][splits][m][2]
+  float* g;            // [B*H][m][d]
+  float* a_s;          // [B*H][m][m]
+  float* z0;           // [B*H][m][m]  Z (even steps)
+  float* z1;           // [B*H][m][m]  Z (odd steps) / X
+  float* zt;           // [B*H][m][m]  Z^T
+  float* ta;           // [B*H][m][m]  transposed right factors
+  float* tb;           // [B*H][m][m]
+  float* gt;           // [B*H][d][m]  G^T
+  float* w;            // [B*H][m][d]
+  __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
+  int* status;
+  int m, d, dpad, m64, splits, iters, kc;  // kc: 32-column K-chunks of an m x m matrix
+  float scale;
+};
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kThreads = 192;
+constexpr int kStages = 6;
+constexpr uint32_t kStageBytes = 32768;  // A chunk 16 KB + B chunk <= 16 KB
+constexpr uint32_t kTmemCols = 128;
+constexpr int kCsPitch = 129;  // floats per row of the column-sum staging block
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// generic-proxy global writes <-> async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// read a float of CTA `rank`'s copy of the shared variable at `p`
+__device__ __forceinline__ float ld_peer(const float* p, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
+    pinv_big(const __grid_constant__ BigPinvMaps maps, const BigPinvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  __shared__ uint64_t full[kStages], empty[kStages], done, fin;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ float rmax_sh[128], rsum_sh[128], rs_sh[128], cs_sh[128], red[8];
+  volatile int* abort_flag = &abort_sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const int r = (int)(rank >> 1), c = (int)(rank & 1);
+  const int bh = blockIdx.x >> 2;
+  const int m = p.m, d = p.d;
+  const int gi = 128 * r + tid;  // this worker's row (warps 0-3)
+  const bool worker = warp < 4;
+  const bool rv = worker && gi < m;
+  const size_t mm = (size_t)m * m;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    mbar_init(&fin, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) tmem_alloc(&tmem_base_sh, kTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  cluster_sync_all();  // every CTA of the cluster is running before any DSMEM access
+
+  uint32_t ph_done = 0;
+  auto wait_done = [&]() -> bool {
+    bool ok = mbar_wait(&done, ph_done, abort_flag, kWaitNs);
+    if (!ok && !*abort_flag) {
+      *abort_flag = 1;
+      atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
+    }
+    ph_done ^= 1;
+    tc_fence_after_sync();
+    return ok;
+  };
+
+  // ---- 1) G = merge of the key-split partials: rows of this row block,
+  // columns [c d/2, (c+1) d/2). G -> g (row-major), G^T -> gt.
+  if (rv) {
+    const int hw = d >> 1, c0 = c * hw;
+    float gm = -INFINITY;
+    for (int sp = 0; sp < p.splits; ++sp)
+      gm = fmaxf(gm, p.gml[(((size_t)bh * p.splits + sp) * m + gi) * 2]);
+    float den = 0.f;
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
+      den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
+    }
+    const float inv = 1.f / den;
+    float* grow = p.g + ((size_t)bh * m + gi) * d;
+    float* gtb = p.gt + (size_t)bh * d * m;
+    for (int j0 = c0; j0 < c0 + hw; j0 += 16) {
+      float acc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
+        const float f = expf(p.gml[prow * 2] - gm);
+        const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + j0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 v = src[e];
+          acc[4 * e] += v.x * f;
+          acc[4 * e + 1] += v.y * f;
+          acc[4 * e + 2] += v.z * f;
+          acc[4 * e + 3] += v.w * f;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] *= inv;
+      float4* go = reinterpret_cast<float4*>(grow + j0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) gtb[(size_t)(j0 + e) * m + gi] = acc[e];
+    }
+  }
+
+  // ---- 2) scores S = Q~ K~^T (rows of block r, columns of block c) in
+  // 3xTF32. Per pass, up to two 32-column chunks of d; chunk slot layout:
+  // Q hi | Q lo | K hi | K lo, 16 KB each.
+  {
+    const int gk = 128 * c + tid;  // K~ row = score column handled by this thread
+    const bool qv_ok = rv, kv_ok = worker && gk < m;
+    const float* qrow = p.qt + ((size_t)bh * m + (qv_ok ? gi : 0)) * d;
+    const float* krow = p.kt + ((size_t)bh * m + (kv_ok ? gk : 0)) * d;
+    const int nchunk = d >> 5;
+    for (int pass = 0; pass * 2 < nchunk; ++pass) {
+      const int ch0 = pass * 2, nch = min(2, nchunk - ch0);
+      if (worker) {
+        for (int cc = 0; cc < nch; ++cc) {
+          uint8_t* slot = sm + cc * 65536;
+          const int col0 = (ch0 + cc) * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 q4 = qv_ok ? *reinterpret_cast<const float4*>(qrow + col0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 k4 = kv_ok ? *reinterpret_cast<const float4*>(krow + col0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 qh = make_float4(tf32_hi(q4.x), tf32_hi(q4.y), tf32_hi(q4.z), tf32_hi(q4.w));
+            const float4 kh = make_float4(tf32_hi(k4.x), tf32_hi(k4.y), tf32_hi(k4.z), tf32_hi(k4.w));
+            const uint32_t off = sw128_offset(tid, e * 4);
+            *reinterpret_cast<float4*>(slot + off) = qh;
+            *reinterpret_cast<float4*>(slot + 16384 + off) =
+                make_float4(q4.x - qh.x, q4.y - qh.y, q4.z - qh.z, q4.w - qh.w);
+            *reinterpret_cast<float4*>(slot + 32768 + off) = kh;
+            *reinterpret_cast<float4*>(slot + 49152 + off) =
+                make_float4(k4.x - kh.x, k4.y - kh.y, k4.z - kh.z, k4.w - kh.w);
+          }
+        }
+        fence_async_smem();
+      }
+      tc_fence_before_sync();
+      __syncthreads();
+      if (warp == 5 && lane == 0 && !*abort_flag) {
+        tc_fence_after_sync();
+        const uint32_t id = idesc_tf32(128, 128);
+        for (int cc = 0; cc < nch; ++cc) {
+          const uint64_t qh = smem_desc(smem_u32(sm + cc * 65536), 16, 1024, SW_128B);
+          const uint64_t ql = qh + (16384 >> 4), kh = qh + (32768 >> 4), kl = qh + (49152 >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t first = (pass == 0 && cc == 0 && kk == 0) ? 0u : 1u;
+            mma_tf32(tmem, qh + kk * 2, kh + kk * 2, id, first);
+            mma_tf32(tmem, qh + kk * 2, kl + kk * 2, id, 1u);
+            mma_tf32(tmem, ql + kk * 2, kh + kk * 2, id, 1u);
+          }
+        }
+        mma_commit(&done);
+      }
+      if (worker) wait_done();
+      tc_fence_before_sync();
+      __syncthreads();
+    }
+  }
+
+  // ---- 3) softmax across the column pair (c = 0, 1) of this row block
+  float a_row_sum = 0.f;  // this CTA's part of the row sum of A_S
+  if (worker) {
+    float mx = -INFINITY;
+    if (!*abort_flag)
+      for (int j0 = 0; j0 < 128; j0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lo + j0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (128 * c + j0 + e < m) mx = fmaxf(mx, __uint_as_float(v[e]));
+      }
+    rmax_sh[tid] = mx;
+  }
+  cluster_sync_all();
+  float part = 0.f;
+  if (worker && !*abort_flag) {
+    const float rmax = fmaxf(rmax_sh[tid], ld_peer(&rmax_sh[tid], rank ^ 1u));
+    for (int j0 = 0; j0 < 128; j0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lo + j0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float x = (rv && 128 * c + j0 + e < m) ? expf((__uint_as_float(v[e]) - rmax) * p.scale) : 0.f;
+        part += x;
+        v[e] = __float_as_uint(x);
+      }
+      tmem_st32(tmem + lo + j0, v);
+    }
+    tmem_st_wait();
+  }
+  if (worker) rsum_sh[tid] = part;
+  cluster_sync_all();
+  float* cs_stage = reinterpret_cast<float*>(sm);  // [128][kCsPitch]
+  if (worker && !*abort_flag) {
+    const float own = rsum_sh[tid], peer = ld_peer(&rsum_sh[tid], rank ^ 1u);
+    const float sum = c == 0 ? own + peer : peer + own;  // same order in both CTAs
+    const float inv = rv ? 1.f / sum : 0.f;
+    float* arow = p.a_s + bh * mm + (size_t)(rv ? gi : 0) * m;
+    for (int j0 = 0; j0 < 128; j0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lo + j0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float x = __uint_as_float(v[e]) * inv;
+        v[e] = __float_as_uint(x);
+        a_row_sum += fabsf(x);
+        cs_stage[tid * kCsPitch + j0 + e] = x;
+      }
+      tmem_st32(tmem + lo + j0, v);
+      if (rv) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int gj = 128 * c + j0 + e;
+          if (gj < m)
+            *reinterpret_cast<float4*>(arow + gj) =
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
+      }
+    }
+    tmem_st_wait();
+  }
+  __syncthreads();
+  if (worker) {
+    // this CTA's part of column tid's abs-sum (four independent partials)
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!*abort_flag)
+      for (int i = 0; i < 128; i += 4) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) s4[t] += fabsf(cs_stage[(i + t) * kCsPitch + tid]);
+      }
+    cs_sh[tid] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    rs_sh[tid] = a_row_sum;
+  }
+  cluster_sync_all();
+  // ||A_S||_1 and ||A_S||_inf from the four CTAs' partials, combined in a
+  // fixed order so that every CTA of the cluster gets the same alpha
+  if (worker) {
+    float cmax = 0.f, rmaxs = 0.f;
+    for (int b = 0; b < 2; ++b) {
+      const float col = ld_peer(&cs_sh[tid], (uint32_t)b) + ld_peer(&cs_sh[tid], (uint32_t)(2 + b));
+      if (128 * b + tid < m) cmax = fmaxf(cmax, col);
+      const float row = ld_peer(&rs_sh[tid], (uint32_t)(2 * b)) + ld_peer(&rs_sh[tid], (uint32_t)(2 * b + 1));
+      if (128 * b + tid < m) rmaxs = fmaxf(rmaxs, row);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      rmaxs = fmaxf(rmaxs, __shfl_xor_sync(0xffffffffu, rmaxs, o));
+    }
+    if (lane == 0) {
+      red[warp] = cmax;
+      red[4 + warp] = rmaxs;
+    }
+  }
+  __syncthreads();
+  // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block)
+  // and Z_0^T = alpha A_S (row store)
+  if (worker && !*abort_flag) {
+    const float n1 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    const float ninf = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
+    const float alpha = 1.f / (n1 * ninf);
+    float* z0 = p.z0 + bh * mm;
+    float* zt = p.zt + bh * mm;
+    for (int j0 = 0; j0 < 128; j0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lo + j0, v);
+      tmem_ld_wait();
+      if (rv) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const int gj = 128 * c + j0 + e;
+          if (gj < m)
+            *reinterpret_cast<float4*>(zt + (size_t)gi * m + gj) =
+                make_float4(alpha * __uint_as_float(v[e]), alpha * __uint_as_float(v[e + 1]),
+                            alpha * __uint_as_float(v[e + 2]), alpha * __uint_as_float(v[e + 3]));
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int gj = 128 * c + j0 + e;
+          if (gj < m) z0[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  fence_proxy_async_all();
+  cluster_sync_all();
+  fence_proxy_async_all();
+  tc_fence_after_sync();
+
+  // ---- 4) the products: 4 per step, then W = Z G
+  const int nprod = 4 * p.iters + 1;
+  const int hw = d >> 1;
+  uint32_t kg_prod = 0, kg_mma = 0;   // ring positions of the producer / issuer
+  uint32_t n_full[kStages] = {};      // loads issued per stage (producer)
+  for (int pi = 0; pi < nprod; ++pi) {
+    const int it = pi >> 2, st = pi & 3;
+    const bool is_w = pi == nprod - 1;
+    const int zc = it & 1;  // Z of this step in z0 (even) / z1 (odd); X and Z' in the other
+    int amap, bmap, b_row0, n_cols;
+    if (is_w) {
+      amap = (p.iters & 1) ? MAP_Z1 : MAP_Z0;
+      bmap = MAP_GT;
+      b_row0 = c * hw;
+      n_cols = hw;
+    } else {
+      amap = st == 0 ? MAP_A : (st == 3 ? (zc ? MAP_Z1 : MAP_Z0) : (zc ? MAP_Z0 : MAP_Z1));
+      bmap = st == 0 ? MAP_ZT : (st == 2 ? MAP_TB : MAP_TA);
+      b_row0 = 128 * c;
+      n_cols = 128;
+    }
+    const uint32_t b_bytes = (uint32_t)n_cols * 128u;
+    if (warp == 4) {
+      if (lane == 0 && !*abort_flag) {
+        for (int k = 0; k < p.kc; ++k, ++kg_prod) {
+          const int s = (int)(kg_prod % kStages);
+          if (kg_prod >= (uint32_t)kStages &&
+              !mbar_wait(&empty[s], ((kg_prod / kStages) - 1) & 1, abort_flag, kWaitNs)) {
+            if (!*abort_flag) {
+              *abort_flag = 1;
+              atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
+            }
+            break;
+          }
+          uint8_t* sa = sm + s * kStageBytes;
+          mbar_arrive_expect_tx(&full[s], 16384u + b_bytes);
+          tma_load_3d(sa, &maps.m[amap], &full[s], 32 * k, 128 * r, bh);
+          tma_load_3d(sa + 16384, &maps.m[bmap], &full[s], 32 * k, b_row0, bh);
+          ++n_full[s];
+        }
+      }
+      __syncwarp();
+    } else if (warp == 5) {
+      if (lane == 0 && !*abort_flag) {
+        const uint32_t id = idesc_tf32(128, n_cols);
+        bool ok = true;
+        for (int k = 0; k < p.kc; ++k, ++kg_mma) {
+          const int s = (int)(kg_mma % kStages);
+          if (!mbar_wait(&full[s], (kg_mma / kStages) & 1, abort_flag, kWaitNs)) {
+            if (!*abort_flag) {
+              *abort_flag = 1;
+              atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
+            }
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a0 = smem_desc(smem_u32(sm + s * kStageBytes), 16, 1024, SW_128B);
+          const uint64_t b0 = smem_desc(smem_u32(sm + s * kStageBytes + 16384), 16, 1024, SW_128B);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_tf32(tmem, a0 + kk * 2, b0 + kk * 2, id, (k > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&done);
+      }
+      __syncwarp();
+    } else if (wait_done()) {
+      // epilogue: thread = row gi of the product block
+      if (is_w) {
+        float* wrow = p.w + ((size_t)bh * m + (rv ? gi : 0)) * d + c * hw;
+        __nv_bfloat16* wt = p.wt + (size_t)bh * p.dpad * p.m64;
+        for (int j0 = 0; j0 < hw; j0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lo + j0, v);
+          tmem_ld_wait();
+          if (rv) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(wrow + j0 + e) =
+                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                              __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          }
+          if (gi < p.m64) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              wt[(size_t)(c * hw + j0 + e) * p.m64 + gi] = __float2bfloat16_rn(rv ? __uint_as_float(v[e]) : 0.f);
+          }
+        }
+        if (c == 1 && gi < p.m64)
+          for (int j = d; j < p.dpad; ++j) wt[(size_t)j * p.m64 + gi] = __float2bfloat16_rn(0.f);
+      } else {
+        // st 0: X -> other Z buffer (row-major), 7I - X -> ta (transposed)
+        // st 1: 15I - Y -> tb (transposed);  st 2: 13I - Y -> ta (transposed)
+        // st 3: Z' = Y / 4 -> other Z buffer (row-major) and zt (transposed)
+        float* zother = (zc ? p.z0 : p.z1) + bh * mm;
+        float* rm_dst = (st == 0 || st == 3) ? zother : nullptr;
+        float* tr_dst = (st == 0 || st == 2) ? p.ta + bh * mm : (st == 1 ? p.tb + bh * mm : p.zt + bh * mm);
+        const float diag = st == 0 ? 7.f : (st == 1 ? 15.f : (st == 2 ? 13.f : 0.f));
+        const float sign = st == 3 ? 1.f : -1.f;
+        const float sc = st == 3 ? 0.25f : 1.f;
+        for (int j0 = 0; j0 < 128; j0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lo + j0, v);
+          tmem_ld_wait();
+          if (rv) {
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = sc * __uint_as_float(v[e]);
+            if (rm_dst) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                const int gj = 128 * c + j0 + e;
+                if (gj < m)
+                  *reinterpret_cast<float4*>(rm_dst + (size_t)gi * m + gj) =
+                      make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int gj = 128 * c + j0 + e;
+              if (gj < m) tr_dst[(size_t)gj * m + gi] = fmaf(sign, x[e], gj == gi ? diag : 0.f);
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before_sync();
+    fence_proxy_async_all();
+    cluster_sync_all();
+    fence_proxy_async_all();
+    tc_fence_after_sync();
+  }
+
+  // ---- teardown: no copy or MMA of this CTA may still be in flight
+  if (warp == 4 && lane == 0 && *abort_flag) {
+    for (int s = 0; s < kStages; ++s)
+      if (n_full[s]) mbar_wait(&full[s], (n_full[s] - 1) & 1, nullptr, kWaitNs);
+  }
+  if (warp == 5 && lane == 0) {
+    mma_commit(&fin);
+    mbar_wait(&fin, 0, nullptr, kWaitNs);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  cluster_sync_all();  // peers may still read this CTA's shared memory until here
+}
+
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
+
+}  // namespace
+
+bool pinv_big_supported(const Shape& s) {
+  return s.dtype == NYS_BF16 && s.m > 128 && s.m <= 256 && s.m % 4 == 0 && s.d % 32 == 0 &&
+         s.d <= 128;
+}
+
+int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const float* gpart,
+                    const float* gml, float* g, float* a_s, float* z, float* scratch, float* w,
+                    void* wt_bf16, int splits, int* status, cudaStream_t stream) {
+  if (!pinv_big_supported(s)) return NYS_ERR_UNSUPPORTED;
+  const size_t BH = (size_t)s.bh(), mm = (size_t)s.m * s.m;
+  BigPinvParams p{};
+  p.qt = qt;
+  p.kt = kt;
+  p.gpart = gpart;
+  p.gml = gml;
+  p.g = g;
+  p.a_s = a_s;
+  p.z0 = z;
+  // scratch holds, per head block of the whole batch: z1, zt, ta, tb, gt
+  p.z1 = scratch;
+  p.zt = scratch + BH * mm;
+  p.ta = scratch + 2 * BH * mm;
+  p.tb = scratch + 3 * BH * mm;
+  p.gt = scratch + 4 * BH * mm;
+  p.w = w;
+  p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
+  p.status = status;
+  p.m = s.m;
+  p.d = s.d;
+  p.dpad = s.dpad();
+  p.m64 = s.m64();
+  p.splits = splits;
+  p.iters = s.iters;
+  p.kc = (s.m + 31) / 32;
+  p.scale = 1.0f / sqrtf((float)s.d);
+
+  BigPinvMaps maps;
+  const float* bufs[6] = {p.a_s, p.z0, p.z1, p.zt, p.ta, p.tb};
+  for (int i = 0; i < 6; ++i) {
+    const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
+    const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)mm * 4};
+    const uint32_t box[3] = {32, 128, 1};
+    if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return NYS_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.d, BH};
+    const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)s.d * s.m * 4};
+    const uint32_t box[3] = {32, (uint32_t)(s.d / 2), 1};
+    if (!make_tensor_map(&maps.m[MAP_GT], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.gt, dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return NYS_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(pinv_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return NYS_ERR_CUDA;
+  KernelScope scope("pinv_big", stream);
+  pinv_big<<<(unsigned)(4 * BH), kThreads, kSmemBytes, stream>>>(maps, p);
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
+
+}  // namespace nys

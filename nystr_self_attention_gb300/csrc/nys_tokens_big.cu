@@ -1,0 +1,350 @@
+// Token rows on the tensor cores for large landmark counts and head widths
+// (m up to 256, d = 128), whose operands do not fit the pipelined token
+// kernel's shared memory. Same computation:
+//   out[t] = softmax(Q[t] K~^T / sqrt(d)) W + sum_j w[h][j] V[t + j - (ks-1)/2]
+// ("Nyströmformer" review page, Proposed method, bullets 3 and 6).
+//
+// Shared memory holds K~ (m x d), W^T (d x m) and the conv's Toeplitz block
+// per head, plus ONE buffer shared by the Q tile and the V halo: V is loaded
+// into it once the F product has consumed Q, while the softmax runs. TMEM:
+// F/P (m columns), PW and CV accumulators (d columns each). One CTA of 128
+// threads walks a contiguous range of 128-token tiles; thread 0 issues TMA
+// and tcgen05, all threads run the softmax and the epilogue. Every wait is
+// bounded; a wait that runs out sets the status word and the CTA winds down.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "nys_internal.h"
+#include "nys_sm100.h"
+#include "nys_tma_host.h"
+
+namespace nys {
+namespace {
+
+using namespace sm100;
+
+struct BigMaps {
+  CUtensorMap q, v, kt, wt;
+};
+
+struct BigParams {
+  const float* conv_w;
+  __nv_bfloat16* out;
+  int* status;
+  int H, n, d, m, m_pad, ks, kc;
+  int tiles_per_head, total_tiles, tiles_per_cta;
+  float c;  // softmax scale * log2(e)
+  uint32_t off_kt, off_wt, off_t, off_qv;
+  uint32_t kt_bytes, wt_bytes, q_bytes, v_bytes;
+};
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int DP = 128, DC = 2;  // head width 128: two 64-column chunks
+constexpr size_t kSmemBudget = 227 * 1024 - 1024;
+
+__device__ __forceinline__ bool ok_or_fail(bool ok, int* status, volatile int* abort_flag) {
+  if (!ok && !*abort_flag) {
+    *abort_flag = 1;
+    atomicExch(status, (int)NYS_ERR_TIMEOUT);
+  }
+  return ok;
+}
+
+__global__ void __launch_bounds__(128, 1) tokens_big(const __grid_constant__ BigMaps maps,
+                                                     const BigParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* kts = sm + p.off_kt;
+  uint8_t* wts = sm + p.off_wt;
+  uint8_t* tbs = sm + p.off_t;
+  uint8_t* qv = sm + p.off_qv;
+  __shared__ uint64_t bar_kw, bar_q, bar_v, bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  volatile int* abort_flag = &abort_sh;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+  const int rad = p.ks > 0 ? (p.ks - 1) / 2 : 0;
+  const int g0 = blockIdx.x * p.tiles_per_cta;
+  const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
+
+  if (tid == 0) {
+    mbar_init(&bar_kw, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_mma, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_sh, 512);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t COL_F = 0, COL_PW = 256, COL_CV = 384;
+
+  uint32_t ph_kw = 0, ph_q = 0, ph_v = 0, ph_mma = 0;
+  bool kw_out = false, q_out = false, v_out = false;  // loads issued, not yet waited on
+  int cur_bh = -1, cur_h = -1;
+  for (int g = g0; g < g1; ++g) {
+    const int bh = g / p.tiles_per_head, t0 = (g % p.tiles_per_head) * 128, h = bh % p.H;
+    // (A) head change: K~, W^T by TMA; Toeplitz block by all threads
+    if (bh != cur_bh) {
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&bar_kw, p.kt_bytes + p.wt_bytes);
+        for (int dc = 0; dc < DC; ++dc)
+          tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bar_kw, dc * 64, 0, bh);
+        for (int mc = 0; mc * 64 < p.m_pad; ++mc)
+          tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bar_kw, mc * 64, 0, bh);
+        kw_out = true;
+      }
+      if (p.kc > 0 && h != cur_h) {
+        const float* wh = p.conv_w + (size_t)h * p.ks;
+        const int kc64 = (p.kc + 63) & ~63;
+        for (int u0 = 0; u0 < kc64; u0 += 8) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int ua = u0 + 2 * e - tid, ub = ua + 1;
+            const float fa = (ua >= 0 && ua < p.ks && u0 + 2 * e < p.kc) ? __ldg(wh + ua) : 0.f;
+            const float fb = (ub >= 0 && ub < p.ks && u0 + 2 * e + 1 < p.kc) ? __ldg(wh + ub) : 0.f;
+            wv[e] = pack_bf16x2(fa, fb);
+          }
+          *reinterpret_cast<uint4*>(tbs + (u0 >> 6) * 16384 + sw128_offset(tid, (u0 & 63) * 2)) =
+              make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        fence_async_smem();
+        cur_h = h;
+      }
+      if (tid == 0 && ok_or_fail(mbar_wait(&bar_kw, ph_kw, abort_flag, kWaitNs), p.status, abort_flag))
+        kw_out = false;
+      ph_kw ^= 1;
+      cur_bh = bh;
+      __syncthreads();
+      if (*abort_flag) break;
+    }
+    // (B) Q tile -> F = Q K~^T
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_q, p.q_bytes);
+      for (int dc = 0; dc < DC; ++dc) tma_load_3d(qv + dc * 16384, &maps.q, &bar_q, dc * 64, t0, bh);
+      q_out = true;
+      if (ok_or_fail(mbar_wait(&bar_q, ph_q, abort_flag, kWaitNs), p.status, abort_flag)) {
+        q_out = false;
+        tc_fence_after_sync();
+        const uint64_t a0 = smem_desc(smem_u32(qv), 16, 1024, SW_128B);
+        const uint64_t b0 = smem_desc(smem_u32(kts), 16, 1024, SW_128B);
+        const uint32_t id = idesc_bf16(128, p.m_pad, false, false);
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk)
+          mma_bf16(tmem + COL_F, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                   b0 + (uint64_t)((kk >> 2) * (p.m_pad * 8) + (kk & 3) * 2), id, kk > 0);
+        mma_commit(&bar_mma);
+      }
+    }
+    ph_q ^= 1;
+    ok_or_fail(mbar_wait(&bar_mma, ph_mma, abort_flag, kWaitNs), p.status, abort_flag);
+    ph_mma ^= 1;
+    __syncthreads();
+    if (*abort_flag) break;
+    tc_fence_after_sync();
+    // (C) V halo into the freed buffer while the softmax runs
+    if (tid == 0 && p.kc > 0) {
+      mbar_arrive_expect_tx(&bar_v, p.v_bytes);
+      for (int dc = 0; dc < DC; ++dc)
+        tma_load_3d(qv + dc * (p.kc * 128), &maps.v, &bar_v, dc * 64, t0 - rad, bh);
+      v_out = true;
+    }
+    float mx = -INFINITY;
+    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lo + COL_F + c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
+    }
+    const float mc = mx * p.c;
+    float l = 0.f;
+    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lo + COL_F + c0, r);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
+        const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
+        l += a + b;
+        pk[e] = pack_bf16x2(a, b);
+      }
+      tmem_st16(tmem + lo + COL_F + (c0 >> 1), pk);
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+    // (D) PW = P W ; CV = T V_halo
+    if (tid == 0) {
+      tc_fence_after_sync();
+      const uint64_t w0 = smem_desc(smem_u32(wts), 16, 1024, SW_128B);
+      const uint32_t idw = idesc_bf16(128, DP, false, false);
+      for (int kk = 0; kk < p.m_pad / 16; ++kk)
+        mma_bf16_tA(tmem + COL_PW, tmem + COL_F + kk * 8,
+                    w0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
+      if (p.kc > 0) {
+        if (ok_or_fail(mbar_wait(&bar_v, ph_v, abort_flag, kWaitNs), p.status, abort_flag)) {
+          v_out = false;
+          tc_fence_after_sync();
+          const uint64_t a0 = smem_desc(smem_u32(tbs), 16, 1024, SW_128B);
+          const uint64_t v0 = smem_desc(smem_u32(qv), p.kc * 128, 1024, SW_128B);
+          const uint32_t idc = idesc_bf16(128, DP, false, true);
+          for (int kk = 0; kk < p.kc / 16; ++kk)
+            mma_bf16(tmem + COL_CV, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                     v0 + (uint64_t)(kk * 128), idc, kk > 0);
+        }
+      }
+      mma_commit(&bar_mma);
+    }
+    if (p.kc > 0) ph_v ^= 1;
+    ok_or_fail(mbar_wait(&bar_mma, ph_mma, abort_flag, kWaitNs), p.status, abort_flag);
+    ph_mma ^= 1;
+    __syncthreads();
+    if (*abort_flag) break;
+    tc_fence_after_sync();
+    // (E) out = PW / l + CV
+    const int t = t0 + tid;
+    const float inv_l = 1.f / l;
+    __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + t) * p.d;
+#pragma unroll
+    for (int c0 = 0; c0 < DP; c0 += 32) {
+      uint32_t a[32], b[32];
+      tmem_ld32(tmem + lo + COL_PW + c0, a);
+      if (p.kc > 0) tmem_ld32(tmem + lo + COL_CV + c0, b);
+      tmem_ld_wait();
+      if (t < p.n && c0 < p.d) {
+        uint32_t o[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
+          if (p.kc > 0) {
+            x0 += __uint_as_float(b[2 * e]);
+            x1 += __uint_as_float(b[2 * e + 1]);
+          }
+          o[e] = pack_bf16x2(x0, x1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+      }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+  }
+  if (tid == 0 && *abort_flag) {
+    // wait (bounded) for copies still in flight
+    if (kw_out) mbar_wait(&bar_kw, ph_kw ^ 1, nullptr, kWaitNs);
+    if (q_out) mbar_wait(&bar_q, ph_q ^ 1, nullptr, kWaitNs);
+    if (v_out) mbar_wait(&bar_v, ph_v ^ 1, nullptr, kWaitNs);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+struct BigPlan {
+  int m_pad, kc;
+  uint32_t kt_bytes, wt_bytes, t_bytes, q_bytes, v_bytes, qv_bytes;
+  size_t smem;
+};
+
+bool plan_big(const Shape& s, BigPlan* pl) {
+  if (s.dtype != NYS_BF16 || s.d != 128) return false;
+  pl->m_pad = ((s.m + 31) / 32) * 32;
+  pl->kc = s.ks > 0 ? ((128 + s.ks - 1 + 15) / 16) * 16 : 0;
+  if (pl->m_pad > 256 || pl->kc > 256) return false;
+  pl->kt_bytes = (uint32_t)pl->m_pad * DP * 2;
+  pl->wt_bytes = (uint32_t)((pl->m_pad + 63) / 64) * DP * 128;
+  pl->t_bytes = pl->kc > 0 ? (uint32_t)((pl->kc + 63) / 64) * 16384 : 0;
+  pl->q_bytes = 128 * DP * 2;
+  pl->v_bytes = (uint32_t)pl->kc * DP * 2;
+  pl->qv_bytes = std::max(pl->q_bytes, pl->v_bytes);
+  pl->smem = (size_t)pl->kt_bytes + pl->wt_bytes + pl->t_bytes + pl->qv_bytes + 1024;
+  return pl->smem <= kSmemBudget;
+}
+
+}  // namespace
+
+bool tokens_big_supported(const Shape& s) {
+  BigPlan pl;
+  return plan_big(s, &pl);
+}
+
+int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* kt_bf16,
+                      const void* wt_bf16, const float* conv_w, void* out, int* status,
+                      int num_sms, cudaStream_t stream) {
+  BigPlan pl;
+  if (!plan_big(s, &pl)) return NYS_ERR_UNSUPPORTED;
+  const uint64_t BH = (uint64_t)s.bh();
+  const int m64 = s.m64();
+  BigMaps maps;
+  {
+    const uint64_t dims[3] = {(uint64_t)s.d, (uint64_t)s.n, BH};
+    const uint64_t strides[2] = {(uint64_t)s.d * 2, (uint64_t)s.n * s.d * 2};
+    const uint32_t boxq[3] = {64, 128, 1};
+    const uint32_t boxv[3] = {64, (uint32_t)(pl.kc > 0 ? pl.kc : 16), 1};
+    if (!make_tensor_map(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, boxq,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, boxv,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+      return NYS_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)DP, (uint64_t)m64, BH};
+    const uint64_t strides[2] = {(uint64_t)DP * 2, (uint64_t)m64 * DP * 2};
+    const uint32_t box[3] = {64, (uint32_t)pl.m_pad, 1};
+    if (!make_tensor_map(&maps.kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kt_bf16, dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return NYS_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)m64, (uint64_t)DP, BH};
+    const uint64_t strides[2] = {(uint64_t)m64 * 2, (uint64_t)m64 * DP * 2};
+    const uint32_t box[3] = {64, (uint32_t)DP, 1};
+    if (!make_tensor_map(&maps.wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, wt_bf16, dims, strides,
+                         box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return NYS_ERR_CUDA;
+  }
+  BigParams p{};
+  p.conv_w = conv_w;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.status = status;
+  p.H = s.H;
+  p.n = s.n;
+  p.d = s.d;
+  p.m = s.m;
+  p.m_pad = pl.m_pad;
+  p.ks = s.ks;
+  p.kc = pl.kc;
+  p.tiles_per_head = (s.n + 127) / 128;
+  p.total_tiles = (int)(BH * p.tiles_per_head);
+  const int ctas = std::min(p.total_tiles, num_sms);
+  p.tiles_per_cta = (p.total_tiles + ctas - 1) / ctas;
+  const int grid = (p.total_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta;
+  p.c = (1.0f / sqrtf((float)s.d)) * 1.4426950408889634f;
+  p.kt_bytes = pl.kt_bytes;
+  p.wt_bytes = pl.wt_bytes;
+  p.q_bytes = pl.q_bytes;
+  p.v_bytes = pl.v_bytes;
+  p.off_kt = 0;
+  p.off_wt = pl.kt_bytes;
+  p.off_t = p.off_wt + pl.wt_bytes;
+  p.off_qv = p.off_t + pl.t_bytes;
+  if (cudaFuncSetAttribute(tokens_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
+      cudaSuccess)
+    return NYS_ERR_CUDA;
+  KernelScope scope("tokens_big", stream);
+  tokens_big<<<grid, 128, pl.smem, stream>>>(maps, p);
+  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+}
+
+}  // namespace nys

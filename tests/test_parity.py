@@ -71,6 +71,10 @@ SMALL = [
     (1, 1, 8, 32, 2, 0, 1),        # no pinv update, 1-tap conv
     (1, 1, 1, 32, 1, 6, 3),        # a single token
     (1, 1, 384, 64, 128, 6, 127),  # widest conv
+    (1, 2, 960, 128, 192, 6, 33),  # d = 128 with m > 128, ragged last tile
+    (2, 1, 640, 128, 160, 6, 0),   # d = 128, m = 160, no conv
+    (2, 10, 1152, 128, 192, 6, 33),  # several heads per CTA range
+    (20, 1, 1152, 128, 192, 4, 9),   # consecutive heads sharing conv taps
 ]
 
 
