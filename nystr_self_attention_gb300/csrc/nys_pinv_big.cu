@@ -154,6 +154,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     float den = 0.f;
     for (int sp = 0; sp < p.splits; ++sp) {
       const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
+      if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial
       den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
     }
     const float inv = 1.f / den;
@@ -165,6 +166,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
       for (int sp = 0; sp < p.splits; ++sp) {
         const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
+        if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
         const float f = expf(p.gml[prow * 2] - gm);
         const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + j0);
 #pragma unroll

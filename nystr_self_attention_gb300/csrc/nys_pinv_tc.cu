@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
     if (live)
       for (int sp = 0; sp < p.splits; ++sp) {
         const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
+        if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial
         den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
       }
     const float inv = live ? 1.f / den : 0.f;
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
       if (live) {
         for (int sp = 0; sp < p.splits; ++sp) {
           const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
+          if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
           const float f = expf(p.gml[prow * 2] - gm);
           const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + c0);
 #pragma unroll

@@ -386,6 +386,7 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
     float num = 0.f, den = 0.f;
     for (int s = 0; s < splits; ++s) {
       const size_t row = ((size_t)bh * splits + s) * m + i;
+      if (gml[row * 2] == -INFINITY) continue;  // empty partial: O never written
       const float f = expf(gml[row * 2] - mx);
       num += gpart[row * d + (e % d)] * f;
       den += gml[row * 2 + 1] * f;
