@@ -1,7 +1,6 @@
 // Landmark kernel, iterative pseudo-inverse and W = Z G on the tensor cores
 // ("Nyströmformer" review page, Proposed method, bullets 2, 3 and 5), for
-// m <= 128 landmarks, one CTA of 256 threads per head (row i of every
-// m x m matrix in TMEM lane i):
+// m <= 128 landmarks:
 //   G   = merge of the key-split partials of softmax(Q~ K^T s) V
 //   A_S = softmax(Q~ K~^T s)   scores as three tf32 products of the hi/lo
 //                              split of Q~ and K~ (hi*hi + hi*lo + lo*hi,
@@ -13,9 +12,18 @@
 //   W   = Z G                                      tcgen05 kind::tf32
 // The products run on tf32 operands with fp32 accumulation and fp32
 // storage; the update is the paper's own (Z recomputed through A_S Z every
-// step), not a reformulation. A_S, Z and X stay in TMEM as A operands
-// (row i in lane i); each product's B operand is written, transposed, into
-// one shared-memory buffer by the epilogue of the product before it.
+// step), not a reformulation.
+//
+// m is padded to MP = 32, 64 or 128 (the zero padding is exact: the padded
+// block of every iterate stays zero) and hp = 128 / MP heads (fewer if d
+// is large) share one CTA of 256 threads, stacked along the 128 TMEM lanes:
+// row i of head slot h is lane h MP + i. One M = 128 MMA then serves all hp
+// heads: the B operand stacks the heads' right factors along N, and each
+// head reads only its own diagonal block of the 128 x (hp MP) result (the
+// off-diagonal blocks mix heads and are never read). A_S is the A operand
+// of X = A_S Z from shared memory; X and Z are A operands in TMEM; each
+// product's B operand is written, transposed, into one shared-memory
+// buffer by the epilogue of the product before it.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -38,11 +46,12 @@ struct PinvParams {
   float* w;            // [B*H][m][d]  stage export
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
   int* status;
-  int m, d, m_pad, dpad, m64, splits, iters;
-  float scale;
+  int BH, m, d, dpad, m64, splits, iters;
+  int hp;         // heads per CTA
+  float scale;    // 1/sqrt(d)
+  float c;        // scale * log2(e)
   uint32_t tmem_cols;
-  uint32_t gbuf_off;  // smem offset of the G^T buffer
-  uint32_t klo_off;   // smem offset of the K~ lo split (prologue)
+  uint32_t abuf_off, bbuf_off, klo_off;  // smem offsets (G^T at 0)
 };
 
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -71,6 +80,10 @@ __device__ __forceinline__ void store_row4(uint8_t* buf, int rows, int row, int 
   *reinterpret_cast<float4*>(buf + kmaj_off(row, c, rows)) = v;
 }
 
+__device__ __forceinline__ float ld_elem(const uint8_t* buf, int rows, int row, int col) {
+  return *reinterpret_cast<const float*>(buf + kmaj_off(row, col, rows));
+}
+
 __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
@@ -80,26 +93,34 @@ __device__ __forceinline__ float tf32_hi(float x) {
 // (half h = w / 4 takes the chunks with index % 2 == h).
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
+template <int MP>
+__global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
+    pinv_tc(const __grid_constant__ PinvParams p) {
+  constexpr int NCH = MP / 32;  // 32-column chunks of a head's m x m block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* bbuf = sm;               // B operand [MP rows x MP] fp32
-  uint8_t* gbuf = sm + p.gbuf_off;  // G^T       [d rows x MP]  fp32
-  uint8_t* khi = sm;                // K~ hi / lo [MP rows x d] (prologue only)
-  uint8_t* klo = sm + p.klo_off;
+  const int hp = p.hp, NP = hp * MP;  // N of the stacked m x m products (<= 128)
+  const int NW = hp * p.d;            // N of the stacked W = Z G (<= 256)
+  uint8_t* gbuf = sm;                 // G^T, heads stacked:   [NW rows x MP]
+  uint8_t* abuf = sm + p.abuf_off;    // A_S (A operand):      [128 rows x MP]
+  uint8_t* bbuf = sm + p.bbuf_off;    // B operand:            [NP rows x MP]
+  uint8_t* khi = abuf;                // K~ hi / lo, stacked:  [NP rows x d]
+  uint8_t* klo = sm + p.klo_off;      //   (score step only, over abuf / bbuf)
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float red_row[4], red_col[kThreads];
+  __shared__ float red_rmax[2][128], red_rsum[2][128], red_rs[2][128], red_cs[2][128];
+  __shared__ float red_q[2][4];  // per lane quarter: largest row / column abs-sum
   volatile int* abort_flag = &abort_sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
-  const int row = quarter * 32 + lane;
-  const int bh = blockIdx.x;
-  const int m = p.m, d = p.d, MP = p.m_pad;
-  const bool live = row < m;
-  const bool in_mp = row < MP;
-  const int nch = MP >> 5;  // 32-column chunks of an m x m matrix
+  const int row = quarter * 32 + lane;     // TMEM lane
+  const int hs = row / MP, li = row % MP;  // head slot (warp-uniform), row in the head
+  const int bh = (int)blockIdx.x * hp + hs;
+  const bool head_ok = hs < hp && bh < p.BH;  // warp-uniform
+  const int m = p.m, d = p.d;
+  const bool live = head_ok && li < m;
+  const bool in_np = row < NP;
 
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
@@ -112,21 +133,34 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t lo = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t COL_A = 0, COL_Z = MP, COL_X = 2 * MP, COL_Y = 3 * MP;
-  const uint32_t COL_QH = 0, COL_QL = d, COL_S = 2 * d;  // prologue only
+  const uint32_t COL_Z = 0, COL_X = MP, COL_D = 2 * MP;  // main loop
+  const uint32_t COL_QH = 0, COL_QL = d, COL_S = 2 * d;  // score step
+  const uint32_t dblk = (uint32_t)(hs * MP);  // this head's block of a stacked result
 
   uint32_t phase = 0;
-  // tf32 product D = A (TMEM columns a_col..) x B (smem, b_rows rows = N),
-  // K = k_dim. Descriptors: one base, then start-address increments.
-  auto issue = [&](uint32_t d_col, uint32_t a_col, const uint8_t* b, int b_rows, int k_dim,
-                   bool acc_first) {
-    const uint64_t d0 = smem_desc(smem_u32(b), 16, 1024, SW_128B);
+  // tf32 product D (+)= A x B, M = 128, N = b_rows, K = k_dim. A from TMEM
+  // columns a_col.. or, if a_smem is set, from shared memory (K-major,
+  // 128 rows); B from shared memory (K-major, b_rows rows).
+  auto issue = [&](uint32_t d_col, uint32_t a_col, const uint8_t* a_smem, const uint8_t* b,
+                   int b_rows, int k_dim, bool acc_first) {
+    const uint64_t b0 = smem_desc(smem_u32(b), 16, 1024, SW_128B);
     const uint32_t id = idesc_tf32(128, b_rows);
-    const uint32_t chunk16 = (uint32_t)b_rows * 8u;  // (b_rows * 128 B) >> 4
+    const uint32_t bchunk = (uint32_t)b_rows * 8u;  // (b_rows * 128 B) >> 4
+    if (a_smem) {
+      const uint64_t a0 = smem_desc(smem_u32(a_smem), 16, 1024, SW_128B);
 #pragma unroll 4
-    for (int kk = 0; kk < k_dim / 8; ++kk) {
-      const uint64_t bd = d0 + (uint64_t)((uint32_t)(kk >> 2) * chunk16 + (uint32_t)(kk & 3) * 2u);
-      mma_tf32_tA(tmem + d_col, tmem + a_col + kk * 8, bd, id, (kk > 0 || acc_first) ? 1u : 0u);
+      for (int kk = 0; kk < k_dim / 8; ++kk) {
+        const uint32_t step = (uint32_t)(kk & 3) * 2u;  // 8 tf32 = 32 B
+        mma_tf32(tmem + d_col, a0 + (uint64_t)((uint32_t)(kk >> 2) * 1024u + step),
+                 b0 + (uint64_t)((uint32_t)(kk >> 2) * bchunk + step), id,
+                 (kk > 0 || acc_first) ? 1u : 0u);
+      }
+    } else {
+#pragma unroll 4
+      for (int kk = 0; kk < k_dim / 8; ++kk) {
+        const uint64_t bd = b0 + (uint64_t)((uint32_t)(kk >> 2) * bchunk + (uint32_t)(kk & 3) * 2u);
+        mma_tf32_tA(tmem + d_col, tmem + a_col + kk * 8, bd, id, (kk > 0 || acc_first) ? 1u : 0u);
+      }
     }
   };
   auto wait_mma = [&]() {
@@ -138,10 +172,69 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
     tc_fence_after_sync();
   };
 
-  // ---- 1) A_S scores S = Q~ K~^T in 3xTF32 on the tensor cores
+  // ---- 1) G = merge of the key-split partials (row li of head bh); G^T
+  // into gbuf (B of W = Z G, head slot hs at rows hs d ..). First, so that
+  // its loads do not wait behind the score steps.
   {
-    const float* krow = p.kt + ((size_t)bh * m + (live ? row : 0)) * d;
-    const float* qrow = p.qt + ((size_t)bh * m + (live ? row : 0)) * d;
+    // running (max, denominator) over the partials' (max, sum) pairs, eight
+    // pairs loaded at a time; empty partials (max = -inf) are skipped
+    float gm = -INFINITY, den = 0.f;
+    if (live)
+      for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
+        float2 ml[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          ml[k] = sp0 + k < p.splits
+                      ? *reinterpret_cast<const float2*>(p.gml + (((size_t)bh * p.splits + sp0 + k) * m + li) * 2)
+                      : make_float2(-INFINITY, 0.f);
+        float cm = gm;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) cm = fmaxf(cm, ml[k].x);
+        if (cm != -INFINITY) {
+          den = gm == -INFINITY ? 0.f : den * expf(gm - cm);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (ml[k].x != -INFINITY) den += ml[k].y * expf(ml[k].x - cm);
+          gm = cm;
+        }
+      }
+    const float inv = live ? 1.f / den : 0.f;
+    float* grow_out = p.g + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
+    for (int c0 = half * 32; c0 < d; c0 += 64) {
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      if (live) {
+#pragma unroll 2
+        for (int sp = 0; sp < p.splits; ++sp) {
+          const size_t prow = ((size_t)bh * p.splits + sp) * m + li;
+          if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
+          const float f = expf(p.gml[prow * 2] - gm);
+          const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + c0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 v = src[e];
+            acc[4 * e] += v.x * f;
+            acc[4 * e + 1] += v.y * f;
+            acc[4 * e + 2] += v.z * f;
+            acc[4 * e + 3] += v.w * f;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] *= inv;
+        float4* go = reinterpret_cast<float4*>(grow_out + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+      }
+      if (hs < hp) store_col32(gbuf, NW, li, hs * d + c0, acc);
+    }
+  }
+
+  // ---- 2) scores S = Q~ K~^T in 3xTF32: Q~ hi / lo rows -> TMEM (A), K~
+  // hi / lo rows -> shared memory (B, head slot hs at rows hs MP ..)
+  {
+    const float* qrow = p.qt + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
+    const float* krow = p.kt + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
     for (int c0 = half * 32; c0 < d; c0 += 64) {
       uint32_t qh[32], ql[32];
 #pragma unroll
@@ -150,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
         const float4 qv = live ? *reinterpret_cast<const float4*>(qrow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 kh = make_float4(tf32_hi(kv.x), tf32_hi(kv.y), tf32_hi(kv.z), tf32_hi(kv.w));
         const float4 kl = make_float4(kv.x - kh.x, kv.y - kh.y, kv.z - kh.z, kv.w - kh.w);
-        if (in_mp) {
-          store_row4(khi, MP, row, c0 + e, kh);
-          store_row4(klo, MP, row, c0 + e, kl);
+        if (in_np) {
+          store_row4(khi, NP, row, c0 + e, kh);
+          store_row4(klo, NP, row, c0 + e, kl);
         }
         const float q4[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -172,192 +265,166 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
   __syncthreads();
   if (tid == 0) {
     tc_fence_after_sync();
-    issue(COL_S, COL_QH, khi, MP, d, false);
-    issue(COL_S, COL_QH, klo, MP, d, true);
-    issue(COL_S, COL_QL, khi, MP, d, true);
+    issue(COL_S, COL_QH, nullptr, khi, NP, d, false);
+    issue(COL_S, COL_QH, nullptr, klo, NP, d, true);
+    issue(COL_S, COL_QL, nullptr, khi, NP, d, true);
     mma_commit(&bar_mma);
   }
   wait_mma();
   __syncthreads();
-  // row softmax of the scores (scale 1/sqrt(d)) by the first half of the
-  // CTA; A_S -> TMEM (A operand) and -> bbuf rows
-  if (half == 0) {
-    float rmax = -INFINITY;
-    for (int j0 = 0; j0 < MP; j0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + COL_S + j0, r);
-      tmem_ld_wait();
+
+  // ---- 3) row softmax over the head's own block of S (scale 1/sqrt(d));
+  // half h takes the chunks c = h, h + 2 (both in flight at once), the two
+  // halves combine the row max and sum through shared memory. A_S rows ->
+  // abuf (A operand of X = A_S Z).
+  {
+    const int nmine = head_ok ? (NCH - half + 1) >> 1 : 0;  // 0, 1 or 2, warp-uniform
+    const int j0 = half * 32, j1 = (half + 2) * 32;
+    uint32_t r0[32], r1[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (j0 + e < m) rmax = fmaxf(rmax, __uint_as_float(r[e]));
-    }
-    float sum = 0.f;
-    for (int j0 = 0; j0 < MP; j0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + COL_S + j0, r);
-      tmem_ld_wait();
+    for (int e = 0; e < 32; ++e) r0[e] = r1[e] = 0u;
+    if (nmine > 0) tmem_ld32(tmem + lo + COL_S + dblk + j0, r0);
+    if (nmine > 1) tmem_ld32(tmem + lo + COL_S + dblk + j1, r1);
+    tmem_ld_wait();
+    float pm = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float x = (live && j0 + e < m) ? expf((__uint_as_float(r[e]) - rmax) * p.scale) : 0.f;
-        sum += x;
-        r[e] = __float_as_uint(x);
-      }
-      tmem_st32(tmem + lo + COL_S + j0, r);
+    for (int e = 0; e < 32; ++e) {
+      if (nmine > 0 && j0 + e < m) pm = fmaxf(pm, __uint_as_float(r0[e]));
+      if (nmine > 1 && j1 + e < m) pm = fmaxf(pm, __uint_as_float(r1[e]));
     }
-    tmem_st_wait();
-    const float inv = live ? 1.f / sum : 0.f;
+    red_rmax[half][row] = pm;
+    __syncthreads();
+    const float mc = fmaxf(red_rmax[0][row], red_rmax[1][row]) * p.c;
+    float ps = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float x0 = (live && nmine > 0 && j0 + e < m) ? fast_exp2(fmaf(__uint_as_float(r0[e]), p.c, -mc)) : 0.f;
+      const float x1 = (live && nmine > 1 && j1 + e < m) ? fast_exp2(fmaf(__uint_as_float(r1[e]), p.c, -mc)) : 0.f;
+      ps += x0 + x1;
+      r0[e] = __float_as_uint(x0);
+      r1[e] = __float_as_uint(x1);
+    }
+    red_rsum[half][row] = ps;
+    __syncthreads();
+    const float inv = live ? 1.f / (red_rsum[0][row] + red_rsum[1][row]) : 0.f;
     float rs = 0.f;
-    for (int j0 = 0; j0 < MP; j0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + COL_S + j0, r);
-      tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float x = __uint_as_float(r[e]) * inv;
-        r[e] = __float_as_uint(x);
-        rs += fabsf(x);
-      }
-      // A_S row -> A operand (only dead Q~ / score columns are overwritten)
-      tmem_st32(tmem + lo + COL_A + j0, r);
-      if (in_mp) {
+    for (int e = 0; e < 32; e += 4) {
+      float a[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          store_row4(bbuf, MP, row, j0 + e,
-                     make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                 __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
+      for (int t = 0; t < 4; ++t) {
+        a[t] = __uint_as_float(r0[e + t]) * inv;
+        a[4 + t] = __uint_as_float(r1[e + t]) * inv;
+        rs += fabsf(a[t]) + fabsf(a[4 + t]);
       }
+      if (half < NCH) store_row4(abuf, 128, row, j0 + e, make_float4(a[0], a[1], a[2], a[3]));
+      if (half + 2 < NCH) store_row4(abuf, 128, row, j1 + e, make_float4(a[4], a[5], a[6], a[7]));
     }
-    // ||A_S||_inf: largest row abs-sum
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) rs = fmaxf(rs, __shfl_xor_sync(0xffffffffu, rs, o));
-    if (lane == 0) red_row[quarter] = rs;
-    tmem_st_wait();
+    red_rs[half][row] = rs;
   }
   __syncthreads();
-  // ||A_S||_1: largest column abs-sum. Thread (row j, half h) sums column j
-  // over half of the rows with four independent partial sums.
+  // ||A_S||_1 per head: thread (row hs MP + j, half) sums column j of its
+  // head over half of the rows (four independent partial sums)
   {
     float c4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (in_mp) {
+    if (live) {
       const int i0 = half * (MP >> 1), i1 = i0 + (MP >> 1);
       for (int i = i0; i < i1; i += 4) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          c4[t] += fabsf(*reinterpret_cast<const float*>(bbuf + kmaj_off(i + t, row, MP)));
+        for (int t = 0; t < 4; ++t) c4[t] += fabsf(ld_elem(abuf, 128, hs * MP + i + t, li));
       }
     }
-    red_col[tid] = (c4[0] + c4[1]) + (c4[2] + c4[3]);
+    red_cs[half][row] = (c4[0] + c4[1]) + (c4[2] + c4[3]);
   }
-  // stage export of A_S: coalesced copy of the bbuf rows
+  // stage export of A_S: coalesced copy of the abuf rows, a warp per row
+  for (int r = warp; r < hp * m; r += kThreads / 32) {
+    const int h2 = r / m, i = r - h2 * m;
+    const int bh2 = (int)blockIdx.x * hp + h2;
+    if (bh2 >= p.BH) break;
+    float* a_out = p.a_s + ((size_t)bh2 * m + i) * m;
+    for (int j = lane; j < m; j += 32) a_out[j] = ld_elem(abuf, 128, h2 * MP + i, j);
+  }
+  __syncthreads();
+  // per lane quarter: largest row abs-sum and largest column abs-sum
+  if (half == 0) {
+    float rs = live ? red_rs[0][row] + red_rs[1][row] : 0.f;
+    float cs = live ? red_cs[0][row] + red_cs[1][row] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rs = fmaxf(rs, __shfl_xor_sync(0xffffffffu, rs, o));
+      cs = fmaxf(cs, __shfl_xor_sync(0xffffffffu, cs, o));
+    }
+    if (lane == 0) {
+      red_q[0][quarter] = rs;
+      red_q[1][quarter] = cs;
+    }
+  }
+  __syncthreads();
+  float alpha = 0.f;
   {
-    float* a_out = p.a_s + (size_t)bh * m * m;
-    for (int e = tid; e < m * m; e += kThreads)
-      a_out[e] = *reinterpret_cast<const float*>(bbuf + kmaj_off(e / m, e % m, MP));
+    // the lane quarters of this head: [hs MP / 32, (hs + 1) MP / 32)
+    float ninf = 0.f, n1 = 0.f;
+    for (int q = hs * MP / 32; q < (hs + 1) * MP / 32 && q < 4; ++q) {
+      ninf = fmaxf(ninf, red_q[0][q]);
+      n1 = fmaxf(n1, red_q[1][q]);
+    }
+    if (head_ok) alpha = 1.f / (n1 * ninf);
   }
-  __syncthreads();
-  if (warp == 0) {
-    float cs = 0.f;
-    for (int j = lane; j < 128; j += 32) cs = fmaxf(cs, red_col[j] + red_col[j + 128]);
+  // Z_0 = alpha A_S^T -> TMEM: row i of Z_0 is alpha * column i of A_S
+  if (head_ok) {
+    for (int c = half; c < NCH; c += 2) {
+      uint32_t r[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cs = fmaxf(cs, __shfl_xor_sync(0xffffffffu, cs, o));
-    if (lane == 0) red_col[0] = cs;
+      for (int e = 0; e < 32; ++e)
+        r[e] = __float_as_uint(alpha * ld_elem(abuf, 128, hs * MP + c * 32 + e, li));
+      tmem_st32(tmem + lo + COL_Z + c * 32, r);
+    }
   }
-  __syncthreads();
-  const float alpha = 1.f / (red_col[0] * fmaxf(fmaxf(red_row[0], red_row[1]), fmaxf(red_row[2], red_row[3])));
-  // Z_0 = alpha A_S^T: row i of Z_0 is alpha * column i of A_S -> TMEM
-  for (int c = half; c < nch; c += 2) {
-    uint32_t r[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      r[e] = __float_as_uint(in_mp ? alpha * *reinterpret_cast<const float*>(bbuf + kmaj_off(c * 32 + e, row, MP)) : 0.f);
-    tmem_st32(tmem + lo + COL_Z + c * 32, r);
-  }
-  __syncthreads();  // every column read done before the rows are rescaled
-  // B operand of X = A_S Z_0: Z_0 stored by columns = alpha * A_S rows
-  if (in_mp)
-    for (int c = half; c < nch; c += 2)
+  // B operand of X = A_S Z_0: row hs MP + j holds column j of Z_0, i.e.
+  // alpha * row j of A_S
+  if (in_np)
+    for (int c = half; c < NCH; c += 2)
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        float4* e4 = reinterpret_cast<float4*>(bbuf + kmaj_off(row, c * 32 + e, MP));
-        float4 v = *e4;
+        float4 v = *reinterpret_cast<const float4*>(abuf + kmaj_off(row, c * 32 + e, 128));
         v.x *= alpha; v.y *= alpha; v.z *= alpha; v.w *= alpha;
-        *e4 = v;
+        store_row4(bbuf, NP, row, c * 32 + e, v);
       }
-  // ---- 2) G = merge of the key-split partials; G^T into gbuf (B of W = Z G)
-  {
-    float gm = -INFINITY;
-    if (live)
-      for (int sp = 0; sp < p.splits; ++sp)
-        gm = fmaxf(gm, p.gml[(((size_t)bh * p.splits + sp) * m + row) * 2]);
-    float den = 0.f;
-    if (live)
-      for (int sp = 0; sp < p.splits; ++sp) {
-        const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
-        if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial
-        den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
-      }
-    const float inv = live ? 1.f / den : 0.f;
-    float* grow_out = p.g + ((size_t)bh * m + (live ? row : 0)) * d;
-    for (int c0 = half * 32; c0 < d; c0 += 64) {
-      float acc[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      if (live) {
-        for (int sp = 0; sp < p.splits; ++sp) {
-          const size_t prow = ((size_t)bh * p.splits + sp) * m + row;
-          if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
-          const float f = expf(p.gml[prow * 2] - gm);
-          const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + c0);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v = src[e];
-            acc[4 * e] += v.x * f;
-            acc[4 * e + 1] += v.y * f;
-            acc[4 * e + 2] += v.z * f;
-            acc[4 * e + 3] += v.w * f;
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] *= inv;
-        float4* go = reinterpret_cast<float4*>(grow_out + c0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
-      }
-      if (in_mp) store_col32(gbuf, d, row, c0, acc);
-    }
-  }
   fence_async_smem();
   tmem_st_wait();
   tc_fence_before_sync();
   __syncthreads();
 
-  // ---- 3) the iteration
-  auto gemm = [&](uint32_t d_col, uint32_t a_col, const uint8_t* b, int b_rows) {
+  // ---- 4) the iteration
+  auto gemm = [&](uint32_t a_col, const uint8_t* a_smem) {
     if (tid == 0) {
       tc_fence_after_sync();
-      issue(d_col, a_col, b, b_rows, MP, false);
+      issue(COL_D, a_col, a_smem, bbuf, NP, MP, false);
       mma_commit(&bar_mma);
     }
     wait_mma();
   };
-  // epilogue: this row of D -> sign * scale * D + diag * I, written
-  // transposed as the next product's B operand (element (i, j) -> storage
-  // row j, column i); optionally also Z <- scale * D in TMEM.
-  auto store_bt = [&](float diag, float sign, float scale_, uint32_t col, bool to_z) {
-    for (int c = half; c < nch; c += 2) {
-      const int j0 = c * 32;
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + col + j0, r);
-      tmem_ld_wait();
-      float v[32];
+  // epilogue: the head's block of this row of D -> sign * scale * D + diag
+  // * I, written transposed as the next product's B operand (element
+  // (i, j) of the head -> storage row hs MP + j, column i); optionally also
+  // scale * D -> TMEM columns to_col.. (an A operand).
+  auto store_bt = [&](float diag, float sign, float scale_, int to_col) {
+    if (head_ok) {
+      for (int c = half; c < NCH; c += 2) {
+        const int j0 = c * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + lo + COL_D + dblk + j0, r);
+        tmem_ld_wait();
+        float v[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float x = scale_ * __uint_as_float(r[e]);
-        r[e] = __float_as_uint(x);
-        v[e] = fmaf(sign, x, (j0 + e == row) ? diag : 0.f);
+        for (int e = 0; e < 32; ++e) {
+          const float x = scale_ * __uint_as_float(r[e]);
+          r[e] = __float_as_uint(x);
+          v[e] = fmaf(sign, x, (j0 + e == li) ? diag : 0.f);
+        }
+        store_col32(bbuf, NP, li, hs * MP + j0, v);
+        if (to_col >= 0) tmem_st32(tmem + lo + (uint32_t)to_col + j0, r);
       }
-      if (in_mp) store_col32(bbuf, MP, row, j0, v);
-      if (to_z) tmem_st32(tmem + lo + COL_Z + j0, r);
     }
     fence_async_smem();
     tmem_st_wait();
@@ -365,28 +432,33 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
     __syncthreads();
   };
   for (int it = 0; it < p.iters && !*abort_flag; ++it) {
-    gemm(COL_X, COL_A, bbuf, MP);             // X = A_S Z
+    gemm(0, abuf);                          // X = A_S Z
     if (*abort_flag) break;
-    store_bt(7.f, -1.f, 1.f, COL_X, false);   // B <- 7I - X
-    gemm(COL_Y, COL_X, bbuf, MP);             // Y = X (7I - X)
+    store_bt(7.f, -1.f, 1.f, (int)COL_X);   // B <- 7I - X ; X -> TMEM
+    gemm(COL_X, nullptr);                   // Y = X (7I - X)
     if (*abort_flag) break;
-    store_bt(15.f, -1.f, 1.f, COL_Y, false);  // B <- 15I - Y
-    gemm(COL_Y, COL_X, bbuf, MP);             // Y = X (15I - ...)
+    store_bt(15.f, -1.f, 1.f, -1);          // B <- 15I - Y
+    gemm(COL_X, nullptr);                   // Y = X (15I - ...)
     if (*abort_flag) break;
-    store_bt(13.f, -1.f, 1.f, COL_Y, false);  // B <- 13I - Y
-    gemm(COL_Y, COL_Z, bbuf, MP);             // Y = Z (13I - ...)
+    store_bt(13.f, -1.f, 1.f, -1);          // B <- 13I - Y
+    gemm(COL_Z, nullptr);                   // Y = Z (13I - ...)
     if (*abort_flag) break;
-    store_bt(0.f, 1.f, 0.25f, COL_Y, true);   // Z <- Y / 4 ; B <- Z by columns
+    store_bt(0.f, 1.f, 0.25f, (int)COL_Z);  // Z <- Y / 4 ; B <- Z by columns
   }
-  // ---- 4) W = Z G
+  // ---- 5) W = Z G (head slot hs in columns hs d ..)
   if (!*abort_flag) {
-    gemm(COL_Y, COL_Z, gbuf, d);
-    if (!*abort_flag) {
-      float* wrow = p.w + ((size_t)bh * m + (live ? row : 0)) * d;
+    if (tid == 0) {
+      tc_fence_after_sync();
+      issue(COL_D, COL_Z, nullptr, gbuf, NW, MP, false);
+      mma_commit(&bar_mma);
+    }
+    wait_mma();
+    if (!*abort_flag && head_ok) {
+      float* wrow = p.w + ((size_t)bh * m + (live ? li : 0)) * d;
       __nv_bfloat16* wt = p.wt + (size_t)bh * p.dpad * p.m64;
       for (int c0 = half * 32; c0 < d; c0 += 64) {
         uint32_t r[32];
-        tmem_ld32(tmem + lo + COL_Y + c0, r);
+        tmem_ld32(tmem + lo + COL_D + hs * d + c0, r);
         tmem_ld_wait();
         if (live) {
           float4* wo = reinterpret_cast<float4*>(wrow + c0);
@@ -395,14 +467,18 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
             wo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
         }
-        if (row < p.m64) {
+        // W^T (bf16, zero padded to m64 columns): column li, and li + MP
+        // where MP < m64
+        for (int lj = li; lj < p.m64; lj += MP) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            wt[(size_t)(c0 + e) * p.m64 + row] = __float2bfloat16_rn(live ? __uint_as_float(r[e]) : 0.f);
+            wt[(size_t)(c0 + e) * p.m64 + lj] =
+                __float2bfloat16_rn(lj == li && live ? __uint_as_float(r[e]) : 0.f);
         }
       }
-      if (half == 0 && row < p.m64)
-        for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + row] = __float2bfloat16_rn(0.f);
+      if (half == 0)
+        for (int lj = li; lj < p.m64; lj += MP)
+          for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + lj] = __float2bfloat16_rn(0.f);
     }
   }
   tc_fence_before_sync();
@@ -410,8 +486,7 @@ __global__ void __launch_bounds__(kThreads, 2) pinv_tc(const PinvParams p) {
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 }
 
-// m rounded up to 32, 64 or 128 (zero padding of A_S is exact: the
-// padded block of every iterate stays zero)
+// m rounded up to 32, 64 or 128
 int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 
 }  // namespace
@@ -432,31 +507,37 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.w = w;
   p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
   p.status = status;
+  p.BH = (int)s.bh();
   p.m = s.m;
   p.d = s.d;
-  p.m_pad = mpad_of(s.m);
   p.dpad = s.dpad();
   p.m64 = s.m64();
   p.splits = splits;
   p.iters = s.iters;
   p.scale = 1.0f / sqrtf((float)s.d);
-  const uint32_t need = std::max<uint32_t>(3 * p.m_pad + std::max(p.m_pad, s.d),
-                                           2 * s.d + p.m_pad);
+  p.c = p.scale * 1.4426950408889634f;
+  const int MP = mpad_of(s.m);
+  p.hp = std::min(128 / MP, 256 / s.d);
+  const int NP = p.hp * MP, NW = p.hp * s.d;
+  const uint32_t need = std::max<uint32_t>(2 * s.d + NP, 2 * MP + std::max(NP, NW));
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
   p.tmem_cols = cols;
-  const size_t bbytes = (size_t)p.m_pad * p.m_pad * 4;
-  const size_t gbytes = (size_t)s.d * p.m_pad * 4;
-  p.gbuf_off = (uint32_t)bbytes;
-  // K~ hi / lo (prologue only) share space with the operand buffers
-  const size_t kbytes = (size_t)p.m_pad * s.d * 4;
-  p.klo_off = (uint32_t)kbytes;
-  const size_t smem = std::max(bbytes + gbytes, 2 * kbytes) + 1024;
-  if (cudaFuncSetAttribute(pinv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  const size_t gbytes = (size_t)NW * MP * 4;
+  const size_t abytes = (size_t)128 * MP * 4;
+  const size_t bbytes = (size_t)NP * MP * 4;
+  const size_t kbytes = (size_t)NP * s.d * 4;  // K~ hi / lo (score step only)
+  p.abuf_off = (uint32_t)gbytes;
+  p.bbuf_off = (uint32_t)(gbytes + abytes);
+  p.klo_off = (uint32_t)(gbytes + kbytes);
+  const size_t smem = gbytes + std::max(abytes + bbytes, 2 * kbytes) + 1024;
+  auto kern = MP == 32 ? pinv_tc<32> : (MP == 64 ? pinv_tc<64> : pinv_tc<128>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return NYS_ERR_CUDA;
+  const unsigned grid = (unsigned)((p.BH + p.hp - 1) / p.hp);
   KernelScope scope("pinv_tc", stream);
-  pinv_tc<<<(unsigned)s.bh(), kThreads, smem, stream>>>(p);
+  kern<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
 }
 
