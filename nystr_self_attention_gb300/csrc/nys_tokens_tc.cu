@@ -7,9 +7,9 @@
 //                done), V halos (ring of 2, freed once the conv is done), and
 //                per head K~ and W^T (1-2 buffers); Q and V streams advance
 //                independently
-//   warp 1       tcgen05 issuer of the F stream; warp 16 issuer of the PW /
-//                conv stream (one issuing thread per stream: each tcgen05.mma
-//                costs its issuing thread tens of cycles):
+//   warp 1       tcgen05 issuer of the F and conv streams (the conv does
+//                not wait for the softmax); warp 16 issuer of the PW stream
+//                (each tcgen05.mma costs its issuing thread tens of cycles):
 //                  F  = Q_tile K~^T          A = Q (smem), B = K~ (smem)
 //                  PW = P W                  A = P (TMEM), B = W^T (smem)
 //                  CV = T V_halo             A = banded Toeplitz of the conv
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       mbar_init(&bars.f_full[i], 1);
       mbar_init(&bars.p_full[i], 128);
       mbar_init(&bars.pw_done[i], 1);
-      mbar_init(&bars.acc_full[i], 1);
+      mbar_init(&bars.acc_full[i], p.kc > 0 ? 2 : 1);  // PW and CV commits
       mbar_init(&bars.acc_empty[i], 128);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars.l_full[i], 128);
@@ -237,13 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------- MMA issuer, F stream
+    // ------------------------------- MMA issuer, F and conv streams
     if (lane == 0 && ntiles > 0) {
       const uint32_t idf = idesc_bf16(128, p.m_pad, false, false);
-      int jf = 0;
-      int hi_f = -1, bh_f = -1;
+      const uint32_t idc = idesc_bf16(128, DP, false, true);
+      const int ncv = p.kc > 0 ? ntiles : 0;
+      int jf = 0, jc = 0;
+      int hi_f = -1, bh_f = -1, hi_c = -1, bh_c = -1;
       uint64_t t_last = globaltimer_ns();
-      while (jf < ntiles) {
+      while (jf < ntiles || jc < ncv) {
         bool prog = false;
         // F stream: F(jf) = Q K~^T into F buffer jf & 1
         if (jf < ntiles) {
@@ -272,6 +274,33 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
             prog = true;
           }
         }
+        // conv stream: CV(jc) = T V_halo into accumulator jc & 1 (does not
+        // wait for the softmax)
+        if (jc < ncv) {
+          const int g = g0 + jc, bh = head_of(g);
+          const bool new_head = bh != bh_c;
+          const int hin = new_head ? hi_c + 1 : hi_c;
+          const bool ok = (!new_head || mbar_test(&bars.t_ready[hin % p.nt], (hin / p.nt) & 1)) &&
+                          mbar_test(&bars.vfull[jc % kNV], (jc / kNV) & 1) &&
+                          (jc < 2 || mbar_test(&bars.acc_empty[jc & 1], ((jc >> 1) - 1) & 1));
+          if (ok) {
+            if (new_head) {
+              bh_c = bh;
+              hi_c = hin;
+            }
+            tc_fence_after_sync();
+            const uint32_t acc = tmem + COL_ACC0 + (jc & 1) * ACC_W;
+            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + (hi_c % p.nt) * p.t_bytes), 16, 1024, SW_128B);
+            const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + (jc % kNV) * p.v_stage), p.kc * 128, 1024, SW_128B);
+            for (int kk = 0; kk < p.kc / 16; ++kk)
+              mma_bf16(acc + DP, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2), v0 + (uint64_t)(kk * 128), idc, kk > 0);
+            mma_commit(&bars.vempty[jc % kNV]);
+            mma_commit(&bars.acc_full[jc & 1]);
+            if (jc + 1 == ntiles || head_of(g + 1) != bh) mma_commit(&bars.t_empty[hi_c % p.nt]);
+            ++jc;
+            prog = true;
+          }
+        }
         if (prog) {
           t_last = globaltimer_ns();
         } else {
@@ -285,24 +314,21 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       }
     }
   } else if (warp == 16) {
-    // ---------------------------------------- MMA issuer, PW / conv stream
+    // ---------------------------------------------- MMA issuer, PW stream
     if (lane == 0 && ntiles > 0) {
       const uint32_t idw = idesc_bf16(128, DP, false, false);
-      const uint32_t idc = idesc_bf16(128, DP, false, true);
       int jp = 0;
       int hi_p = -1, bh_p = -1;
       uint64_t t_last = globaltimer_ns();
       while (jp < ntiles) {
         bool prog = false;
-        // PW stream: PW(jp) = P W and CV(jp) = T V into accumulator jp & 1
+        // PW stream: PW(jp) = P W into accumulator jp & 1
         {
           const int g = g0 + jp, bh = head_of(g);
           const bool new_head = bh != bh_p;
           const int hin = new_head ? hi_p + 1 : hi_p;
-          const bool ok = (p.kc == 0 || !new_head || mbar_test(&bars.t_ready[hin % p.nt], (hin / p.nt) & 1)) &&
-                          mbar_test(&bars.p_full[jp & 1], (jp >> 1) & 1) &&
-                          (jp < 2 || mbar_test(&bars.acc_empty[jp & 1], ((jp >> 1) - 1) & 1)) &&
-                          (p.kc == 0 || mbar_test(&bars.vfull[jp % kNV], (jp / kNV) & 1));
+          const bool ok = mbar_test(&bars.p_full[jp & 1], (jp >> 1) & 1) &&
+                          (jp < 2 || mbar_test(&bars.acc_empty[jp & 1], ((jp >> 1) - 1) & 1));
           if (ok) {
             if (new_head) {
               bh_p = bh;
@@ -314,19 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
             const uint32_t pcol = tmem + COL_F0 + (jp & 1) * p.m_pad;
             for (int kk = 0; kk < p.m_pad / 16; ++kk)
               mma_bf16_tA(acc, pcol + kk * 8, b0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
-            if (p.kc > 0) {
-              const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + (hi_p % p.nt) * p.t_bytes), 16, 1024, SW_128B);
-              const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + (jp % kNV) * p.v_stage), p.kc * 128, 1024, SW_128B);
-              for (int kk = 0; kk < p.kc / 16; ++kk)
-                mma_bf16(acc + DP, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2), v0 + (uint64_t)(kk * 128), idc, kk > 0);
-              mma_commit(&bars.vempty[jp % kNV]);
-            }
             mma_commit(&bars.acc_full[jp & 1]);
             mma_commit(&bars.pw_done[jp & 1]);
-            if (jp + 1 == ntiles || head_of(g + 1) != bh) {
-              mma_commit(&bars.kw_empty[hi_p % p.nkw]);
-              if (p.kc > 0) mma_commit(&bars.t_empty[hi_p % p.nt]);
-            }
+            if (jp + 1 == ntiles || head_of(g + 1) != bh) mma_commit(&bars.kw_empty[hi_p % p.nkw]);
             ++jp;
             prog = true;
           }
@@ -370,33 +386,62 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t fcol = tmem + lo + COL_F0 + grp * p.m_pad;
+    const bool full_m = p.m == p.m_pad && (p.m_pad & 63) == 0;
     for (int j = grp; j < ntiles; j += 2) {
       if (!__all_sync(0xffffffffu, wait_or_fail(&bars.f_full[grp], (j >> 1) & 1, p.status, abort_flag))) break;
       tc_fence_after_sync();
-      float mx = -INFINITY;
-      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(fcol + c0, r);
-        tmem_ld_wait();
+      float mx = -INFINITY, l = 0.f;
+      if (full_m) {
+        // m is a multiple of 64: no masks. Tile max with two 32-column
+        // chunks in flight at a time.
+        for (int c0 = 0; c0 < p.m_pad; c0 += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(fcol + c0, r0);
+          tmem_ld32(fcol + c0 + 32, r1);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
-      }
-      const float mc = mx * p.c;
-      float l = 0.f;
-      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(fcol + c0, r);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
-          const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
-          l += a + b;
-          pk[e] = pack_bf16x2(a, b);
+          for (int e = 0; e < 32; ++e)
+            mx = fmaxf(mx, fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])));
         }
-        tmem_st16(fcol + (c0 >> 1), pk);
+        const float mc = mx * p.c;
+        for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(fcol + c0, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc));
+            const float b = fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc));
+            l += a + b;
+            pk[e] = pack_bf16x2(a, b);
+          }
+          tmem_st16(fcol + (c0 >> 1), pk);
+        }
+      } else {
+        for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(fcol + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
+        }
+        const float mc = mx * p.c;
+        for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(fcol + c0, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
+            const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
+            l += a + b;
+            pk[e] = pack_bf16x2(a, b);
+          }
+          tmem_st16(fcol + (c0 >> 1), pk);
+        }
       }
       tmem_st_wait();
       lbuf[(j & 3) * 128 + row] = l;
