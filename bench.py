@@ -212,12 +212,13 @@ def run_reference(args, wl):
 KERNEL_BYTES = {
     "landmarks_vec": 2.0, "landmarks_simt": 2.0,  # read Q, K
     "rows_tc": 2.0, "rows_simt": 2.0,             # read K, V
-    "tokens_tc": 3.0, "tokens_simt": 3.0,          # read Q, V; write out
+    "tokens_tc": 3.0, "tokens_simt": 3.0, "tokens_big": 3.0,  # read Q, V; write out
 }
 KERNEL_SOURCES = {
     "landmarks_vec": "nys_simt.cu", "landmarks_simt": "nys_simt.cu", "rows_simt": "nys_simt.cu",
     "pinv_simt": "nys_simt.cu", "tokens_simt": "nys_simt.cu", "rows_tc": "nys_rows_tc.cu",
-    "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu",
+    "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu", "pinv_big": "nys_pinv_big.cu",
+    "tokens_big": "nys_tokens_big.cu",
 }
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates
 
@@ -266,7 +267,7 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
                 "peak_source": f"hbm_gbs ({peak_src})"}
     flops = pinv_flops(wl) / per_step
     achieved = flops / t_launch / 1e12
-    if kernel == "pinv_tc":
+    if kernel in ("pinv_tc", "pinv_big"):
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
         return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -277,6 +278,27 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
             "algorithmic_flops": flops,
             "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
+
+
+def pass_roofline(wl, ms_per_step, peaks, peak_src):
+    """Whole forward pass against its own roofline: two streaming passes over
+    Q, K and V plus the output write (7 T e bytes) at the measured HBM rate,
+    and the dense contractions (landmark rows S and P V, token F and P W, the
+    conv as a banded product, the pseudo-inverse) at the tensor rate; the
+    slower of the two is the roofline time."""
+    te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
+    nbytes = 7.0 * te
+    n_tok = wl.B * wl.H * wl.n
+    mm_flops = n_tok * (2.0 * wl.m * wl.d * 2 + 2.0 * wl.m * wl.d * 2 + 2.0 * wl.ks * wl.d)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_mma = mm_flops / (peaks["bf16_tflops"] * 1e12) + pinv_flops(wl) / (
+        peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
+    t_roof = max(t_hbm, t_mma)
+    return {"bytes": nbytes, "flops": mm_flops + pinv_flops(wl), "t_hbm_us": t_hbm * 1e6,
+            "t_tensor_us": t_mma * 1e6, "bound": "hbm" if t_hbm >= t_mma else "tensor",
+            "t_roofline_us": t_roof * 1e6, "t_measured_us": ms_per_step * 1e3,
+            "frac": t_roof / (ms_per_step / 1e3),
+            "peak_source": f"hbm_gbs, bf16_tflops ({peak_src}); tf32 = bf16 x 1.1/2.25"}
 
 
 def run_ours(args, wl):
@@ -447,7 +469,8 @@ def run_ours(args, wl):
         "config": {"workload": wl.describe(), "tokens_per_step": tokens_step,
                    "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
                    "parallelism": f"replicas x{world} (independent heads, no collective)"},
-        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "pass_roofline": pass_roofline(wl, ms_per_step, peaks, peak_src),
+        "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": launches,
     }
     print(json.dumps(line), flush=True)
