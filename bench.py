@@ -60,6 +60,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_over_ranks(x, op, device, world):
+    """x reduced with op (a torch.distributed ReduceOp) over all ranks; x
+    itself on a single rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=op)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step, world, steps, elapsed_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank_step * world * steps / (elapsed_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -358,9 +375,7 @@ def run_ours(args, wl):
         per = e0.elapsed_time(e1) / 10 / 1e3
         steps = int(max(20, min(200000, 3.0 / max(per, 1e-7))))
         if world > 1:
-            t = torch.tensor([steps], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MIN)
-            steps = int(t.item())
+            steps = int(reduce_over_ranks(steps, dist.ReduceOp.MIN, dev, world))
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -381,13 +396,11 @@ def run_ours(args, wl):
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = reduce_over_ranks(elapsed_ms, dist.ReduceOp.MAX, dev, world)
     assert N.nystrom_get_status(stream) == N.NYS_OK
 
     tokens_step = wl.tokens
-    value = tokens_step * world * steps / (elapsed_ms / 1e3)
+    value = job_throughput(tokens_step, world, steps, elapsed_ms)
     ms_per_step = elapsed_ms / steps
 
     # per-kernel times (CUDA events on the launch stream) over a second pass of
@@ -442,9 +455,7 @@ def run_ours(args, wl):
         t1 = time.perf_counter()
         dt_e2e = t1 - t0
         if world > 1:
-            t = torch.tensor([dt_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt_e2e = float(t.item())
+            dt_e2e = reduce_over_ranks(dt_e2e, dist.ReduceOp.MAX, dev, world)
         e2e = {"value": tokens_step * world * e2e_steps / dt_e2e, "unit": "tokens/s",
                "h2d_bytes_per_step": 3 * wl.tokens * d * esz + wl.H * wl.ks * 4,
                "d2h_bytes_per_step": wl.tokens * d * esz, "steps": e2e_steps,
