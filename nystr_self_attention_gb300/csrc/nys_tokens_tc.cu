@@ -84,6 +84,45 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, int
   return false;
 }
 
+// A walk over the CTA's tiles that tracks the head and the tile within it
+// incrementally (the polling loops below do no division).
+struct TileWalk {
+  int j;       // tile within the CTA's range
+  int bh, t;   // head, tile within the head
+  bool first;  // first tile of a head (or of the range)
+  __device__ void init(int g0, int tph) {
+    j = 0;
+    bh = g0 / tph;
+    t = g0 - bh * tph;
+    first = true;
+  }
+  __device__ bool last(int tph, int ntiles) const { return t == tph - 1 || j == ntiles - 1; }
+  __device__ void next(int tph) {
+    ++j;
+    first = ++t == tph;
+    if (first) {
+      t = 0;
+      ++bh;
+    }
+  }
+};
+
+// Slot and phase parity of a ring of n buffers, advanced one use at a time.
+struct Ring {
+  int i;
+  uint32_t ph;
+  __device__ void init() {
+    i = 0;
+    ph = 0;
+  }
+  __device__ void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 // One 16-byte chunk (8 taps) of row t of the Toeplitz block: column u holds
 // w[u - t] for 0 <= u - t < ks and u < kc, else 0.
 __device__ __forceinline__ void toeplitz_chunk(uint8_t* tbuf, const float* wh, int ks, int kc,
@@ -168,50 +207,60 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       tma_prefetch(&maps.v);
       tma_prefetch(&maps.kt);
       tma_prefetch(&maps.wt);
-      int jq = 0, jv = p.kc > 0 ? 0 : ntiles, hi = -1, cur_bh = -1;
+      const int tph = p.tiles_per_head;
+      TileWalk wq, wv;
+      wq.init(g0, tph);
+      wv.init(g0, tph);
+      Ring rq, rv, rk;  // Q stages, V stages, per-head K~ / W^T buffers
+      rq.init();
+      rv.init();
+      rk.init();
+      const int nv_tiles = p.kc > 0 ? ntiles : 0;
+      int heads = 0;  // per-head loads issued
       uint32_t nq_issued[3] = {0, 0, 0}, nv_issued[2] = {0, 0}, nkw_issued[2] = {0, 0};
       uint64_t t_last = globaltimer_ns();
-      while (jq < ntiles || jv < ntiles) {
+      while (wq.j < ntiles || wv.j < nv_tiles) {
         bool prog = false;
-        if (jq < ntiles) {
-          const int g = g0 + jq, bh = head_of(g), sq = jq % p.nq;
-          const bool new_head = bh != cur_bh;
-          const int kb = (hi + 1) % p.nkw;
-          const bool kw_ok = !new_head || hi + 1 < p.nkw ||
-                             mbar_test(&bars.kw_empty[kb], (((hi + 1) / p.nkw) - 1) & 1);
-          const bool q_ok = jq < p.nq || mbar_test(&bars.qempty[sq], ((jq / p.nq) - 1) & 1);
+        if (wq.j < ntiles) {
+          const bool new_head = wq.first;
+          const bool kw_ok = !new_head || heads < p.nkw || mbar_test(&bars.kw_empty[rk.i], rk.ph ^ 1u);
+          const bool q_ok = wq.j < p.nq || mbar_test(&bars.qempty[rq.i], rq.ph ^ 1u);
           if (kw_ok && q_ok) {
             if (new_head) {
-              cur_bh = bh;
-              ++hi;
+              const int kb = rk.i;
               uint8_t* kts = sm + p.off_kt + kb * kw_bytes;
               uint8_t* wts = kts + p.kt_bytes;
               mbar_arrive_expect_tx(&bars.kw_full[kb], kw_bytes);
               for (int dc = 0; dc < DC; ++dc)
-                tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bars.kw_full[kb], dc * 64, 0, bh);
+                tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bars.kw_full[kb], dc * 64, 0, wq.bh);
               for (int mc = 0; mc * 64 < p.m_pad; ++mc)
-                tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bars.kw_full[kb], mc * 64, 0, bh);
+                tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bars.kw_full[kb], mc * 64, 0, wq.bh);
               ++nkw_issued[kb];
+              ++heads;
+              rk.next(p.nkw);
             }
+            const int sq = rq.i;
             uint8_t* qs = sm + p.off_q + sq * p.q_stage;
             mbar_arrive_expect_tx(&bars.qfull[sq], p.q_stage);
             for (int dc = 0; dc < DC; ++dc)
-              tma_load_3d(qs + dc * 16384, &maps.q, &bars.qfull[sq], dc * 64, (g % p.tiles_per_head) * 128, bh);
+              tma_load_3d(qs + dc * 16384, &maps.q, &bars.qfull[sq], dc * 64, wq.t * 128, wq.bh);
             ++nq_issued[sq];
-            ++jq;
+            rq.next(p.nq);
+            wq.next(tph);
             prog = true;
           }
         }
-        if (jv < jq) {
-          const int g = g0 + jv, sv = jv % kNV;
-          if (jv < kNV || mbar_test(&bars.vempty[sv], ((jv / kNV) - 1) & 1)) {
+        if (wv.j < wq.j && wv.j < nv_tiles) {
+          const int sv = rv.i;
+          if (wv.j < kNV || mbar_test(&bars.vempty[sv], rv.ph ^ 1u)) {
             uint8_t* vs = sm + p.off_v + sv * p.v_stage;
             mbar_arrive_expect_tx(&bars.vfull[sv], p.v_stage);
             for (int dc = 0; dc < DC; ++dc)
               tma_load_3d(vs + dc * (p.kc * 128), &maps.v, &bars.vfull[sv], dc * 64,
-                          (g % p.tiles_per_head) * 128 - rad, head_of(g));
+                          wv.t * 128 - rad, wv.bh);
             ++nv_issued[sv];
-            ++jv;
+            rv.next(kNV);
+            wv.next(tph);
             prog = true;
           }
         }
@@ -242,62 +291,70 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
       const uint32_t idf = idesc_bf16(128, p.m_pad, false, false);
       const uint32_t idc = idesc_bf16(128, DP, false, true);
       const int ncv = p.kc > 0 ? ntiles : 0;
-      int jf = 0, jc = 0;
-      int hi_f = -1, bh_f = -1, hi_c = -1, bh_c = -1;
+      const int tph = p.tiles_per_head;
+      TileWalk wf, wc;
+      wf.init(g0, tph);
+      wc.init(g0, tph);
+      Ring rqf, rkf, rtc, rvc;  // Q stages, K~ buffers, Toeplitz buffers, V stages
+      rqf.init();
+      rkf.init();
+      rtc.init();
+      rvc.init();
+      int kcur = 0, tcur = 0;  // buffers of the current head
       uint64_t t_last = globaltimer_ns();
-      while (jf < ntiles || jc < ncv) {
+      while (wf.j < ntiles || wc.j < ncv) {
         bool prog = false;
-        // F stream: F(jf) = Q K~^T into F buffer jf & 1
-        if (jf < ntiles) {
-          const int g = g0 + jf, bh = head_of(g);
-          const bool new_head = bh != bh_f;
-          const int kb = (new_head ? hi_f + 1 : hi_f) % p.nkw;
-          const bool ok = (!new_head || mbar_test(&bars.kw_full[kb], ((hi_f + 1) / p.nkw) & 1)) &&
-                          mbar_test(&bars.qfull[jf % p.nq], (jf / p.nq) & 1) &&
+        // F stream: F(j) = Q K~^T into F buffer j & 1
+        if (wf.j < ntiles) {
+          const int jf = wf.j;
+          const bool new_head = wf.first;
+          const bool ok = (!new_head || mbar_test(&bars.kw_full[rkf.i], rkf.ph)) &&
+                          mbar_test(&bars.qfull[rqf.i], rqf.ph) &&
                           (jf < 2 || mbar_test(&bars.pw_done[jf & 1], ((jf >> 1) - 1) & 1));
           if (ok) {
             if (new_head) {
-              bh_f = bh;
-              ++hi_f;
+              kcur = rkf.i;
+              rkf.next(p.nkw);
             }
             tc_fence_after_sync();
-            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_q + (jf % p.nq) * p.q_stage), 16, 1024, SW_128B);
-            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + kb * kw_bytes), 16, 1024, SW_128B);
+            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_q + rqf.i * p.q_stage), 16, 1024, SW_128B);
+            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + kcur * kw_bytes), 16, 1024, SW_128B);
             const uint32_t dcol = tmem + COL_F0 + (jf & 1) * p.m_pad;
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk)
               mma_bf16(dcol, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
                        b0 + (uint64_t)((kk >> 2) * (p.m_pad * 8) + (kk & 3) * 2), idf, kk > 0);
             mma_commit(&bars.f_full[jf & 1]);
-            mma_commit(&bars.qempty[jf % p.nq]);
-            ++jf;
+            mma_commit(&bars.qempty[rqf.i]);
+            rqf.next(p.nq);
+            wf.next(tph);
             prog = true;
           }
         }
-        // conv stream: CV(jc) = T V_halo into accumulator jc & 1 (does not
+        // conv stream: CV(j) = T V_halo into accumulator j & 1 (does not
         // wait for the softmax)
-        if (jc < ncv) {
-          const int g = g0 + jc, bh = head_of(g);
-          const bool new_head = bh != bh_c;
-          const int hin = new_head ? hi_c + 1 : hi_c;
-          const bool ok = (!new_head || mbar_test(&bars.t_ready[hin % p.nt], (hin / p.nt) & 1)) &&
-                          mbar_test(&bars.vfull[jc % kNV], (jc / kNV) & 1) &&
+        if (wc.j < ncv) {
+          const int jc = wc.j;
+          const bool new_head = wc.first;
+          const bool ok = (!new_head || mbar_test(&bars.t_ready[rtc.i], rtc.ph)) &&
+                          mbar_test(&bars.vfull[rvc.i], rvc.ph) &&
                           (jc < 2 || mbar_test(&bars.acc_empty[jc & 1], ((jc >> 1) - 1) & 1));
           if (ok) {
             if (new_head) {
-              bh_c = bh;
-              hi_c = hin;
+              tcur = rtc.i;
+              rtc.next(p.nt);
             }
             tc_fence_after_sync();
             const uint32_t acc = tmem + COL_ACC0 + (jc & 1) * ACC_W;
-            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + (hi_c % p.nt) * p.t_bytes), 16, 1024, SW_128B);
-            const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + (jc % kNV) * p.v_stage), p.kc * 128, 1024, SW_128B);
+            const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + tcur * p.t_bytes), 16, 1024, SW_128B);
+            const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + rvc.i * p.v_stage), p.kc * 128, 1024, SW_128B);
             for (int kk = 0; kk < p.kc / 16; ++kk)
               mma_bf16(acc + DP, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2), v0 + (uint64_t)(kk * 128), idc, kk > 0);
-            mma_commit(&bars.vempty[jc % kNV]);
+            mma_commit(&bars.vempty[rvc.i]);
             mma_commit(&bars.acc_full[jc & 1]);
-            if (jc + 1 == ntiles || head_of(g + 1) != bh) mma_commit(&bars.t_empty[hi_c % p.nt]);
-            ++jc;
+            if (wc.last(tph, ntiles)) mma_commit(&bars.t_empty[tcur]);
+            rvc.next(kNV);
+            wc.next(tph);
             prog = true;
           }
         }
@@ -317,33 +374,35 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
     // ---------------------------------------------- MMA issuer, PW stream
     if (lane == 0 && ntiles > 0) {
       const uint32_t idw = idesc_bf16(128, DP, false, false);
-      int jp = 0;
-      int hi_p = -1, bh_p = -1;
+      const int tph = p.tiles_per_head;
+      TileWalk wp;
+      wp.init(g0, tph);
+      Ring rkp;  // per-head W^T buffers
+      rkp.init();
+      int kcur = 0;
       uint64_t t_last = globaltimer_ns();
-      while (jp < ntiles) {
+      while (wp.j < ntiles) {
         bool prog = false;
-        // PW stream: PW(jp) = P W into accumulator jp & 1
+        // PW stream: PW(j) = P W into accumulator j & 1
         {
-          const int g = g0 + jp, bh = head_of(g);
-          const bool new_head = bh != bh_p;
-          const int hin = new_head ? hi_p + 1 : hi_p;
+          const int jp = wp.j;
           const bool ok = mbar_test(&bars.p_full[jp & 1], (jp >> 1) & 1) &&
                           (jp < 2 || mbar_test(&bars.acc_empty[jp & 1], ((jp >> 1) - 1) & 1));
           if (ok) {
-            if (new_head) {
-              bh_p = bh;
-              hi_p = hin;
+            if (wp.first) {
+              kcur = rkp.i;
+              rkp.next(p.nkw);
             }
             tc_fence_after_sync();
             const uint32_t acc = tmem + COL_ACC0 + (jp & 1) * ACC_W;
-            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + (hi_p % p.nkw) * kw_bytes + p.kt_bytes), 16, 1024, SW_128B);
+            const uint64_t b0 = smem_desc(smem_u32(sm + p.off_kt + kcur * kw_bytes + p.kt_bytes), 16, 1024, SW_128B);
             const uint32_t pcol = tmem + COL_F0 + (jp & 1) * p.m_pad;
             for (int kk = 0; kk < p.m_pad / 16; ++kk)
               mma_bf16_tA(acc, pcol + kk * 8, b0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
             mma_commit(&bars.acc_full[jp & 1]);
             mma_commit(&bars.pw_done[jp & 1]);
-            if (jp + 1 == ntiles || head_of(g + 1) != bh) mma_commit(&bars.kw_empty[hi_p % p.nkw]);
-            ++jp;
+            if (wp.last(tph, ntiles)) mma_commit(&bars.kw_empty[kcur]);
+            wp.next(tph);
             prog = true;
           }
         }
