@@ -5,12 +5,18 @@
 // ("Nyströmformer" review page, Proposed method, bullets 3 and 6).
 //
 // Shared memory holds K~ (m x d), W^T (d x m) and the conv's Toeplitz block
-// per head, plus ONE buffer shared by the Q tile and the V halo: V is loaded
-// into it once the F product has consumed Q, while the softmax runs. TMEM:
-// F/P (m columns), PW and CV accumulators (d columns each). One CTA of 128
-// threads walks a contiguous range of 128-token tiles; thread 0 issues TMA
-// and tcgen05, all threads run the softmax and the epilogue. Every wait is
-// bounded; a wait that runs out sets the status word and the CTA winds down.
+// per head, plus ONE buffer shared by the Q tile and the V halo. TMEM: F/P
+// (m columns), PW and CV accumulators (d columns each). One CTA per SM
+// walks a contiguous range of 128-token tiles with five warps:
+//   warp 4, one thread: TMA copies and tcgen05 products, in program order
+//     per tile j:  F(j) = Q K~^T (once P V of tile j-1 is done) -> V halo
+//     into the freed buffer -> CV(j) = T V (during the softmax of j) -> the
+//     next Q tile into the buffer CV(j) freed -> PW(j) = P W (after the
+//     softmax)
+//   warps 0-3: softmax of tile j (thread = token row, P over F in TMEM),
+//     then its epilogue out = PW / rowsum + CV, while F(j+1) is computed
+// Every wait is bounded; a wait that runs out sets the status word, both
+// roles wind down, copies in flight are awaited and TMEM is freed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -42,38 +48,54 @@ struct BigParams {
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int DP = 128, DC = 2;  // head width 128: two 64-column chunks
 constexpr size_t kSmemBudget = 227 * 1024 - 1024;
+constexpr int kThreads = 160;
 
-__device__ __forceinline__ bool ok_or_fail(bool ok, int* status, volatile int* abort_flag) {
-  if (!ok && !*abort_flag) {
+struct BigBars {
+  uint64_t kw, q, v;           // TMA: K~ / W^T, Q tile, V halo
+  uint64_t f, cv, pw;          // products done
+  uint64_t p, epi, t;          // softmax warps: P written, accumulators read, Toeplitz built
+  uint64_t fin;
+};
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, int* status,
+                                             volatile int* abort_flag) {
+  if (mbar_wait(bar, parity, abort_flag, kWaitNs)) return true;
+  if (!*abort_flag) {
     *abort_flag = 1;
     atomicExch(status, (int)NYS_ERR_TIMEOUT);
   }
-  return ok;
+  return false;
 }
 
-__global__ void __launch_bounds__(128, 1) tokens_big(const __grid_constant__ BigMaps maps,
-                                                     const BigParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant__ BigMaps maps,
+                                                          const __grid_constant__ BigParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* kts = sm + p.off_kt;
   uint8_t* wts = sm + p.off_wt;
   uint8_t* tbs = sm + p.off_t;
   uint8_t* qv = sm + p.off_qv;
-  __shared__ uint64_t bar_kw, bar_q, bar_v, bar_mma;
+  __shared__ BigBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rad = p.ks > 0 ? (p.ks - 1) / 2 : 0;
   const int g0 = blockIdx.x * p.tiles_per_cta;
-  const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
+  const int ntiles = min(p.total_tiles, g0 + p.tiles_per_cta) - g0;
+  const int tph = p.tiles_per_head;
 
   if (tid == 0) {
-    mbar_init(&bar_kw, 1);
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_v, 1);
-    mbar_init(&bar_mma, 1);
+    mbar_init(&bars.kw, 1);
+    mbar_init(&bars.q, 1);
+    mbar_init(&bars.v, 1);
+    mbar_init(&bars.f, 1);
+    mbar_init(&bars.cv, 1);
+    mbar_init(&bars.pw, 1);
+    mbar_init(&bars.p, 128);
+    mbar_init(&bars.epi, 128);
+    mbar_init(&bars.t, 128);
+    mbar_init(&bars.fin, 1);
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -84,24 +106,125 @@ __global__ void __launch_bounds__(128, 1) tokens_big(const __grid_constant__ Big
   const uint32_t tmem = tmem_base_sh;
   const uint32_t COL_F = 0, COL_PW = 256, COL_CV = 384;
 
-  uint32_t ph_kw = 0, ph_q = 0, ph_v = 0, ph_mma = 0;
-  bool kw_out = false, q_out = false, v_out = false;  // loads issued, not yet waited on
-  int cur_bh = -1, cur_h = -1;
-  for (int g = g0; g < g1; ++g) {
-    const int bh = g / p.tiles_per_head, t0 = (g % p.tiles_per_head) * 128, h = bh % p.H;
-    // (A) head change: K~, W^T by TMA; Toeplitz block by all threads
-    if (bh != cur_bh) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&bar_kw, p.kt_bytes + p.wt_bytes);
-        for (int dc = 0; dc < DC; ++dc)
-          tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bar_kw, dc * 64, 0, bh);
-        for (int mc = 0; mc * 64 < p.m_pad; ++mc)
-          tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bar_kw, mc * 64, 0, bh);
-        kw_out = true;
+  if (warp == 4) {
+    // ------------------------------------------------------------- control
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch(&maps.q);
+      tma_prefetch(&maps.v);
+      tma_prefetch(&maps.kt);
+      tma_prefetch(&maps.wt);
+      const uint32_t idf = idesc_bf16(128, p.m_pad, false, false);
+      const uint32_t idw = idesc_bf16(128, DP, false, false);
+      const uint32_t idc = idesc_bf16(128, DP, false, true);
+      uint32_t n_kw = 0, n_q = 0, n_v = 0, n_t = 0;  // copies issued / Toeplitz blocks awaited
+      int cur_bh = -1, cur_h = -1;
+      int bh = g0 / tph, t = g0 - (g0 / tph) * tph;  // head and tile within it
+      auto load_q = [&](int tile_bh, int tile_t) {
+        mbar_arrive_expect_tx(&bars.q, p.q_bytes);
+        for (int dc = 0; dc < DC; ++dc) tma_load_3d(qv + dc * 16384, &maps.q, &bars.q, dc * 64, tile_t * 128, tile_bh);
+        ++n_q;
+      };
+      load_q(bh, t);
+      for (int j = 0; j < ntiles; ++j) {
+        const int h = bh % p.H;
+        // F(j): the F region is free once P V of tile j-1 is done
+        if (j > 0 && !wait_or_fail(&bars.pw, (j - 1) & 1, p.status, abort_flag)) break;
+        if (bh != cur_bh) {
+          mbar_arrive_expect_tx(&bars.kw, p.kt_bytes + p.wt_bytes);
+          for (int dc = 0; dc < DC; ++dc)
+            tma_load_3d(kts + dc * (p.m_pad * 128), &maps.kt, &bars.kw, dc * 64, 0, bh);
+          for (int mc = 0; mc * 64 < p.m_pad; ++mc)
+            tma_load_3d(wts + mc * (DP * 128), &maps.wt, &bars.kw, mc * 64, 0, bh);
+          ++n_kw;
+          if (!wait_or_fail(&bars.kw, (n_kw - 1) & 1, p.status, abort_flag)) break;
+          cur_bh = bh;
+        }
+        if (!wait_or_fail(&bars.q, (n_q - 1) & 1, p.status, abort_flag)) break;
+        tc_fence_after_sync();
+        {
+          const uint64_t a0 = smem_desc(smem_u32(qv), 16, 1024, SW_128B);
+          const uint64_t b0 = smem_desc(smem_u32(kts), 16, 1024, SW_128B);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk)
+            mma_bf16(tmem + COL_F, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                     b0 + (uint64_t)((kk >> 2) * (p.m_pad * 8) + (kk & 3) * 2), idf, kk > 0);
+          mma_commit(&bars.f);
+        }
+        if (p.kc > 0) {
+          // V halo into the buffer F(j) has consumed
+          if (!wait_or_fail(&bars.f, j & 1, p.status, abort_flag)) break;
+          mbar_arrive_expect_tx(&bars.v, p.v_bytes);
+          for (int dc = 0; dc < DC; ++dc)
+            tma_load_3d(qv + dc * (p.kc * 128), &maps.v, &bars.v, dc * 64, t * 128 - rad, bh);
+          ++n_v;
+          // CV(j): V loaded, Toeplitz block of head h built, CV accumulator
+          // read by the epilogue of tile j-1
+          bool ok = wait_or_fail(&bars.v, (n_v - 1) & 1, p.status, abort_flag);
+          if (ok && h != cur_h) {
+            ++n_t;
+            ok = wait_or_fail(&bars.t, (n_t - 1) & 1, p.status, abort_flag);
+            cur_h = h;
+          }
+          if (ok && j > 0) ok = wait_or_fail(&bars.epi, (j - 1) & 1, p.status, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t a0 = smem_desc(smem_u32(tbs), 16, 1024, SW_128B);
+          const uint64_t v0 = smem_desc(smem_u32(qv), p.kc * 128, 1024, SW_128B);
+          for (int kk = 0; kk < p.kc / 16; ++kk)
+            mma_bf16(tmem + COL_CV, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                     v0 + (uint64_t)(kk * 128), idc, kk > 0);
+          mma_commit(&bars.cv);
+          // the next Q tile into the buffer CV(j) frees
+          if (j + 1 < ntiles) {
+            if (!wait_or_fail(&bars.cv, j & 1, p.status, abort_flag)) break;
+            load_q(t + 1 == tph ? bh + 1 : bh, t + 1 == tph ? 0 : t + 1);
+          }
+        } else {
+          if (j > 0 && !wait_or_fail(&bars.epi, (j - 1) & 1, p.status, abort_flag)) break;
+          if (j + 1 < ntiles) {
+            if (!wait_or_fail(&bars.f, j & 1, p.status, abort_flag)) break;
+            load_q(t + 1 == tph ? bh + 1 : bh, t + 1 == tph ? 0 : t + 1);
+          }
+        }
+        // PW(j) once the softmax has written P
+        if (!wait_or_fail(&bars.p, j & 1, p.status, abort_flag)) break;
+        tc_fence_after_sync();
+        {
+          const uint64_t w0 = smem_desc(smem_u32(wts), 16, 1024, SW_128B);
+          for (int kk = 0; kk < p.m_pad / 16; ++kk)
+            mma_bf16_tA(tmem + COL_PW, tmem + COL_F + kk * 8,
+                        w0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
+          mma_commit(&bars.pw);
+        }
+        if (++t == tph) {
+          t = 0;
+          ++bh;
+        }
       }
+      if (*abort_flag) {
+        // wait (bounded) for the copies still in flight
+        if (n_kw) mbar_wait(&bars.kw, (n_kw - 1) & 1, nullptr, kWaitNs);
+        if (n_q) mbar_wait(&bars.q, (n_q - 1) & 1, nullptr, kWaitNs);
+        if (n_v) mbar_wait(&bars.v, (n_v - 1) & 1, nullptr, kWaitNs);
+      }
+      // no product of this CTA may be in flight when TMEM is freed
+      mma_commit(&bars.fin);
+      mbar_wait(&bars.fin, 0, nullptr, kWaitNs);
+    }
+  } else {
+    // ---------------------------------------- softmax and epilogue, warps 0-3
+    const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t fcol = tmem + lo + COL_F;
+    const bool full_m = p.m == p.m_pad && (p.m_pad & 63) == 0;
+    int bh = g0 / tph, t = g0 - (g0 / tph) * tph, cur_h = -1;
+    const int kc64 = (p.kc + 63) & ~63;
+    for (int j = 0; j < ntiles; ++j) {
+      const int h = bh % p.H;
       if (p.kc > 0 && h != cur_h) {
+        // Toeplitz block of head h: row tid, column u holds w[u - tid]. Its
+        // previous reader, CV(j-1), completed before PW(j-1), which the
+        // epilogue of tile j-1 waited for.
         const float* wh = p.conv_w + (size_t)h * p.ks;
-        const int kc64 = (p.kc + 63) & ~63;
         for (int u0 = 0; u0 < kc64; u0 += 8) {
           uint32_t wv[4];
 #pragma unroll
@@ -115,136 +238,86 @@ __global__ void __launch_bounds__(128, 1) tokens_big(const __grid_constant__ Big
               make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         fence_async_smem();
+        mbar_arrive(&bars.t);
         cur_h = h;
       }
-      if (tid == 0 && ok_or_fail(mbar_wait(&bar_kw, ph_kw, abort_flag, kWaitNs), p.status, abort_flag))
-        kw_out = false;
-      ph_kw ^= 1;
-      cur_bh = bh;
-      __syncthreads();
-      if (*abort_flag) break;
-    }
-    // (B) Q tile -> F = Q K~^T
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_q, p.q_bytes);
-      for (int dc = 0; dc < DC; ++dc) tma_load_3d(qv + dc * 16384, &maps.q, &bar_q, dc * 64, t0, bh);
-      q_out = true;
-      if (ok_or_fail(mbar_wait(&bar_q, ph_q, abort_flag, kWaitNs), p.status, abort_flag)) {
-        q_out = false;
-        tc_fence_after_sync();
-        const uint64_t a0 = smem_desc(smem_u32(qv), 16, 1024, SW_128B);
-        const uint64_t b0 = smem_desc(smem_u32(kts), 16, 1024, SW_128B);
-        const uint32_t id = idesc_bf16(128, p.m_pad, false, false);
-#pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk)
-          mma_bf16(tmem + COL_F, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
-                   b0 + (uint64_t)((kk >> 2) * (p.m_pad * 8) + (kk & 3) * 2), id, kk > 0);
-        mma_commit(&bar_mma);
-      }
-    }
-    ph_q ^= 1;
-    ok_or_fail(mbar_wait(&bar_mma, ph_mma, abort_flag, kWaitNs), p.status, abort_flag);
-    ph_mma ^= 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-    // (C) V halo into the freed buffer while the softmax runs
-    if (tid == 0 && p.kc > 0) {
-      mbar_arrive_expect_tx(&bar_v, p.v_bytes);
-      for (int dc = 0; dc < DC; ++dc)
-        tma_load_3d(qv + dc * (p.kc * 128), &maps.v, &bar_v, dc * 64, t0 - rad, bh);
-      v_out = true;
-    }
-    float mx = -INFINITY;
-    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + COL_F + c0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
-    }
-    const float mc = mx * p.c;
-    float l = 0.f;
-    for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lo + COL_F + c0, r);
-      tmem_ld_wait();
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float a = (c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
-        const float b = (c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
-        l += a + b;
-        pk[e] = pack_bf16x2(a, b);
-      }
-      tmem_st16(tmem + lo + COL_F + (c0 >> 1), pk);
-    }
-    tmem_st_wait();
-    tc_fence_before_sync();
-    __syncthreads();
-    // (D) PW = P W ; CV = T V_halo
-    if (tid == 0) {
+      // softmax of F(j): P (bf16) over F
+      if (!__all_sync(0xffffffffu, wait_or_fail(&bars.f, j & 1, p.status, abort_flag))) break;
       tc_fence_after_sync();
-      const uint64_t w0 = smem_desc(smem_u32(wts), 16, 1024, SW_128B);
-      const uint32_t idw = idesc_bf16(128, DP, false, false);
-      for (int kk = 0; kk < p.m_pad / 16; ++kk)
-        mma_bf16_tA(tmem + COL_PW, tmem + COL_F + kk * 8,
-                    w0 + (uint64_t)((kk >> 2) * (DP * 8) + (kk & 3) * 2), idw, kk > 0);
-      if (p.kc > 0) {
-        if (ok_or_fail(mbar_wait(&bar_v, ph_v, abort_flag, kWaitNs), p.status, abort_flag)) {
-          v_out = false;
-          tc_fence_after_sync();
-          const uint64_t a0 = smem_desc(smem_u32(tbs), 16, 1024, SW_128B);
-          const uint64_t v0 = smem_desc(smem_u32(qv), p.kc * 128, 1024, SW_128B);
-          const uint32_t idc = idesc_bf16(128, DP, false, true);
-          for (int kk = 0; kk < p.kc / 16; ++kk)
-            mma_bf16(tmem + COL_CV, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
-                     v0 + (uint64_t)(kk * 128), idc, kk > 0);
+      float mx = -INFINITY, l = 0.f;
+      if (full_m) {
+        for (int c0 = 0; c0 < p.m_pad; c0 += 64) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(fcol + c0, r0);
+          tmem_ld32(fcol + c0 + 32, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx = fmaxf(mx, fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])));
+        }
+      } else {
+        for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(fcol + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + e < p.m) mx = fmaxf(mx, __uint_as_float(r[e]));
         }
       }
-      mma_commit(&bar_mma);
-    }
-    if (p.kc > 0) ph_v ^= 1;
-    ok_or_fail(mbar_wait(&bar_mma, ph_mma, abort_flag, kWaitNs), p.status, abort_flag);
-    ph_mma ^= 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-    // (E) out = PW / l + CV
-    const int t = t0 + tid;
-    const float inv_l = 1.f / l;
-    __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + t) * p.d;
-#pragma unroll
-    for (int c0 = 0; c0 < DP; c0 += 32) {
-      uint32_t a[32], b[32];
-      tmem_ld32(tmem + lo + COL_PW + c0, a);
-      if (p.kc > 0) tmem_ld32(tmem + lo + COL_CV + c0, b);
-      tmem_ld_wait();
-      if (t < p.n && c0 < p.d) {
-        uint32_t o[16];
+      const float mc = mx * p.c;
+      for (int c0 = 0; c0 < p.m_pad; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(fcol + c0, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
-          if (p.kc > 0) {
-            x0 += __uint_as_float(b[2 * e]);
-            x1 += __uint_as_float(b[2 * e + 1]);
-          }
-          o[e] = pack_bf16x2(x0, x1);
+          const float a = (full_m || c0 + 2 * e < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
+          const float b = (full_m || c0 + 2 * e + 1 < p.m) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
+          l += a + b;
+          pk[e] = pack_bf16x2(a, b);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        tmem_st16(fcol + (c0 >> 1), pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.p);
+      // epilogue: out = PW / l + CV once PW(j) (and CV(j) before it) is done
+      if (!__all_sync(0xffffffffu, wait_or_fail(&bars.pw, j & 1, p.status, abort_flag))) break;
+      tc_fence_after_sync();
+      const int tok = t * 128 + tid;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + tok) * p.d;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+      for (int c0 = 0; c0 < DP; c0 += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lo + COL_PW + c0, a);
+        if (p.kc > 0) tmem_ld32(tmem + lo + COL_CV + c0, b);
+        tmem_ld_wait();
+        if (tok < p.n) {
+          uint32_t o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
+            if (p.kc > 0) {
+              x0 += __uint_as_float(b[2 * e]);
+              x1 += __uint_as_float(b[2 * e + 1]);
+            }
+            o[e] = pack_bf16x2(x0, x1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&bars.epi);
+      if (++t == tph) {
+        t = 0;
+        ++bh;
       }
     }
-    tc_fence_before_sync();
-    __syncthreads();
-  }
-  if (tid == 0 && *abort_flag) {
-    // wait (bounded) for copies still in flight
-    if (kw_out) mbar_wait(&bar_kw, ph_kw ^ 1, nullptr, kWaitNs);
-    if (q_out) mbar_wait(&bar_q, ph_q ^ 1, nullptr, kWaitNs);
-    if (v_out) mbar_wait(&bar_v, ph_v ^ 1, nullptr, kWaitNs);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -343,7 +416,7 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
       cudaSuccess)
     return NYS_ERR_CUDA;
   KernelScope scope("tokens_big", stream);
-  tokens_big<<<grid, 128, pl.smem, stream>>>(maps, p);
+  tokens_big<<<grid, kThreads, pl.smem, stream>>>(maps, p);
   return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
 }
 
