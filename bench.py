@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="c2", choices=workloads.ORDER,
                    help="workload (default c2: B=32 H=12 n=512 d=64 m=64, bf16)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's batch size B (smaller cases for profiler captures)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -490,6 +492,9 @@ def run_ours(args, wl):
 def main():
     args = parse_args()
     wl = workloads.WORKLOADS[args.config]
+    if args.batch is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, B=args.batch)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
