@@ -256,19 +256,27 @@ def kernel_source_hash(kernel):
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def measured_traffic(kernel, workload):
+def measured_traffic(kernel, wl):
     """DRAM bytes per launch from profiles/dram_traffic.txt (written from an ncu
-    capture), only if the kernel's source is unchanged since the capture."""
+    capture), only if the kernel's source is unchanged since the capture. A
+    workload captured at a smaller batch (entry "<name>b<B>") is scaled to
+    this batch: every kernel streams each head once, so its bytes grow with
+    the number of heads."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     h = kernel_source_hash(kernel)
+    scaled = None
     for line in open(path):
         parts = line.split()
-        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and \
-                parts[1] == workload and parts[2] == h:
+        if len(parts) != 4 or line.startswith("#") or parts[0] != kernel or parts[2] != h:
+            continue
+        if parts[1] == wl.name:
             return float(parts[3])
-    return None
+        tag = parts[1]
+        if tag.startswith(wl.name + "b") and tag[len(wl.name) + 1:].isdigit():
+            scaled = float(parts[3]) * wl.B / int(tag[len(wl.name) + 1:])
+    return scaled
 
 
 def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
@@ -277,7 +285,7 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
     that many head groups), so one launch covers 1/per_step of the work."""
     t_launch = ms / launches / 1e3
     te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes / per_step
-    traffic = measured_traffic(kernel, wl.name)
+    traffic = measured_traffic(kernel, wl)
     if kernel in KERNEL_BYTES:
         achieved = KERNEL_BYTES[kernel] * te / t_launch / 1e9
         return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
