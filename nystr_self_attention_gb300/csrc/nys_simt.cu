@@ -183,13 +183,24 @@ landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restr
       continue;
     }
     if (lane < vpr) {
+      // V consecutive means as 16-byte stores (rows are d >= 8 elements,
+      // lane * V elements in: 16-byte aligned)
       float* out = outf + (size_t)i * d + lane * V;
 #pragma unroll
-      for (int e = 0; e < V; ++e) out[e] = acc[e] * inv;
+      for (int e = 0; e < V; e += 4)
+        *reinterpret_cast<float4*>(out + e) =
+            make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
       if (outb) {
         __nv_bfloat16* ob = outb + ((size_t)bh * m64 + i) * dpad + lane * V;
+        if constexpr (V == 8) {
+          __nv_bfloat162 h2[4];
 #pragma unroll
-        for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+          for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+          *reinterpret_cast<uint4*>(ob) = *reinterpret_cast<const uint4*>(h2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+        }
       }
     }
     if (outb)
