@@ -446,9 +446,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok) mma_commit(&done);
       }
       __syncwarp();
-    } else if (wait_done()) {
+    } else {
       // epilogue: thread = row gi of the product block
-      if (is_w) {
+      const bool ok_epi = __all_sync(0xffffffffu, wait_done());  // warp-uniform: TMEM loads are warp-wide
+      if (is_w && ok_epi) {
         float* wrow = p.w + ((size_t)bh * m + (rv ? gi : 0)) * d + c * hw;
         __nv_bfloat16* wt = p.wt + (size_t)bh * p.dpad * p.m64;
         for (int j0 = 0; j0 < hw; j0 += 16) {
@@ -470,39 +471,54 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (c == 1 && gi < p.m64)
           for (int j = d; j < p.dpad; ++j) wt[(size_t)j * p.m64 + gi] = __float2bfloat16_rn(0.f);
-      } else {
+      } else if (!is_w) {
         // st 0: X -> other Z buffer (row-major), 7I - X -> ta (transposed)
         // st 1: 15I - Y -> tb (transposed);  st 2: 13I - Y -> ta (transposed)
         // st 3: Z' = Y / 4 -> other Z buffer (row-major) and zt (transposed)
-        float* zother = (zc ? p.z0 : p.z1) + bh * mm;
-        float* rm_dst = (st == 0 || st == 3) ? zother : nullptr;
-        float* tr_dst = (st == 0 || st == 2) ? p.ta + bh * mm : (st == 1 ? p.tb + bh * mm : p.zt + bh * mm);
+        // Both blocks are staged in the (now idle) operand ring as four
+        // SWIZZLE_128B boxes of [128 rows x 32 columns] and leave by TMA
+        // stores; the store clips what lies beyond m.
+        const int rm_map = (st == 0 || st == 3) ? (zc ? MAP_Z0 : MAP_Z1) : -1;
+        const int tr_map = (st == 0 || st == 2) ? MAP_TA : (st == 1 ? MAP_TB : MAP_ZT);
         const float diag = st == 0 ? 7.f : (st == 1 ? 15.f : (st == 2 ? 13.f : 0.f));
         const float sign = st == 3 ? 1.f : -1.f;
         const float sc = st == 3 ? 0.25f : 1.f;
-        for (int j0 = 0; j0 < 128; j0 += 32) {
+        uint8_t* rm_stage = sm;          // box b: block columns [32 b, 32 b + 32), row = tid
+        uint8_t* tr_stage = sm + 65536;  // box b = warp: block rows [32 b, ..) as columns
+        for (int j0 = 0; ok_epi && j0 < 128; j0 += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + lo + j0, v);
           tmem_ld_wait();
-          if (rv) {
-            float x[32];
+          float x[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = sc * __uint_as_float(v[e]);
-            if (rm_dst) {
+          for (int e = 0; e < 32; ++e) x[e] = sc * __uint_as_float(v[e]);
+          if (rm_map >= 0) {
+            uint8_t* box = rm_stage + (j0 >> 5) * 16384;
 #pragma unroll
-              for (int e = 0; e < 32; e += 4) {
-                const int gj = 128 * c + j0 + e;
-                if (gj < m)
-                  *reinterpret_cast<float4*>(rm_dst + (size_t)gi * m + gj) =
-                      make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int gj = 128 * c + j0 + e;
-              if (gj < m) tr_dst[(size_t)gj * m + gi] = fmaf(sign, x[e], gj == gi ? diag : 0.f);
-            }
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(box + sw128_offset(tid, q4 * 16)) =
+                  make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
           }
+          uint8_t* tbox = tr_stage + warp * 16384;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int gj = 128 * c + j0 + e;
+            *reinterpret_cast<float*>(tbox + sw128_offset(j0 + e, lane * 4)) =
+                fmaf(sign, x[e], gj == gi ? diag : 0.f);
+          }
+        }
+        fence_async_smem();
+        // the four epilogue warps, all of them whatever their wait gave (a
+        // wait that ran out has set the abort flag: no store then)
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (tid == 0 && !*abort_flag) {
+          if (rm_map >= 0)
+            for (int b = 0; b < 4; ++b)
+              tma_store_3d(&maps.m[rm_map], rm_stage + b * 16384, 128 * c + 32 * b, 128 * r, bh);
+          for (int b = 0; b < 4; ++b)
+            tma_store_3d(&maps.m[tr_map], tr_stage + b * 16384, 128 * r + 32 * b, 128 * c, bh);
+          bulk_commit();
+          bulk_wait0();  // written before the cluster barrier publishes them
         }
       }
     }
