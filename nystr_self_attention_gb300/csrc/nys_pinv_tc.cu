@@ -336,14 +336,6 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     }
     red_cs[half][row] = (c4[0] + c4[1]) + (c4[2] + c4[3]);
   }
-  // stage export of A_S: coalesced copy of the abuf rows, a warp per row
-  for (int r = warp; r < hp * m; r += kThreads / 32) {
-    const int h2 = r / m, i = r - h2 * m;
-    const int bh2 = (int)blockIdx.x * hp + h2;
-    if (bh2 >= p.BH) break;
-    float* a_out = p.a_s + ((size_t)bh2 * m + i) * m;
-    for (int j = lane; j < m; j += 32) a_out[j] = ld_elem(abuf, 128, h2 * MP + i, j);
-  }
   __syncthreads();
   // per lane quarter: largest row abs-sum and largest column abs-sum
   if (half == 0) {
@@ -396,12 +388,27 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   __syncthreads();
 
   // ---- 4) the iteration
+  // Stage export of A_S (abuf is constant from here on): eight rows per call,
+  // a warp per row, coalesced. It runs while thread 0 issues a product's
+  // MMAs, when the other threads would only wait.
+  int exp_row = 0;
+  auto export_rows = [&]() {
+    const int r = exp_row + warp;
+    exp_row += kThreads / 32;
+    if (r >= hp * m) return;
+    const int h2 = r / m, i = r - h2 * m;
+    const int bh2 = (int)blockIdx.x * hp + h2;
+    if (bh2 >= p.BH) return;
+    float* a_out = p.a_s + ((size_t)bh2 * m + i) * m;
+    for (int j = lane; j < m; j += 32) a_out[j] = ld_elem(abuf, 128, h2 * MP + i, j);
+  };
   auto gemm = [&](uint32_t a_col, const uint8_t* a_smem) {
     if (tid == 0) {
       tc_fence_after_sync();
       issue(COL_D, a_col, a_smem, bbuf, NP, MP, false);
       mma_commit(&bar_mma);
     }
+    if (exp_row < hp * m) export_rows();
     wait_mma();
   };
   // epilogue: the head's block of this row of D -> sign * scale * D + diag
@@ -445,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     if (*abort_flag) break;
     store_bt(0.f, 1.f, 0.25f, (int)COL_Z);  // Z <- Y / 4 ; B <- Z by columns
   }
+  while (exp_row < hp * m) export_rows();  // what the products did not cover
   // ---- 5) W = Z G (head slot hs in columns hs d ..)
   if (!*abort_flag) {
     if (tid == 0) {
