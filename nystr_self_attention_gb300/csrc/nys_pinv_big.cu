@@ -145,39 +145,65 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   // ---- 1) G = merge of the key-split partials: rows of this row block,
-  // columns [c d/2, (c+1) d/2). G -> g (row-major), G^T -> gt.
+  // columns [c d/2, (c+1) d/2). G -> g (row-major), G^T -> gt. One pass
+  // over the splits per 16-column chunk, four splits at a time with all
+  // their loads in flight; a running (max, denominator) rescales the
+  // accumulated row as in an online softmax, and an empty partial (max =
+  // -inf, rows never written) contributes nothing.
   if (rv) {
     const int hw = d >> 1, c0 = c * hw;
-    float gm = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp)
-      gm = fmaxf(gm, p.gml[(((size_t)bh * p.splits + sp) * m + gi) * 2]);
-    float den = 0.f;
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
-      if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial
-      den += p.gml[prow * 2 + 1] * expf(p.gml[prow * 2] - gm);
-    }
-    const float inv = 1.f / den;
     float* grow = p.g + ((size_t)bh * m + gi) * d;
     float* gtb = p.gt + (size_t)bh * d * m;
+    const float2* ml_base = reinterpret_cast<const float2*>(p.gml) + (size_t)bh * p.splits * m + gi;
+    const float* gp_base = p.gpart + ((size_t)bh * p.splits * m + gi) * d;
     for (int j0 = c0; j0 < c0 + hw; j0 += 16) {
       float acc[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-      for (int sp = 0; sp < p.splits; ++sp) {
-        const size_t prow = ((size_t)bh * p.splits + sp) * m + gi;
-        if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
-        const float f = expf(p.gml[prow * 2] - gm);
-        const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + j0);
+      float gm = -INFINITY, den = 0.f;
+      for (int sp = 0; sp < p.splits; sp += 4) {
+        float2 ml[4];
+        float4 v[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 v = src[e];
-          acc[4 * e] += v.x * f;
-          acc[4 * e + 1] += v.y * f;
-          acc[4 * e + 2] += v.z * f;
-          acc[4 * e + 3] += v.w * f;
+        for (int k = 0; k < 4; ++k) {
+          const int spk = sp + k < p.splits ? sp + k : sp;
+          ml[k] = __ldg(ml_base + (size_t)spk * m);
+          const float4* src = reinterpret_cast<const float4*>(gp_base + (size_t)spk * m * d + j0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[k][e] = __ldg(src + e);
         }
+        bool ok[4];
+        float cm = gm;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ok[k] = sp + k < p.splits && ml[k].x != -INFINITY;
+          if (ok[k]) cm = fmaxf(cm, ml[k].x);
+        }
+        if (cm == -INFINITY) continue;  // nothing yet
+        const float r = gm == -INFINITY ? 0.f : expf(gm - cm);
+        float f[4];
+        den *= r;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[k] = ok[k] ? expf(ml[k].x - cm) : 0.f;
+          den += ok[k] ? ml[k].y * f[k] : 0.f;
+        }
+        gm = cm;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] *= r;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (ok[k]) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[4 * e] = fmaf(v[k][e].x, f[k], acc[4 * e]);
+              acc[4 * e + 1] = fmaf(v[k][e].y, f[k], acc[4 * e + 1]);
+              acc[4 * e + 2] = fmaf(v[k][e].z, f[k], acc[4 * e + 2]);
+              acc[4 * e + 3] = fmaf(v[k][e].w, f[k], acc[4 * e + 3]);
+            }
+          }
       }
+      const float inv = 1.f / den;
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] *= inv;
       float4* go = reinterpret_cast<float4*>(grow + j0);
@@ -203,19 +229,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < nch; ++cc) {
           uint8_t* slot = sm + cc * 65536;
           const int col0 = (ch0 + cc) * 32;
+          // all 16 loads in flight before the first shared-memory store
+          float4 q4[8], k4[8];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 q4 = qv_ok ? *reinterpret_cast<const float4*>(qrow + col0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 k4 = kv_ok ? *reinterpret_cast<const float4*>(krow + col0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 qh = make_float4(tf32_hi(q4.x), tf32_hi(q4.y), tf32_hi(q4.z), tf32_hi(q4.w));
-            const float4 kh = make_float4(tf32_hi(k4.x), tf32_hi(k4.y), tf32_hi(k4.z), tf32_hi(k4.w));
-            const uint32_t off = sw128_offset(tid, e * 4);
+          for (int e = 0; e < 8; ++e) {
+            q4[e] = qv_ok ? __ldg(reinterpret_cast<const float4*>(qrow + col0) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            k4[e] = kv_ok ? __ldg(reinterpret_cast<const float4*>(krow + col0) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 qh = make_float4(tf32_hi(q4[e].x), tf32_hi(q4[e].y), tf32_hi(q4[e].z), tf32_hi(q4[e].w));
+            const float4 kh = make_float4(tf32_hi(k4[e].x), tf32_hi(k4[e].y), tf32_hi(k4[e].z), tf32_hi(k4[e].w));
+            const uint32_t off = sw128_offset(tid, e * 16);
             *reinterpret_cast<float4*>(slot + off) = qh;
             *reinterpret_cast<float4*>(slot + 16384 + off) =
-                make_float4(q4.x - qh.x, q4.y - qh.y, q4.z - qh.z, q4.w - qh.w);
+                make_float4(q4[e].x - qh.x, q4[e].y - qh.y, q4[e].z - qh.z, q4[e].w - qh.w);
             *reinterpret_cast<float4*>(slot + 32768 + off) = kh;
             *reinterpret_cast<float4*>(slot + 49152 + off) =
-                make_float4(k4.x - kh.x, k4.y - kh.y, k4.z - kh.z, k4.w - kh.w);
+                make_float4(k4[e].x - kh.x, k4[e].y - kh.y, k4[e].z - kh.z, k4[e].w - kh.w);
           }
         }
         fence_async_smem();

@@ -174,52 +174,51 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
 
   // ---- 1) G = merge of the key-split partials (row li of head bh); G^T
   // into gbuf (B of W = Z G, head slot hs at rows hs d ..). First, so that
-  // its loads do not wait behind the score steps.
+  // its loads do not wait behind the score steps. One pass over the splits,
+  // two at a time with all their loads in flight: a running (max,
+  // denominator) rescales the accumulated rows as in an online softmax; an
+  // empty partial (max = -inf, rows never written) contributes nothing.
   {
-    // running (max, denominator) over the partials' (max, sum) pairs, eight
-    // pairs loaded at a time; empty partials (max = -inf) are skipped
-    float gm = -INFINITY, den = 0.f;
-    if (live)
-      for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
-        float2 ml[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          ml[k] = sp0 + k < p.splits
-                      ? *reinterpret_cast<const float2*>(p.gml + (((size_t)bh * p.splits + sp0 + k) * m + li) * 2)
-                      : make_float2(-INFINITY, 0.f);
-        float cm = gm;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) cm = fmaxf(cm, ml[k].x);
-        if (cm != -INFINITY) {
-          den = gm == -INFINITY ? 0.f : den * expf(gm - cm);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (ml[k].x != -INFINITY) den += ml[k].y * expf(ml[k].x - cm);
-          gm = cm;
-        }
-      }
-    const float inv = live ? 1.f / den : 0.f;
     float* grow_out = p.g + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
     for (int c0 = half * 32; c0 < d; c0 += 64) {
       float acc[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) acc[e] = 0.f;
       if (live) {
-#pragma unroll 2
-        for (int sp = 0; sp < p.splits; ++sp) {
-          const size_t prow = ((size_t)bh * p.splits + sp) * m + li;
-          if (p.gml[prow * 2] == -INFINITY) continue;  // empty partial: O never written
-          const float f = expf(p.gml[prow * 2] - gm);
-          const float4* src = reinterpret_cast<const float4*>(p.gpart + prow * d + c0);
+        float gm = -INFINITY, den = 0.f;
+        for (int sp = 0; sp < p.splits; sp += 2) {
+          const bool two = sp + 1 < p.splits;
+          const size_t pr0 = ((size_t)bh * p.splits + sp) * m + li;
+          const size_t pr1 = two ? pr0 + (size_t)m : pr0;
+          const float2 ml0 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr0);
+          const float2 ml1 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr1);
+          const float4* s0 = reinterpret_cast<const float4*>(p.gpart + pr0 * d + c0);
+          const float4* s1 = reinterpret_cast<const float4*>(p.gpart + pr1 * d + c0);
+          float4 v0[8], v1[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float4 v = src[e];
-            acc[4 * e] += v.x * f;
-            acc[4 * e + 1] += v.y * f;
-            acc[4 * e + 2] += v.z * f;
-            acc[4 * e + 3] += v.w * f;
+            v0[e] = __ldg(s0 + e);
+            v1[e] = __ldg(s1 + e);
+          }
+          const bool ok0 = ml0.x != -INFINITY, ok1 = two && ml1.x != -INFINITY;
+          const float cm = fmaxf(gm, fmaxf(ok0 ? ml0.x : -INFINITY, ok1 ? ml1.x : -INFINITY));
+          if (cm == -INFINITY) continue;  // nothing yet
+          const float r = gm == -INFINITY ? 0.f : expf(gm - cm);
+          const float f0 = ok0 ? expf(ml0.x - cm) : 0.f;
+          const float f1 = ok1 ? expf(ml1.x - cm) : 0.f;
+          den = den * r + (ok0 ? ml0.y * f0 : 0.f) + (ok1 ? ml1.y * f1 : 0.f);
+          gm = cm;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 a0 = ok0 ? v0[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 a1 = ok1 ? v1[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[4 * e] = fmaf(acc[4 * e], r, fmaf(a0.x, f0, a1.x * f1));
+            acc[4 * e + 1] = fmaf(acc[4 * e + 1], r, fmaf(a0.y, f0, a1.y * f1));
+            acc[4 * e + 2] = fmaf(acc[4 * e + 2], r, fmaf(a0.z, f0, a1.z * f1));
+            acc[4 * e + 3] = fmaf(acc[4 * e + 3], r, fmaf(a0.w, f0, a1.w * f1));
           }
         }
+        const float inv = 1.f / den;
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] *= inv;
         float4* go = reinterpret_cast<float4*>(grow_out + c0);
@@ -236,23 +235,31 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     const float* qrow = p.qt + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
     const float* krow = p.kt + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
     for (int c0 = half * 32; c0 < d; c0 += 64) {
+      // all 16 loads in flight before the first shared-memory store
+      float4 kv[8], qv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        kv[e] = live ? __ldg(reinterpret_cast<const float4*>(krow + c0) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[e] = live ? __ldg(reinterpret_cast<const float4*>(qrow + c0) + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (in_np) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 kh = make_float4(tf32_hi(kv[e].x), tf32_hi(kv[e].y), tf32_hi(kv[e].z), tf32_hi(kv[e].w));
+          store_row4(khi, NP, row, c0 + 4 * e, kh);
+          store_row4(klo, NP, row, c0 + 4 * e,
+                     make_float4(kv[e].x - kh.x, kv[e].y - kh.y, kv[e].z - kh.z, kv[e].w - kh.w));
+        }
+      }
       uint32_t qh[32], ql[32];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 kv = live ? *reinterpret_cast<const float4*>(krow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 qv = live ? *reinterpret_cast<const float4*>(qrow + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 kh = make_float4(tf32_hi(kv.x), tf32_hi(kv.y), tf32_hi(kv.z), tf32_hi(kv.w));
-        const float4 kl = make_float4(kv.x - kh.x, kv.y - kh.y, kv.z - kh.z, kv.w - kh.w);
-        if (in_np) {
-          store_row4(khi, NP, row, c0 + e, kh);
-          store_row4(klo, NP, row, c0 + e, kl);
-        }
-        const float q4[4] = {qv.x, qv.y, qv.z, qv.w};
+      for (int e = 0; e < 8; ++e) {
+        const float q4[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float hh = tf32_hi(q4[t]);
-          qh[e + t] = __float_as_uint(hh);
-          ql[e + t] = __float_as_uint(q4[t] - hh);
+          qh[4 * e + t] = __float_as_uint(hh);
+          ql[4 * e + t] = __float_as_uint(q4[t] - hh);
         }
       }
       tmem_st32(tmem + lo + COL_QH + c0, qh);
