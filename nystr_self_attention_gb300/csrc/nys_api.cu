@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -22,6 +23,19 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int set_cuda_error(cudaError_t e) {
   g_last_error = cudaGetErrorString(e);
+  return NYS_ERR_CUDA;
+}
+
+int error_in(const char* step, int rc) {
+  if (rc == NYS_ERR_CUDA) g_last_error = std::string(step) + ": " + g_last_error;
+  return rc;
+}
+
+int tensor_map_error(const char* file, int line) {
+  char msg[160];
+  const char* base = std::strrchr(file, '/');
+  std::snprintf(msg, sizeof msg, "tensor map encoding failed (%s:%d)", base ? base + 1 : file, line);
+  g_last_error = msg;
   return NYS_ERR_CUDA;
 }
 
@@ -131,7 +145,6 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
   cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
   if (e != cudaSuccess) return set_cuda_error(e);
   const int rc = launch_forward(s, q, k, v, conv_w, out, ws, L, stream, dev);
-  if (rc == NYS_ERR_CUDA) g_last_error = cudaGetErrorString(cudaGetLastError());
   return rc;
 }
 
@@ -145,7 +158,7 @@ Layout make_layout(const Shape& s) {
   // path: whole 128-key tiles).
   L.tiles_per_split = 0;
   if (s.dtype == NYS_BF16) {
-    rows_tc_split(s, &L.splits, &L.tiles_per_split);
+    rows_tc_split(s, rows_tc_ctas(s), &L.splits, &L.tiles_per_split);
   } else {
     const long long rb = (s.m + 7) / 8;
     long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);

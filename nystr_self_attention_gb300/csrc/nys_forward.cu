@@ -9,6 +9,13 @@
 // stream lets one group's pseudo-inverse overlap the other groups' streaming
 // steps. The groups share the workspace arrays (each at its own head
 // offset), so the workspace layout does not depend on the grouping.
+//
+// Where the batch stays in one group and the tensor-core pseudo-inverse
+// needs at most half of the SMs (few heads, long sequences), its chain of
+// products runs on a second stream beside the landmark-row pass instead of
+// after it: Z depends only on the landmarks. The landmark-row pass is then
+// spread over the SMs the pseudo-inverse leaves free, and W = Z G is formed
+// by a short kernel once both are done.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -25,6 +32,7 @@ constexpr int kMaxGroups = 8;
 
 struct DeviceStreams {
   std::mutex mu;
+  std::mutex enqueue;  // one multi-stream enqueue at a time (shared events)
   bool ready = false;
   cudaStream_t aux[kMaxGroups] = {};
   cudaEvent_t fork = nullptr;
@@ -63,13 +71,17 @@ int choose_groups(const Shape& s) {
   return g;
 }
 
+// SM count the plan assumes (GB300); the layout must not depend on the
+// device a workspace size is asked for on.
+constexpr int kPlanSms = 152;
+
 template <typename T>
 T* at(char* ws, size_t off) { return reinterpret_cast<T*>(ws + off); }
 
 // The four steps for heads [bh0, bh0 + sg.bh()) of the full problem.
 int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, const void* k,
               const void* v, const float* conv_w, void* out, char* ws, const Layout& L,
-              cudaStream_t st) {
+              cudaStream_t st, DeviceStreams* beside) {
   const size_t esz = full.dtype == NYS_FP32 ? 4 : 2;
   const size_t tok = (size_t)bh0 * full.n * full.d * esz;
   const void* qg = static_cast<const char*>(q) + tok;
@@ -97,32 +109,65 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
   __nv_bfloat16* wt_b = bf16 ? at<__nv_bfloat16>(ws, L.wt_bf16) + bh0 * pad : nullptr;
 
   int rc = launch_landmarks(sg, qg, kg, qt, kt, qt_b, kt_b, st);
-  if (rc != NYS_OK) return rc;
+  if (rc != NYS_OK) return error_in("landmarks", rc);
+  if (beside) {  // Z on the second stream while the landmark rows stream K, V
+    cudaStream_t aux = beside->aux[1];
+    cudaError_t e = cudaEventRecord(beside->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, beside->fork, 0);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    rc = launch_rows_tc(sg, qt_b, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st);
+    if (rc != NYS_OK) return error_in("landmark rows", rc);
+    rc = launch_pinv_tc(sg, qt, kt, nullptr, nullptr, nullptr, a, z, nullptr, nullptr, L.splits,
+                        status, aux);
+    if (rc != NYS_OK) return error_in("pseudo-inverse", rc);
+    e = cudaEventRecord(beside->join[1], aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, beside->join[1], 0);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    rc = error_in("W = Z G", launch_w_tc(sg, z, gp, gml, g, w, wt_b, L.splits, status, st));
+  } else {
   rc = bf16 ? launch_rows_tc(sg, qt_b, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st)
             : launch_rows_simt(sg, qt, kg, vg, gp, gml, L.splits, st);
-  if (rc != NYS_OK) return rc;
+  if (rc != NYS_OK) return error_in("landmark rows", rc);
   rc = pinv_tc_supported(full)
-           ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, w, wt_b, L.splits, status, st)
+           ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, nullptr, w, wt_b, L.splits, status, st)
        : pinv_big_supported(full)
            ? launch_pinv_big(sg, qt, kt, gp, gml, g, a, z, scr, w, wt_b, L.splits, status, st)
            : launch_pinv_simt(sg, qt, kt, gp, gml, g, a, z, w, scr, bf16_ops ? wt_b : nullptr,
                               L.splits, st);
+    rc = error_in("pseudo-inverse", rc);
+  }
   if (rc != NYS_OK) return rc;
-  if (tc_tokens) return launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
-  if (big_tokens) return launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
-  return launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
+  if (tc_tokens)
+    rc = launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+  else if (big_tokens)
+    rc = launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+  else
+    rc = launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
+  return error_in("token rows", rc);
 }
 
 }  // namespace
+
+bool z_beside_rows(const Shape& s) {
+  return s.dtype == NYS_BF16 && pinv_tc_supported(s) && s.d % 32 == 0 && choose_groups(s) == 1 &&
+         2 * (long long)pinv_tc_ctas(s) <= kPlanSms;
+}
+
+int rows_tc_ctas(const Shape& s) {
+  return z_beside_rows(s) ? kPlanSms - pinv_tc_ctas(s) : kPlanSms;
+}
 
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,
                    const float* conv_w, void* out, char* ws, const Layout& L,
                    cudaStream_t stream, int dev) {
   const int groups = choose_groups(s);
-  if (groups <= 1) return run_group(s, s, 0, q, k, v, conv_w, out, ws, L, stream);
+  const bool beside = groups <= 1 && z_beside_rows(s);
+  if (groups <= 1 && !beside) return run_group(s, s, 0, q, k, v, conv_w, out, ws, L, stream, nullptr);
   int rc = ensure_streams(dev);
   if (rc != NYS_OK) return rc;
   DeviceStreams& d = g_streams[dev];
+  std::lock_guard<std::mutex> lk(d.enqueue);
+  if (beside) return run_group(s, s, 0, q, k, v, conv_w, out, ws, L, stream, &d);
   cudaError_t e = cudaEventRecord(d.fork, stream);
   for (int i = 1; i < groups && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(d.aux[i], d.fork, 0);
   if (e != cudaSuccess) return set_cuda_error(e);
@@ -130,7 +175,7 @@ int launch_forward(const Shape& s, const void* q, const void* k, const void* v,
   sg.B = s.B / groups;
   for (int i = 0; i < groups; ++i) {
     rc = run_group(s, sg, (long long)i * sg.bh(), q, k, v, conv_w, out, ws, L,
-                   i == 0 ? stream : d.aux[i]);
+                   i == 0 ? stream : d.aux[i], nullptr);
     if (rc != NYS_OK) return rc;
   }
   for (int i = 1; i < groups && e == cudaSuccess; ++i) {

@@ -63,6 +63,15 @@ class KernelScope {
 
 // Host helpers of the C ABI (nys_api.cu).
 int set_cuda_error(cudaError_t e);  // remembers the message, returns NYS_ERR_CUDA
+// rc unchanged; a CUDA error's message gets the failing step's name in front.
+int error_in(const char* step, int rc);
+// A tensor map the driver would not encode: NYS_ERR_CUDA, message names the site.
+int tensor_map_error(const char* file, int line);
+// After a launch: NYS_OK, or NYS_ERR_CUDA with the launch error's message kept.
+inline int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? NYS_OK : set_cuda_error(e);
+}
 int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype);
 int check_args(const void* q, const void* k, const void* v, const float* conv_w, const void* out,
                int B, int H, int n, int d, int m, int iters, int ks, int dtype);
@@ -91,7 +100,14 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
 // Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs. `s` may be
 // a group of heads of the full problem: splits / tiles_per_split come from
 // the full problem's layout.
-void rows_tc_split(const Shape& s, int* splits, int* tiles_per_split);
+void rows_tc_split(const Shape& s, int ctas, int* splits, int* tiles_per_split);
+
+// Forward-pass plan (nys_forward.cu), a function of the shape alone so that
+// the workspace layout matches the launches: whether the pseudo-inverse runs
+// beside the landmark-row pass, and the CTAs the tensor-core landmark-row
+// pass spreads its tiles over.
+bool z_beside_rows(const Shape& s);
+int rows_tc_ctas(const Shape& s);
 int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
                    float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream);
 
@@ -107,10 +123,18 @@ int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float
                        const float* w, const float* conv_w, void* out, cudaStream_t stream);
 
 // Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
+// With z set, Z only: no merge of the partials, no W (gpart, gml, g, w and
+// wt_bf16 unused); Z -> z [B*H][m][m] fp32.
 bool pinv_tc_supported(const Shape& s);
+int pinv_tc_ctas(const Shape& s);  // CTAs of one launch over all of s's heads
 int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,
-                   const float* gml, float* g, float* a_s, float* w, void* wt_bf16, int splits,
-                   int* status, cudaStream_t stream);
+                   const float* gml, float* g, float* a_s, float* z, float* w, void* wt_bf16,
+                   int splits, int* status, cudaStream_t stream);
+// W = Z G on the tensor cores from Z and the key-split partials (merged
+// here), 16 columns of one head per CTA, for the plan that computes Z beside the
+// landmark-row pass; d % 16 == 0. Writes G, W (stage exports) and W^T bf16.
+int launch_w_tc(const Shape& s, const float* z, const float* gpart, const float* gml, float* g,
+                float* w, void* wt_bf16, int splits, int* status, cudaStream_t stream);
 
 // Clustered tensor-core pseudo-inverse (nys_pinv_big.cu), bf16 path,
 // 128 < m <= 256. `scratch` is the group's block of Layout::scratch.

@@ -623,7 +623,7 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
     const uint32_t box[3] = {32, 128, 1};
     if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.d, BH};
@@ -631,14 +631,14 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
     const uint32_t box[3] = {32, (uint32_t)(s.d / 2), 1};
     if (!make_tensor_map(&maps.m[MAP_GT], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.gt, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   if (cudaFuncSetAttribute(pinv_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   KernelScope scope("pinv_big", stream);
   pinv_big<<<(unsigned)(4 * BH), kThreads, kSmemBytes, stream>>>(maps, p);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace nys

@@ -43,6 +43,7 @@ struct PinvParams {
   const float* gml;    // [B*H][splits][m][2]
   float* g;            // [B*H][m][d]  stage export
   float* a_s;          // [B*H][m][m]  stage export
+  float* z;            // [B*H][m][m]  Z-only mode: Z out (no merge, no W)
   float* w;            // [B*H][m][d]  stage export
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
   int* status;
@@ -178,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   // two at a time with all their loads in flight: a running (max,
   // denominator) rescales the accumulated rows as in an online softmax; an
   // empty partial (max = -inf, rows never written) contributes nothing.
-  {
+  const bool z_only = p.z != nullptr;  // uniform
+  if (!z_only) {
     float* grow_out = p.g + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
     for (int c0 = half * 32; c0 < d; c0 += 64) {
       float acc[32];
@@ -460,8 +462,29 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     store_bt(0.f, 1.f, 0.25f, (int)COL_Z);  // Z <- Y / 4 ; B <- Z by columns
   }
   while (exp_row < hp * m) export_rows();  // what the products did not cover
+  // ---- 5) Z-only mode: Z (TMEM columns COL_Z.., this thread's row) out
+  if (z_only && !*abort_flag && head_ok) {  // warp-uniform: the TMEM loads are collective
+    float* zrow = p.z + ((size_t)bh * m + (live ? li : 0)) * m;
+    for (int c0 = half * 32; c0 < m; c0 += 64) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lo + COL_Z + c0, r);
+      tmem_ld_wait();
+      if (!live) continue;
+      if (c0 + 32 <= m && (m & 3) == 0) {
+        float4* zo = reinterpret_cast<float4*>(zrow + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          zo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                              __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c0 + e < m) zrow[c0 + e] = __uint_as_float(r[e]);
+      }
+    }
+  }
   // ---- 5) W = Z G (head slot hs in columns hs d ..)
-  if (!*abort_flag) {
+  if (!z_only && !*abort_flag) {
     if (tid == 0) {
       tc_fence_after_sync();
       issue(COL_D, COL_Z, nullptr, gbuf, NW, MP, false);
@@ -501,6 +524,169 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
 }
 
+// W = Z G for the plan that computes Z beside the landmark-row pass (Z
+// needs only the landmarks). CTA (cb, head) forms the 16 columns [16 cb,
+// 16 cb + 16) of W: Z -> shared memory (A operand, K-major, zero padded to
+// 128 x MP), those columns of G merged here from the key-split partials and
+// written transposed (B operand, K-major, N = 16), one tf32 product M = 128,
+// N = 16, K = MP into TMEM; then W (fp32 stage export) and W^T as bf16
+// [dpad][m64] with zero padding (CTA 0 also writes the zero columns d ..
+// dpad - 1). Global loads are row-contiguous across a warp's lanes and all
+// of a thread's loads are issued before any is used.
+struct WParams {
+  const float* z;      // [B*H][m][m]
+  const float* gpart;  // [B*H][splits][m][d]
+  const float* gml;    // [B*H][splits][m][2]
+  float* g;            // [B*H][m][d]  stage export
+  float* w;            // [B*H][m][d]  stage export
+  __nv_bfloat16* wt;   // [B*H][dpad][m64]
+  int* status;
+  int m, d, dpad, m64, splits;
+};
+
+constexpr int kWCols = 16;
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 1) w_tc(const __grid_constant__ WParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* abuf = sm;                  // Z:   [128 rows x MP]
+  uint8_t* gbuf = sm + 128 * MP * 4;   // G^T: [16 rows x MP]
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m = p.m, d = p.d, c0 = (int)blockIdx.x * kWCols;
+  const long long bh = blockIdx.y;
+  if (tid == 0) {
+    mbar_init(&bar_mma, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_sh, 32);
+
+  // Z: float4 (r, q) = Z[r][4q .. 4q + 3], q fastest; zeros outside m x m
+  {
+    constexpr int Q = MP / 4, NV = 128 * Q / kThreads;
+    const float* zh = p.z + bh * m * m;
+    float4 v[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const int e = tid + u * kThreads, r = e / Q, c = (e % Q) * 4;
+      if ((m & 3) == 0)
+        v[u] = r < m && c < m ? __ldg(reinterpret_cast<const float4*>(zh + (size_t)r * m + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      else {
+        const float* zr = zh + (size_t)(r < m ? r : 0) * m;
+        v[u] = make_float4(r < m && c < m ? __ldg(zr + c) : 0.f, r < m && c + 1 < m ? __ldg(zr + c + 1) : 0.f,
+                           r < m && c + 2 < m ? __ldg(zr + c + 2) : 0.f, r < m && c + 3 < m ? __ldg(zr + c + 3) : 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const int e = tid + u * kThreads;
+      store_row4(abuf, 128, e / Q, (e % Q) * 4, v[u]);
+    }
+  }
+
+  // G columns c0 .. c0 + 15: element (i, q) = columns c0 + 4q .. + 3 of row
+  // i, q fastest. Splits eight at a time, online rescaling; an empty partial
+  // (max = -inf) was never written and is skipped. Element (i, c0 + j) goes
+  // to gbuf storage row j, column i (rows i >= m: zeros).
+  for (int e = tid; e < MP * 4; e += kThreads) {
+    const int i = e >> 2, q = e & 3;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < m) {
+      const float2* ml_row = reinterpret_cast<const float2*>(p.gml) + bh * p.splits * m + i;
+      const float4* src = reinterpret_cast<const float4*>(p.gpart + (bh * p.splits * m + i) * d + c0) + q;
+      const size_t sstride = (size_t)m * d / 4;  // float4s between splits
+      float gm = -INFINITY, den = 0.f;
+      for (int sp = 0; sp < p.splits; sp += 8) {
+        float2 ml[8];
+        float4 o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int s2 = sp + k < p.splits ? sp + k : sp;
+          ml[k] = __ldg(ml_row + (size_t)s2 * m);
+          o[k] = __ldg(src + (size_t)s2 * sstride);
+        }
+        float cm = gm;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (sp + k < p.splits && ml[k].x != -INFINITY) cm = fmaxf(cm, ml[k].x);
+        if (cm == -INFINITY) continue;  // only empty partials so far
+        const float rs = gm == -INFINITY ? 0.f : expf(gm - cm);
+        den *= rs;
+        acc = make_float4(acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (sp + k < p.splits && ml[k].x != -INFINITY) {
+            const float f = expf(ml[k].x - cm);
+            den = fmaf(ml[k].y, f, den);
+            acc = make_float4(fmaf(o[k].x, f, acc.x), fmaf(o[k].y, f, acc.y), fmaf(o[k].z, f, acc.z),
+                              fmaf(o[k].w, f, acc.w));
+          }
+        gm = cm;
+      }
+      const float inv = 1.f / den;
+      acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      reinterpret_cast<float4*>(p.g + (bh * m + i) * d + c0)[q] = acc;
+    }
+    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q, i, kWCols)) = acc.x;
+    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 1, i, kWCols)) = acc.y;
+    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 2, i, kWCols)) = acc.z;
+    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 3, i, kWCols)) = acc.w;
+  }
+  fence_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  const uint32_t tmem = tmem_base_sh;
+  if (tid == 0) {
+    tc_fence_after_sync();
+    const uint64_t a0 = smem_desc(smem_u32(abuf), 16, 1024, SW_128B);
+    const uint64_t b0 = smem_desc(smem_u32(gbuf), 16, 1024, SW_128B);
+    const uint32_t id = idesc_tf32(128, kWCols);
+    constexpr uint32_t bchunk = kWCols * 8u;  // (16 rows * 128 B) >> 4
+#pragma unroll
+    for (int kk = 0; kk < MP / 8; ++kk) {
+      const uint32_t step = (uint32_t)(kk & 3) * 2u;
+      mma_tf32(tmem, a0 + (uint64_t)((uint32_t)(kk >> 2) * 1024u + step),
+               b0 + (uint64_t)((uint32_t)(kk >> 2) * bchunk + step), id, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&bar_mma);
+  }
+  const bool ok = mbar_wait(&bar_mma, 0, &abort_sh, kWaitNs);
+  if (!ok) {
+    abort_sh = 1;
+    atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
+  }
+  tc_fence_after_sync();
+  // warps 0-3: W row `row` = TMEM lane row, the block's 16 columns
+  if (warp < 4 && __all_sync(0xffffffffu, ok)) {
+    const int row = warp * 32 + lane;
+    uint32_t r[16];
+    tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), r);
+    tmem_ld_wait();
+    if (row < m) {
+      float4* wo = reinterpret_cast<float4*>(p.w + (bh * m + row) * d + c0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        wo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                            __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+    }
+    if (row < p.m64) {
+      __nv_bfloat16* wt = p.wt + bh * p.dpad * p.m64 + row;
+#pragma unroll
+      for (int e = 0; e < kWCols; ++e)
+        wt[(size_t)(c0 + e) * p.m64] = __float2bfloat16_rn(row < m ? __uint_as_float(r[e]) : 0.f);
+      if (blockIdx.x == 0)
+        for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64] = __float2bfloat16_rn(0.f);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 32);
+}
+
 // m rounded up to 32, 64 or 128
 int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 
@@ -508,11 +694,17 @@ int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 
 bool pinv_tc_supported(const Shape& s) { return s.dtype == NYS_BF16 && s.m <= 128; }
 
+int pinv_tc_ctas(const Shape& s) {
+  const int hp = std::min(128 / mpad_of(s.m), 256 / s.d);
+  return (int)((s.bh() + hp - 1) / hp);
+}
+
 int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,
-                   const float* gml, float* g, float* a_s, float* w, void* wt_bf16, int splits,
-                   int* status, cudaStream_t stream) {
+                   const float* gml, float* g, float* a_s, float* z, float* w, void* wt_bf16,
+                   int splits, int* status, cudaStream_t stream) {
   if (!pinv_tc_supported(s)) return NYS_ERR_UNSUPPORTED;
   PinvParams p{};
+  p.z = z;
   p.qt = qt;
   p.kt = kt;
   p.gpart = gpart;
@@ -549,11 +741,38 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   auto kern = MP == 32 ? pinv_tc<32> : (MP == 64 ? pinv_tc<64> : pinv_tc<128>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   const unsigned grid = (unsigned)((p.BH + p.hp - 1) / p.hp);
   KernelScope scope("pinv_tc", stream);
   kern<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
+}
+
+int launch_w_tc(const Shape& s, const float* z, const float* gpart, const float* gml, float* g,
+                float* w, void* wt_bf16, int splits, int* status, cudaStream_t stream) {
+  if (!pinv_tc_supported(s) || s.d % kWCols != 0) return NYS_ERR_UNSUPPORTED;
+  WParams p{};
+  p.z = z;
+  p.gpart = gpart;
+  p.gml = gml;
+  p.g = g;
+  p.w = w;
+  p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
+  p.status = status;
+  p.m = s.m;
+  p.d = s.d;
+  p.dpad = s.dpad();
+  p.m64 = s.m64();
+  p.splits = splits;
+  const int MP = mpad_of(s.m);
+  const size_t smem = (size_t)(128 + kWCols) * MP * 4 + 1024;
+  auto kern = MP == 32 ? w_tc<32> : (MP == 64 ? w_tc<64> : w_tc<128>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return set_cuda_error(cudaGetLastError());
+  KernelScope scope("w_tc", stream);
+  kern<<<dim3((unsigned)(s.d / kWCols), (unsigned)s.bh()), kThreads, smem, stream>>>(p);
+  return launch_status();
 }
 
 }  // namespace nys

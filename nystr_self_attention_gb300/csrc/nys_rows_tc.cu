@@ -559,8 +559,8 @@ int nq_of(const Shape& s) { return s.m > 128 ? 1 : 2; }
 // full-GPU launch gets tiles_per_cta consecutive tiles of the flattened
 // (head, tile) space; a head is touched by at most pieces ranges, each giving
 // one partial (m > 128) or two (m <= 128).
-void rows_tc_split(const Shape& s, int* parts, int* tiles_per_cta) {
-  constexpr long long kCtas = 152;
+void rows_tc_split(const Shape& s, int ctas, int* parts, int* tiles_per_cta) {
+  const long long kCtas = ctas > 0 ? ctas : 1;
   const long long n_tiles = (s.n + 127) / 128;
   const long long total = n_tiles * s.bh();
   long long tpc = (total + kCtas - 1) / kCtas;
@@ -584,7 +584,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
     const uint32_t box[3] = {64, 128, 1};
     if (!make_tensor_map(&maps.qt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qt_bf16, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)s.d, (uint64_t)s.n, BH};
@@ -594,7 +594,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   if (DP == 64) {
     const uint64_t dims[2] = {(uint64_t)s.d, BH * (uint64_t)parts * (uint64_t)s.m};
@@ -602,7 +602,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
     const uint32_t box[2] = {32, 32};
     if (!make_tensor_map(&maps.gp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, gpart, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   RowParams p{};
   p.gpart = gpart;
@@ -631,10 +631,10 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
   const int grid = (p.total + p.tpc - 1) / p.tpc;
   auto kern = DP == 64 ? rows_tc<64> : rows_tc<128>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   KernelScope scope("rows_tc", stream);
   kern<<<grid, kThreads, smem, stream>>>(maps, p);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace nys

@@ -610,7 +610,7 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
     landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, (unsigned)s.bh()), 256, 0, stream>>>(
         qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
   }
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 template <typename T>
@@ -624,7 +624,7 @@ int rows_t(const Shape& s, const float* qt, const void* k, const void* v, float*
   rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, splits, (unsigned)s.bh()), 128, smem, stream>>>(
       qt, static_cast<const T*>(k), static_cast<const T*>(v), gp, gml, s.n, s.d, s.m, splits, kps,
       scale);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 template <typename T>
@@ -637,12 +637,12 @@ int tokens_t(const Shape& s, const void* q, const void* v, const float* kt, cons
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(tokens_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   KernelScope ks_("tokens_simt", stream);
   tokens_simt<T><<<dim3((s.n + TK_ROWS - 1) / TK_ROWS, (unsigned)s.bh()), 256, smem, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(v), kt, w, conv_w, static_cast<T*>(out), s.H,
       s.n, s.d, s.m, s.ks, scale);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace
@@ -666,7 +666,7 @@ int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const flo
   pinv_simt<<<(unsigned)s.bh(), 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scratch, wt_b, s.d,
                                                   s.m, splits, s.iters,
                                                   1.0f / sqrtf((float)s.d), s.m64(), s.dpad());
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,

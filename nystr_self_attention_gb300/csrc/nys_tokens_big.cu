@@ -369,7 +369,7 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, boxv,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)DP, (uint64_t)m64, BH};
@@ -377,7 +377,7 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
     const uint32_t box[3] = {64, (uint32_t)pl.m_pad, 1};
     if (!make_tensor_map(&maps.kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)m64, (uint64_t)DP, BH};
@@ -385,7 +385,7 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
     const uint32_t box[3] = {64, (uint32_t)DP, 1};
     if (!make_tensor_map(&maps.wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, wt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   BigParams p{};
   p.conv_w = conv_w;
@@ -414,10 +414,10 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
   p.off_qv = p.off_t + pl.t_bytes;
   if (cudaFuncSetAttribute(tokens_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
       cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   KernelScope scope("tokens_big", stream);
   tokens_big<<<grid, kThreads, pl.smem, stream>>>(maps, p);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace nys

@@ -630,7 +630,7 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, boxv,
                          CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)DP, (uint64_t)pl.m64, BH};
@@ -638,7 +638,7 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
     const uint32_t box[3] = {64, (uint32_t)pl.m_pad, 1};
     if (!make_tensor_map(&maps.kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)pl.m64, (uint64_t)DP, BH};
@@ -646,7 +646,7 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
     const uint32_t box[3] = {64, (uint32_t)DP, 1};
     if (!make_tensor_map(&maps.wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, wt_bf16, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return NYS_ERR_CUDA;
+      return tensor_map_error(__FILE__, __LINE__);
   }
 
   TokParams p{};
@@ -684,10 +684,10 @@ int launch_tokens_tc(const Shape& s, const void* q, const void* v, const void* k
   auto kern = DP == 64 ? tokens_tc<64> : tokens_tc<128>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
       cudaSuccess)
-    return NYS_ERR_CUDA;
+    return set_cuda_error(cudaGetLastError());
   KernelScope scope("tokens_tc", stream);
   kern<<<grid, kThreads, pl.smem, stream>>>(maps, p);
-  return cudaGetLastError() == cudaSuccess ? NYS_OK : NYS_ERR_CUDA;
+  return launch_status();
 }
 
 }  // namespace nys

@@ -95,13 +95,21 @@ def test_small_shapes(shape, dtype):
 
 # ------------------------------------------------------------------ stages ----
 
+# few heads: the pseudo-inverse runs beside the landmark-row pass and W = Z G
+# is formed afterwards; 256 heads: two head groups, the pseudo-inverse
+# kernel merges G and forms W itself
+STAGE_SHAPES = [(2, 2, 512, 64, 64), (16, 16, 256, 64, 64)]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_stage_intermediates(dtype):
+@pytest.mark.parametrize("shape", STAGE_SHAPES, ids=[f"B{s[0]}H{s[1]}" for s in STAGE_SHAPES])
+def test_stage_intermediates(shape, dtype):
     import nystr_self_attention_gb300 as N
-    wl = workloads.custom(2, 2, 512, 64, 64, 6, 33, dtype)
+    B, H, n, d, m = shape
+    wl = workloads.custom(B, H, n, d, m, 6, 33, dtype)
     inp = workloads.make_inputs(wl, seed=3)
     _, ws = run_gpu(inp, workspace=True)
-    heads = [(0, 0), (1, 1)]
+    heads = [(0, 0), (B - 1, H - 1)]
     ref = oracle_heads(inp, heads)
     st = {name: stage(ws, wl, code, rows, cols) for name, code, rows, cols in (
         ("q_tilde", N.NYS_STAGE_Q_TILDE, wl.m, wl.d), ("k_tilde", N.NYS_STAGE_K_TILDE, wl.m, wl.d),
