@@ -24,6 +24,10 @@
 // of X = A_S Z from shared memory; X and Z are A operands in TMEM; each
 // product's B operand is written, transposed, into one shared-memory
 // buffer by the epilogue of the product before it.
+//
+// Z-only mode (z given): no merge and no W; Z goes out in fp32 so that the
+// kernel can run before the key-split partials exist. The second kernel
+// here, w_tc, then merges G and forms W = Z G (16 columns per CTA).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -173,63 +177,17 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     tc_fence_after_sync();
   };
 
-  // ---- 1) G = merge of the key-split partials (row li of head bh); G^T
-  // into gbuf (B of W = Z G, head slot hs at rows hs d ..). First, so that
-  // its loads do not wait behind the score steps. One pass over the splits,
-  // two at a time with all their loads in flight: a running (max,
-  // denominator) rescales the accumulated rows as in an online softmax; an
-  // empty partial (max = -inf, rows never written) contributes nothing.
+  // ---- 1) the merge of G runs after the iteration (W is its only user);
+  // its partial rows are prefetched into L2 here so that it then waits on
+  // L2 rather than on DRAM
   const bool z_only = p.z != nullptr;  // uniform
-  if (!z_only) {
-    float* grow_out = p.g + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
-    for (int c0 = half * 32; c0 < d; c0 += 64) {
-      float acc[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-      if (live) {
-        float gm = -INFINITY, den = 0.f;
-        for (int sp = 0; sp < p.splits; sp += 2) {
-          const bool two = sp + 1 < p.splits;
-          const size_t pr0 = ((size_t)bh * p.splits + sp) * m + li;
-          const size_t pr1 = two ? pr0 + (size_t)m : pr0;
-          const float2 ml0 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr0);
-          const float2 ml1 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr1);
-          const float4* s0 = reinterpret_cast<const float4*>(p.gpart + pr0 * d + c0);
-          const float4* s1 = reinterpret_cast<const float4*>(p.gpart + pr1 * d + c0);
-          float4 v0[8], v1[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v0[e] = __ldg(s0 + e);
-            v1[e] = __ldg(s1 + e);
-          }
-          const bool ok0 = ml0.x != -INFINITY, ok1 = two && ml1.x != -INFINITY;
-          const float cm = fmaxf(gm, fmaxf(ok0 ? ml0.x : -INFINITY, ok1 ? ml1.x : -INFINITY));
-          if (cm == -INFINITY) continue;  // nothing yet
-          const float r = gm == -INFINITY ? 0.f : expf(gm - cm);
-          const float f0 = ok0 ? expf(ml0.x - cm) : 0.f;
-          const float f1 = ok1 ? expf(ml1.x - cm) : 0.f;
-          den = den * r + (ok0 ? ml0.y * f0 : 0.f) + (ok1 ? ml1.y * f1 : 0.f);
-          gm = cm;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 a0 = ok0 ? v0[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 a1 = ok1 ? v1[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-            acc[4 * e] = fmaf(acc[4 * e], r, fmaf(a0.x, f0, a1.x * f1));
-            acc[4 * e + 1] = fmaf(acc[4 * e + 1], r, fmaf(a0.y, f0, a1.y * f1));
-            acc[4 * e + 2] = fmaf(acc[4 * e + 2], r, fmaf(a0.z, f0, a1.z * f1));
-            acc[4 * e + 3] = fmaf(acc[4 * e + 3], r, fmaf(a0.w, f0, a1.w * f1));
-          }
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] *= inv;
-        float4* go = reinterpret_cast<float4*>(grow_out + c0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
-      }
-      if (hs < hp) store_col32(gbuf, NW, li, hs * d + c0, acc);
+  if (!z_only && live)
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const size_t prow = ((size_t)bh * p.splits + sp) * m + li;
+      for (int c0 = half * 32; c0 < d; c0 += 64)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gpart + prow * d + c0));
+      if (half == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gml + prow * 2));
     }
-  }
 
   // ---- 2) scores S = Q~ K~^T in 3xTF32: Q~ hi / lo rows -> TMEM (A), K~
   // hi / lo rows -> shared memory (B, head slot hs at rows hs MP ..)
@@ -397,13 +355,15 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   __syncthreads();
 
   // ---- 4) the iteration
-  // Stage export of A_S (abuf is constant from here on): eight rows per call,
-  // a warp per row, coalesced. It runs while thread 0 issues a product's
-  // MMAs, when the other threads would only wait.
+  // Stage export of A_S (abuf is constant from here on): seven rows per
+  // call, one per warp 1-7, coalesced. It runs while thread 0 issues a
+  // product's MMAs, when the other threads would only wait; warp 0 (the
+  // issuer's) takes no rows, so the export never delays the issue.
   int exp_row = 0;
   auto export_rows = [&]() {
-    const int r = exp_row + warp;
-    exp_row += kThreads / 32;
+    const int r = exp_row + warp - 1;
+    exp_row += kThreads / 32 - 1;
+    if (warp == 0) return;
     if (r >= hp * m) return;
     const int h2 = r / m, i = r - h2 * m;
     const int bh2 = (int)blockIdx.x * hp + h2;
@@ -424,22 +384,34 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   // * I, written transposed as the next product's B operand (element
   // (i, j) of the head -> storage row hs MP + j, column i); optionally also
   // scale * D -> TMEM columns to_col.. (an A operand).
+  auto store_chunk = [&](int j0, uint32_t (&r)[32], float diag, float sign, float scale_,
+                         int to_col) {
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float x = scale_ * __uint_as_float(r[e]);
+      r[e] = __float_as_uint(x);
+      v[e] = fmaf(sign, x, (j0 + e == li) ? diag : 0.f);
+    }
+    store_col32(bbuf, NP, li, hs * MP + j0, v);
+    if (to_col >= 0) tmem_st32(tmem + lo + (uint32_t)to_col + j0, r);
+  };
   auto store_bt = [&](float diag, float sign, float scale_, int to_col) {
     if (head_ok) {
-      for (int c = half; c < NCH; c += 2) {
-        const int j0 = c * 32;
-        uint32_t r[32];
-        tmem_ld32(tmem + lo + COL_D + dblk + j0, r);
+      if constexpr (NCH == 4) {  // chunks half and half + 2: both loads in flight
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lo + COL_D + dblk + half * 32, r0);
+        tmem_ld32(tmem + lo + COL_D + dblk + (half + 2) * 32, r1);
         tmem_ld_wait();
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = scale_ * __uint_as_float(r[e]);
-          r[e] = __float_as_uint(x);
-          v[e] = fmaf(sign, x, (j0 + e == li) ? diag : 0.f);
+        store_chunk(half * 32, r0, diag, sign, scale_, to_col);
+        store_chunk((half + 2) * 32, r1, diag, sign, scale_, to_col);
+      } else {
+        for (int c = half; c < NCH; c += 2) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lo + COL_D + dblk + c * 32, r);
+          tmem_ld_wait();
+          store_chunk(c * 32, r, diag, sign, scale_, to_col);
         }
-        store_col32(bbuf, NP, li, hs * MP + j0, v);
-        if (to_col >= 0) tmem_st32(tmem + lo + (uint32_t)to_col + j0, r);
       }
     }
     fence_async_smem();
@@ -462,6 +434,66 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     store_bt(0.f, 1.f, 0.25f, (int)COL_Z);  // Z <- Y / 4 ; B <- Z by columns
   }
   while (exp_row < hp * m) export_rows();  // what the products did not cover
+  // ---- 5a) G = merge of the key-split partials (row li of head bh); G^T
+  // into gbuf (B of W = Z G, head slot hs at rows hs d ..). One pass over
+  // the splits, two at a time with all their loads in flight: a running
+  // (max, denominator) rescales the accumulated rows as in an online
+  // softmax; an empty partial (max = -inf, rows never written) contributes
+  // nothing.
+  if (!z_only) {
+    float* grow_out = p.g + ((size_t)(live ? bh : 0) * m + (live ? li : 0)) * d;
+    for (int c0 = half * 32; c0 < d; c0 += 64) {
+      float acc[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+      if (live) {
+        float gm = -INFINITY, den = 0.f;
+        for (int sp = 0; sp < p.splits; sp += 2) {
+          const bool two = sp + 1 < p.splits;
+          const size_t pr0 = ((size_t)bh * p.splits + sp) * m + li;
+          const size_t pr1 = two ? pr0 + (size_t)m : pr0;
+          const float2 ml0 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr0);
+          const float2 ml1 = __ldg(reinterpret_cast<const float2*>(p.gml) + pr1);
+          const float4* s0 = reinterpret_cast<const float4*>(p.gpart + pr0 * d + c0);
+          const float4* s1 = reinterpret_cast<const float4*>(p.gpart + pr1 * d + c0);
+          float4 v0[8], v1[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            v0[e] = __ldg(s0 + e);
+            v1[e] = __ldg(s1 + e);
+          }
+          const bool ok0 = ml0.x != -INFINITY, ok1 = two && ml1.x != -INFINITY;
+          const float cm = fmaxf(gm, fmaxf(ok0 ? ml0.x : -INFINITY, ok1 ? ml1.x : -INFINITY));
+          if (cm == -INFINITY) continue;  // nothing yet
+          const float r = gm == -INFINITY ? 0.f : expf(gm - cm);
+          const float f0 = ok0 ? expf(ml0.x - cm) : 0.f;
+          const float f1 = ok1 ? expf(ml1.x - cm) : 0.f;
+          den = den * r + (ok0 ? ml0.y * f0 : 0.f) + (ok1 ? ml1.y * f1 : 0.f);
+          gm = cm;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 a0 = ok0 ? v0[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 a1 = ok1 ? v1[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[4 * e] = fmaf(acc[4 * e], r, fmaf(a0.x, f0, a1.x * f1));
+            acc[4 * e + 1] = fmaf(acc[4 * e + 1], r, fmaf(a0.y, f0, a1.y * f1));
+            acc[4 * e + 2] = fmaf(acc[4 * e + 2], r, fmaf(a0.z, f0, a1.z * f1));
+            acc[4 * e + 3] = fmaf(acc[4 * e + 3], r, fmaf(a0.w, f0, a1.w * f1));
+          }
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] *= inv;
+        float4* go = reinterpret_cast<float4*>(grow_out + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+      }
+      if (hs < hp) store_col32(gbuf, NW, li, hs * d + c0, acc);
+    }
+  }
+
+  fence_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
   // ---- 5) Z-only mode: Z (TMEM columns COL_Z.., this thread's row) out
   if (z_only && !*abort_flag && head_ok) {  // warp-uniform: the TMEM loads are collective
     float* zrow = p.z + ((size_t)bh * m + (live ? li : 0)) * m;
