@@ -237,7 +237,7 @@ KERNEL_SOURCES = {
     "landmarks_vec": "nys_simt.cu", "landmarks_simt": "nys_simt.cu", "rows_simt": "nys_simt.cu",
     "pinv_simt": "nys_simt.cu", "tokens_simt": "nys_simt.cu", "rows_tc": "nys_rows_tc.cu",
     "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu", "pinv_big": "nys_pinv_big.cu",
-    "tokens_big": "nys_tokens_big.cu", "w_tc": "nys_pinv_tc.cu",
+    "tokens_big": "nys_tokens_big.cu", "w_tc": "nys_pinv_tc.cu", "merge_g": "nys_simt.cu",
 }
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates
 
@@ -294,6 +294,8 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
                 "peak_source": f"hbm_gbs ({peak_src})"}
     if kernel == "w_tc":  # W = Z G alone
         flops = wl.heads * 2.0 * wl.m * wl.m * wl.d / per_step
+    elif kernel == "merge_g":  # rescale-and-add of the key-split partials
+        flops = wl.heads * 2.0 * wl.m * wl.d / per_step
     else:
         flops = pinv_flops(wl) / per_step
     achieved = flops / t_launch / 1e12

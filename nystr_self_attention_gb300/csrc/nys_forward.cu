@@ -14,8 +14,9 @@
 // needs at most half of the SMs (few heads, long sequences), its chain of
 // products runs on a second stream beside the landmark-row pass instead of
 // after it: Z depends only on the landmarks. The landmark-row pass is then
-// spread over the SMs the pseudo-inverse leaves free, and W = Z G is formed
-// by a short kernel once both are done.
+// spread over the SMs the pseudo-inverse leaves free, G is merged from its
+// partials while Z is still being formed, and W = Z G is formed by a short
+// kernel once both are done.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -54,26 +55,47 @@ int ensure_streams(int dev) {
   return NYS_OK;
 }
 
-// Number of head groups: only for the tensor-core path with short
-// sequences, where the pseudo-inverse dominates; whole batch entries per
-// group. NYS_HEAD_GROUPS overrides the choice (tuning).
-int choose_groups(const Shape& s) {
-  static int override_groups = [] {
+// SM count the plan assumes (GB300); the layout must not depend on the
+// device a workspace size is asked for on.
+constexpr int kPlanSms = 152;
+// SMs the landmark-row pass keeps at least when the pseudo-inverse runs
+// beside it
+constexpr int kMinRowSms = 48;
+
+int groups_override() {
+  static int v = [] {
     const char* e = std::getenv("NYS_HEAD_GROUPS");
     return e ? std::atoi(e) : 0;
   }();
+  return v;
+}
+
+// SMs the pseudo-inverse's CTAs take beside the landmark rows: one CTA per
+// SM while they fit in half of the GPU, else two per SM (m <= 64: two
+// CTAs' shared memory and TMEM fit one SM); 0 if the plan does not apply.
+int pinv_beside_sms(const Shape& s) {
+  if (s.dtype != NYS_BF16 || !pinv_tc_supported(s) || s.d % 16 != 0) return 0;
+  if (groups_override() > 1) return 0;
+  const int ctas = pinv_tc_ctas(s);
+  if (2 * ctas <= kPlanSms) return ctas;
+  if (s.m <= 64 && (ctas + 1) / 2 <= kPlanSms - kMinRowSms) return (ctas + 1) / 2;
+  return 0;
+}
+
+// Number of head groups: only for the tensor-core path with short
+// sequences, where the pseudo-inverse dominates and does not run beside the
+// landmark rows; whole batch entries per group. NYS_HEAD_GROUPS overrides
+// the choice (tuning).
+int choose_groups(const Shape& s) {
+  const int override_groups = groups_override();
   int g = 1;
-  if (s.dtype == NYS_BF16 && s.n <= 2048 && s.bh() >= 256) g = 2;
+  if (s.dtype == NYS_BF16 && s.n <= 2048 && s.bh() >= 256 && pinv_beside_sms(s) == 0) g = 2;
   if (override_groups > 0) g = override_groups;
   if (g > kMaxGroups) g = kMaxGroups;
   if (g > s.B) g = s.B;
   while (g > 1 && s.B % g != 0) --g;
   return g;
 }
-
-// SM count the plan assumes (GB300); the layout must not depend on the
-// device a workspace size is asked for on.
-constexpr int kPlanSms = 152;
 
 template <typename T>
 T* at(char* ws, size_t off) { return reinterpret_cast<T*>(ws + off); }
@@ -120,10 +142,12 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
     rc = launch_pinv_tc(sg, qt, kt, nullptr, nullptr, nullptr, a, z, nullptr, nullptr, L.splits,
                         status, aux);
     if (rc != NYS_OK) return error_in("pseudo-inverse", rc);
+    rc = launch_merge_g(sg, gp, gml, g, L.splits, st);  // while Z is still being formed
+    if (rc != NYS_OK) return error_in("merge of G", rc);
     e = cudaEventRecord(beside->join[1], aux);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, beside->join[1], 0);
     if (e != cudaSuccess) return set_cuda_error(e);
-    rc = error_in("W = Z G", launch_w_tc(sg, z, gp, gml, g, w, wt_b, L.splits, status, st));
+    rc = error_in("W = Z G", launch_w_tc(sg, z, g, w, wt_b, status, st));
   } else {
   rc = bf16 ? launch_rows_tc(sg, qt_b, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st)
             : launch_rows_simt(sg, qt, kg, vg, gp, gml, L.splits, st);
@@ -148,13 +172,10 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
 
 }  // namespace
 
-bool z_beside_rows(const Shape& s) {
-  return s.dtype == NYS_BF16 && pinv_tc_supported(s) && s.d % 32 == 0 && choose_groups(s) == 1 &&
-         2 * (long long)pinv_tc_ctas(s) <= kPlanSms;
-}
+bool z_beside_rows(const Shape& s) { return pinv_beside_sms(s) > 0 && choose_groups(s) == 1; }
 
 int rows_tc_ctas(const Shape& s) {
-  return z_beside_rows(s) ? kPlanSms - pinv_tc_ctas(s) : kPlanSms;
+  return z_beside_rows(s) ? kPlanSms - pinv_beside_sms(s) : kPlanSms;
 }
 
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,

@@ -121,6 +121,10 @@ int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const flo
                      __nv_bfloat16* wt_b, int splits, cudaStream_t stream);
 int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,
                        const float* w, const float* conv_w, void* out, cudaStream_t stream);
+// G = merge of the key-split partials (CUDA cores, one thread per 4
+// elements of G), for the plan that computes Z beside the landmark rows.
+int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,
+                   cudaStream_t stream);
 
 // Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
 // With z set, Z only: no merge of the partials, no W (gpart, gml, g, w and
@@ -130,11 +134,11 @@ int pinv_tc_ctas(const Shape& s);  // CTAs of one launch over all of s's heads
 int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,
                    const float* gml, float* g, float* a_s, float* z, float* w, void* wt_bf16,
                    int splits, int* status, cudaStream_t stream);
-// W = Z G on the tensor cores from Z and the key-split partials (merged
-// here), 16 columns of one head per CTA, for the plan that computes Z beside the
-// landmark-row pass; d % 16 == 0. Writes G, W (stage exports) and W^T bf16.
-int launch_w_tc(const Shape& s, const float* z, const float* gpart, const float* gml, float* g,
-                float* w, void* wt_bf16, int splits, int* status, cudaStream_t stream);
+// W = Z G on the tensor cores from Z and the merged G, for the plan that
+// computes Z beside the landmark-row pass; d % 16 == 0. Writes W (stage
+// export) and W^T bf16.
+int launch_w_tc(const Shape& s, const float* z, const float* g, float* w, void* wt_bf16,
+                int* status, cudaStream_t stream);
 
 // Clustered tensor-core pseudo-inverse (nys_pinv_big.cu), bf16 path,
 // 128 < m <= 256. `scratch` is the group's block of Layout::scratch.

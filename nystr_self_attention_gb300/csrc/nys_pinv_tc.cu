@@ -557,45 +557,44 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
 }
 
 // W = Z G for the plan that computes Z beside the landmark-row pass (Z
-// needs only the landmarks). CTA (cb, head) forms the 16 columns [16 cb,
-// 16 cb + 16) of W: Z -> shared memory (A operand, K-major, zero padded to
-// 128 x MP), those columns of G merged here from the key-split partials and
-// written transposed (B operand, K-major, N = 16), one tf32 product M = 128,
-// N = 16, K = MP into TMEM; then W (fp32 stage export) and W^T as bf16
-// [dpad][m64] with zero padding (CTA 0 also writes the zero columns d ..
-// dpad - 1). Global loads are row-contiguous across a warp's lanes and all
-// of a thread's loads are issued before any is used.
+// needs only the landmarks; G is merged from the key-split partials by a
+// CUDA-core kernel after that pass). CTA (cb, head) forms the NC columns
+// [NC cb, NC cb + NC) of W: Z -> shared memory (A operand, K-major, zero
+// padded to 128 x MP), those columns of G written transposed (B operand,
+// K-major, N = NC), one tf32 product M = 128, N = NC, K = MP into TMEM; then
+// W (fp32 stage export) and W^T as bf16 [dpad][m64] with zero padding (CTA 0
+// also writes the zero columns d .. dpad - 1). Global loads are
+// row-contiguous across a warp's lanes.
 struct WParams {
   const float* z;      // [B*H][m][m]
-  const float* gpart;  // [B*H][splits][m][d]
-  const float* gml;    // [B*H][splits][m][2]
-  float* g;            // [B*H][m][d]  stage export
+  const float* g;      // [B*H][m][d]  G (merged)
   float* w;            // [B*H][m][d]  stage export
   __nv_bfloat16* wt;   // [B*H][dpad][m64]
   int* status;
-  int m, d, dpad, m64, splits;
+  int m, d, dpad, m64;
 };
 
-constexpr int kWCols = 16;
-
-template <int MP>
-__global__ void __launch_bounds__(kThreads, 1) w_tc(const __grid_constant__ WParams p) {
+// NC: columns of W per CTA (16, 32 or 64)
+template <int MP, int NC>
+__global__ void __launch_bounds__(kThreads, 3) w_tc(const __grid_constant__ WParams p) {
+  constexpr int NQ = NC / 4;                          // float4s of a G row block
+  constexpr uint32_t kCols = NC < 32 ? 32u : (uint32_t)NC;  // TMEM columns
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* abuf = sm;                  // Z:   [128 rows x MP]
-  uint8_t* gbuf = sm + 128 * MP * 4;   // G^T: [16 rows x MP]
+  uint8_t* gbuf = sm + 128 * MP * 4;   // G^T: [NC rows x MP]
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m = p.m, d = p.d, c0 = (int)blockIdx.x * kWCols;
+  const int m = p.m, d = p.d, c0 = (int)blockIdx.x * NC;
   const long long bh = blockIdx.y;
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
     abort_sh = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base_sh, 32);
+  if (warp == 0) tmem_alloc(&tmem_base_sh, kCols);
 
   // Z: float4 (r, q) = Z[r][4q .. 4q + 3], q fastest; zeros outside m x m
   {
@@ -620,53 +619,27 @@ __global__ void __launch_bounds__(kThreads, 1) w_tc(const __grid_constant__ WPar
     }
   }
 
-  // G columns c0 .. c0 + 15: element (i, q) = columns c0 + 4q .. + 3 of row
-  // i, q fastest. Splits eight at a time, online rescaling; an empty partial
-  // (max = -inf) was never written and is skipped. Element (i, c0 + j) goes
-  // to gbuf storage row j, column i (rows i >= m: zeros).
-  for (int e = tid; e < MP * 4; e += kThreads) {
-    const int i = e >> 2, q = e & 3;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < m) {
-      const float2* ml_row = reinterpret_cast<const float2*>(p.gml) + bh * p.splits * m + i;
-      const float4* src = reinterpret_cast<const float4*>(p.gpart + (bh * p.splits * m + i) * d + c0) + q;
-      const size_t sstride = (size_t)m * d / 4;  // float4s between splits
-      float gm = -INFINITY, den = 0.f;
-      for (int sp = 0; sp < p.splits; sp += 8) {
-        float2 ml[8];
-        float4 o[8];
+  // G columns c0 .. c0 + NC - 1: element (i, q) = columns c0 + 4q .. + 3 of
+  // row i, q fastest, all loads of a thread in flight; element (i, c0 + j)
+  // goes to gbuf storage row j, column i (rows i >= m: zeros)
+  {
+    constexpr int NE = (MP * NQ + kThreads - 1) / kThreads;
+    float4 gv[NE];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int s2 = sp + k < p.splits ? sp + k : sp;
-          ml[k] = __ldg(ml_row + (size_t)s2 * m);
-          o[k] = __ldg(src + (size_t)s2 * sstride);
-        }
-        float cm = gm;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (sp + k < p.splits && ml[k].x != -INFINITY) cm = fmaxf(cm, ml[k].x);
-        if (cm == -INFINITY) continue;  // only empty partials so far
-        const float rs = gm == -INFINITY ? 0.f : expf(gm - cm);
-        den *= rs;
-        acc = make_float4(acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (sp + k < p.splits && ml[k].x != -INFINITY) {
-            const float f = expf(ml[k].x - cm);
-            den = fmaf(ml[k].y, f, den);
-            acc = make_float4(fmaf(o[k].x, f, acc.x), fmaf(o[k].y, f, acc.y), fmaf(o[k].z, f, acc.z),
-                              fmaf(o[k].w, f, acc.w));
-          }
-        gm = cm;
-      }
-      const float inv = 1.f / den;
-      acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      reinterpret_cast<float4*>(p.g + (bh * m + i) * d + c0)[q] = acc;
+    for (int u = 0; u < NE; ++u) {
+      const int e = tid + u * kThreads, i = e / NQ, q = e % NQ;
+      gv[u] = e < MP * NQ && i < m ? __ldg(reinterpret_cast<const float4*>(p.g + (bh * m + i) * d + c0) + q)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q, i, kWCols)) = acc.x;
-    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 1, i, kWCols)) = acc.y;
-    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 2, i, kWCols)) = acc.z;
-    *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 3, i, kWCols)) = acc.w;
+#pragma unroll
+    for (int u = 0; u < NE; ++u) {
+      const int e = tid + u * kThreads, i = e / NQ, q = e % NQ;
+      if (e >= MP * NQ) break;
+      *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q, i, NC)) = gv[u].x;
+      *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 1, i, NC)) = gv[u].y;
+      *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 2, i, NC)) = gv[u].z;
+      *reinterpret_cast<float*>(gbuf + kmaj_off(4 * q + 3, i, NC)) = gv[u].w;
+    }
   }
   fence_async_smem();
   tc_fence_before_sync();
@@ -676,8 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1) w_tc(const __grid_constant__ WPar
     tc_fence_after_sync();
     const uint64_t a0 = smem_desc(smem_u32(abuf), 16, 1024, SW_128B);
     const uint64_t b0 = smem_desc(smem_u32(gbuf), 16, 1024, SW_128B);
-    const uint32_t id = idesc_tf32(128, kWCols);
-    constexpr uint32_t bchunk = kWCols * 8u;  // (16 rows * 128 B) >> 4
+    const uint32_t id = idesc_tf32(128, NC);
+    constexpr uint32_t bchunk = NC * 8u;  // (NC rows * 128 B) >> 4
 #pragma unroll
     for (int kk = 0; kk < MP / 8; ++kk) {
       const uint32_t step = (uint32_t)(kk & 3) * 2u;
@@ -692,31 +665,34 @@ __global__ void __launch_bounds__(kThreads, 1) w_tc(const __grid_constant__ WPar
     atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
   }
   tc_fence_after_sync();
-  // warps 0-3: W row `row` = TMEM lane row, the block's 16 columns
+  // warps 0-3: W row `row` = TMEM lane row, the block's NC columns
   if (warp < 4 && __all_sync(0xffffffffu, ok)) {
     const int row = warp * 32 + lane;
-    uint32_t r[16];
-    tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16), r);
-    tmem_ld_wait();
-    if (row < m) {
-      float4* wo = reinterpret_cast<float4*>(p.w + (bh * m + row) * d + c0);
+    __nv_bfloat16* wt = p.wt + bh * p.dpad * p.m64 + row;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        wo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                            __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
-    }
-    if (row < p.m64) {
-      __nv_bfloat16* wt = p.wt + bh * p.dpad * p.m64 + row;
+    for (int j0 = 0; j0 < NC; j0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + j0, r);
+      tmem_ld_wait();
+      if (row < m) {
+        float4* wo = reinterpret_cast<float4*>(p.w + (bh * m + row) * d + c0 + j0);
 #pragma unroll
-      for (int e = 0; e < kWCols; ++e)
-        wt[(size_t)(c0 + e) * p.m64] = __float2bfloat16_rn(row < m ? __uint_as_float(r[e]) : 0.f);
-      if (blockIdx.x == 0)
-        for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64] = __float2bfloat16_rn(0.f);
+        for (int e = 0; e < 4; ++e)
+          wo[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                              __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+      }
+      if (row < p.m64) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          wt[(size_t)(c0 + j0 + e) * p.m64] = __float2bfloat16_rn(row < m ? __uint_as_float(r[e]) : 0.f);
+      }
     }
+    if (blockIdx.x == 0 && row < p.m64)
+      for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64] = __float2bfloat16_rn(0.f);
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 32);
+  if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
 // m rounded up to 32, 64 or 128
@@ -771,8 +747,10 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.klo_off = (uint32_t)(gbytes + kbytes);
   const size_t smem = gbytes + std::max(abytes + bbytes, 2 * kbytes) + 1024;
   auto kern = MP == 32 ? pinv_tc<32> : (MP == 64 ? pinv_tc<64> : pinv_tc<128>);
+  // (two CTAs per SM for MP <= 64: the largest shared-memory carveout)
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return set_cuda_error(cudaGetLastError());
   const unsigned grid = (unsigned)((p.BH + p.hp - 1) / p.hp);
   KernelScope scope("pinv_tc", stream);
@@ -780,13 +758,11 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   return launch_status();
 }
 
-int launch_w_tc(const Shape& s, const float* z, const float* gpart, const float* gml, float* g,
-                float* w, void* wt_bf16, int splits, int* status, cudaStream_t stream) {
-  if (!pinv_tc_supported(s) || s.d % kWCols != 0) return NYS_ERR_UNSUPPORTED;
+int launch_w_tc(const Shape& s, const float* z, const float* g, float* w, void* wt_bf16,
+                int* status, cudaStream_t stream) {
+  if (!pinv_tc_supported(s) || s.d % 16 != 0) return NYS_ERR_UNSUPPORTED;
   WParams p{};
   p.z = z;
-  p.gpart = gpart;
-  p.gml = gml;
   p.g = g;
   p.w = w;
   p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
@@ -795,15 +771,22 @@ int launch_w_tc(const Shape& s, const float* z, const float* gpart, const float*
   p.d = s.d;
   p.dpad = s.dpad();
   p.m64 = s.m64();
-  p.splits = splits;
   const int MP = mpad_of(s.m);
-  const size_t smem = (size_t)(128 + kWCols) * MP * 4 + 1024;
-  auto kern = MP == 32 ? w_tc<32> : (MP == 64 ? w_tc<64> : w_tc<128>);
+  // whole heads per CTA (d <= 64) when the heads alone fill the GPU, else
+  // 16-column blocks for more CTAs in flight
+  const int NC = (s.bh() >= 152 && s.d <= 64) ? s.d : 16;
+  const size_t smem = (size_t)(128 + NC) * MP * 4 + 1024;
+  void (*kern)(WParams) = nullptr;
+  if (NC == 16) kern = MP == 32 ? w_tc<32, 16> : (MP == 64 ? w_tc<64, 16> : w_tc<128, 16>);
+  else if (NC == 32) kern = MP == 32 ? w_tc<32, 32> : (MP == 64 ? w_tc<64, 32> : w_tc<128, 32>);
+  else kern = MP == 32 ? w_tc<32, 64> : (MP == 64 ? w_tc<64, 64> : w_tc<128, 64>);
+  // three CTAs per SM: the largest shared-memory carveout
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return set_cuda_error(cudaGetLastError());
   KernelScope scope("w_tc", stream);
-  kern<<<dim3((unsigned)(s.d / kWCols), (unsigned)s.bh()), kThreads, smem, stream>>>(p);
+  kern<<<dim3((unsigned)(s.d / NC), (unsigned)s.bh()), kThreads, smem, stream>>>(p);
   return launch_status();
 }
 

@@ -127,84 +127,76 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
     for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
 }
 
-// Small segments (seg * d / V = 32 * VPL 16-byte vectors, VPL <= 4): one
-// warp takes SPW = 8 / VPL consecutive segments of one (tensor, head) and
-// issues all of its loads before reducing, so each warp keeps 8 vectors per
-// lane in flight. grid: (ceil(2 * B*H * ceil(m64 / SPW) / 8)), block 256.
-template <typename T, int VPL>
+// Small segments (seg * d / V <= 128 16-byte vectors): one warp takes
+// SPW = 32 / VPR consecutive segments of one (tensor, head); lane l owns
+// segment l / VPR and column group l % VPR (V columns) and sums that
+// segment's rows for its columns itself (no shuffles), eight rows' loads in
+// flight at a time; a warp-wide load covers SPW rows of 16 * VPR bytes.
+// Padding rows (m <= i < m64) get zeros in the bf16 copies.
+// grid: (ceil(2 * B*H * ceil(m64 / SPW) / 8)), block 256.
+template <typename T>
 __global__ void __launch_bounds__(256)
 landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
                 float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
                 __nv_bfloat16* __restrict__ kt_b, long long n_heads, int n, int d, int m, int m64,
                 int dpad) {
   constexpr int V = 16 / sizeof(T);
-  constexpr int SPW = 8 / VPL;
-  const int nblk = (m64 + SPW - 1) / SPW;
+  const int vpr = d / V, spw = 32 / vpr;
+  const int nblk = (m64 + spw - 1) / spw;
   const long long job = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (job >= 2 * n_heads * nblk) return;
   const int tensor = (int)(job / (n_heads * nblk));
   const long long rest = job - (long long)tensor * n_heads * nblk;
   const long long bh = rest / nblk;
-  const int i0 = (int)(rest % nblk) * SPW;
-  const int seg = n / m, vpr = d / V;
-  const T* base = (tensor == 0 ? q : k) + (size_t)bh * n * d;
+  const int sl = lane / vpr, cg = lane - sl * vpr;
+  const int i = (int)(rest % nblk) * spw + sl;
+  const int seg = n / m;
   __nv_bfloat16* outb = tensor == 0 ? qt_b : kt_b;
-  float* outf = (tensor == 0 ? qt : kt) + (size_t)bh * m * d;
-  uint4 buf[SPW][VPL];
+  if (i >= m64) return;
+  if (i >= m) {
+    if (outb)
+      for (int c = cg * V; c < dpad; c += vpr * V)
 #pragma unroll
-  for (int si = 0; si < SPW; ++si) {
-    const int i = i0 + si;
-    const uint4* src4 = reinterpret_cast<const uint4*>(base + (size_t)i * seg * d);
-#pragma unroll
-    for (int u = 0; u < VPL; ++u)
-      buf[si][u] = (i < m) ? __ldg(src4 + lane + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+        for (int e = 0; e < V; ++e) outb[((size_t)bh * m64 + i) * dpad + c + e] = __float2bfloat16_rn(0.f);
+    return;
   }
-  const float inv = 1.f / (float)seg;
+  const uint4* src = reinterpret_cast<const uint4*>((tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)i * seg) * d) + cg;
+  float acc[V];
 #pragma unroll
-  for (int si = 0; si < SPW; ++si) {
-    const int i = i0 + si;
-    float acc[V];
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  for (int r0 = 0; r0 < seg; r0 += 8) {
+    uint4 u[8];
 #pragma unroll
-    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    for (int r = 0; r < 8; ++r) u[r] = r0 + r < seg ? __ldg(src + (size_t)(r0 + r) * vpr) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-      const T* x = reinterpret_cast<const T*>(&buf[si][u]);
+    for (int r = 0; r < 8; ++r) {
+      const T* x = reinterpret_cast<const T*>(&u[r]);
 #pragma unroll
       for (int e = 0; e < V; ++e) acc[e] += ld(x + e);
     }
-    for (int o = vpr; o < 32; o <<= 1)
+  }
+  const float inv = 1.f / (float)seg;
+  // V consecutive means as 16-byte stores (cg * V elements into a row of
+  // d >= 8: 16-byte aligned)
+  float* out = (tensor == 0 ? qt : kt) + ((size_t)bh * m + i) * d + cg * V;
 #pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-    if (i >= m64) continue;
-    if (i >= m) {
-      if (outb)
-        for (int c = lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
-      continue;
+  for (int e = 0; e < V; e += 4)
+    *reinterpret_cast<float4*>(out + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
+  if (outb) {
+    __nv_bfloat16* ob = outb + ((size_t)bh * m64 + i) * dpad + cg * V;
+    if constexpr (V == 8) {
+      __nv_bfloat162 h2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+      *reinterpret_cast<uint4*>(ob) = *reinterpret_cast<const uint4*>(h2);
+    } else {
+#pragma unroll
+      for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
     }
-    if (lane < vpr) {
-      // V consecutive means as 16-byte stores (rows are d >= 8 elements,
-      // lane * V elements in: 16-byte aligned)
-      float* out = outf + (size_t)i * d + lane * V;
+    for (int c = d + cg * V; c < dpad; c += vpr * V)
 #pragma unroll
-      for (int e = 0; e < V; e += 4)
-        *reinterpret_cast<float4*>(out + e) =
-            make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
-      if (outb) {
-        __nv_bfloat16* ob = outb + ((size_t)bh * m64 + i) * dpad + lane * V;
-        if constexpr (V == 8) {
-          __nv_bfloat162 h2[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-          *reinterpret_cast<uint4*>(ob) = *reinterpret_cast<const uint4*>(h2);
-        } else {
-#pragma unroll
-          for (int e = 0; e < V; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
-        }
-      }
-    }
-    if (outb)
-      for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
+      for (int e = 0; e < V; ++e) outb[((size_t)bh * m64 + i) * dpad + c + e] = __float2bfloat16_rn(0.f);
   }
 }
 
@@ -303,6 +295,59 @@ rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __rest
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- merge G
+// G = merge of the key-split partials (bullets 3 and 6: softmax(Q~ K^T s) V
+// from the per-range sums). One thread per float4 of G; splits eight at a
+// time with all their loads in flight, a running (max, denominator) that
+// rescales the accumulated sum as in an online softmax; an empty partial
+// (max = -inf) was never written and contributes nothing.
+// grid ceil(B*H * m * d / 4 / 256), block 256.
+__global__ void __launch_bounds__(256)
+merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __restrict__ g,
+        long long total4, int m, int d, int splits) {
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (e >= total4) return;
+  const int d4 = d >> 2;
+  const long long row = e / d4;  // bh * m + i
+  const int q = (int)(e - row * d4);
+  const long long bh = row / m;
+  const int i = (int)(row - bh * m);
+  const float2* ml = reinterpret_cast<const float2*>(gml) + bh * splits * m + i;
+  const float4* src = reinterpret_cast<const float4*>(gp + ((size_t)bh * splits * m + i) * d) + q;
+  const size_t sstride = (size_t)m * d4;  // float4s between splits
+  float gm = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < splits; sp += 8) {
+    float2 mk[8];
+    float4 o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s2 = sp + k < splits ? sp + k : sp;
+      mk[k] = __ldg(ml + (size_t)s2 * m);
+      o[k] = __ldg(src + (size_t)s2 * sstride);
+    }
+    float cm = gm;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (sp + k < splits && mk[k].x != -INFINITY) cm = fmaxf(cm, mk[k].x);
+    if (cm == -INFINITY) continue;  // only empty partials so far
+    const float rs = gm == -INFINITY ? 0.f : expf(gm - cm);
+    den *= rs;
+    acc = make_float4(acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (sp + k < splits && mk[k].x != -INFINITY) {
+        const float f = expf(mk[k].x - cm);
+        den = fmaf(mk[k].y, f, den);
+        acc = make_float4(fmaf(o[k].x, f, acc.x), fmaf(o[k].y, f, acc.y), fmaf(o[k].z, f, acc.z),
+                          fmaf(o[k].w, f, acc.w));
+      }
+    gm = cm;
+  }
+  const float inv = 1.f / den;
+  reinterpret_cast<float4*>(g)[e] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // -------------------------------------------------------------------- pinv
@@ -588,18 +633,12 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
   const T* kk = static_cast<const T*>(k);
   const int vpr = s.d / (16 / (int)sizeof(T));
   const long long nvec = (long long)s.seg() * vpr;
-  if (32 % vpr == 0 && (nvec == 32 || nvec == 64 || nvec == 128)) {
-    const int vpl = (int)(nvec / 32);
-    const int spw = 8 / vpl;
+  if (32 % vpr == 0 && nvec <= 128) {
+    const int spw = 32 / vpr;
     const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
     const unsigned grid = (unsigned)((jobs + 7) / 8);
     KernelScope ks_("landmarks_vec", stream);
-    if (vpl == 1)
-      landmarks_small<T, 1><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
-    else if (vpl == 2)
-      landmarks_small<T, 2><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
-    else
-      landmarks_small<T, 4><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+    landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
   } else if (32 % vpr == 0) {
     const long long jobs = 2ll * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
@@ -666,6 +705,15 @@ int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const flo
   pinv_simt<<<(unsigned)s.bh(), 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scratch, wt_b, s.d,
                                                   s.m, splits, s.iters,
                                                   1.0f / sqrtf((float)s.d), s.m64(), s.dpad());
+  return launch_status();
+}
+
+int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,
+                   cudaStream_t stream) {
+  if (s.d % 4 != 0) return NYS_ERR_UNSUPPORTED;
+  const long long total4 = s.bh() * s.m * (s.d / 4);
+  KernelScope ks_("merge_g", stream);
+  merge_g<<<(unsigned)((total4 + 255) / 256), 256, 0, stream>>>(gp, gml, g, total4, s.m, s.d, splits);
   return launch_status();
 }
 

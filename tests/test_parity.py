@@ -75,6 +75,8 @@ SMALL = [
     (2, 1, 640, 128, 160, 6, 0),   # d = 128, m = 160, no conv
     (2, 10, 1152, 128, 192, 6, 33),  # several heads per CTA range
     (20, 1, 1152, 128, 192, 4, 9),   # consecutive heads sharing conv taps
+    (4, 32, 256, 64, 128, 6, 9),     # pseudo-inverse after the landmark rows (128 CTAs)
+    (8, 48, 128, 64, 64, 6, 5),      # pseudo-inverse two CTAs per SM beside the rows
 ]
 
 
@@ -96,9 +98,10 @@ def test_small_shapes(shape, dtype):
 # ------------------------------------------------------------------ stages ----
 
 # few heads: the pseudo-inverse runs beside the landmark-row pass and W = Z G
-# is formed afterwards; 256 heads: two head groups, the pseudo-inverse
-# kernel merges G and forms W itself
-STAGE_SHAPES = [(2, 2, 512, 64, 64), (16, 16, 256, 64, 64)]
+# is formed afterwards; 128 heads of m = 128 (one CTA each, more than half of
+# the SMs): the pseudo-inverse runs after the landmark rows, merges G and
+# forms W itself
+STAGE_SHAPES = [(2, 2, 512, 64, 64), (16, 8, 512, 64, 128)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
