@@ -128,11 +128,17 @@ int nystrom_attn_fwd_noalloc(const void* q, const void* k, const void* v,
 
 /*
  * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
- * copies q, k, v, conv_w to the device, runs nystrom_attn_fwd on `stream`,
- * copies out back and waits for the stream. Host buffers should be pinned
- * (page-locked) for full copy speed; pageable memory works but is slower.
- * Device staging buffers are allocated and cached per device (grown with
- * cudaMalloc when needed). Synchronous: out_host is complete on return.
+ * copies q, k, v, conv_w to the device, runs the forward pass on `stream`,
+ * copies out back and waits for the stream. The batch is processed in up
+ * to four chunks of whole batch entries, pipelined: a chunk's inputs are
+ * copied up (on a library stream) while the previous chunk is computed on
+ * `stream` and the one before it is copied back (on another library
+ * stream). Host buffers should be pinned (page-locked) for full copy speed;
+ * pageable memory works but is slower. Device staging buffers are
+ * allocated and cached per device (grown with cudaMalloc when needed); one
+ * host-entry call per device runs at a time. Synchronous: out_host is
+ * complete on return; nystrom_get_status then reports the status of all
+ * chunks.
  */
 int nystrom_attn_fwd_host(const void* q_host, const void* k_host,
                           const void* v_host, const float* conv_w_host,

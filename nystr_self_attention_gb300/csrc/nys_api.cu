@@ -101,6 +101,8 @@ int check_device(int* dev_out) {
 }
 
 namespace {
+constexpr int kHostChunks = 4;  // batch chunks of the pipelined host entry
+
 struct DeviceCache {
   std::mutex mu;
   void* ws = nullptr;
@@ -108,6 +110,12 @@ struct DeviceCache {
   void* last_ws = nullptr;  // status word of the most recent call
   void* stage = nullptr;    // host-entry staging buffers
   size_t stage_bytes = 0;
+  // host entry: one call at a time per device (it owns the staging buffers);
+  // copy streams and events of its pipeline, created on first use
+  std::mutex host_mu;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_in[kHostChunks] = {}, ev_comp[kHostChunks] = {};
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -135,15 +143,17 @@ int ensure_buffer(void** ptr, size_t* have, size_t need) {
 }  // namespace
 
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
-        void* out, char* ws, cudaStream_t stream, int dev) {
+        void* out, char* ws, cudaStream_t stream, int dev, bool clear_status) {
   const Layout L = make_layout(s);
   {
     std::lock_guard<std::mutex> lk(g_dev[dev].mu);
     g_dev[dev].last_ws = ws;
   }
   // each call starts with a clear status word (kernels only ever set it)
-  cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return set_cuda_error(e);
+  if (clear_status) {
+    cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
   const int rc = launch_forward(s, q, k, v, conv_w, out, ws, L, stream, dev);
   return rc;
 }
@@ -259,34 +269,82 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_
   int dev = 0;
   rc = check_device(&dev);
   if (rc != NYS_OK) return rc;
+  DeviceCache& dc = g_dev[dev];
+  std::lock_guard<std::mutex> host_lk(dc.host_mu);
+  const size_t esz = dtype == NYS_FP32 ? 4 : 2;
   const size_t elems = (size_t)B * H * n * d;
-  const size_t tb = align256(elems * (dtype == NYS_FP32 ? 4 : 2));
+  const size_t tb = align256(elems * esz);
   const size_t wb = align256((size_t)H * (conv_ks > 0 ? conv_ks : 1) * 4);
   char* base = nullptr;
   {
-    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
-    rc = ensure_buffer(&g_dev[dev].stage, &g_dev[dev].stage_bytes, 4 * tb + wb);
+    std::lock_guard<std::mutex> lk(dc.mu);
+    rc = ensure_buffer(&dc.stage, &dc.stage_bytes, 4 * tb + wb);
     if (rc != NYS_OK) return rc;
-    base = static_cast<char*>(g_dev[dev].stage);
+    base = static_cast<char*>(dc.stage);
   }
   char *dq = base, *dk = base + tb, *dv = base + 2 * tb, *dout = base + 3 * tb;
   float* dw = reinterpret_cast<float*>(base + 4 * tb);
-  const size_t bytes = elems * (dtype == NYS_FP32 ? 4 : 2);
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(dq, q_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(dk, k_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(dv, v_host, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+  cudaError_t e = cudaSuccess;
+  if (!dc.h2d) {
+    e = cudaStreamCreateWithFlags(&dc.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&dc.d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dc.ev_start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dc.ev_done, cudaEventDisableTiming);
+    for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+      e = cudaEventCreateWithFlags(&dc.ev_in[c], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dc.ev_comp[c], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  // Pipeline over chunks of whole batch entries: chunk c's inputs go up on
+  // the h2d stream while chunk c - 1 is computed on `stream` and chunk c - 2's
+  // output comes back on the d2h stream (the two copy directions overlap;
+  // uploading q, k and v on separate streams was slower).
+  int chunks = B < kHostChunks ? B : kHostChunks;
+  while (B % chunks != 0) --chunks;
+  const int bc = B / chunks;
+  const size_t cbytes = (size_t)bc * H * n * d * esz;
+  const Shape sc{bc, H, n, d, m, iters, conv_ks, dtype};
+  char* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(dc.mu);
+    rc = ensure_buffer(&dc.ws, &dc.ws_bytes, make_layout(sc).total);
+    if (rc != NYS_OK) return rc;
+    ws = static_cast<char*>(dc.ws);
+  }
+  if ((e = cudaEventRecord(dc.ev_start, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(dc.h2d, dc.ev_start, 0)) != cudaSuccess)
     return set_cuda_error(e);
   if (conv_ks > 0 &&
       (e = cudaMemcpyAsync(dw, conv_w_host, (size_t)H * conv_ks * 4, cudaMemcpyHostToDevice,
-                           stream)) != cudaSuccess)
+                           dc.h2d)) != cudaSuccess)
     return set_cuda_error(e);
-  rc = nystrom_attn_fwd(dq, dk, dv, conv_ks > 0 ? dw : nullptr, dout, B, H, n, d, m, iters,
-                        conv_ks, dtype, stream);
-  if (rc != NYS_OK) return rc;
-  if ((e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+  for (int c = 0; c < chunks; ++c) {
+    const size_t off = (size_t)c * cbytes;
+    if ((e = cudaMemcpyAsync(dq + off, static_cast<const char*>(q_host) + off, cbytes,
+                             cudaMemcpyHostToDevice, dc.h2d)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk + off, static_cast<const char*>(k_host) + off, cbytes,
+                             cudaMemcpyHostToDevice, dc.h2d)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv + off, static_cast<const char*>(v_host) + off, cbytes,
+                             cudaMemcpyHostToDevice, dc.h2d)) != cudaSuccess ||
+        (e = cudaEventRecord(dc.ev_in[c], dc.h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, dc.ev_in[c], 0)) != cudaSuccess)
+      return set_cuda_error(e);
+    // the chunks share the library workspace (in stream order) and its
+    // status word, which only the first clears
+    rc = run(sc, dq + off, dk + off, dv + off, conv_ks > 0 ? dw : nullptr, dout + off, ws, stream,
+             dev, c == 0);
+    if (rc != NYS_OK) return rc;
+    if ((e = cudaEventRecord(dc.ev_comp[c], stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(dc.d2h, dc.ev_comp[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(static_cast<char*>(out_host) + off, dout + off, cbytes,
+                             cudaMemcpyDeviceToHost, dc.d2h)) != cudaSuccess)
+      return set_cuda_error(e);
+  }
+  if ((e = cudaEventRecord(dc.ev_done, dc.d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, dc.ev_done, 0)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess)
     return set_cuda_error(e);
-  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return set_cuda_error(e);
   return NYS_OK;
 }
 

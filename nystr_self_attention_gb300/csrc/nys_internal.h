@@ -76,9 +76,10 @@ int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype)
 int check_args(const void* q, const void* k, const void* v, const float* conv_w, const void* out,
                int B, int H, int n, int d, int m, int iters, int ks, int dtype);
 int check_device(int* dev_out);  // current device, must be compute capability 10.3
-// Clears the status word and enqueues the forward pass with workspace `ws`.
+// Clears the status word (unless told not to) and enqueues the forward
+// pass with workspace `ws`.
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
-        void* out, char* ws, cudaStream_t stream, int dev);
+        void* out, char* ws, cudaStream_t stream, int dev, bool clear_status = true);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();
