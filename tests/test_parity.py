@@ -77,6 +77,9 @@ SMALL = [
     (20, 1, 1152, 128, 192, 4, 9),   # consecutive heads sharing conv taps
     (4, 32, 256, 64, 128, 6, 9),     # pseudo-inverse after the landmark rows (128 CTAs)
     (8, 48, 128, 64, 64, 6, 5),      # pseudo-inverse two CTAs per SM beside the rows
+    (1, 152, 128, 64, 64, 4, 3),     # 76 pseudo-inverse CTAs: one per SM, the last such shape
+    (1, 154, 128, 64, 64, 4, 3),     # 77 CTAs: two per SM
+    (2, 210, 128, 32, 64, 2, 3),     # 210 CTAs: too many beside the rows, two head groups
 ]
 
 
