@@ -387,28 +387,29 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
         ++cnt_s;
         tc_fence_after_sync();
         if (warp_live) {
-          // tile max: all four column chunks of S in flight at once
+          // tile max: all four column chunks of S in flight at once; on a
+          // full tile of live rows the chunks stay in registers for the
+          // exponentials (S is read from TMEM once)
           float tmax = -INFINITY;
-          {
-            uint32_t r0[32], r1[32], r2[32], r3[32];
-            tmem_ld32(scol, r0);
-            tmem_ld32(scol + 32, r1);
-            tmem_ld32(scol + 64, r2);
-            tmem_ld32(scol + 96, r3);
-            tmem_ld_wait();
-            if (key0 + 128 <= p.n) {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(scol, r0);
+          tmem_ld32(scol + 32, r1);
+          tmem_ld32(scol + 64, r2);
+          tmem_ld32(scol + 96, r3);
+          tmem_ld_wait();
+          const bool fast = warp_all_live && key0 + 128 <= p.n;  // warp-uniform
+          if (key0 + 128 <= p.n) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                tmax = fmaxf(tmax, fmaxf(fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])),
-                                         fmaxf(__uint_as_float(r2[e]), __uint_as_float(r3[e]))));
-            } else {
+            for (int e = 0; e < 32; ++e)
+              tmax = fmaxf(tmax, fmaxf(fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])),
+                                       fmaxf(__uint_as_float(r2[e]), __uint_as_float(r3[e]))));
+          } else {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                if (key0 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r0[e]));
-                if (key0 + 32 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r1[e]));
-                if (key0 + 64 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r2[e]));
-                if (key0 + 96 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r3[e]));
-              }
+            for (int e = 0; e < 32; ++e) {
+              if (key0 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r0[e]));
+              if (key0 + 32 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r1[e]));
+              if (key0 + 64 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r2[e]));
+              if (key0 + 96 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r3[e]));
             }
           }
           const bool rebase = live && (m_run == -INFINITY || (tmax - m_run) * p.c > kRebase);
@@ -418,26 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
             l_run *= alpha;
             m_run = tmax;
           }
-          if (mine > 0 && __any_sync(0xffffffffu, rebase)) {
-            // rescale the accumulator rows (the group's earlier P V are done)
-#pragma unroll 1
-            for (int c0 = 0; c0 < DP; c0 += 32) {
-              uint32_t r[32];
-              tmem_ld32(ocol + c0, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(ocol + c0, r);
-            }
-          }
           const float mc = m_run * p.c;
-          if (warp_all_live && key0 + 128 <= p.n) {
-            // P = 2^(S c - M c), no masks
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-              uint32_t r[32];
-              tmem_ld32(scol + c0, r);
-              tmem_ld_wait();
+          if (fast) {
+            // P = 2^(S c - M c), no masks, from the registers; P of chunk c
+            // goes to columns c0 / 2 .. (already read)
+            auto exp_chunk = [&](int c0, const uint32_t (&r)[32]) {
               uint32_t pk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
@@ -447,7 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
                 pk[e] = pack_bf16x2(a, b);
               }
               tmem_st16(scol + (c0 >> 1), pk);
-            }
+            };
+            exp_chunk(0, r0);
+            exp_chunk(32, r1);
+            exp_chunk(64, r2);
+            exp_chunk(96, r3);
           } else {
             // padding rows and keys past the end give P = 0
 #pragma unroll 1
@@ -465,6 +455,19 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
                 pk[e] = pack_bf16x2(a, b);
               }
               tmem_st16(scol + (c0 >> 1), pk);
+            }
+          }
+          if (mine > 0 && __any_sync(0xffffffffu, rebase)) {
+            // rescale the accumulator rows before this item's P V (the
+            // group's earlier P V are done: S of this item waited for them)
+#pragma unroll 1
+            for (int c0 = 0; c0 < DP; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld32(ocol + c0, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(ocol + c0, r);
             }
           }
           tmem_st_wait();
