@@ -299,23 +299,22 @@ rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __rest
 
 // ---------------------------------------------------------------- merge G
 // G = merge of the key-split partials (bullets 3 and 6: softmax(Q~ K^T s) V
-// from the per-range sums). One thread per float4 of G; splits eight at a
-// time with all their loads in flight, a running (max, denominator) that
+// from the per-range sums). One thread per float4 of G (a column of CTAs
+// per head: no 64-bit index divisions); splits eight at a time with all
+// their loads in flight, a running (max, denominator) that
 // rescales the accumulated sum as in an online softmax; an empty partial
 // (max = -inf) was never written and contributes nothing.
-// grid ceil(B*H * m * d / 4 / 256), block 256.
+// grid (B*H, ceil(m * d / 4 / 256)), block 256.
 __global__ void __launch_bounds__(256)
-merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __restrict__ g,
-        long long total4, int m, int d, int splits) {
-  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
-  if (e >= total4) return;
+merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __restrict__ g, int m,
+        int d, int splits) {
   const int d4 = d >> 2;
-  const long long row = e / d4;  // bh * m + i
-  const int q = (int)(e - row * d4);
-  const long long bh = row / m;
-  const int i = (int)(row - bh * m);
-  const float2* ml = reinterpret_cast<const float2*>(gml) + bh * splits * m + i;
-  const float4* src = reinterpret_cast<const float4*>(gp + ((size_t)bh * splits * m + i) * d) + q;
+  const int e = (int)blockIdx.y * 256 + (int)threadIdx.x;  // float4 of this head's G
+  if (e >= m * d4) return;
+  const long long bh = blockIdx.x;
+  const int i = e / d4;
+  const float2* ml = reinterpret_cast<const float2*>(gml) + (bh * splits * m + i);
+  const float4* src = reinterpret_cast<const float4*>(gp) + bh * splits * m * d4 + e;
   const size_t sstride = (size_t)m * d4;  // float4s between splits
   float gm = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -347,7 +346,7 @@ merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __re
     gm = cm;
   }
   const float inv = 1.f / den;
-  reinterpret_cast<float4*>(g)[e] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  reinterpret_cast<float4*>(g)[bh * m * d4 + e] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // -------------------------------------------------------------------- pinv
@@ -711,9 +710,10 @@ int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const flo
 int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,
                    cudaStream_t stream) {
   if (s.d % 4 != 0) return NYS_ERR_UNSUPPORTED;
-  const long long total4 = s.bh() * s.m * (s.d / 4);
+  const int per_head4 = s.m * (s.d / 4);
   KernelScope ks_("merge_g", stream);
-  merge_g<<<(unsigned)((total4 + 255) / 256), 256, 0, stream>>>(gp, gml, g, total4, s.m, s.d, splits);
+  merge_g<<<dim3((unsigned)s.bh(), (unsigned)((per_head4 + 255) / 256)), 256, 0, stream>>>(
+      gp, gml, g, s.m, s.d, splits);
   return launch_status();
 }
 
