@@ -27,7 +27,8 @@
 //
 // Z-only mode (z given): no merge and no W; Z goes out in fp32 so that the
 // kernel can run before the key-split partials exist. The second kernel
-// here, w_tc, then merges G and forms W = Z G (16 columns per CTA).
+// here, w_tc, then forms W = Z G from Z and the G merged by merge_g (16 to
+// 64 columns of a head per CTA).
 #include <cuda_bf16.h>
 
 #include <algorithm>
