@@ -7,12 +7,14 @@
 //
 // Persistent CTAs, one per SM, each take an equal contiguous range of the
 // flattened (head, 128-key tile) space; the part of the range inside one
-// head is a "unit" and yields that CTA's partial(s) for the head. Two
+// head is a "unit" and yields that CTA's partial for the head. Two
 // softmax warpgroups work in ping-pong on two independent streams of work
 // items, each with its own S/P buffer and O accumulator in TMEM:
 //   m > 128:  group g = landmark rows [128 g, 128 g + 128): both groups use
 //             every K/V tile, so K and V are read once for all m rows;
-//   m <= 128: group g = alternate key tiles of the unit (two partials).
+//   m <= 128: group g = alternate key tiles of the unit; at the unit's end
+//             group 0 combines both groups' (max, sum, O) into the one
+//             partial.
 // Per item (group g, key tile j):
 //   S_g = Q~_g K_j^T         tcgen05, A = Q~ (smem), B = K tile (smem)
 //   online softmax           thread = landmark row, from TMEM; the running
@@ -72,6 +74,7 @@ struct Bars {
   uint64_t full[8], empty[8];  // K/V slots
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_full[2], o_empty[2];
+  uint64_t x_ready;  // m <= 128: group 1's (max, sum) of the unit handed to group 0
   uint64_t fin;
 };
 
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
   uint8_t* stage_s = sm + p.nq * qbuf_bytes;            // [8 warps][kStageWarp]
   uint8_t* kv_s = stage_s + 8 * kStageWarp;             // [ns][TILE]
   __shared__ Bars bars;
+  __shared__ float xm_s[128], xl_s[128];  // group 1's (max, sum) per row, m <= 128
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   volatile int* abort_flag = &abort_sh;
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
       mbar_init(&bars.o_empty[i], 128);
     }
     mbar_init(&bars.fin, 2);
+    mbar_init(&bars.x_ready, 128);
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -479,15 +484,55 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
         ++mine;
       }
       if (!ok) break;
-      // epilogue of this unit: partial O (unnormalised), max, sum. A group
-      // with no item in the unit writes only (max, sum) = (-inf, 0): the
-      // merge skips such partials.
+      // epilogue of this unit: one partial O (unnormalised), max, sum. For
+      // m > 128 each group writes its rows; for m <= 128 the two groups
+      // covered alternate key tiles of the same rows: group 1 hands its
+      // (max, sum) to group 0, which writes the combined partial and frees
+      // both accumulators. A unit without items writes (max, sum) = (-inf,
+      // 0): the merges skip such partials.
       if (!__all_sync(0xffffffffu, wait_or_fail(&bars.o_full[g], cnt_o & 1, p.status, abort_flag))) break;
       ++cnt_o;
       tc_fence_after_sync();
-      const int part = p.big ? u.piece : 2 * u.piece + g;
+      if (!p.big && g == 1) {
+        xm_s[lr] = mine > 0 ? m_run : -INFINITY;
+        xl_s[lr] = mine > 0 ? l_run : 0.f;
+        mbar_arrive(&bars.x_ready);
+        tglob += U;
+        continue;
+      }
+      float m_out = mine > 0 ? m_run : -INFINITY, l_out = mine > 0 ? l_run : 0.f;
+      float a0 = 1.f, a1 = 0.f;  // weights of this group's and group 1's O
+      if (!p.big) {
+        if (!__all_sync(0xffffffffu, wait_or_fail(&bars.x_ready, (cnt_o - 1) & 1, p.status, abort_flag))) break;
+        const float m1 = xm_s[lr], l1 = xl_s[lr];
+        const float mx = fmaxf(m_out, m1);
+        a0 = m_out == -INFINITY ? 0.f : fast_exp2((m_out - mx) * p.c);
+        a1 = m1 == -INFINITY ? 0.f : fast_exp2((m1 - mx) * p.c);
+        l_out = l_out * a0 + l1 * a1;
+        m_out = mx;
+      }
+      const uint32_t ocol1 = tmem + lo + COL_O + DP;  // group 1's O, same rows
+      // combined chunk of O: a0 O_g + a1 O_1 (a zero weight drops its term,
+      // whatever an accumulator without items holds)
+      auto o_chunk = [&](int c0, uint32_t (&r)[32]) {
+        tmem_ld32(ocol + c0, r);
+        if (!p.big) {
+          uint32_t r1[32];
+          tmem_ld32(ocol1 + c0, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x0 = a0 != 0.f ? a0 * __uint_as_float(r[e]) : 0.f;
+            const float x1 = a1 != 0.f ? a1 * __uint_as_float(r1[e]) : 0.f;
+            r[e] = __float_as_uint(x0 + x1);
+          }
+        } else {
+          tmem_ld_wait();
+        }
+      };
+      const int part = u.piece;
       const size_t prow = ((size_t)u.bh * p.parts + part) * p.m + row;
-      if (warp_live && mine > 0) {
+      if (warp_live && __any_sync(0xffffffffu, m_out != -INFINITY)) {
         if (kStageWarp > 0 && warp_all_live) {
           uint8_t* st = stage_s + warp * kStageWarp;
           if (lane == 0) bulk_wait_read0();  // this warp's previous store has read st
@@ -495,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
 #pragma unroll
           for (int b = 0; b < DP / 32; ++b) {
             uint32_t r[32];
-            tmem_ld32(ocol + 32 * b, r);
-            tmem_ld_wait();
+            o_chunk(32 * b, r);
             uint8_t* box = st + b * 4096 + lane * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -515,8 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
 #pragma unroll
           for (int c0 = 0; c0 < DP; c0 += 32) {
             uint32_t r[32];
-            tmem_ld32(ocol + c0, r);
-            tmem_ld_wait();
+            o_chunk(c0, r);
             if (live && c0 < p.d) {
               float4* dst = reinterpret_cast<float4*>(o + c0);
 #pragma unroll
@@ -529,15 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
       }
       tc_fence_before_sync();
       mbar_arrive(&bars.o_empty[g]);
+      if (!p.big) mbar_arrive(&bars.o_empty[1]);  // group 1's accumulator, read above
       if (live) {
-        p.gml[prow * 2 + 0] = m_run * p.scale;  // -inf for an empty partial
-        p.gml[prow * 2 + 1] = l_run;
+        p.gml[prow * 2 + 0] = m_out * p.scale;  // -inf for an empty partial
+        p.gml[prow * 2 + 1] = l_out;
       }
       // the head's last range also marks the partial slots no range uses
       if (u.last_piece && live) {
         for (int pc = u.piece + 1; pc < p.pieces_max; ++pc) {
-          const int part2 = p.big ? pc : 2 * pc + g;
-          const size_t prow2 = ((size_t)u.bh * p.parts + part2) * p.m + row;
+          const size_t prow2 = ((size_t)u.bh * p.parts + pc) * p.m + row;
           p.gml[prow2 * 2 + 0] = -INFINITY;
           p.gml[prow2 * 2 + 1] = 0.f;
         }
@@ -561,7 +604,7 @@ int nq_of(const Shape& s) { return s.m > 128 ? 1 : 2; }
 // Ranges of the tensor-core landmark-row kernel (host math): every CTA of a
 // full-GPU launch gets tiles_per_cta consecutive tiles of the flattened
 // (head, tile) space; a head is touched by at most pieces ranges, each giving
-// one partial (m > 128) or two (m <= 128).
+// one partial.
 void rows_tc_split(const Shape& s, int ctas, int* parts, int* tiles_per_cta) {
   const long long kCtas = ctas > 0 ? ctas : 1;
   const long long n_tiles = (s.n + 127) / 128;
@@ -571,7 +614,7 @@ void rows_tc_split(const Shape& s, int ctas, int* parts, int* tiles_per_cta) {
   long long pieces = (n_tiles + tpc - 1) / tpc + 1;
   if (pieces > n_tiles) pieces = n_tiles;
   *tiles_per_cta = (int)tpc;
-  *parts = (int)(s.m > 128 ? pieces : 2 * pieces);
+  *parts = (int)pieces;
 }
 
 int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const void* v, float* gpart,
@@ -619,7 +662,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
   p.total = (int)(BH * p.n_tiles);
   p.parts = parts;
   p.big = s.m > 128 ? 1 : 0;
-  p.pieces_max = p.big ? parts : parts / 2;
+  p.pieces_max = parts;
   p.scale = 1.0f / sqrtf((float)s.d);
   p.c = p.scale * 1.4426950408889634f;
   const size_t tile = (size_t)(DP / 64) * 16384;
