@@ -102,8 +102,20 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int v = lane; v < nvec; v += 32) {
+  // eight 16-byte loads in flight per lane, then the sums
+  int v = lane;
+  for (; v + 7 * 32 < nvec; v += 8 * 32) {
+    uint4 u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) u[r] = __ldg(src4 + v + 32 * r);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const T* x = reinterpret_cast<const T*>(&u[r]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += ld(x + e);
+    }
+  }
+  for (; v < nvec; v += 32) {
     const uint4 u = __ldg(src4 + v);
     const T* x = reinterpret_cast<const T*>(&u);
 #pragma unroll
