@@ -312,11 +312,13 @@ rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __rest
 // ---------------------------------------------------------------- merge G
 // G = merge of the key-split partials (bullets 3 and 6: softmax(Q~ K^T s) V
 // from the per-range sums). One thread per float4 of G (a column of CTAs
-// per head: no 64-bit index divisions); splits eight at a time with all
-// their loads in flight, a running (max, denominator) that
-// rescales the accumulated sum as in an online softmax; an empty partial
-// (max = -inf) was never written and contributes nothing.
+// per head: no 64-bit index divisions); splits in batches of SB (no more
+// than there are, up to eight) with all their loads in flight, a running
+// (max, denominator) that rescales the accumulated sum as in an online
+// softmax; an empty partial (max = -inf) was never written and contributes
+// nothing.
 // grid (B*H, ceil(m * d / 4 / 256)), block 256.
+template <int SB>  // splits per batch of loads (2, 4 or 8)
 __global__ void __launch_bounds__(256)
 merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __restrict__ g, int m,
         int d, int splits) {
@@ -330,25 +332,25 @@ merge_g(const float* __restrict__ gp, const float* __restrict__ gml, float* __re
   const size_t sstride = (size_t)m * d4;  // float4s between splits
   float gm = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sp = 0; sp < splits; sp += 8) {
-    float2 mk[8];
-    float4 o[8];
+  for (int sp = 0; sp < splits; sp += SB) {
+    float2 mk[SB];
+    float4 o[SB];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < SB; ++k) {
       const int s2 = sp + k < splits ? sp + k : sp;
       mk[k] = __ldg(ml + (size_t)s2 * m);
       o[k] = __ldg(src + (size_t)s2 * sstride);
     }
     float cm = gm;
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < SB; ++k)
       if (sp + k < splits && mk[k].x != -INFINITY) cm = fmaxf(cm, mk[k].x);
     if (cm == -INFINITY) continue;  // only empty partials so far
     const float rs = gm == -INFINITY ? 0.f : expf(gm - cm);
     den *= rs;
     acc = make_float4(acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < SB; ++k)
       if (sp + k < splits && mk[k].x != -INFINITY) {
         const float f = expf(mk[k].x - cm);
         den = fmaf(mk[k].y, f, den);
@@ -724,8 +726,13 @@ int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, 
   if (s.d % 4 != 0) return NYS_ERR_UNSUPPORTED;
   const int per_head4 = s.m * (s.d / 4);
   KernelScope ks_("merge_g", stream);
-  merge_g<<<dim3((unsigned)s.bh(), (unsigned)((per_head4 + 255) / 256)), 256, 0, stream>>>(
-      gp, gml, g, s.m, s.d, splits);
+  const dim3 grid((unsigned)s.bh(), (unsigned)((per_head4 + 255) / 256));
+  if (splits <= 2)
+    merge_g<2><<<grid, 256, 0, stream>>>(gp, gml, g, s.m, s.d, splits);
+  else if (splits <= 4)
+    merge_g<4><<<grid, 256, 0, stream>>>(gp, gml, g, s.m, s.d, splits);
+  else
+    merge_g<8><<<grid, 256, 0, stream>>>(gp, gml, g, s.m, s.d, splits);
   return launch_status();
 }
 
