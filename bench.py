@@ -54,6 +54,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU work budget of the oracle baseline sample")
+    p.add_argument("--scan-n", default=None,
+                   help="comma-separated sequence lengths: time one pass at each n with the "
+                        "workload's other sizes fixed, one JSON line per n (linear-time check)")
     return p.parse_args()
 
 
@@ -333,6 +336,82 @@ def pass_roofline(wl, ms_per_step, peaks, peak_src):
             "peak_source": f"hbm_gbs, bf16_tflops ({peak_src}); tf32 = bf16 x 1.1/2.25"}
 
 
+def resident_inputs(inp, dev):
+    """Device copies of one drawn workload: as many (q, k, v, out) sets as it
+    takes for their total to exceed twice L2 (steps rotate over them), the
+    conv weights, and the bytes of one set."""
+    import torch
+    wl = inp.wl
+
+    def upload(x, bits):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    q0, k0, v0 = upload(inp.q, inp.q_bits), upload(inp.k, inp.k_bits), upload(inp.v, inp.v_bits)
+    w = torch.from_numpy(inp.conv_w).to(dev)
+    set_bytes = 4 * q0.numel() * q0.element_size()
+    nsets = max(1, min(8, -(-2 * L2_BYTES // set_bytes)))
+    sets = [(q0, k0, v0, torch.empty_like(q0))]
+    for _ in range(nsets - 1):
+        sets.append((q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)))
+    return sets, w, set_bytes
+
+
+def run_scan(args, wl):
+    """Time of one pass against the sequence length with every other size of
+    the workload fixed: linear time shows as flat tokens/s. One JSON line per
+    n (not the benchmark line)."""
+    import dataclasses
+
+    import torch
+
+    from nystr_self_attention_gb300 import build as nbuild
+    nbuild.build()
+    import nystr_self_attention_gb300 as N
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    dt_code = N.NYS_BF16 if wl.dtype == "bf16" else N.NYS_FP32
+    for n in [int(x) for x in args.scan_n.split(",") if x]:
+        wn = dataclasses.replace(wl, n=n)
+        if n % wn.m != 0:
+            print(json.dumps({"scan": "n", "n": n, "skipped": f"n is not a multiple of m={wn.m}"}))
+            continue
+        sets, w, _ = resident_inputs(workloads.make_inputs(wn), dev)
+
+        def step(i):
+            q, k, v, out = sets[i % len(sets)]
+            N.nystrom_attn_fwd(q, k, v, w, out, wn.B, wn.H, n, wn.d, wn.m, wn.iters, wn.ks,
+                               dt_code, stream)
+
+        for i in range(max(3, args.warmup)):
+            step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = args.steps if args.steps is not None else 50
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert N.nystrom_get_status(stream) == N.NYS_OK
+        ms = e0.elapsed_time(e1) / steps
+        print(json.dumps({
+            "scan": "n", "workload": wn.describe(), "n": n, "steps": steps, "ms_per_step": ms,
+            "tokens_per_s": wn.tokens / (ms / 1e3),
+            "ns_per_token_per_head": ms * 1e6 / n,
+            "pass_roofline_frac": pass_roofline(wn, ms, peaks, peak_src)["frac"],
+            "l2": f"{len(sets)} rotating input sets"}), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -351,19 +430,9 @@ def run_ours(args, wl):
     inp = workloads.make_inputs(wl)
     dt_code = N.NYS_BF16 if wl.dtype == "bf16" else N.NYS_FP32
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-
-    def upload(x, bits):
-        if wl.dtype == "bf16":
-            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(x).to(dev)
-
-    q0, k0, v0 = upload(inp.q, inp.q_bits), upload(inp.k, inp.k_bits), upload(inp.v, inp.v_bits)
-    w = torch.from_numpy(inp.conv_w).to(dev)
-    set_bytes = 4 * q0.numel() * q0.element_size()
-    nsets = max(1, min(8, -(-2 * L2_BYTES // set_bytes)))
-    sets = [(q0, k0, v0, torch.empty_like(q0))]
-    for _ in range(nsets - 1):
-        sets.append((q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)))
+    sets, w, set_bytes = resident_inputs(inp, dev)
+    nsets = len(sets)
+    q0, k0, v0 = sets[0][:3]
     B, H, n, d, m = wl.B, wl.H, wl.n, wl.d, wl.m
 
     def step(i):
@@ -510,6 +579,8 @@ def main():
         wl = dataclasses.replace(wl, B=args.batch)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.scan_n:
+        run_scan(args, wl)
     else:
         run_ours(args, wl)
 
