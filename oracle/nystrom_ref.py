@@ -28,7 +28,8 @@ run a fixed number of times with no early exit.
 
 Readings where the page is silent (each listed in the design notes):
 * all three softmaxes use the scale 1/sqrt(d) (d = head dimension);
-* segment i is rows [i*n/m, (i+1)*n/m) and n must be a multiple of m;
+* segment i is rows [floor(i*n/m), floor((i+1)*n/m)), which is n/m rows each
+  when m divides n and otherwise lengths floor(n/m) and ceil(n/m); m <= n;
 * ||.||_1 is the largest column abs-sum and ||.||_inf the largest row
   abs-sum, of each head's own A_S;
 * the depthwise convolution runs along the sequence with one filter of odd
@@ -44,7 +45,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "segment_means", "softmax_rows", "landmark_kernel", "pinv_initial",
+    "segment_bounds", "segment_means", "softmax_rows", "landmark_kernel", "pinv_initial",
     "pinv_step", "pinv_iterative", "landmark_rows", "token_rows",
     "depthwise_conv_seq", "nystrom_head", "nystrom_attention",
     "softmax_attention", "svd_pinv",
@@ -55,18 +56,29 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def segment_bounds(n, m):
+    """Row ranges of the m contiguous segments of n rows: segment i is rows
+    [floor(i n / m), floor((i + 1) n / m)). When m divides n every segment
+    has n/m rows; otherwise the lengths are floor(n/m) and ceil(n/m), spread
+    evenly (the reading used where n is not a multiple of m). Needs
+    1 <= m <= n so that no segment is empty."""
+    if m < 1 or m > n:
+        raise ValueError(f"segment means need 1 <= m <= n (n={n}, m={m})")
+    return [(i * n // m, (i + 1) * n // m) for i in range(m)]
+
+
 def segment_means(x, m):
     """Segment-means landmarks (Proposed method, bullet 4).
 
     x: [n, d]. Returns [m, d] whose row i is the plain average of the rows of
-    the i-th of m contiguous segments of equal length n/m.
+    segment i (see ``segment_bounds``).
     """
     x = _f64(x)
     n, d = x.shape
-    if m < 1 or n % m != 0:
-        raise ValueError(f"segment means need n % m == 0 (n={n}, m={m})")
-    seg = n // m
-    return x.reshape(m, seg, d).mean(axis=1)
+    out = np.empty((m, d))
+    for i, (lo, hi) in enumerate(segment_bounds(n, m)):
+        out[i] = x[lo:hi].mean(axis=0)
+    return out
 
 
 def softmax_rows(s):

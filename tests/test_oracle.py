@@ -45,30 +45,50 @@ def test_closed_form_worked_example():
 # ---------------------------------------------------------- segment means ----
 
 def brute_segment_means(x, m):
+    """Row t belongs to segment i iff floor(i n/m) <= t < floor((i+1) n/m),
+    i.e. i = ceil((t+1) m / n) - 1: each row is sent to its segment by that
+    formula and the rows of a segment are averaged one by one."""
     n, d = len(x), len(x[0])
-    seg = n // m
-    out = []
-    for i in range(m):
-        row = []
+    sums = [[0.0] * d for _ in range(m)]
+    counts = [0] * m
+    for t in range(n):
+        i = ((t + 1) * m + n - 1) // n - 1
+        counts[i] += 1
         for c in range(d):
-            tot = 0.0
-            for t in range(i * seg, (i + 1) * seg):
-                tot += x[t][c]
-            row.append(tot / seg)
-        out.append(row)
-    return np.array(out)
+            sums[i][c] += x[t][c]
+    return np.array([[sums[i][c] / counts[i] for c in range(d)] for i in range(m)])
 
 
-@pytest.mark.parametrize("n,m,d", [(12, 3, 2), (8, 8, 3), (9, 1, 4), (64, 16, 5)])
+@pytest.mark.parametrize("n,m,d", [(12, 3, 2), (8, 8, 3), (9, 1, 4), (64, 16, 5),
+                                   (10, 3, 2), (1000, 48, 3), (300, 256, 2), (5, 2, 3)])
 def test_segment_means_brute_force(n, m, d):
     x = rng(n * 31 + m).standard_normal((n, d))
     np.testing.assert_allclose(R.segment_means(x, m), brute_segment_means(x.tolist(), m),
-                               rtol=1e-15, atol=1e-15)
+                               rtol=1e-14, atol=1e-15)
 
 
-def test_segment_means_rejects_ragged():
+@pytest.mark.parametrize("n,m", [(10, 3), (1000, 48), (300, 256), (7, 7), (64, 16), (9, 1)])
+def test_segment_bounds_cover_the_rows_evenly(n, m):
+    b = R.segment_bounds(n, m)
+    assert b[0][0] == 0 and b[-1][1] == n
+    assert all(b[i][1] == b[i + 1][0] for i in range(m - 1))
+    assert {hi - lo for lo, hi in b} <= {n // m, -(-n // m)}
+    if n % m == 0:
+        assert all(hi - lo == n // m for lo, hi in b)
+
+
+def test_segment_means_of_piecewise_constant_rows_are_the_constants():
+    n, m = 1000, 48
+    vals = rng(5).standard_normal((m, 3))
+    x = np.empty((n, 3))
+    for i, (lo, hi) in enumerate(R.segment_bounds(n, m)):
+        x[lo:hi] = vals[i]
+    np.testing.assert_allclose(R.segment_means(x, m), vals, rtol=1e-15, atol=1e-15)
+
+
+def test_segment_means_reject_more_landmarks_than_rows():
     with pytest.raises(ValueError):
-        R.segment_means(np.zeros((10, 2)), 3)
+        R.segment_means(np.zeros((10, 2)), 11)
 
 
 # ---------------------------------------------------------------- softmax ----

@@ -28,8 +28,11 @@ MUTATIONS = {
     "conv_flipped": ("out[lo:hi] += w[j] * v[lo + shift:hi + shift]",
                      "out[lo:hi] += w[ks - 1 - j] * v[lo + shift:hi + shift]"),
     "conv_off_by_one": ("shift = j - r", "shift = j - r - 1"),
-    "strided_segments": ("return x.reshape(m, seg, d).mean(axis=1)",
-                         "return x.reshape(seg, m, d).mean(axis=0)"),
+    "strided_segments": ("out[i] = x[lo:hi].mean(axis=0)",
+                         "out[i] = x[i::m].mean(axis=0)"),
+    "remainder_in_last_segment": (
+        "return [(i * n // m, (i + 1) * n // m) for i in range(m)]",
+        "return [(i * (n // m), (i + 1) * (n // m) if i < m - 1 else n) for i in range(m)]"),
     "z_transposed": ("w_mat = z @ g", "w_mat = z.T @ g"),
     "conv_dropped": ('"out": att + conv', '"out": att'),
 }

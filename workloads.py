@@ -126,6 +126,8 @@ def make_inputs(wl: Workload, seed: int | None = None, ks: int | None = None) ->
     else:
         w = np.zeros((wl.H, 0), dtype=np.float32)
     if wl.drift > 0:
+        if wl.n % wl.m != 0:
+            raise ValueError("the segment drift needs n to be a multiple of m")
         u = rng.standard_normal((wl.B, wl.H, wl.m, 4), dtype=np.float32)
         p = rng.standard_normal((wl.B, wl.H, 4, wl.d), dtype=np.float32)
         seg_off = (np.float32(wl.drift) * np.matmul(u, p) / np.float32(2.0)).astype(np.float32)
