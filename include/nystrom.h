@@ -4,7 +4,9 @@
  *
  * What it computes, per head (b, h) of q, k, v in [B, H, n, d]:
  *
- *   Q~, K~ = segment means of Q and K over m contiguous segments of n/m rows
+ *   Q~, K~ = segment means of Q and K over m contiguous segments; segment
+ *            i is rows [floor(i n/m), floor((i+1) n/m)), i.e. n/m rows each
+ *            when m divides n, else floor(n/m) or ceil(n/m) rows
  *            ("Nyströmformer" review page, Proposed method, bullet 4)
  *   A_S    = softmax(Q~ K~^T / sqrt(d))                       (bullet 2)
  *   Z      = iterative Moore-Penrose inverse of A_S, `iters` updates of
@@ -29,7 +31,7 @@
  *  - conv_w: [H][conv_ks] float32 (for both dtypes); may be NULL when
  *    conv_ks == 0.
  *  - Shape rules (else NYS_ERR_SHAPE, nothing launched): B, H, n, d, m >= 1;
- *    n % m == 0; m <= 256; d % 8 == 0 and d <= 128; for NYS_BF16 also
+ *    m <= n; m <= 256; d % 8 == 0 and d <= 128; for NYS_BF16 also
  *    d in {32, 64, 128}; 0 <= iters <= 64; conv_ks == 0 or odd and <= 127;
  *    B*H*n*d < 2^40.
  *  - Scale: every softmax uses 1/sqrt(d).

@@ -47,7 +47,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype) {
   if (dtype != NYS_FP32 && dtype != NYS_BF16) return NYS_ERR_ARG;
   if (B < 1 || H < 1 || n < 1 || d < 1 || m < 1) return NYS_ERR_SHAPE;
-  if (n % m != 0 || m > 256) return NYS_ERR_SHAPE;
+  if (m > n || m > 256) return NYS_ERR_SHAPE;
   if (d % 8 != 0 || d > 128) return NYS_ERR_SHAPE;
   if (dtype == NYS_BF16 && d != 32 && d != 64 && d != 128) return NYS_ERR_SHAPE;
   if (iters < 0 || iters > 64) return NYS_ERR_SHAPE;

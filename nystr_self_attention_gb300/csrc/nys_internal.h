@@ -14,7 +14,7 @@ namespace nys {
 struct Shape {
   int B, H, n, d, m, iters, ks, dtype;
   long long bh() const { return (long long)B * H; }
-  int seg() const { return n / m; }
+  int seg_max() const { return (int)(((long long)n + m - 1) / m); }  // rows of the longest segment
   int m64() const { return ((m + 63) / 64) * 64; }  // m rounded up to 64
   int dpad() const { return d <= 64 ? 64 : 128; }   // d rounded up to a 64-column chunk
 };

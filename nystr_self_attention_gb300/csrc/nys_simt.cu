@@ -38,6 +38,14 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // ---------------------------------------------------------------- landmarks
+// Segment i of n rows split into m: rows [lo, lo + len) with
+// lo = floor(i n / m), so every segment has n/m rows when m divides n and
+// floor(n/m) or ceil(n/m) rows otherwise (m <= n: none is empty).
+__device__ __forceinline__ void segment_rows(int i, int n, int m, int& lo, int& len) {
+  lo = (int)((long long)i * n / m);
+  len = (int)((long long)(i + 1) * n / m) - lo;
+}
+
 // grid (ceil(m64*dpad/256), B*H), block 256: one thread per landmark element
 // of the padded [m64][dpad] grid. Writes Q~, K~ (fp32, [m][d]) and, when
 // kt_b is given, K~ as bf16 [m64][dpad] with zeros in the padding.
@@ -49,13 +57,15 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
   const long long bh = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= m64 * dpad) return;
-  const int i = idx / dpad, c = idx % dpad, seg = n / m;
+  const int i = idx / dpad, c = idx % dpad;
   if (i >= m || c >= d) {
     if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(0.f);
     if (qt_b) qt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(0.f);
     return;
   }
-  const size_t base = ((size_t)bh * n + (size_t)i * seg) * d + c;
+  int lo, seg;
+  segment_rows(i, n, m, lo, seg);
+  const size_t base = ((size_t)bh * n + (size_t)lo) * d + c;
   float sq = 0.f, sk = 0.f;
   for (int t = 0; t < seg; ++t) {
     sq += ld(q + base + (size_t)t * d);
@@ -69,7 +79,7 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
 }
 
 // Segment means with one warp per (tensor, head, segment). A segment is
-// seg consecutive rows, i.e. one contiguous block of seg*d elements; lanes
+// len consecutive rows, i.e. one contiguous block of len*d elements; lanes
 // stream it with 16-byte loads. With V elements per load and VPR = d / V
 // loads per row dividing 32, lane l always sees column group l % VPR, so
 // the per-column sums finish with shuffles over lanes l, l+VPR, ... .
@@ -95,8 +105,10 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
       for (int c = lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
     return;
   }
-  const int seg = n / m, vpr = d / V;
-  const T* src = (tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)i * seg) * d;
+  int lo, seg;
+  segment_rows(i, n, m, lo, seg);
+  const int vpr = d / V;
+  const T* src = (tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)lo) * d;
   const uint4* src4 = reinterpret_cast<const uint4*>(src);
   const int nvec = seg * vpr;
   float acc[V];
@@ -139,11 +151,13 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
     for (int c = d + lane; c < dpad; c += 32) outb[((size_t)bh * m64 + i) * dpad + c] = __float2bfloat16_rn(0.f);
 }
 
-// Small segments (seg * d / V <= 128 16-byte vectors): one warp takes
+// Small segments (ceil(n/m) * d / V <= 128 16-byte vectors): one warp takes
 // SPW = 32 / VPR consecutive segments of one (tensor, head); lane l owns
 // segment l / VPR and column group l % VPR (V columns) and sums that
 // segment's rows for its columns itself (no shuffles), eight rows' loads in
-// flight at a time; a warp-wide load covers SPW rows of 16 * VPR bytes.
+// flight at a time; a warp-wide load covers SPW rows of 16 * VPR bytes. The
+// warp runs to the longest segment's length; shorter segments' lanes skip
+// the rows past their own end.
 // Padding rows (m <= i < m64) get zeros in the bf16 copies.
 // grid: (ceil(2 * B*H * ceil(m64 / SPW) / 8)), block 256.
 template <typename T>
@@ -163,7 +177,7 @@ landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restr
   const long long bh = rest / nblk;
   const int sl = lane / vpr, cg = lane - sl * vpr;
   const int i = (int)(rest % nblk) * spw + sl;
-  const int seg = n / m;
+  const int seg_max = (int)(((long long)n + m - 1) / m);
   __nv_bfloat16* outb = tensor == 0 ? qt_b : kt_b;
   if (i >= m64) return;
   if (i >= m) {
@@ -173,11 +187,13 @@ landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restr
         for (int e = 0; e < V; ++e) outb[((size_t)bh * m64 + i) * dpad + c + e] = __float2bfloat16_rn(0.f);
     return;
   }
-  const uint4* src = reinterpret_cast<const uint4*>((tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)i * seg) * d) + cg;
+  int lo, seg;
+  segment_rows(i, n, m, lo, seg);
+  const uint4* src = reinterpret_cast<const uint4*>((tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)lo) * d) + cg;
   float acc[V];
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  for (int r0 = 0; r0 < seg; r0 += 8) {
+  for (int r0 = 0; r0 < seg_max; r0 += 8) {
     uint4 u[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) u[r] = r0 + r < seg ? __ldg(src + (size_t)(r0 + r) * vpr) : make_uint4(0u, 0u, 0u, 0u);
@@ -645,7 +661,7 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
   const T* qq = static_cast<const T*>(q);
   const T* kk = static_cast<const T*>(k);
   const int vpr = s.d / (16 / (int)sizeof(T));
-  const long long nvec = (long long)s.seg() * vpr;
+  const long long nvec = (long long)s.seg_max() * vpr;
   if (32 % vpr == 0 && nvec <= 128) {
     const int spw = 32 / vpr;
     const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);

@@ -62,7 +62,7 @@ def call(N, q=16, k=16, v=16, w=16, out=16, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), -1), (dict(out=None), -1), (dict(w=None), -1), (dict(dtype=2), -1),
-    (dict(B=0), -2), (dict(n=65), -2), (dict(m=512, n=512), -2), (dict(d=48), -2),
+    (dict(B=0), -2), (dict(n=4), -2), (dict(m=512, n=512), -2), (dict(d=48), -2),
     (dict(d=12, dtype=0), -2), (dict(d=256), -2), (dict(iters=-1), -2), (dict(iters=65), -2),
     (dict(ks=4), -2), (dict(ks=129), -2), (dict(ks=-1), -2),
     (dict(q=24), -3), (dict(out=8), -3), (dict(w=18), -3),
@@ -79,7 +79,8 @@ def test_conv_weights_may_be_null_without_conv(N):
 
 def test_workspace_sizes(N):
     assert N.nystrom_attn_workspace_bytes(32, 12, 512, 64, 64, 1) > 0
-    assert N.nystrom_attn_workspace_bytes(1, 1, 100, 64, 64, 1) == 0
+    assert N.nystrom_attn_workspace_bytes(1, 1, 100, 64, 64, 1) > 0  # ragged segments
+    assert N.nystrom_attn_workspace_bytes(1, 1, 48, 64, 64, 1) == 0  # m > n
     assert N.nystrom_attn_workspace_bytes(1, 1, 512, 64, 64, 1) % 256 == 0
     a = N.nystrom_attn_workspace_bytes(2, 16, 32768, 128, 256, 1)
     b = N.nystrom_attn_workspace_bytes(4, 16, 32768, 128, 256, 1)
@@ -102,10 +103,10 @@ def test_workspace_entry_checks(N):
 def test_host_entry_checks(N):
     lib = N.load_library()
     assert lib.nystrom_attn_fwd_host(None, 16, 16, 16, 16, 2, 3, 64, 64, 8, 6, 5, 1, None) == -1
-    assert lib.nystrom_attn_fwd_host(16, 16, 16, 16, 16, 2, 3, 65, 64, 8, 6, 5, 1, None) == -2
+    assert lib.nystrom_attn_fwd_host(16, 16, 16, 16, 16, 2, 3, 4, 64, 8, 6, 5, 1, None) == -2
 
 
 def test_binding_raises_on_error(N):
     with pytest.raises(N.NystromError) as e:
-        N.nystrom_attn_fwd(16, 16, 16, 16, 16, 2, 3, 65, 64, 8, 6, 5, 1, stream=0)
+        N.nystrom_attn_fwd(16, 16, 16, 16, 16, 2, 3, 4, 64, 8, 6, 5, 1, stream=0)
     assert e.value.code == -2

@@ -80,6 +80,17 @@ SMALL = [
     (1, 152, 128, 64, 64, 4, 3),     # 76 pseudo-inverse CTAs: one per SM, the last such shape
     (1, 154, 128, 64, 64, 4, 3),     # 77 CTAs: two per SM
     (2, 210, 128, 32, 64, 2, 3),     # 210 CTAs: too many beside the rows, two head groups
+    (2, 1, 777, 32, 64, 6, 5),       # n not a multiple of m: segments of 12 and 13 rows
+    (1, 2, 5000, 64, 64, 6, 9),      # segments of 78 and 79 rows (long-segment landmark kernel)
+    (1, 1, 300, 128, 256, 8, 33),    # segments of 1 and 2 rows, m > 128
+]
+
+# float32 only: head sizes outside {32, 64, 128} (the CUDA-core landmark
+# kernel), with and without ragged segments
+SMALL_F32 = [
+    (1, 2, 333, 96, 16, 6, 5),
+    (2, 1, 250, 8, 32, 4, 3),
+    (1, 1, 1000, 40, 48, 6, 0),
 ]
 
 
@@ -96,6 +107,11 @@ def test_small_shapes(shape, dtype):
         att_ref = R.nystrom_attention(inp.q, inp.k, inp.v, np.zeros((H, 0)), m, iters)
         got_att, _ = run_gpu(inp, ks=0)
         assert rel_err(got_att, att_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("shape", SMALL_F32, ids=[f"B{s[0]}H{s[1]}n{s[2]}d{s[3]}m{s[4]}i{s[5]}k{s[6]}" for s in SMALL_F32])
+def test_small_shapes_f32_head_sizes(shape):
+    test_small_shapes(shape, "f32")
 
 
 # ------------------------------------------------------------------ stages ----
