@@ -18,6 +18,7 @@ import scipy.special
 from oracle import nystrom_ref as R
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_n4_m2.json")
+GOLDEN_RAGGED = os.path.join(os.path.dirname(__file__), "golden", "closed_form_n8_m3.json")
 
 
 def rng(seed):
@@ -26,11 +27,13 @@ def rng(seed):
 
 # ---------------------------------------------------------------- golden ----
 
-def test_closed_form_worked_example():
-    """Hand-derived n=4, m=2, d=64 example (tests/golden): pins the 1/sqrt(d)
-    scale, segment means, which axis each softmax runs over, Z_0, the update's
-    constants, the F (Z (B V)) association and the conv orientation."""
-    f = json.load(open(GOLDEN))
+@pytest.mark.parametrize("path", [GOLDEN, GOLDEN_RAGGED], ids=["n4_m2", "n8_m3"])
+def test_closed_form_worked_example(path):
+    """Hand-derived (n, m) = (4, 2) and (8, 3), d=64 examples (tests/golden):
+    pin the 1/sqrt(d) scale, segment means (n=8: segments of 2, 3, 3 rows), which
+    axis each softmax runs over, Z_0, the update's constants, the F (Z (B V))
+    association and the conv orientation."""
+    f = json.load(open(path))
     q, k, v = (np.array(f[x]) for x in ("q", "k", "v"))
     for case in f["cases"]:
         r = R.nystrom_head(q, k, v, np.array(f["conv_w"]), f["m"], case["iters"])

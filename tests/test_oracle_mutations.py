@@ -33,6 +33,10 @@ MUTATIONS = {
     "remainder_in_last_segment": (
         "return [(i * n // m, (i + 1) * n // m) for i in range(m)]",
         "return [(i * (n // m), (i + 1) * (n // m) if i < m - 1 else n) for i in range(m)]"),
+    "remainder_in_first_segments": (
+        "return [(i * n // m, (i + 1) * n // m) for i in range(m)]",
+        "return [(i * (n // m) + min(i, n % m), (i + 1) * (n // m) + min(i + 1, n % m))"
+        " for i in range(m)]"),
     "z_transposed": ("w_mat = z @ g", "w_mat = z.T @ g"),
     "conv_dropped": ('"out": att + conv', '"out": att'),
 }
