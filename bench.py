@@ -562,6 +562,7 @@ def run_ours(args, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded normal draws, bf16-rounded where bf16)",
         "config": {"workload": wl.describe(), "tokens_per_step": tokens_step,
+                   "plan": N.nystrom_plan_describe(B, H, n, d, m, wl.iters, wl.ks, dt_code),
                    "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
                    "parallelism": f"replicas x{world} (independent heads, no collective)"},
         "roofline": roofline, "pass_roofline": pass_roofline(wl, ms_per_step, peaks, peak_src),

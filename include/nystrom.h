@@ -169,6 +169,27 @@ long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m,
                                     int dtype, int stage);
 
 /*
+ * nystrom_plan_describe - the kernels a forward call of this shape
+ * launches, in order, as one line of text: the plan ("serial": each step
+ * after the previous one; "z-beside-rows": the pseudo-inverse's chain of
+ * products on a second stream beside the landmark-row pass, then the merge
+ * of G and W = Z G; "head-groups": the batch split into groups of whole
+ * batch entries, each group's steps on its own stream), the number of head
+ * groups, and per step the kernel with its host-side sizes (the landmark-row
+ * pass's CTAs, key ranges per head and 128-key tiles per CTA; the
+ * pseudo-inverse's CTAs and, beside the rows, the SMs they take). The plan is
+ * the one for a 152-SM GB300 and is a function of the shape alone.
+ * Host only: needs no GPU and launches nothing.
+ * buf: host memory of `len` bytes (may be NULL when len == 0); receives at
+ * most len - 1 characters and a terminating NUL.
+ * Returns the length of the full description (without the NUL), or a
+ * negative nys_status_t: NYS_ERR_SHAPE / NYS_ERR_ARG for a shape the forward
+ * call would reject, NYS_ERR_ARG for len < 0 or a NULL buf with len > 0.
+ */
+int nystrom_plan_describe(int B, int H, int n, int d, int m, int iters,
+                          int conv_ks, int dtype, char* buf, int len);
+
+/*
  * nystrom_get_status - waits for `stream`, then returns and clears the
  * device-side status word of the most recent call on the current device
  * (NYS_OK, or NYS_ERR_TIMEOUT if a bounded wait inside a kernel ran out).

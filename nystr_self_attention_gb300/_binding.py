@@ -25,6 +25,7 @@ _SIG = {
     "nystrom_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "nystrom_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "nystrom_attn_stage_offset": (ctypes.c_longlong, [_I, _I, _I, _I, _I, _I, _I]),
+    "nystrom_plan_describe": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_char_p, _I]),
     "nystrom_get_status": (_I, [_P]),
     "nystrom_strerror": (ctypes.c_char_p, [_I]),
     "nystrom_last_error_string": (ctypes.c_char_p, []),
@@ -130,6 +131,16 @@ def nystrom_attn_fwd_host(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, d
 
 def nystrom_attn_stage_offset(B, H, n, d, m, dtype, stage) -> int:
     return load_library().nystrom_attn_stage_offset(B, H, n, d, m, dtype, stage)
+
+
+def nystrom_plan_describe(B, H, n, d, m, iters, conv_ks, dtype) -> str:
+    """The kernels a forward call of this shape launches (host only)."""
+    lib = load_library()
+    need = _check(lib.nystrom_plan_describe(B, H, n, d, m, iters, conv_ks, dtype, None, 0),
+                  "nystrom_plan_describe")
+    buf = ctypes.create_string_buffer(need + 1)
+    lib.nystrom_plan_describe(B, H, n, d, m, iters, conv_ks, dtype, buf, need + 1)
+    return buf.value.decode()
 
 
 def nystrom_get_status(stream=None) -> int:

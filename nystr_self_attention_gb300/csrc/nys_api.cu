@@ -224,6 +224,20 @@ long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m, int dtype
   }
 }
 
+int nystrom_plan_describe(int B, int H, int n, int d, int m, int iters, int conv_ks, int dtype,
+                          char* buf, int len) {
+  const int rc = check_shape(B, H, n, d, m, iters, conv_ks, dtype);
+  if (rc != NYS_OK) return rc;
+  if (len < 0 || (len > 0 && !buf)) return NYS_ERR_ARG;
+  const std::string text = describe_plan(Shape{B, H, n, d, m, iters, conv_ks, dtype});
+  if (len > 0) {
+    const size_t c = text.size() < (size_t)len - 1 ? text.size() : (size_t)len - 1;
+    memcpy(buf, text.data(), c);
+    buf[c] = '\0';
+  }
+  return (int)text.size();
+}
+
 int nystrom_attn_fwd_ws(const void* q, const void* k, const void* v, const float* conv_w,
                         void* out, int B, int H, int n, int d, int m, int iters, int conv_ks,
                         int dtype, void* workspace, size_t ws_bytes, nys_stream_t stream) {

@@ -206,4 +206,42 @@ int launch_forward(const Shape& s, const void* q, const void* k, const void* v,
   return e == cudaSuccess ? NYS_OK : set_cuda_error(e);
 }
 
+std::string describe_plan(const Shape& s) {
+  const Layout L = make_layout(s);
+  const int groups = choose_groups(s);
+  const bool beside = groups <= 1 && z_beside_rows(s);
+  Shape sg = s;
+  sg.B = s.B / groups;
+  const bool bf16 = s.dtype == NYS_BF16;
+  const bool tc_tokens = tokens_tc_smem(s) > 0;
+  const bool big_tokens = !tc_tokens && tokens_big_supported(s);
+  std::string out = beside ? "plan=z-beside-rows" : groups > 1 ? "plan=head-groups" : "plan=serial";
+  out += " groups=" + std::to_string(groups);
+  const LandmarkKernel lk = landmark_kernel(sg);
+  out += std::string(" landmarks=") + (lk == LandmarkKernel::Small ? "landmarks_small"
+                                       : lk == LandmarkKernel::Vec ? "landmarks_vec"
+                                                                   : "landmarks_simt");
+  if (bf16) {
+    const long long total = (long long)((s.n + 127) / 128) * sg.bh();
+    const long long ctas = (total + L.tiles_per_split - 1) / L.tiles_per_split;
+    out += " rows=rows_tc[ctas=" + std::to_string(ctas) + ",parts=" + std::to_string(L.splits) +
+           ",tiles_per_cta=" + std::to_string(L.tiles_per_split) + "]";
+  } else {
+    out += " rows=rows_simt[splits=" + std::to_string(L.splits) + "]";
+  }
+  if (beside) {
+    out += " pinv=pinv_tc[z-only,ctas=" + std::to_string(pinv_tc_ctas(sg)) +
+           ",sms=" + std::to_string(pinv_beside_sms(s)) + "]";
+    out += " merge=merge_g w=w_tc";
+  } else if (pinv_tc_supported(s)) {
+    out += " pinv=pinv_tc[ctas=" + std::to_string(pinv_tc_ctas(sg)) + "]";
+  } else if (pinv_big_supported(s)) {
+    out += " pinv=pinv_big[clusters=" + std::to_string(sg.bh()) + "]";
+  } else {
+    out += " pinv=pinv_simt";
+  }
+  out += tc_tokens ? " tokens=tokens_tc" : big_tokens ? " tokens=tokens_big" : " tokens=tokens_simt";
+  return out;
+}
+
 }  // namespace nys

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include "nystrom.h"
 
@@ -113,6 +114,11 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
                    float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream);
 
 // CUDA-core steps (nys_simt.cu); `s` may be a group of heads.
+// Segment-mean kernel for a shape: landmarks_small (a warp per 32/VPR short
+// segments), landmarks_vec (a warp per segment) or landmarks_simt (a thread
+// per landmark element, head sizes whose 16-byte row vectors do not divide 32).
+enum class LandmarkKernel { Small, Vec, Simt };
+LandmarkKernel landmark_kernel(const Shape& s);
 int launch_landmarks(const Shape& s, const void* q, const void* k, float* qt, float* kt,
                      __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream);
 int launch_rows_simt(const Shape& s, const float* qt, const void* k, const void* v, float* gp,
@@ -147,6 +153,10 @@ bool pinv_big_supported(const Shape& s);
 int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const float* gpart,
                     const float* gml, float* g, float* a_s, float* z, float* scratch, float* w,
                     void* wt_bf16, int splits, int* status, cudaStream_t stream);
+
+// One line naming the kernels a forward call of this shape launches, in
+// order, with the plan's host-side sizes (nys_forward.cu). Host only.
+std::string describe_plan(const Shape& s);
 
 // Enqueue the whole forward pass (nys_forward.cu). Pointers are device
 // pointers; ws has Layout::total bytes; dev is the current device. Returns

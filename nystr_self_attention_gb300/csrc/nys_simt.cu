@@ -661,14 +661,14 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
   const T* qq = static_cast<const T*>(q);
   const T* kk = static_cast<const T*>(k);
   const int vpr = s.d / (16 / (int)sizeof(T));
-  const long long nvec = (long long)s.seg_max() * vpr;
-  if (32 % vpr == 0 && nvec <= 128) {
+  const LandmarkKernel which = landmark_kernel(s);
+  if (which == LandmarkKernel::Small) {
     const int spw = 32 / vpr;
     const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
     const unsigned grid = (unsigned)((jobs + 7) / 8);
     KernelScope ks_("landmarks_vec", stream);
     landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
-  } else if (32 % vpr == 0) {
+  } else if (which == LandmarkKernel::Vec) {
     const long long jobs = 2ll * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
     landmarks_vec<T><<<(unsigned)((jobs + 7) / 8), 256, 0, stream>>>(
@@ -714,6 +714,14 @@ int tokens_t(const Shape& s, const void* q, const void* v, const float* kt, cons
 }
 
 }  // namespace
+
+LandmarkKernel landmark_kernel(const Shape& s) {
+  const int vpr = s.d / (16 / (s.dtype == NYS_FP32 ? 4 : 2));  // 16-byte vectors per row
+  const long long nvec = (long long)s.seg_max() * vpr;
+  if (32 % vpr == 0 && nvec <= 128) return LandmarkKernel::Small;
+  if (32 % vpr == 0) return LandmarkKernel::Vec;
+  return LandmarkKernel::Simt;
+}
 
 int launch_landmarks(const Shape& s, const void* q, const void* k, float* qt, float* kt,
                      __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream) {
