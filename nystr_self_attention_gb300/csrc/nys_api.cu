@@ -119,8 +119,12 @@ struct DeviceCache {
 };
 DeviceCache g_dev[kMaxDevices];
 
-// Grow-only device buffer. cudaFree synchronises the device.
-int ensure_buffer(void** ptr, size_t* have, size_t need) {
+// Grows a cached device buffer to `need` bytes. The old buffer is freed
+// with cudaFree, which waits for all work on the device, so no earlier call
+// still uses it; the new one is zeroed on `stream`, ahead of the work the
+// caller enqueues there next (a memset on the legacy stream would not be
+// ordered before work on a non-blocking stream).
+int ensure_buffer(void** ptr, size_t* have, size_t need, cudaStream_t stream) {
   if (*have >= need) return NYS_OK;
   if (*ptr) {
     cudaFree(*ptr);
@@ -134,7 +138,7 @@ int ensure_buffer(void** ptr, size_t* have, size_t need) {
     cudaGetLastError();
     return NYS_ERR_NOMEM;
   }
-  e = cudaMemset(*ptr, 0, need);
+  e = cudaMemsetAsync(*ptr, 0, need, stream);
   if (e != cudaSuccess) return set_cuda_error(e);
   *have = need;
   return NYS_OK;
@@ -266,7 +270,7 @@ int nystrom_attn_fwd(const void* q, const void* k, const void* v, const float* c
   char* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_dev[dev].mu);
-    rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, L.total);
+    rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, L.total, stream);
     if (rc != NYS_OK) return rc;
     ws = static_cast<char*>(g_dev[dev].ws);
   }
@@ -292,7 +296,7 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_
   char* base = nullptr;
   {
     std::lock_guard<std::mutex> lk(dc.mu);
-    rc = ensure_buffer(&dc.stage, &dc.stage_bytes, 4 * tb + wb);
+    rc = ensure_buffer(&dc.stage, &dc.stage_bytes, 4 * tb + wb, stream);
     if (rc != NYS_OK) return rc;
     base = static_cast<char*>(dc.stage);
   }
@@ -322,7 +326,7 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_
   char* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(dc.mu);
-    rc = ensure_buffer(&dc.ws, &dc.ws_bytes, make_layout(sc).total);
+    rc = ensure_buffer(&dc.ws, &dc.ws_bytes, make_layout(sc).total, stream);
     if (rc != NYS_OK) return rc;
     ws = static_cast<char*>(dc.ws);
   }
