@@ -159,6 +159,19 @@ class ClockSampler:
                 "samples_in_timed_region": len(inside)}
 
 
+REJECTING_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_rejected(clocks: dict) -> bool:
+    """A timed region that saw a hardware or thermal slowdown, or whose SM
+    clock sat well below its maximum with no reason given (a clock lock left
+    by someone else), does not stand. sw_power_cap alone is kept."""
+    if any(r in clocks.get("reasons", []) for r in REJECTING_REASONS):
+        return True
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    return bool(sm and smax and sm < 0.8 * smax and not clocks.get("reasons"))
+
+
 # --------------------------------------------------------------- CPU oracle ----
 
 def oracle_sample(inp, budget_s: float, max_heads: int | None = None):
@@ -461,24 +474,32 @@ def run_ours(args, wl):
         if world > 1:
             steps = int(reduce_over_ranks(steps, dist.ReduceOp.MIN, dev, world))
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    launches0 = N.nystrom_launch_count()
-    barrier()
-    t_wall0 = time.time()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(steps):
-        step(i)
-    ev1.record(stream)
-    barrier()
-    t_wall1 = time.time()
-    launches = N.nystrom_launch_count() - launches0
-    elapsed_ms = ev0.elapsed_time(ev1)
-    time.sleep(0.2)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    def timed_region():
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        launches0 = N.nystrom_launch_count()
+        barrier()
+        t_wall0 = time.time()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+        t_wall1 = time.time()
+        n_launch = N.nystrom_launch_count() - launches0
+        ms = ev0.elapsed_time(ev1)
+        time.sleep(0.2)
+        sampler.stop()
+        return ms, n_launch, sampler.summary(t_wall0, t_wall1)
+
+    elapsed_ms, launches, clocks = timed_region()
+    # a throttled or clock-locked run is measured once more (on every rank)
+    if reduce_over_ranks(float(clocks_rejected(clocks)), dist.ReduceOp.MAX, dev, world) > 0:
+        first = clocks
+        elapsed_ms, launches, clocks = timed_region()
+        clocks["remeasured_after"] = {"reasons": first["reasons"], "sm_mhz": first["sm_mhz"]}
     if world > 1:
         elapsed_ms = reduce_over_ranks(elapsed_ms, dist.ReduceOp.MAX, dev, world)
     assert N.nystrom_get_status(stream) == N.NYS_OK

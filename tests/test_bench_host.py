@@ -87,3 +87,16 @@ def test_kernel_sources_exist():
     src = os.path.join(bench.ROOT, "nystr_self_attention_gb300", "csrc")
     for kernel, f in bench.KERNEL_SOURCES.items():
         assert os.path.isfile(os.path.join(src, f)), kernel
+
+
+@pytest.mark.parametrize("clocks,rejected", [
+    ({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, False),
+    ({"sm_mhz": 1900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}, False),
+    ({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown"]}, True),
+    ({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": ["sw_thermal_slowdown"]}, True),
+    ({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []}, True),  # a leftover clock lock
+    ({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}, False),
+    ({"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}, False),  # no nvidia-smi
+])
+def test_clock_rejection_rule(clocks, rejected):
+    assert bench.clocks_rejected(clocks) is rejected
