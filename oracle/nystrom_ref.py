@@ -35,7 +35,10 @@ Readings where the page is silent (each listed in the design notes):
 * the depthwise convolution runs along the sequence with one filter of odd
   width ks per head, shared by all d channels, as a cross-correlation with
   (ks-1)/2 zero rows padded on each side, no bias, and is added to S_hat V;
-* ks = 0 means no convolution term.
+* ks = 0 means no convolution term;
+* variants (not on the page): per-channel filters [d, ks] apply channel c's
+  own taps to channel c; a padded sequence (``nystrom_head_padded``) behaves
+  as its unpadded prefix, with zero output rows for the padding.
 
 Every function works in float64 on numpy arrays and is written for a reader
 to check against the page by eye, not for speed.
@@ -48,7 +51,8 @@ __all__ = [
     "segment_bounds", "segment_means", "softmax_rows", "landmark_kernel", "pinv_initial",
     "pinv_step", "pinv_iterative", "landmark_rows", "token_rows",
     "depthwise_conv_seq", "nystrom_head", "nystrom_attention",
-    "softmax_attention", "svd_pinv",
+    "softmax_attention", "svd_pinv", "depthwise_conv_seq_channels", "conv_of",
+    "masked_softmax_rows", "nystrom_head_padded",
 ]
 
 
@@ -168,7 +172,8 @@ def depthwise_conv_seq(v, w):
 def nystrom_head(q, k, v, w, m, iters):
     """One head of Nyström self-attention, returning every intermediate.
 
-    q, k, v: [n, d]; w: [ks] conv filter (ks may be 0); m landmarks;
+    q, k, v: [n, d]; w: [ks] conv filter shared by the channels (ks may be
+    0), or [d, ks] filters, one per channel; m landmarks;
     ``iters`` pseudo-inverse updates. The output uses the association
     F (Z (B V)), which never forms an n x n or n x m product with V
     (Proposed method, bullet 6: linear time).
@@ -181,18 +186,21 @@ def nystrom_head(q, k, v, w, m, iters):
     g = landmark_rows(q_tilde, k, v)
     w_mat = z @ g
     att = token_rows(q, k_tilde, w_mat)
-    conv = depthwise_conv_seq(v, w)
+    conv = conv_of(v, w)
     return {
         "q_tilde": q_tilde, "k_tilde": k_tilde, "a_s": a_s, "z": z,
         "g": g, "w": w_mat, "att": att, "conv": conv, "out": att + conv,
     }
 
 
-def nystrom_attention(q, k, v, conv_w, m, iters, heads=None):
-    """Forward pass over [B, H, n, d] inputs with conv weights [H, ks].
+def nystrom_attention(q, k, v, conv_w, m, iters, heads=None, lengths=None):
+    """Forward pass over [B, H, n, d] inputs with conv weights [H, ks] (one
+    filter per head) or [H, d, ks] (one per channel).
 
     Returns out [B, H, n, d] in float64. ``heads`` optionally restricts the
     work to a list of (b, h) pairs; the other heads are left as NaN.
+    ``lengths`` optionally gives each batch entry's number of tokens; the
+    rows past it are padding (see ``nystrom_head_padded``).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     conv_w = _f64(conv_w)
@@ -200,8 +208,84 @@ def nystrom_attention(q, k, v, conv_w, m, iters, heads=None):
     out = np.full((B, H, n, d), np.nan)
     todo = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in todo:
-        out[b, h] = nystrom_head(q[b, h], k[b, h], v[b, h], conv_w[h], m, iters)["out"]
+        if lengths is None:
+            out[b, h] = nystrom_head(q[b, h], k[b, h], v[b, h], conv_w[h], m, iters)["out"]
+        else:
+            out[b, h] = nystrom_head_padded(q[b, h], k[b, h], v[b, h], conv_w[h], m, iters,
+                                            int(lengths[b]))["out"]
     return out
+
+
+# ------------------------------------------------------------------ variants
+# Two points the page leaves open, each with the reading used here: a
+# depthwise filter per channel instead of per head, and padded sequences.
+
+def depthwise_conv_seq_channels(v, w):
+    """Depthwise convolution along the sequence with one filter per channel
+    (bullet 6 says only "depthwise convolution"; this reading gives channel
+    c its own taps): out[t, c] = sum_j w[c, j] * V[t + j - (ks-1)/2, c],
+    rows of V outside [0, n) read as zero. w: [d, ks], odd ks."""
+    v, w = _f64(v), _f64(w)
+    n, d = v.shape
+    if w.ndim != 2 or w.shape[0] != d:
+        raise ValueError("per-channel filters need shape [d, ks]")
+    ks = w.shape[1]
+    out = np.zeros_like(v)
+    if ks == 0:
+        return out
+    if ks % 2 != 1:
+        raise ValueError("conv width must be odd")
+    r = (ks - 1) // 2
+    for t in range(n):
+        for j in range(ks):
+            u = t + j - r
+            if 0 <= u < n:
+                out[t] += w[:, j] * v[u]
+    return out
+
+
+def conv_of(v, w):
+    """The conv term for a shared filter [ks] or per-channel filters [d, ks]."""
+    w = _f64(w)
+    return depthwise_conv_seq_channels(v, w) if w.ndim == 2 else depthwise_conv_seq(v, w)
+
+
+def masked_softmax_rows(s, valid):
+    """Row-wise softmax over the columns where ``valid`` is true; the other
+    columns get weight 0."""
+    return softmax_rows(np.where(np.asarray(valid)[None, :], _f64(s), -np.inf))
+
+
+def nystrom_head_padded(q, k, v, w, m, iters, length):
+    """One head whose n rows hold ``length`` tokens followed by padding (the
+    page mentions no masking; this is the reading that padding takes part in
+    nothing):
+
+    * the landmarks are the segment means of the ``length`` tokens
+      (``segment_bounds(length, m)``; needs m <= length);
+    * padded keys are masked out of softmax(Q~ K^T / sqrt(d)); A_S and
+      softmax(Q K~^T / sqrt(d)) see only landmarks;
+    * padded rows of V read as zero in the convolution;
+    * the output rows of padding are zero.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n, d = q.shape
+    if not 1 <= length <= n:
+        raise ValueError(f"length must be in [1, n] (n={n}, length={length})")
+    valid = np.arange(n) < length
+    q_tilde = segment_means(q[:length], m)
+    k_tilde = segment_means(k[:length], m)
+    a_s = landmark_kernel(q_tilde, k_tilde)
+    z = pinv_iterative(a_s, iters)
+    g = masked_softmax_rows(q_tilde @ k.T / np.sqrt(d), valid) @ v
+    w_mat = z @ g
+    att = token_rows(q, k_tilde, w_mat)
+    conv = conv_of(np.where(valid[:, None], v, 0.0), w)
+    return {
+        "q_tilde": q_tilde, "k_tilde": k_tilde, "a_s": a_s, "z": z, "g": g, "w": w_mat,
+        "att": np.where(valid[:, None], att, 0.0), "conv": np.where(valid[:, None], conv, 0.0),
+        "out": np.where(valid[:, None], att + conv, 0.0),
+    }
 
 
 def softmax_attention(q, k, v):

@@ -321,3 +321,75 @@ def test_approximation_error_vs_exact_attention_is_reported():
         errs[m] = np.abs(att - exact).max() / np.abs(exact).max()
     assert all(np.isfinite(list(errs.values())))
     assert errs[64] < 1e-8 < errs[8]
+
+
+# ---------------------------------------------------------------- variants ----
+
+def test_per_channel_conv_matches_scipy_column_by_column():
+    g = rng(41)
+    n, d, ks = 50, 6, 9
+    v = g.standard_normal((n, d))
+    w = g.standard_normal((d, ks))
+    got = R.depthwise_conv_seq_channels(v, w)
+    for c in range(d):
+        np.testing.assert_allclose(got[:, c], scipy.signal.correlate(v[:, c], w[c], mode="same"),
+                                   atol=1e-13)
+
+
+def test_per_channel_conv_with_equal_filters_is_the_shared_conv():
+    g = rng(42)
+    v = g.standard_normal((40, 5))
+    w = g.standard_normal(7)
+    np.testing.assert_allclose(R.depthwise_conv_seq_channels(v, np.tile(w, (5, 1))),
+                               R.depthwise_conv_seq(v, w), atol=1e-14)
+
+
+def test_per_channel_delta_filters_shift_each_channel():
+    """Channel c's filter is a delta at tap c: out[t, c] = V[t + c - 2, c]."""
+    n, d, ks = 12, 5, 5
+    v = rng(43).standard_normal((n, d))
+    w = np.eye(d, ks)
+    out = R.depthwise_conv_seq_channels(v, w)
+    for c in range(d):
+        shift = c - 2
+        for t in range(n):
+            want = v[t + shift, c] if 0 <= t + shift < n else 0.0
+            assert out[t, c] == want
+
+
+@pytest.mark.parametrize("n,length,m,ks", [(64, 64, 8, 5), (64, 40, 8, 5), (100, 77, 16, 9),
+                                           (33, 1, 1, 3), (48, 48, 48, 0)])
+def test_padded_head_is_its_unpadded_prefix(n, length, m, ks):
+    """Masked formulation (key mask, zeroed V rows, zeroed output rows) against
+    the plain forward pass on the first ``length`` rows alone."""
+    g = rng(n + length)
+    q, k, v = (g.standard_normal((n, 16)) for _ in range(3))
+    w = g.standard_normal(ks)
+    pad = R.nystrom_head_padded(q, k, v, w, m, 6, length)
+    ref = R.nystrom_head(q[:length], k[:length], v[:length], w, m, 6)
+    np.testing.assert_allclose(pad["out"][:length], ref["out"], atol=1e-12)
+    assert (pad["out"][length:] == 0).all()
+    np.testing.assert_allclose(pad["g"], ref["g"], atol=1e-13)
+
+
+def test_padded_head_with_per_channel_filters():
+    g = rng(44)
+    n, length, d = 70, 50, 8
+    q, k, v = (g.standard_normal((n, d)) for _ in range(3))
+    w = g.standard_normal((d, 7))
+    pad = R.nystrom_head_padded(q, k, v, w, 10, 6, length)
+    ref = R.nystrom_head(q[:length], k[:length], v[:length], w, 10, 6)
+    np.testing.assert_allclose(pad["out"][:length], ref["out"], atol=1e-12)
+
+
+def test_batched_lengths_and_channel_filters():
+    g = rng(45)
+    B, H, n, d = 2, 2, 40, 8
+    q, k, v = (g.standard_normal((B, H, n, d)) for _ in range(3))
+    w = g.standard_normal((H, d, 5))
+    out = R.nystrom_attention(q, k, v, w, 4, 6, lengths=[40, 25])
+    for b, length in ((0, 40), (1, 25)):
+        for h in range(H):
+            ref = R.nystrom_head(q[b, h, :length], k[b, h, :length], v[b, h, :length], w[h], 4, 6)
+            np.testing.assert_allclose(out[b, h, :length], ref["out"], atol=1e-12)
+            assert (out[b, h, length:] == 0).all()

@@ -38,6 +38,13 @@ MUTATIONS = {
         "return [(i * (n // m) + min(i, n % m), (i + 1) * (n // m) + min(i + 1, n % m))"
         " for i in range(m)]"),
     "z_transposed": ("w_mat = z @ g", "w_mat = z.T @ g"),
+    "padding_keys_unmasked": ("g = masked_softmax_rows(q_tilde @ k.T / np.sqrt(d), valid) @ v",
+                              "g = softmax_rows(q_tilde @ k.T / np.sqrt(d)) @ v"),
+    "padding_read_by_conv": ("conv = conv_of(np.where(valid[:, None], v, 0.0), w)",
+                             "conv = conv_of(v, w)"),
+    "padded_landmarks_over_all_rows": ("q_tilde = segment_means(q[:length], m)",
+                                       "q_tilde = segment_means(q, m)"),
+    "channel_filters_shared": ("out[t] += w[:, j] * v[u]", "out[t] += w[0, j] * v[u]"),
     "conv_dropped": ('"out": att + conv', '"out": att'),
 }
 
