@@ -110,3 +110,18 @@ def test_binding_raises_on_error(N):
     with pytest.raises(N.NystromError) as e:
         N.nystrom_attn_fwd(16, 16, 16, 16, 16, 2, 3, 4, 64, 8, 6, 5, 1, stream=0)
     assert e.value.code == -2
+
+
+def test_no_cpu_path(N):
+    """There is no CPU implementation behind the ABI: CPU tensors are refused
+    and, on a machine without a GB300, a well-formed call fails instead of
+    computing anything."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("checks the behaviour without a GPU")
+    q = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        N.nystrom_attention(q, q, q, None, 8, 6)
+    with pytest.raises(N.NystromError) as e:
+        N.nystrom_attn_fwd(16, 16, 16, 16, 16, 1, 1, 64, 64, 8, 6, 5, N.NYS_BF16, stream=0)
+    assert e.value.code == N.NYS_ERR_UNSUPPORTED
