@@ -1,0 +1,110 @@
+"""The arithmetic plan of the GPU path, emulated in numpy on the CPU, against
+the fp64 oracle: bf16 operands with fp32 accumulation for the streaming
+contractions (landmark rows S and P V, token F and P W, the conv taps), A_S
+scores close to fp32, tf32 operands with fp32 storage for the pseudo-inverse
+products. The emulation is a model of the rounding, not the kernels; it
+shows that the plan itself leaves room under the parity bar (2e-2 for bf16
+inputs), and that the rejected alternative (iterating X <- X q(X) instead of
+recomputing A_S Z every update) does not.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import nystrom_ref as R
+
+BAR = 2e-2
+
+
+def bf16(x):
+    return workloads.round_to_bf16(np.asarray(x, dtype=np.float32))[0].astype(np.float64)
+
+
+def tf32(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + 0xFFF + ((u >> 13) & 1)) >> 13) << 13
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def f32(x):
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def mm_bf16(a, b):
+    return f32(bf16(a) @ bf16(b))
+
+
+def mm_tf32(a, b):
+    return f32(tf32(a) @ tf32(b))
+
+
+def softmax_f32(s):
+    s = f32(s)
+    e = f32(np.exp(s - s.max(axis=1, keepdims=True)))
+    return e, f32(e.sum(axis=1, keepdims=True))
+
+
+def pinv_tf32(a, iters, z_form=True):
+    a = f32(a)
+    z = f32(a.T / (np.abs(a).sum(0).max() * np.abs(a).sum(1).max()))
+    eye = np.eye(a.shape[0])
+    if z_form:
+        for _ in range(iters):
+            x = mm_tf32(a, z)
+            y1 = mm_tf32(x, 7 * eye - x)
+            y2 = mm_tf32(x, 15 * eye - y1)
+            z = f32(0.25 * mm_tf32(z, 13 * eye - y2))
+        return z
+    x = mm_tf32(a, z)  # X <- X q(X), Z only at the end: Z = Z_0 prod q(X_k)
+    for _ in range(iters):
+        q = f32(0.25 * (13 * eye - mm_tf32(x, 15 * eye - mm_tf32(x, 7 * eye - x))))
+        z = mm_tf32(z, q)
+        x = mm_tf32(x, q)
+    return z
+
+
+def emulated_head(q, k, v, w, m, iters, z_form=True):
+    n, d = q.shape
+    s = 1.0 / np.sqrt(d)
+    q_t, k_t = f32(R.segment_means(q, m)), f32(R.segment_means(k, m))
+    a_s = R.landmark_kernel(q_t, k_t)  # 3xTF32 scores: close to fp32
+    z = pinv_tf32(a_s, iters, z_form)
+    p, l = softmax_f32(mm_bf16(q_t * s, k.T))      # landmark rows: S, exp, P V
+    g = f32(mm_bf16(p, v) / l)
+    w_mat = mm_tf32(z, g)
+    p, l = softmax_f32(mm_bf16(q * s, k_t.T))      # token rows: F, exp, P W
+    att = f32(mm_bf16(p, w_mat) / l)
+    conv = R.depthwise_conv_seq(v, bf16(w))        # banded product, bf16 taps and V
+    return att + conv, att
+
+
+@pytest.mark.parametrize("name,n", [("c2", 512), ("c3", 1024), ("c4", 1024)])
+def test_plan_leaves_room_under_the_bar(name, n):
+    wl = workloads.WORKLOADS[name]
+    small = workloads.custom(1, 2, n, wl.d, wl.m, wl.iters, wl.ks, "bf16", wl.scale, wl.drift,
+                             name=name)
+    inp = workloads.make_inputs(small, seed=99)
+    for h in range(2):
+        q, k, v = inp.q[0, h], inp.k[0, h], inp.v[0, h]
+        ref = R.nystrom_head(q, k, v, inp.conv_w[h], wl.m, wl.iters)
+        out, att = emulated_head(q, k, v, inp.conv_w[h], wl.m, wl.iters)
+        assert np.abs(out - ref["out"]).max() / np.abs(ref["out"]).max() < BAR / 2
+        assert np.abs(att - ref["att"]).max() / np.abs(ref["att"]).max() < BAR / 2
+
+
+def test_the_rejected_iteration_drifts():
+    """Iterating X <- X q(X) (no A_S Z recomputed) lets tf32 rounding build
+    up: its error is several times the Z-form's."""
+    wl = workloads.WORKLOADS["c2"]
+    small = workloads.custom(1, 4, 512, wl.d, wl.m, wl.iters, 0, "bf16", name="c2")
+    inp = workloads.make_inputs(small, seed=7, ks=0)
+    worst = {True: 0.0, False: 0.0}
+    for h in range(4):
+        q, k, v = inp.q[0, h], inp.k[0, h], inp.v[0, h]
+        a_s = R.landmark_kernel(R.segment_means(q, wl.m), R.segment_means(k, wl.m))
+        z_ref = R.pinv_iterative(a_s, wl.iters)
+        for z_form in (True, False):
+            z = pinv_tf32(a_s, wl.iters, z_form)
+            worst[z_form] = max(worst[z_form], np.abs(z - z_ref).max() / np.abs(z_ref).max())
+    assert worst[False] > 3 * worst[True]
