@@ -46,8 +46,16 @@ def parse_args():
                    help="timed steps (default: enough for about 3 s)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="c2", choices=workloads.ORDER,
-                   help="workload (default c2: B=32 H=12 n=512 d=64 m=64, bf16)")
+    p.add_argument("--config", default="c5", choices=workloads.ORDER,
+                   help="workload (default c5, the largest: B=2 H=16 n=32768 d=128 m=256, bf16)")
+    p.add_argument("--others", default="c2,c3,c4",
+                   help="comma-separated workloads timed briefly after the main one and "
+                        "reported under other_workloads ('' for none)")
+    p.add_argument("--no-scan", action="store_true",
+                   help="skip the sequence-length scan reported under linear_scan")
+    p.add_argument("--min-region-s", type=float, default=1.0,
+                   help="repeat the K-step timed region until this much wall time has passed "
+                        "(so the clock sampler sees the timed work)")
     p.add_argument("--batch", type=int, default=None,
                    help="override the workload's batch size B (smaller cases for profiler captures)")
     p.add_argument("--no-e2e", action="store_true")
@@ -93,14 +101,15 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks ----
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 100 ms."""
+    """nvidia-smi clock / throttle-reason samples every `period_ms` ms."""
     FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw",
               "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
               "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu_index = gpu_index
+        self.period_ms = period_ms
         self.samples = []
         self.proc = None
         self.thread = None
@@ -109,7 +118,8 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
         except OSError:
             self.proc = None
             return
@@ -245,12 +255,13 @@ def run_reference(args, wl):
 # Per-kernel roofline model: algorithmic HBM bytes in units of T*e
 # (T = B*H*n*d elements, e = element bytes), or algorithmic flops.
 KERNEL_BYTES = {
-    "landmarks_vec": 2.0, "landmarks_simt": 2.0,  # read Q, K
+    "landmarks_vec": 2.0, "landmarks_small": 2.0, "landmarks_simt": 2.0,  # read Q, K
     "rows_tc": 2.0, "rows_simt": 2.0,             # read K, V
     "tokens_tc": 3.0, "tokens_simt": 3.0, "tokens_big": 3.0,  # read Q, V; write out
 }
 KERNEL_SOURCES = {
-    "landmarks_vec": "nys_simt.cu", "landmarks_simt": "nys_simt.cu", "rows_simt": "nys_simt.cu",
+    "landmarks_vec": "nys_simt.cu", "landmarks_small": "nys_simt.cu",
+    "landmarks_simt": "nys_simt.cu", "rows_simt": "nys_simt.cu",
     "pinv_simt": "nys_simt.cu", "tokens_simt": "nys_simt.cu", "rows_tc": "nys_rows_tc.cu",
     "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu", "pinv_big": "nys_pinv_big.cu",
     "tokens_big": "nys_tokens_big.cu", "w_tc": "nys_pinv_tc.cu", "merge_g": "nys_simt.cu",
@@ -258,10 +269,11 @@ KERNEL_SOURCES = {
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates
 
 
-def pinv_flops(wl):
-    """Algorithmic flops of the landmark kernel, the iteration and W = Z G."""
+def pinv_flops(wl, with_w=True):
+    """Algorithmic flops of the landmark kernel, the iteration and (unless a
+    separate kernel forms it) W = Z G."""
     m, d = wl.m, wl.d
-    return wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + 2.0 * m * m * d)
+    return wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + (2.0 * m * m * d if with_w else 0.0))
 
 
 def kernel_source_hash(kernel):
@@ -295,10 +307,13 @@ def measured_traffic(kernel, wl):
     return scaled
 
 
-def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
+def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src, w_separate=False):
     """Roofline of one kernel: `launches` launches took `ms` in total, and
     `per_step` launches make up one forward pass (the batch is split into
-    that many head groups), so one launch covers 1/per_step of the work."""
+    that many head groups), so one launch covers 1/per_step of the work.
+    Per-kernel times are short event-timed launches, so the tensor peak is
+    the burst figure. `w_separate`: W = Z G is formed by its own kernel
+    (w_tc), so the pseudo-inverse kernel is not credited with it."""
     t_launch = ms / launches / 1e3
     te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes / per_step
     traffic = measured_traffic(kernel, wl)
@@ -313,14 +328,14 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src):
     elif kernel == "merge_g":  # rescale-and-add of the key-split partials
         flops = wl.heads * 2.0 * wl.m * wl.d / per_step
     else:
-        flops = pinv_flops(wl) / per_step
+        flops = pinv_flops(wl, with_w=not w_separate) / per_step
     achieved = flops / t_launch / 1e12
     if kernel in ("pinv_tc", "pinv_big"):
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * TF32_OVER_BF16
+        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
         return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_flops": flops,
-                "peak_source": f"bf16_tflops_sustained ({peak_src}) x 1.1/2.25 (tf32/bf16 nominal)"}
+                "peak_source": f"bf16_tflops burst ({peak_src}) x 1.1/2.25 (tf32/bf16 nominal)"}
     peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
     return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -371,12 +386,115 @@ def resident_inputs(inp, dev):
     return sets, w, set_bytes
 
 
-def run_scan(args, wl):
+def device_inputs(wl, dev, seed):
+    """Seeded device-side draws of a workload's shape (timing only: the
+    sequence-length scan needs no oracle, so its inputs are drawn on the GPU
+    with a seeded generator instead of on the host): rotating (q, k, v, out)
+    sets whose total exceeds twice L2, conv weights, bytes of one set."""
+    import torch
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    shape = (wl.B, wl.H, wl.n, wl.d)
+
+    def draw():
+        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * wl.scale).to(tdt)
+
+    ks = max(wl.ks, 1)
+    w = torch.randn((wl.H, ks), generator=gen, device=dev, dtype=torch.float32) / float(np.sqrt(ks))
+    set_bytes = 4 * wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
+    nsets = max(1, min(8, -(-2 * L2_BYTES // set_bytes)))
+    sets = [(draw(), draw(), draw(), torch.empty(shape, device=dev, dtype=tdt)) for _ in range(nsets)]
+    return sets, w, set_bytes
+
+
+def time_regions(N, step, steps, stream, barrier, regions):
+    """Exactly `regions` timed regions of `steps` steps each, back to back,
+    each bracketed by a barrier + synchronize and timed with CUDA events on
+    the launch stream. Returns the per-region milliseconds and the library's
+    kernel launches over all regions."""
+    import torch
+    launches0 = N.nystrom_launch_count()
+    out = []
+    i0 = 0
+    for _ in range(regions):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        ev0.record(stream)
+        for i in range(steps):
+            step(i0 + i)
+        ev1.record(stream)
+        barrier()
+        out.append(ev0.elapsed_time(ev1))
+        i0 += steps
+    return out, N.nystrom_launch_count() - launches0
+
+
+def spread(vals):
+    v = sorted(vals)
+    q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
+    return {"min": v[0], "p10": q(0.1), "median": statistics.median(v), "p90": q(0.9), "max": v[-1],
+            "n": len(v)}
+
+
+def time_brief(N, wl, sets, w, stream, steps=20, seconds=0.3):
+    """Time a workload briefly (no clocks, no profile): median of K-step
+    regions over about `seconds` of wall time."""
+    import torch
+    dt_code = N.NYS_BF16 if wl.dtype == "bf16" else N.NYS_FP32
+
+    def step(i):
+        q, k, v, out = sets[i % len(sets)]
+        N.nystrom_attn_fwd(q, k, v, w, out, wl.B, wl.H, wl.n, wl.d, wl.m, wl.iters, wl.ks,
+                           dt_code, stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+
+    for i in range(5):
+        step(i)
+    first, _ = time_regions(N, step, steps, stream, barrier, 1)
+    regions = max(3, int(np.ceil(seconds / max(first[0] / 1e3, 1e-6))))
+    region_ms, _ = time_regions(N, step, steps, stream, barrier, regions)
+    assert N.nystrom_get_status(stream) == N.NYS_OK
+    ms = statistics.median(region_ms) / steps
+    return ms, spread([r / steps for r in region_ms])
+
+
+def linear_scan(N, wl, dev, stream, peaks, peak_src, ns):
     """Time of one pass against the sequence length with every other size of
-    the workload fixed: linear time shows as flat tokens/s. One JSON line per
-    n (not the benchmark line)."""
+    the workload fixed (linear time shows as a constant time per token), and
+    a least-squares line t = a + b n over the points."""
     import dataclasses
 
+    import torch
+    points = []
+    for n in ns:
+        wn = dataclasses.replace(wl, n=n)
+        if n % wn.m != 0:
+            continue
+        sets, w, _ = device_inputs(wn, dev, seed=7000 + n)
+        ms, sp = time_brief(N, wn, sets, w, stream)
+        points.append({"n": n, "ms_per_step": ms, "tokens_per_s": wn.tokens / (ms / 1e3),
+                       "ns_per_token_per_head": ms * 1e6 / n,
+                       "pass_roofline_frac": pass_roofline(wn, ms, peaks, peak_src)["frac"],
+                       "spread_ms": sp})
+        del sets
+        torch.cuda.empty_cache()
+    fit = None
+    if len(points) >= 2:
+        x = np.array([p_["n"] for p_ in points], dtype=np.float64)
+        y = np.array([p_["ms_per_step"] * 1e3 for p_ in points])
+        b, a = np.polyfit(x, y, 1)
+        fit = {"intercept_us": float(a), "us_per_1k_tokens_of_n": float(b * 1e3),
+               "max_rel_residual": float(np.max(np.abs(a + b * x - y) / y))}
+    return {"shape": f"B={wl.B} H={wl.H} d={wl.d} m={wl.m} iters={wl.iters} ks={wl.ks} {wl.dtype}",
+            "inputs": "seeded device draws (torch.Generator), rotating sets past L2",
+            "points": points, "fit_t_vs_n": fit}
+
+
+def run_scan(args, wl):
+    """--scan-n: the sequence-length scan alone, one JSON line."""
     import torch
 
     from nystr_self_attention_gb300 import build as nbuild
@@ -388,41 +506,10 @@ def run_scan(args, wl):
         return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
-    dt_code = N.NYS_BF16 if wl.dtype == "bf16" else N.NYS_FP32
-    for n in [int(x) for x in args.scan_n.split(",") if x]:
-        wn = dataclasses.replace(wl, n=n)
-        if n % wn.m != 0:
-            print(json.dumps({"scan": "n", "n": n, "skipped": f"n is not a multiple of m={wn.m}"}))
-            continue
-        sets, w, _ = resident_inputs(workloads.make_inputs(wn), dev)
-
-        def step(i):
-            q, k, v, out = sets[i % len(sets)]
-            N.nystrom_attn_fwd(q, k, v, w, out, wn.B, wn.H, n, wn.d, wn.m, wn.iters, wn.ks,
-                               dt_code, stream)
-
-        for i in range(max(3, args.warmup)):
-            step(i)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        steps = args.steps if args.steps is not None else 50
-        e0.record(stream)
-        for i in range(steps):
-            step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        assert N.nystrom_get_status(stream) == N.NYS_OK
-        ms = e0.elapsed_time(e1) / steps
-        print(json.dumps({
-            "scan": "n", "workload": wn.describe(), "n": n, "steps": steps, "ms_per_step": ms,
-            "tokens_per_s": wn.tokens / (ms / 1e3),
-            "ns_per_token_per_head": ms * 1e6 / n,
-            "pass_roofline_frac": pass_roofline(wn, ms, peaks, peak_src)["frac"],
-            "l2": f"{len(sets)} rotating input sets"}), flush=True)
-        del sets
-        torch.cuda.empty_cache()
+    ns = [int(x) for x in args.scan_n.split(",") if x]
+    print(json.dumps({"scan": "n", **linear_scan(N, wl, dev, torch.cuda.current_stream(), peaks,
+                                                 peak_src, ns)}), flush=True)
 
 
 def run_ours(args, wl):
@@ -447,6 +534,7 @@ def run_ours(args, wl):
     nsets = len(sets)
     q0, k0, v0 = sets[0][:3]
     B, H, n, d, m = wl.B, wl.H, wl.n, wl.d, wl.m
+    plan = N.nystrom_plan_describe(B, H, n, d, m, wl.iters, wl.ks, dt_code)
 
     def step(i):
         q, k, v, out = sets[i % nsets]
@@ -474,37 +562,38 @@ def run_ours(args, wl):
         if world > 1:
             steps = int(reduce_over_ranks(steps, dist.ReduceOp.MIN, dev, world))
 
-    def timed_region():
+    def measure():
+        """The K-step timed region, repeated back to back until at least
+        --min-region-s of wall time has passed (the same number of regions on
+        every rank), with nvidia-smi sampling clocks throughout."""
+        first, _ = time_regions(N, step, steps, stream, barrier, 1)
+        regions = max(1, int(np.ceil(args.min_region_s / max(first[0] / 1e3, 1e-6))))
+        if world > 1:
+            regions = int(reduce_over_ranks(regions, dist.ReduceOp.MAX, dev, world))
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.3)
-        launches0 = N.nystrom_launch_count()
-        barrier()
         t_wall0 = time.time()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for i in range(steps):
-            step(i)
-        ev1.record(stream)
-        barrier()
+        region_ms, n_launch = time_regions(N, step, steps, stream, barrier, regions)
         t_wall1 = time.time()
-        n_launch = N.nystrom_launch_count() - launches0
-        ms = ev0.elapsed_time(ev1)
         time.sleep(0.2)
         sampler.stop()
-        return ms, n_launch, sampler.summary(t_wall0, t_wall1)
+        if world > 1:
+            t = torch.tensor(region_ms, device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            region_ms = t.tolist()
+        return region_ms, n_launch, sampler.summary(t_wall0, t_wall1)
 
-    elapsed_ms, launches, clocks = timed_region()
+    region_ms, launches, clocks = measure()
     # a throttled or clock-locked run is measured once more (on every rank)
     if reduce_over_ranks(float(clocks_rejected(clocks)), dist.ReduceOp.MAX, dev, world) > 0:
         first = clocks
-        elapsed_ms, launches, clocks = timed_region()
+        region_ms, launches, clocks = measure()
         clocks["remeasured_after"] = {"reasons": first["reasons"], "sm_mhz": first["sm_mhz"]}
-    if world > 1:
-        elapsed_ms = reduce_over_ranks(elapsed_ms, dist.ReduceOp.MAX, dev, world)
     assert N.nystrom_get_status(stream) == N.NYS_OK
 
     tokens_step = wl.tokens
+    elapsed_ms = statistics.median(region_ms)  # one K-step region
     value = job_throughput(tokens_step, world, steps, elapsed_ms)
     ms_per_step = elapsed_ms / steps
 
@@ -519,6 +608,7 @@ def run_ours(args, wl):
     N.nystrom_profile_enable(False)
     prof = N.nystrom_profile_read()
     peaks, peak_src = load_peaks()
+    w_separate = "w=w_tc" in plan
     roofline = None
     kernels = {}
     if prof:
@@ -527,7 +617,8 @@ def run_ours(args, wl):
             kernels[name] = {"launches_per_step": cnt / prof_steps, "us_per_launch": ms / cnt * 1e3,
                              "share": ms / tot}
             per_step = max(1, round(cnt / prof_steps))
-            kernels[name]["roofline"] = roofline_for(name, ms, cnt, per_step, wl, peaks, peak_src)
+            kernels[name]["roofline"] = roofline_for(name, ms, cnt, per_step, wl, peaks, peak_src,
+                                                     w_separate)
         dom = max(prof, key=lambda k: prof[k][0])
         roofline = dict(kernels[dom]["roofline"])
         for v in kernels.values():
@@ -565,6 +656,32 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": 3 * wl.tokens * d * esz + wl.H * wl.ks * 4,
                "d2h_bytes_per_step": wl.tokens * d * esz, "steps": e2e_steps,
                "api": "nystrom_attn_fwd_host"}
+        del hq, hk, hv, hout
+
+    # the other workloads and the sequence-length scan ride along (one GPU)
+    others = None
+    scan = None
+    if world == 1:
+        del sets, q0, k0, v0
+        torch.cuda.empty_cache()
+        names = [x for x in args.others.split(",") if x and x != wl.name]
+        if names:
+            others = {}
+            for nm in names:
+                wo = workloads.WORKLOADS[nm]
+                so, wwo, _ = resident_inputs(workloads.make_inputs(wo), dev)
+                ms, sp = time_brief(N, wo, so, wwo, stream)
+                others[nm] = {"workload": wo.describe(), "tokens_per_s": wo.tokens / (ms / 1e3),
+                              "ms_per_step": ms, "spread_ms": sp,
+                              "pass_roofline_frac": pass_roofline(wo, ms, peaks, peak_src)["frac"],
+                              "plan": N.nystrom_plan_describe(
+                                  wo.B, wo.H, wo.n, wo.d, wo.m, wo.iters, wo.ks,
+                                  N.NYS_BF16 if wo.dtype == "bf16" else N.NYS_FP32)}
+                del so
+                torch.cuda.empty_cache()
+        if not args.no_scan and wl.dtype == "bf16":
+            ns = sorted({max(wl.m, wl.n >> 3), max(wl.m, wl.n >> 2), max(wl.m, wl.n >> 1), wl.n})
+            scan = linear_scan(N, wl, dev, stream, peaks, peak_src, ns)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -580,15 +697,19 @@ def run_ours(args, wl):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_spread": spread([r / steps for r in region_ms]),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded normal draws, bf16-rounded where bf16)",
-        "config": {"workload": wl.describe(), "tokens_per_step": tokens_step,
-                   "plan": N.nystrom_plan_describe(B, H, n, d, m, wl.iters, wl.ks, dt_code),
+        "config": {"workload": wl.describe(), "tokens_per_step": tokens_step, "plan": plan,
                    "l2": f"{nsets} rotating input sets ({nsets * set_bytes / 2**20:.0f} MiB) > L2",
+                   "timed_regions": f"{len(region_ms)} back-to-back regions of {steps} steps; "
+                                    "value and ms_per_step from the median region",
                    "parallelism": f"replicas x{world} (independent heads, no collective)"},
         "roofline": roofline, "pass_roofline": pass_roofline(wl, ms_per_step, peaks, peak_src),
         "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clocks, "gpu_launches": launches,
+        "clocks": clocks, "gpu_launches": launches // max(1, len(region_ms)),
+        "gpu_launches_all_regions": launches,
+        "other_workloads": others, "linear_scan": scan,
     }
     print(json.dumps(line), flush=True)
 

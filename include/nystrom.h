@@ -88,7 +88,10 @@ int nystrom_attn_fwd(const void* q, const void* k, const void* v,
 /*
  * nystrom_attn_workspace_bytes - bytes of device workspace that
  * nystrom_attn_fwd_ws needs for this shape (0 if the shape is invalid).
- * Pure host arithmetic; touches no GPU.
+ * Host arithmetic only; launches nothing. The size depends on the SM count
+ * of the current device (the plan spreads work over its SMs; 152, a GB300,
+ * when no device can be queried), so ask with the device current that will
+ * run the call.
  */
 size_t nystrom_attn_workspace_bytes(int B, int H, int n, int d, int m,
                                     int dtype);
@@ -118,7 +121,11 @@ int nystrom_attn_fwd_ws(const void* q, const void* k, const void* v,
  * NYS_ERR_NOMEM before anything is enqueued.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. All calls share the one array and it keeps the previous call's
+ * capture. The first call on a device of a shape whose plan runs on more
+ * than one stream (see nystrom_plan_describe) also creates the library's
+ * auxiliary streams and events for that device, as every entry point does;
+ * they hold no device memory of the caller's and live until exit. All calls
+ * share the one array and it keeps the previous call's
  * contents; the library clears what must start at zero on every call. Calls
  * that overlap on the GPU (different streams, or different host threads,
  * same device) race on the array: serialise them.
@@ -154,7 +161,7 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host,
  * float32 arrays per head (b*H + h major):
  *   NYS_STAGE_Q_TILDE [m][d], NYS_STAGE_K_TILDE [m][d], NYS_STAGE_G [m][d]
  *   (= softmax(Q~ K^T/sqrt d) V), NYS_STAGE_A_S [m][m], NYS_STAGE_W [m][d]
- *   (= Z G).
+ *   (= Z G), NYS_STAGE_Z [m][m] (Z after `iters` updates).
  * nystrom_attn_stage_offset returns the byte offset of `stage` in the
  * workspace for this shape, or -1 for an invalid shape or stage.
  */
@@ -163,7 +170,8 @@ typedef enum {
   NYS_STAGE_K_TILDE = 1,
   NYS_STAGE_G = 2,
   NYS_STAGE_A_S = 3,
-  NYS_STAGE_W = 4
+  NYS_STAGE_W = 4,
+  NYS_STAGE_Z = 5
 } nys_stage_t;
 long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m,
                                     int dtype, int stage);
@@ -178,8 +186,9 @@ long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m,
  * groups, and per step the kernel with its host-side sizes (the landmark-row
  * pass's CTAs, key ranges per head and 128-key tiles per CTA; the
  * pseudo-inverse's CTAs and, beside the rows, the SMs they take). The plan is
- * the one for a 152-SM GB300 and is a function of the shape alone.
- * Host only: needs no GPU and launches nothing.
+ * a function of the shape and of the current device's SM count (152, a
+ * GB300, when no device can be queried).
+ * Host only: launches nothing.
  * buf: host memory of `len` bytes (may be NULL when len == 0); receives at
  * most len - 1 characters and a terminating NUL.
  * Returns the length of the full description (without the NUL), or a

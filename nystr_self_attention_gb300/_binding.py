@@ -10,7 +10,7 @@ import os
 NYS_FP32, NYS_BF16 = 0, 1
 NYS_OK, NYS_ERR_ARG, NYS_ERR_SHAPE, NYS_ERR_ALIGN = 0, -1, -2, -3
 NYS_ERR_UNSUPPORTED, NYS_ERR_NOMEM, NYS_ERR_CUDA, NYS_ERR_TIMEOUT = -4, -5, -6, -7
-NYS_STAGE_Q_TILDE, NYS_STAGE_K_TILDE, NYS_STAGE_G, NYS_STAGE_A_S, NYS_STAGE_W = range(5)
+NYS_STAGE_Q_TILDE, NYS_STAGE_K_TILDE, NYS_STAGE_G, NYS_STAGE_A_S, NYS_STAGE_W, NYS_STAGE_Z = range(6)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnystrom.so")
 _lib = None

@@ -68,14 +68,19 @@ int check_args(const void* q, const void* k, const void* v, const float* conv_w,
   return NYS_OK;
 }
 
-int num_sms() {
+int plan_sms() {
   static int cache[kMaxDevices] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;
+  }
   if (cache[dev] == 0) {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      return 152;
+    }
     cache[dev] = v;
   }
   return cache[dev];
@@ -175,7 +180,8 @@ Layout make_layout(const Shape& s) {
     rows_tc_split(s, rows_tc_ctas(s), &L.splits, &L.tiles_per_split);
   } else {
     const long long rb = (s.m + 7) / 8;
-    long long want = (4 * 152 + rb * (long long)bh - 1) / (rb * (long long)bh);
+    const long long sms = plan_sms();
+    long long want = (4 * sms + rb * (long long)bh - 1) / (rb * (long long)bh);
     long long cap = s.n / 32 > 0 ? s.n / 32 : 1;
     if (want > cap) want = cap;
     if (want < 1) want = 1;
@@ -224,6 +230,7 @@ long long nystrom_attn_stage_offset(int B, int H, int n, int d, int m, int dtype
     case NYS_STAGE_G: return (long long)L.g;
     case NYS_STAGE_A_S: return (long long)L.a_s;
     case NYS_STAGE_W: return (long long)L.w;
+    case NYS_STAGE_Z: return (long long)L.z;
     default: return -1;
   }
 }

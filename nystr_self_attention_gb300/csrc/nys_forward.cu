@@ -20,7 +20,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "nys_internal.h"
@@ -55,42 +54,28 @@ int ensure_streams(int dev) {
   return NYS_OK;
 }
 
-// SM count the plan assumes (GB300); the layout must not depend on the
-// device a workspace size is asked for on.
-constexpr int kPlanSms = 152;
 // SMs the landmark-row pass keeps at least when the pseudo-inverse runs
 // beside it
 constexpr int kMinRowSms = 48;
-
-int groups_override() {
-  static int v = [] {
-    const char* e = std::getenv("NYS_HEAD_GROUPS");
-    return e ? std::atoi(e) : 0;
-  }();
-  return v;
-}
 
 // SMs the pseudo-inverse's CTAs take beside the landmark rows: one CTA per
 // SM while they fit in half of the GPU, else two per SM (m <= 64: two
 // CTAs' shared memory and TMEM fit one SM); 0 if the plan does not apply.
 int pinv_beside_sms(const Shape& s) {
   if (s.dtype != NYS_BF16 || !pinv_tc_supported(s) || s.d % 16 != 0) return 0;
-  if (groups_override() > 1) return 0;
+  const int sms = plan_sms();
   const int ctas = pinv_tc_ctas(s);
-  if (2 * ctas <= kPlanSms) return ctas;
-  if (s.m <= 64 && (ctas + 1) / 2 <= kPlanSms - kMinRowSms) return (ctas + 1) / 2;
+  if (2 * ctas <= sms) return ctas;
+  if (s.m <= 64 && (ctas + 1) / 2 <= sms - kMinRowSms) return (ctas + 1) / 2;
   return 0;
 }
 
 // Number of head groups: only for the tensor-core path with short
 // sequences, where the pseudo-inverse dominates and does not run beside the
-// landmark rows; whole batch entries per group. NYS_HEAD_GROUPS overrides
-// the choice (tuning).
+// landmark rows; whole batch entries per group.
 int choose_groups(const Shape& s) {
-  const int override_groups = groups_override();
   int g = 1;
   if (s.dtype == NYS_BF16 && s.n <= 2048 && s.bh() >= 256 && pinv_beside_sms(s) == 0) g = 2;
-  if (override_groups > 0) g = override_groups;
   if (g > kMaxGroups) g = kMaxGroups;
   if (g > s.B) g = s.B;
   while (g > 1 && s.B % g != 0) --g;
@@ -153,7 +138,7 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
             : launch_rows_simt(sg, qt, kg, vg, gp, gml, L.splits, st);
   if (rc != NYS_OK) return error_in("landmark rows", rc);
   rc = pinv_tc_supported(full)
-           ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, nullptr, w, wt_b, L.splits, status, st)
+           ? launch_pinv_tc(sg, qt, kt, gp, gml, g, a, z, w, wt_b, L.splits, status, st)
        : pinv_big_supported(full)
            ? launch_pinv_big(sg, qt, kt, gp, gml, g, a, z, scr, w, wt_b, L.splits, status, st)
            : launch_pinv_simt(sg, qt, kt, gp, gml, g, a, z, w, scr, bf16_ops ? wt_b : nullptr,
@@ -162,9 +147,9 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
   }
   if (rc != NYS_OK) return rc;
   if (tc_tokens)
-    rc = launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+    rc = launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else if (big_tokens)
-    rc = launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, num_sms(), st);
+    rc = launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else
     rc = launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
   return error_in("token rows", rc);
@@ -175,7 +160,8 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
 bool z_beside_rows(const Shape& s) { return pinv_beside_sms(s) > 0 && choose_groups(s) == 1; }
 
 int rows_tc_ctas(const Shape& s) {
-  return z_beside_rows(s) ? kPlanSms - pinv_beside_sms(s) : kPlanSms;
+  const int sms = plan_sms();
+  return z_beside_rows(s) ? sms - pinv_beside_sms(s) : sms;
 }
 
 int launch_forward(const Shape& s, const void* q, const void* k, const void* v,

@@ -82,8 +82,10 @@ int check_device(int* dev_out);  // current device, must be compute capability 1
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
         void* out, char* ws, cudaStream_t stream, int dev, bool clear_status = true);
 
-// Number of SMs of the current device (cached per device).
-int num_sms();
+// SM count the forward-pass plan and the workspace layout are made for:
+// the current device's, or 152 (GB300) when no device can be queried
+// (host-only queries on a machine without a GPU).
+int plan_sms();
 
 // Tensor-core token kernel (nys_tokens_tc.cu): shared memory it needs for
 // this shape, 0 if the shape is outside what it handles.
@@ -134,8 +136,8 @@ int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, 
                    cudaStream_t stream);
 
 // Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
-// With z set, Z only: no merge of the partials, no W (gpart, gml, g, w and
-// wt_bf16 unused); Z -> z [B*H][m][m] fp32.
+// Z -> z [B*H][m][m] fp32 when z is set. With gpart == nullptr, Z only: no
+// merge of the partials, no W (gml, g, w and wt_bf16 unused; z required).
 bool pinv_tc_supported(const Shape& s);
 int pinv_tc_ctas(const Shape& s);  // CTAs of one launch over all of s's heads
 int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float* gpart,

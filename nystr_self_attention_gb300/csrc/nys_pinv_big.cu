@@ -596,9 +596,11 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.gml = gml;
   p.g = g;
   p.a_s = a_s;
-  p.z0 = z;
-  // scratch holds, per head block of the whole batch: z1, zt, ta, tb, gt
-  p.z1 = scratch;
+  // scratch holds, per head block of the whole batch: the second Z, zt,
+  // ta, tb, gt. Z alternates between z0 (even updates) and z1; the buffers
+  // are assigned so that the last Z lands in `z` (stage export).
+  p.z0 = (s.iters & 1) ? scratch : z;
+  p.z1 = (s.iters & 1) ? z : scratch;
   p.zt = scratch + BH * mm;
   p.ta = scratch + 2 * BH * mm;
   p.tb = scratch + 3 * BH * mm;

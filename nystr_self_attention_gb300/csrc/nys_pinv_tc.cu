@@ -48,11 +48,12 @@ struct PinvParams {
   const float* gml;    // [B*H][splits][m][2]
   float* g;            // [B*H][m][d]  stage export
   float* a_s;          // [B*H][m][m]  stage export
-  float* z;            // [B*H][m][m]  Z-only mode: Z out (no merge, no W)
+  float* z;            // [B*H][m][m]  Z out (stage export; the Z-only mode's result)
   float* w;            // [B*H][m][d]  stage export
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
   int* status;
   int BH, m, d, dpad, m64, splits, iters;
+  int z_only;     // Z only: no merge of the partials, no W
   int hp;         // heads per CTA
   float scale;    // 1/sqrt(d)
   float c;        // scale * log2(e)
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   // ---- 1) the merge of G runs after the iteration (W is its only user);
   // its partial rows are prefetched into L2 here so that it then waits on
   // L2 rather than on DRAM
-  const bool z_only = p.z != nullptr;  // uniform
+  const bool z_only = p.z_only != 0;  // uniform
   if (!z_only && live)
     for (int sp = 0; sp < p.splits; ++sp) {
       const size_t prow = ((size_t)bh * p.splits + sp) * m + li;
@@ -495,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   fence_async_smem();
   tc_fence_before_sync();
   __syncthreads();
-  // ---- 5) Z-only mode: Z (TMEM columns COL_Z.., this thread's row) out
-  if (z_only && !*abort_flag && head_ok) {  // warp-uniform: the TMEM loads are collective
+  // ---- 5) Z (TMEM columns COL_Z.., this thread's row) out
+  if (p.z && !*abort_flag && head_ok) {  // warp-uniform: the TMEM loads are collective
     float* zrow = p.z + ((size_t)bh * m + (live ? li : 0)) * m;
     for (int c0 = half * 32; c0 < m; c0 += 64) {
       uint32_t r[32];
@@ -714,6 +715,7 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   if (!pinv_tc_supported(s)) return NYS_ERR_UNSUPPORTED;
   PinvParams p{};
   p.z = z;
+  p.z_only = gpart == nullptr ? 1 : 0;
   p.qt = qt;
   p.kt = kt;
   p.gpart = gpart;
@@ -775,7 +777,7 @@ int launch_w_tc(const Shape& s, const float* z, const float* g, float* w, void* 
   const int MP = mpad_of(s.m);
   // whole heads per CTA (d <= 64) when the heads alone fill the GPU, else
   // 16-column blocks for more CTAs in flight
-  const int NC = (s.bh() >= 152 && s.d <= 64) ? s.d : 16;
+  const int NC = (s.bh() >= plan_sms() && s.d <= 64) ? s.d : 16;
   const size_t smem = (size_t)(128 + NC) * MP * 4 + 1024;
   void (*kern)(WParams) = nullptr;
   if (NC == 16) kern = MP == 32 ? w_tc<32, 16> : (MP == 64 ? w_tc<64, 16> : w_tc<128, 16>);

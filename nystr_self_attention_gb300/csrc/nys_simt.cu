@@ -666,7 +666,7 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
     const int spw = 32 / vpr;
     const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
     const unsigned grid = (unsigned)((jobs + 7) / 8);
-    KernelScope ks_("landmarks_vec", stream);
+    KernelScope ks_("landmarks_small", stream);
     landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
   } else if (which == LandmarkKernel::Vec) {
     const long long jobs = 2ll * s.bh() * s.m64();

@@ -28,14 +28,37 @@ def test_head_groups_split_the_bytes_of_a_launch():
     assert two["algorithmic_bytes"] == one["algorithmic_bytes"] / 2
 
 
-def test_pseudo_inverse_roofline_is_tf32_of_the_sustained_peak():
+def test_pseudo_inverse_roofline_is_tf32_of_the_burst_peak():
+    """Per-kernel times are short event-timed launches: the burst bf16 peak,
+    scaled to tf32 by the nominal ratio."""
     wl = workloads.WORKLOADS["c5"]
     r = bench.roofline_for("pinv_big", 1.0, 4, 1, wl, PEAKS, "measured")
     m, d = wl.m, wl.d
     flops = wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + 2.0 * m * m * d)
     assert r["bound"] == "tensor" and r["algorithmic_flops"] == flops
-    assert r["peak"] == pytest.approx(1600.0 * 1.1 / 2.25)
+    assert r["peak"] == pytest.approx(1800.0 * 1.1 / 2.25)
     assert r["achieved"] == pytest.approx(flops / 250e-6 / 1e12)
+
+
+def test_pseudo_inverse_not_credited_with_w_when_w_tc_forms_it():
+    wl = workloads.WORKLOADS["c3"]
+    m, d = wl.m, wl.d
+    r = bench.roofline_for("pinv_tc", 1.0, 4, 1, wl, PEAKS, "measured", w_separate=True)
+    assert r["algorithmic_flops"] == wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3)
+    w = bench.roofline_for("w_tc", 1.0, 4, 1, wl, PEAKS, "measured", w_separate=True)
+    assert w["algorithmic_flops"] == wl.heads * 2.0 * m * m * d
+
+
+def test_small_landmark_kernel_has_its_own_bytes():
+    wl = workloads.WORKLOADS["c2"]
+    te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
+    r = bench.roofline_for("landmarks_small", 0.2, 10, 1, wl, PEAKS, "measured")
+    assert r["kernel"] == "landmarks_small" and r["algorithmic_bytes"] == 2 * te
+
+
+def test_spread_of_regions():
+    s = bench.spread([3.0, 1.0, 2.0, 5.0, 4.0])
+    assert s["min"] == 1.0 and s["max"] == 5.0 and s["median"] == 3.0 and s["n"] == 5
 
 
 def test_pass_roofline_is_the_slower_of_bytes_and_flops():

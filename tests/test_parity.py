@@ -120,7 +120,8 @@ def test_small_shapes_f32_head_sizes(shape):
 # is formed afterwards; 128 heads of m = 128 (one CTA each, more than half of
 # the SMs): the pseudo-inverse runs after the landmark rows, merges G and
 # forms W itself
-STAGE_SHAPES = [(2, 2, 512, 64, 64), (16, 8, 512, 64, 128)]
+STAGE_SHAPES = [(2, 2, 512, 64, 64), (16, 8, 512, 64, 128), (1, 2, 1024, 128, 256),
+                (2, 1, 640, 128, 160)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -136,8 +137,10 @@ def test_stage_intermediates(shape, dtype):
     st = {name: stage(ws, wl, code, rows, cols) for name, code, rows, cols in (
         ("q_tilde", N.NYS_STAGE_Q_TILDE, wl.m, wl.d), ("k_tilde", N.NYS_STAGE_K_TILDE, wl.m, wl.d),
         ("g", N.NYS_STAGE_G, wl.m, wl.d), ("a_s", N.NYS_STAGE_A_S, wl.m, wl.m),
-        ("w", N.NYS_STAGE_W, wl.m, wl.d))}
-    tol = {"q_tilde": 1e-6, "k_tilde": 1e-6, "a_s": 1e-5,
+        ("z", N.NYS_STAGE_Z, wl.m, wl.m), ("w", N.NYS_STAGE_W, wl.m, wl.d))}
+    # Z: the iterate after 6 updates, fp32 (CUDA cores) or tf32 products
+    # with fp32 storage (tensor cores), relative to its largest entry
+    tol = {"q_tilde": 1e-6, "k_tilde": 1e-6, "a_s": 1e-5, "z": 1e-4 if dtype == "f32" else 1e-2,
            "g": 1e-5 if dtype == "f32" else 1e-2, "w": 1e-4 if dtype == "f32" else 2e-2}
     for (b, h) in heads:
         i = b * wl.H + h
@@ -159,30 +162,30 @@ def full_inputs(name):
     return _cache[name]
 
 
-def sampled_heads(wl):
-    heads = {(0, 0), (wl.B - 1, wl.H - 1)}
-    g = np.random.default_rng(99)
-    heads.add((int(g.integers(wl.B)), int(g.integers(wl.H))))
-    return sorted(heads)
-
-
 @pytest.mark.parametrize("name", FULL)
 def test_full_workload(name):
     """Every configuration at its full size, in the launch configuration the
-    benchmark times; the oracle checks sampled heads (heads are independent),
-    full output and attention alone."""
+    benchmark times, compared with the oracle on EVERY head (heads are
+    independent, so the oracle runs head by head): the full output and the
+    attention term alone, each head against the bar."""
     inp = full_inputs(name)
     wl = inp.wl
-    heads = sampled_heads(wl)
-    ref = oracle_heads(inp, heads)
     got, _ = run_gpu(inp)
     got_att, _ = run_gpu(inp, ks=0)
     assert np.isfinite(got).all() and np.isfinite(got_att).all()
-    for b, h in heads:
-        e_out = rel_err(got[b, h], ref[(b, h)]["out"])
-        e_att = rel_err(got_att[b, h], ref[(b, h)]["att"])
-        print(f"{name} head ({b},{h}): out {e_out:.2e}  attention {e_att:.2e}")
-        assert e_out <= TOL[wl.dtype] and e_att <= TOL[wl.dtype]
+    worst = (0.0, 0.0)
+    failed = []
+    for b in range(wl.B):
+        for h in range(wl.H):
+            ref = R.nystrom_head(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.conv_w[h], wl.m,
+                                 wl.iters)
+            e_out = rel_err(got[b, h], ref["out"])
+            e_att = rel_err(got_att[b, h], ref["att"])
+            worst = (max(worst[0], e_out), max(worst[1], e_att))
+            if e_out > TOL[wl.dtype] or e_att > TOL[wl.dtype]:
+                failed.append(((b, h), e_out, e_att))
+    print(f"{name}: {wl.heads} heads, worst out {worst[0]:.2e}, worst attention {worst[1]:.2e}")
+    assert not failed, failed[:8]
 
 
 # ------------------------------------------------------------ entry points ----
