@@ -136,6 +136,42 @@ int nystrom_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                              int dtype, nys_stream_t stream);
 
 /*
+ * nystrom_attn_fwd_ex - the forward pass with the two variants the page
+ * leaves open (Proposed method, bullets 4 and 6), as readings of it:
+ *  - conv_layout NYS_CONV_PER_HEAD: conv_w is [H][conv_ks], one filter per
+ *    head shared by its d channels (as nystrom_attn_fwd);
+ *    NYS_CONV_PER_CHANNEL: conv_w is [H][d][conv_ks] float32, channel c of
+ *    head h has its own taps conv_w[h][c][.] ("depthwise": one filter per
+ *    channel).
+ *  - lengths_host: HOST int32 [B], or NULL. Batch entry b holds
+ *    lengths_host[b] real tokens in rows [0, lengths_host[b]) of its n rows,
+ *    the rest is padding, which takes part in nothing: the landmarks are the
+ *    segment means of the real tokens (segments over lengths_host[b] rows),
+ *    padded keys are masked out of softmax(Q~ K^T / sqrt(d)), padded rows of
+ *    V read as zero in the convolution, and the output rows of padding are
+ *    zero. The real rows' result equals that of the unpadded sequence. Each
+ *    length must satisfy m <= lengths_host[b] <= n (else NYS_ERR_SHAPE).
+ *    Padded rows of q, k, v must hold finite values (they are read, then
+ *    masked). The array is copied to the device inside the call.
+ * workspace: caller-owned device workspace of ws_bytes >=
+ * nystrom_attn_workspace_bytes(...) bytes, 256-byte aligned, as for
+ * nystrom_attn_fwd_ws; or NULL to use the library's cached workspace (as
+ * nystrom_attn_fwd does).
+ * With NYS_CONV_PER_HEAD and no lengths the result is that of
+ * nystrom_attn_fwd. The variants run the token pass for the attention term
+ * alone and add the convolution (and zero the padding rows) in a pass of
+ * their own, on the CUDA cores.
+ * Returns NYS_OK or a negative nys_status_t (NYS_ERR_ARG for an unknown
+ * conv_layout).
+ */
+typedef enum { NYS_CONV_PER_HEAD = 0, NYS_CONV_PER_CHANNEL = 1 } nys_conv_layout_t;
+int nystrom_attn_fwd_ex(const void* q, const void* k, const void* v,
+                        const float* conv_w, void* out, int B, int H, int n,
+                        int d, int m, int iters, int conv_ks, int dtype,
+                        int conv_layout, const int* lengths_host,
+                        void* workspace, size_t ws_bytes, nys_stream_t stream);
+
+/*
  * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
  * copies q, k, v, conv_w to the device, runs the forward pass on `stream`,
  * copies out back and waits for the stream. The batch is processed in up

@@ -11,6 +11,7 @@ NYS_FP32, NYS_BF16 = 0, 1
 NYS_OK, NYS_ERR_ARG, NYS_ERR_SHAPE, NYS_ERR_ALIGN = 0, -1, -2, -3
 NYS_ERR_UNSUPPORTED, NYS_ERR_NOMEM, NYS_ERR_CUDA, NYS_ERR_TIMEOUT = -4, -5, -6, -7
 NYS_STAGE_Q_TILDE, NYS_STAGE_K_TILDE, NYS_STAGE_G, NYS_STAGE_A_S, NYS_STAGE_W, NYS_STAGE_Z = range(6)
+NYS_CONV_PER_HEAD, NYS_CONV_PER_CHANNEL = 0, 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnystrom.so")
 _lib = None
@@ -24,6 +25,8 @@ _SIG = {
                                  ctypes.c_size_t, _P]),
     "nystrom_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "nystrom_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "nystrom_attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                                 ctypes.c_size_t, _P]),
     "nystrom_attn_stage_offset": (ctypes.c_longlong, [_I, _I, _I, _I, _I, _I, _I]),
     "nystrom_plan_describe": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_char_p, _I]),
     "nystrom_get_status": (_I, [_P]),
@@ -120,6 +123,22 @@ def nystrom_attn_fwd_noalloc(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks
                                                B, H, n, d, m, iters, conv_ks, dtype,
                                                _stream(stream)),
                   "nystrom_attn_fwd_noalloc")
+
+
+def nystrom_attn_fwd_ex(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype,
+                        conv_layout=NYS_CONV_PER_HEAD, lengths=None, workspace=None, ws_bytes=0,
+                        stream=None):
+    """The forward pass with per-channel conv filters and/or padded sequences
+    (see include/nystrom.h). `lengths`: a host sequence of B ints, or None."""
+    lib = load_library()
+    lens = None
+    if lengths is not None:
+        lens = (ctypes.c_int * B)(*[int(x) for x in lengths])
+    return _check(lib.nystrom_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(conv_w), _ptr(out),
+                                          B, H, n, d, m, iters, conv_ks, dtype, conv_layout,
+                                          ctypes.cast(lens, ctypes.c_void_p) if lens is not None
+                                          else None, _ptr(workspace), ws_bytes, _stream(stream)),
+                  "nystrom_attn_fwd_ex")
 
 
 def nystrom_attn_fwd_host(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype, stream=None):

@@ -204,6 +204,7 @@ Layout make_layout(const Shape& s) {
   L.qt_bf16 = take(pad_bf16);
   L.kt_bf16 = take(pad_bf16);
   L.wt_bf16 = take(pad_bf16);
+  L.lengths = take((size_t)s.B * 4);
   L.total = off;
   return L;
 }
@@ -280,6 +281,44 @@ int nystrom_attn_fwd(const void* q, const void* k, const void* v, const float* c
     rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, L.total, stream);
     if (rc != NYS_OK) return rc;
     ws = static_cast<char*>(g_dev[dev].ws);
+  }
+  return run(s, q, k, v, conv_w, out, ws, stream, dev);
+}
+
+int nystrom_attn_fwd_ex(const void* q, const void* k, const void* v, const float* conv_w,
+                        void* out, int B, int H, int n, int d, int m, int iters, int conv_ks,
+                        int dtype, int conv_layout, const int* lengths_host, void* workspace,
+                        size_t ws_bytes, nys_stream_t stream) {
+  int rc = check_args(q, k, v, conv_w, out, B, H, n, d, m, iters, conv_ks, dtype);
+  if (rc != NYS_OK) return rc;
+  if (conv_layout != NYS_CONV_PER_HEAD && conv_layout != NYS_CONV_PER_CHANNEL) return NYS_ERR_ARG;
+  if (lengths_host)
+    for (int b = 0; b < B; ++b)
+      if (lengths_host[b] < m || lengths_host[b] > n) return NYS_ERR_SHAPE;
+  Shape s{B, H, n, d, m, iters, conv_ks, dtype};
+  s.conv_layout = conv_layout;
+  const Layout L = make_layout(s);
+  if (workspace) {
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NYS_ERR_ALIGN;
+    if (ws_bytes < L.total) return NYS_ERR_NOMEM;
+  }
+  int dev = 0;
+  rc = check_device(&dev);
+  if (rc != NYS_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  if (!ws) {
+    std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+    rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, L.total, stream);
+    if (rc != NYS_OK) return rc;
+    ws = static_cast<char*>(g_dev[dev].ws);
+  }
+  if (lengths_host) {
+    // ordered on the stream before the kernels that read it; the host array
+    // may be reused as soon as the call returns
+    const cudaError_t e = cudaMemcpyAsync(ws + L.lengths, lengths_host, (size_t)B * sizeof(int),
+                                          cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    s.lengths = reinterpret_cast<const int*>(ws + L.lengths);
   }
   return run(s, q, k, v, conv_w, out, ws, stream, dev);
 }

@@ -85,10 +85,13 @@ int choose_groups(const Shape& s) {
 template <typename T>
 T* at(char* ws, size_t off) { return reinterpret_cast<T*>(ws + off); }
 
-// The four steps for heads [bh0, bh0 + sg.bh()) of the full problem.
-int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, const void* k,
+// The four steps for heads [bh0, bh0 + sg.bh()) of the full problem (whole
+// batch entries: bh0 is a multiple of H).
+int run_group(const Shape& full, const Shape& sg_in, long long bh0, const void* q, const void* k,
               const void* v, const float* conv_w, void* out, char* ws, const Layout& L,
               cudaStream_t st, DeviceStreams* beside) {
+  Shape sg = sg_in;
+  if (full.lengths) sg.lengths = full.lengths + bh0 / full.H;
   const size_t esz = full.dtype == NYS_FP32 ? 4 : 2;
   const size_t tok = (size_t)bh0 * full.n * full.d * esz;
   const void* qg = static_cast<const char*>(q) + tok;
@@ -146,13 +149,18 @@ int run_group(const Shape& full, const Shape& sg, long long bh0, const void* q, 
     rc = error_in("pseudo-inverse", rc);
   }
   if (rc != NYS_OK) return rc;
+  Shape stok = sg;  // the token pass: with the variants, the attention term alone
+  if (full.separate_conv()) stok.ks = 0;
   if (tc_tokens)
-    rc = launch_tokens_tc(sg, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
+    rc = launch_tokens_tc(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else if (big_tokens)
-    rc = launch_tokens_big(sg, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
+    rc = launch_tokens_big(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else
-    rc = launch_tokens_simt(sg, qg, vg, kt, w, conv_w, og, st);
-  return error_in("token rows", rc);
+    rc = launch_tokens_simt(stok, qg, vg, kt, w, stok.ks > 0 ? conv_w : nullptr, og, st);
+  rc = error_in("token rows", rc);
+  if (rc == NYS_OK && full.separate_conv())
+    rc = error_in("convolution", launch_conv_mask(sg, vg, conv_w, og, st));
+  return rc;
 }
 
 }  // namespace
@@ -227,6 +235,7 @@ std::string describe_plan(const Shape& s) {
     out += " pinv=pinv_simt";
   }
   out += tc_tokens ? " tokens=tokens_tc" : big_tokens ? " tokens=tokens_big" : " tokens=tokens_simt";
+  if (s.separate_conv()) out += " conv=conv_mask";
   return out;
 }
 

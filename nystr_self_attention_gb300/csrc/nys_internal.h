@@ -14,6 +14,14 @@ namespace nys {
 // One forward call's shape, validated.
 struct Shape {
   int B, H, n, d, m, iters, ks, dtype;
+  // variants (nystrom_attn_fwd_ex): per batch entry number of real tokens
+  // (device int32 [B], null: every row is a token), conv filter layout
+  const int* lengths = nullptr;
+  int conv_layout = NYS_CONV_PER_HEAD;
+  // the fused token kernels cover per-head filters on unpadded inputs; the
+  // variants run the token kernels for the attention term alone and add the
+  // convolution (and zero the padding rows) in a pass of their own
+  bool separate_conv() const { return lengths != nullptr || conv_layout != NYS_CONV_PER_HEAD; }
   long long bh() const { return (long long)B * H; }
   int seg_max() const { return (int)(((long long)n + m - 1) / m); }  // rows of the longest segment
   int m64() const { return ((m + 63) / 64) * 64; }  // m rounded up to 64
@@ -36,6 +44,7 @@ struct Layout {
   size_t qt_bf16;  // bf16 [m64][dpad]    Q~, zero padded (tensor-core operand)
   size_t kt_bf16;  // bf16 [m64][dpad]    K~, zero padded (tensor-core operand)
   size_t wt_bf16;  // bf16 [dpad][m64]    W^T, zero padded (tensor-core operand)
+  size_t lengths;  // int32 [B]           tokens per batch entry (padded-sequence variant)
   size_t total;
   int splits;      // key splits of the landmark-row pass
   int tiles_per_split;  // 128-key tiles per split (tensor-core landmark-row pass)
@@ -130,6 +139,10 @@ int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const flo
                      __nv_bfloat16* wt_b, int splits, cudaStream_t stream);
 int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,
                        const float* w, const float* conv_w, void* out, cudaStream_t stream);
+// out += DWConv(V) for per-channel filters and/or padded sequences (zeros the
+// padding rows; with s.ks == 0 only that). out holds the attention term.
+int launch_conv_mask(const Shape& s, const void* v, const float* conv_w, void* out,
+                     cudaStream_t stream);
 // G = merge of the key-split partials (CUDA cores, one thread per 4
 // elements of G), for the plan that computes Z beside the landmark rows.
 int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,

@@ -63,6 +63,8 @@ struct RowParams {
   int nq, ns;      // Q~ buffers; K/V slots
   float c;         // scale * log2(e)
   float scale;     // 1/sqrt(d)
+  const int* lengths;  // per batch entry: keys past it are padding (null: n)
+  int H;
 };
 
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -379,6 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
     Unit u;
     while (next_unit(p, pos, r1, u)) {
       const int U = p.big ? 2 * u.ntile : u.ntile;
+      // keys of this head: padding past its length gives P = 0 (a tile that
+      // lies wholly in the padding leaves the running max at -inf)
+      const int nk = p.lengths ? p.lengths[u.bh / p.H] : p.n;
       float m_run = -INFINITY, l_run = 0.f;
       int mine = 0;
       bool ok = true;
@@ -402,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
           tmem_ld32(scol + 64, r2);
           tmem_ld32(scol + 96, r3);
           tmem_ld_wait();
-          const bool fast = warp_all_live && key0 + 128 <= p.n;  // warp-uniform
-          if (key0 + 128 <= p.n) {
+          const bool fast = warp_all_live && key0 + 128 <= nk;  // warp-uniform
+          if (key0 + 128 <= nk) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               tmax = fmaxf(tmax, fmaxf(fmaxf(__uint_as_float(r0[e]), __uint_as_float(r1[e])),
@@ -411,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              if (key0 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r0[e]));
-              if (key0 + 32 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r1[e]));
-              if (key0 + 64 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r2[e]));
-              if (key0 + 96 + e < p.n) tmax = fmaxf(tmax, __uint_as_float(r3[e]));
+              if (key0 + e < nk) tmax = fmaxf(tmax, __uint_as_float(r0[e]));
+              if (key0 + 32 + e < nk) tmax = fmaxf(tmax, __uint_as_float(r1[e]));
+              if (key0 + 64 + e < nk) tmax = fmaxf(tmax, __uint_as_float(r2[e]));
+              if (key0 + 96 + e < nk) tmax = fmaxf(tmax, __uint_as_float(r3[e]));
             }
           }
           const bool rebase = live && (m_run == -INFINITY || (tmax - m_run) * p.c > kRebase);
@@ -454,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int ka = key0 + c0 + 2 * e;
-                const float a = (live && ka < p.n) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
-                const float b = (live && ka + 1 < p.n) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
+                const float a = (live && ka < nk) ? fast_exp2(fmaf(__uint_as_float(r[2 * e]), p.c, -mc)) : 0.f;
+                const float b = (live && ka + 1 < nk) ? fast_exp2(fmaf(__uint_as_float(r[2 * e + 1]), p.c, -mc)) : 0.f;
                 l_run += a + b;
                 pk[e] = pack_bf16x2(a, b);
               }
@@ -665,6 +670,8 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
   p.pieces_max = parts;
   p.scale = 1.0f / sqrtf((float)s.d);
   p.c = p.scale * 1.4426950408889634f;
+  p.lengths = s.lengths;
+  p.H = s.H;
   const size_t tile = (size_t)(DP / 64) * 16384;
   p.nq = nq_of(s);
   const size_t qbytes = (size_t)p.nq * (p.big ? 2 : 1) * tile;

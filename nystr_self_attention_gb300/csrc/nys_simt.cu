@@ -53,7 +53,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
                float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
-               __nv_bfloat16* __restrict__ kt_b, int n, int d, int m, int m64, int dpad) {
+               __nv_bfloat16* __restrict__ kt_b, int n, int d, int m, int m64, int dpad,
+               const int* __restrict__ lengths, int H) {
   const long long bh = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= m64 * dpad) return;
@@ -64,7 +65,7 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
     return;
   }
   int lo, seg;
-  segment_rows(i, n, m, lo, seg);
+  segment_rows(i, lengths ? lengths[bh / H] : n, m, lo, seg);
   const size_t base = ((size_t)bh * n + (size_t)lo) * d + c;
   float sq = 0.f, sk = 0.f;
   for (int t = 0; t < seg; ++t) {
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(256)
 landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
               float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
               __nv_bfloat16* __restrict__ kt_b, long long n_heads, int n, int d, int m, int m64,
-              int dpad) {
+              int dpad, const int* __restrict__ lengths, int H) {
   constexpr int V = 16 / sizeof(T);
   const long long job = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -106,7 +107,7 @@ landmarks_vec(const T* __restrict__ q, const T* __restrict__ k, float* __restric
     return;
   }
   int lo, seg;
-  segment_rows(i, n, m, lo, seg);
+  segment_rows(i, lengths ? lengths[bh / H] : n, m, lo, seg);
   const int vpr = d / V;
   const T* src = (tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)lo) * d;
   const uint4* src4 = reinterpret_cast<const uint4*>(src);
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(256)
 landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restrict__ qt,
                 float* __restrict__ kt, __nv_bfloat16* __restrict__ qt_b,
                 __nv_bfloat16* __restrict__ kt_b, long long n_heads, int n, int d, int m, int m64,
-                int dpad) {
+                int dpad, const int* __restrict__ lengths, int H) {
   constexpr int V = 16 / sizeof(T);
   const int vpr = d / V, spw = 32 / vpr;
   const int nblk = (m64 + spw - 1) / spw;
@@ -188,7 +189,7 @@ landmarks_small(const T* __restrict__ q, const T* __restrict__ k, float* __restr
     return;
   }
   int lo, seg;
-  segment_rows(i, n, m, lo, seg);
+  segment_rows(i, lengths ? lengths[bh / H] : n, m, lo, seg);  // seg <= seg_max (length <= n)
   const uint4* src = reinterpret_cast<const uint4*>((tensor == 0 ? q : k) + ((size_t)bh * n + (size_t)lo) * d) + cg;
   float acc[V];
 #pragma unroll
@@ -237,7 +238,7 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __restrict__ v,
           float* __restrict__ gpart, float* __restrict__ gml, int n, int d, int m, int splits,
-          int keys_per_split, float scale) {
+          int keys_per_split, float scale, const int* __restrict__ lengths, int H) {
   extern __shared__ float sm[];
   float* sq = sm;                          // [8][d]
   float* sk = sq + RW_ROWS * d;            // [32][d+1]
@@ -256,7 +257,9 @@ rows_simt(const float* __restrict__ qt, const T* __restrict__ k, const T* __rest
   for (int j = 0; j < 8; ++j) acc[j] = 0.f;
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
   const int key0 = split * keys_per_split;
-  const int key1 = min(n, key0 + keys_per_split);
+  // keys past the head's length (padding) take no part: a range that lies
+  // wholly in the padding leaves an empty partial (max = -inf)
+  const int key1 = min(lengths ? lengths[bh / H] : n, key0 + keys_per_split);
   const T* kb = k + (size_t)bh * n * d;
   const T* vb = v + (size_t)bh * n * d;
   for (int kc = key0; kc < key1; kc += RW_KEYS) {
@@ -655,6 +658,80 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
   }
 }
 
+// -------------------------------------------------------------- conv, mask
+// The depthwise convolution added to an output that holds the attention
+// term alone, for the forms the fused token kernels do not cover: filters
+// per channel ([H][d][ks]: channel c of head h has its own taps) and padded
+// sequences (a batch entry's rows at or past its length are padding: they
+// read as zero in the convolution and their output rows are zero). With
+// ks = 0 it only zeroes the padding rows.
+//   out[t][c] = t < L ? out[t][c] + sum_j w[j] V[t + j - (ks-1)/2][c] : 0,
+//   V rows outside [0, L) read as zero, L = the entry's length (n if none).
+// grid (ceil(n / CV_ROWS), B*H), block (d / CV_COLS... ) = CV_THREADS: a CTA
+// takes CV_ROWS output rows of one head; their V rows with the halo are
+// staged in shared memory (fp32), each thread computes whole columns of
+// outputs for a strip of rows.
+constexpr int CV_ROWS = 64, CV_THREADS = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(CV_THREADS)
+conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
+          int d, int ks, int per_channel, const int* __restrict__ lengths) {
+  extern __shared__ float sv[];  // [CV_ROWS + ks - 1][d]
+  const long long bh = blockIdx.y;
+  const int h = (int)(bh % H);
+  const int len = lengths ? lengths[bh / H] : n;
+  const int t0 = blockIdx.x * CV_ROWS;
+  const int rad = ks > 0 ? (ks - 1) / 2 : 0;
+  const int vrows = CV_ROWS + 2 * rad;
+  const T* vb = v + (size_t)bh * n * d;
+  T* ob = out + (size_t)bh * n * d;
+  if (ks > 0 && t0 < len) {
+    for (int e = threadIdx.x; e < vrows * d; e += CV_THREADS) {
+      const int u = t0 - rad + e / d, c = e % d;
+      sv[e] = (u >= 0 && u < len) ? ld(vb + (size_t)u * d + c) : 0.f;
+    }
+  }
+  __syncthreads();
+  // thread -> column c and a strip of rows: d columns x (CV_THREADS / d) strips
+  const int strips = CV_THREADS / d;
+  const int c = threadIdx.x % d, strip = threadIdx.x / d;
+  if (strip >= strips) return;
+  const float* wc = w ? (per_channel ? w + ((size_t)h * d + c) * ks : w + (size_t)h * ks) : nullptr;
+  for (int r = strip; r < CV_ROWS; r += strips) {
+    const int t = t0 + r;
+    if (t >= n) break;
+    T* o = ob + (size_t)t * d + c;
+    if (t >= len) {
+      st(o, 0.f);
+      continue;
+    }
+    float acc = ld(o);
+    if (ks > 0) {
+      float cv = 0.f;
+      const float* x = sv + (size_t)r * d + c;
+      for (int j = 0; j < ks; ++j) cv = fmaf(wc[j], x[(size_t)j * d], cv);
+      acc += cv;
+    }
+    st(o, acc);
+  }
+}
+
+template <typename T>
+int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, cudaStream_t stream) {
+  const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
+  const size_t smem = s.ks > 0 ? sizeof(float) * (size_t)(CV_ROWS + 2 * rad) * s.d : 0;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(conv_mask<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return set_cuda_error(cudaGetLastError());
+  KernelScope ks_("conv_mask", stream);
+  conv_mask<T><<<dim3((s.n + CV_ROWS - 1) / CV_ROWS, (unsigned)s.bh()), CV_THREADS, smem, stream>>>(
+      static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d,
+      s.ks, s.conv_layout == NYS_CONV_PER_CHANNEL ? 1 : 0, s.lengths);
+  return launch_status();
+}
+
 template <typename T>
 int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* kt,
                 __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream) {
@@ -667,16 +744,17 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
     const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
     const unsigned grid = (unsigned)((jobs + 7) / 8);
     KernelScope ks_("landmarks_small", stream);
-    landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+    landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad(),
+                                                  s.lengths, s.H);
   } else if (which == LandmarkKernel::Vec) {
     const long long jobs = 2ll * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
     landmarks_vec<T><<<(unsigned)((jobs + 7) / 8), 256, 0, stream>>>(
-        qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad());
+        qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad(), s.lengths, s.H);
   } else {
     KernelScope ks_("landmarks_simt", stream);
     landmarks_simt<T><<<dim3((s.m64() * s.dpad() + 255) / 256, (unsigned)s.bh()), 256, 0, stream>>>(
-        qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad());
+        qq, kk, qt, kt, qt_b, kt_b, s.n, s.d, s.m, s.m64(), s.dpad(), s.lengths, s.H);
   }
   return launch_status();
 }
@@ -691,7 +769,7 @@ int rows_t(const Shape& s, const float* qt, const void* k, const void* v, float*
   KernelScope ks_("rows_simt", stream);
   rows_simt<T><<<dim3((s.m + RW_ROWS - 1) / RW_ROWS, splits, (unsigned)s.bh()), 128, smem, stream>>>(
       qt, static_cast<const T*>(k), static_cast<const T*>(v), gp, gml, s.n, s.d, s.m, splits, kps,
-      scale);
+      scale, s.lengths, s.H);
   return launch_status();
 }
 
@@ -758,6 +836,13 @@ int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, 
   else
     merge_g<8><<<grid, 256, 0, stream>>>(gp, gml, g, s.m, s.d, splits);
   return launch_status();
+}
+
+int launch_conv_mask(const Shape& s, const void* v, const float* conv_w, void* out,
+                     cudaStream_t stream) {
+  if (s.d > CV_THREADS) return NYS_ERR_UNSUPPORTED;
+  return s.dtype == NYS_FP32 ? conv_mask_t<float>(s, v, conv_w, out, stream)
+                             : conv_mask_t<__nv_bfloat16>(s, v, conv_w, out, stream);
 }
 
 int launch_tokens_simt(const Shape& s, const void* q, const void* v, const float* kt,

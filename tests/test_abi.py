@@ -125,3 +125,22 @@ def test_no_cpu_path(N):
     with pytest.raises(N.NystromError) as e:
         N.nystrom_attn_fwd(16, 16, 16, 16, 16, 1, 1, 64, 64, 8, 6, 5, N.NYS_BF16, stream=0)
     assert e.value.code == N.NYS_ERR_UNSUPPORTED
+
+
+def test_fwd_ex_rejects_bad_variant_arguments(N):
+    lib = N.load_library()
+    a = GOOD
+
+    def ex(layout=0, lengths=None, ws=None, ws_bytes=0):
+        arr = None
+        if lengths is not None:
+            arr = (ctypes.c_int * len(lengths))(*lengths)
+        return lib.nystrom_attn_fwd_ex(16, 16, 16, 16, 16, a["B"], a["H"], a["n"], a["d"], a["m"],
+                                       a["iters"], a["ks"], a["dtype"], layout,
+                                       ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
+                                       ws, ws_bytes, None)
+    assert ex(layout=2) == N.NYS_ERR_ARG
+    assert ex(lengths=[a["m"] - 1, a["n"]]) == N.NYS_ERR_SHAPE   # shorter than m
+    assert ex(lengths=[a["n"] + 1, a["n"]]) == N.NYS_ERR_SHAPE   # longer than n
+    assert ex(ws=256 + 16) == N.NYS_ERR_ALIGN                    # workspace not 256-aligned
+    assert ex(ws=256, ws_bytes=8) == N.NYS_ERR_NOMEM              # workspace too small

@@ -83,6 +83,9 @@ SMALL = [
     (2, 1, 777, 32, 64, 6, 5),       # n not a multiple of m: segments of 12 and 13 rows
     (1, 2, 5000, 64, 64, 6, 9),      # segments of 78 and 79 rows (long-segment landmark kernel)
     (1, 1, 300, 128, 256, 8, 33),    # segments of 1 and 2 rows, m > 128
+    (1, 2, 640, 64, 192, 6, 9),      # m > 128 with d = 64: W in 32-column halves
+    (2, 1, 384, 32, 160, 0, 5),      # m > 128, d = 32, no update: W = Z_0 G
+    (1, 1, 512, 128, 256, 1, 3),     # m > 128, a single (odd) update
 ]
 
 # float32 only: head sizes outside {32, 64, 128} (the CUDA-core landmark

@@ -146,3 +146,24 @@ def custom(B, H, n, d, m, iters, ks, dtype, scale=1.0, drift=0.0, name="custom")
     """A workload of any shape (tests use it for tiny, ragged and edge cases).
     Its seed must be passed to :func:`make_inputs` explicitly."""
     return Workload(name, B, H, n, d, m, iters, ks, dtype, scale, drift)
+
+
+def conv_channels(H: int, d: int, ks: int, seed: int) -> np.ndarray:
+    """Per-channel depthwise-conv weights ``[H, d, ks]`` (float32), normal
+    with variance ``1/ks`` like the per-head filters, from their own seeded
+    generator (the per-channel variant of the convolution)."""
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((H, d, ks), dtype=np.float32)
+            * np.float32(1.0 / np.sqrt(ks))).astype(np.float32)
+
+
+def lengths_for(B: int, n: int, m: int, seed: int) -> np.ndarray:
+    """Tokens per batch entry for the padded-sequence variant: int32 ``[B]``
+    uniform in ``[m, n]``, with the first entry at ``n`` (no padding) and,
+    for ``B > 1``, the second at ``m`` (the shortest allowed)."""
+    rng = np.random.default_rng(seed)
+    out = rng.integers(m, n + 1, size=B).astype(np.int32)
+    out[0] = n
+    if B > 1:
+        out[1] = m
+    return out
