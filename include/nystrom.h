@@ -77,7 +77,11 @@ typedef enum {
  * Uses a workspace the library allocates and caches per device (grown with
  * cudaMalloc when a call needs more; growing synchronises the device).
  * iters: number of pseudo-inverse updates ("about 6", Proposed method,
- * bullet 5); run exactly, no early exit.
+ * bullet 5); run exactly, no early exit. For NYS_BF16 inputs up to 8 updates
+ * run on the tensor cores (tf32 products, fp32 storage); with more, the
+ * pseudo-inverse runs in fp32 on the CUDA cores, since the iteration
+ * amplifies tf32 rounding by the condition number of A_S as it inverts more
+ * of its small singular values (slower, same result bar).
  * Returns NYS_OK or a negative nys_status_t.
  */
 int nystrom_attn_fwd(const void* q, const void* k, const void* v,
@@ -260,6 +264,20 @@ unsigned long long nystrom_launch_count(void);
 int nystrom_profile_enable(int on);
 int nystrom_profile_read(int max_kernels, char* names, int name_len,
                          double* total_ms, long long* launches);
+
+/*
+ * nystrom_debug_stall_pinv - testing the device-side timeout path. With
+ * on = 1, every later forward call whose pseudo-inverse runs in the
+ * tensor-core kernel for m <= 128 (bf16 inputs) makes that kernel wait, at
+ * its start and before any copy or product is in flight, on a barrier phase
+ * that nothing completes; the bounded wait runs out after 1 ms, the kernel
+ * records NYS_ERR_TIMEOUT in the status word and skips its remaining work
+ * (its outputs, and the call's output, are then undefined), and
+ * nystrom_get_status reports NYS_ERR_TIMEOUT with the CUDA context intact.
+ * on = 0 (the default) turns it off. Process-wide; not for production use.
+ * Returns NYS_OK, or NYS_ERR_ARG for on other than 0 or 1.
+ */
+int nystrom_debug_stall_pinv(int on);
 
 /* Static description of a status code. Never NULL. */
 const char* nystrom_strerror(int code);

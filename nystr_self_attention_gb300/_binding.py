@@ -34,6 +34,7 @@ _SIG = {
     "nystrom_last_error_string": (ctypes.c_char_p, []),
     "nystrom_launch_count": (ctypes.c_ulonglong, []),
     "nystrom_profile_enable": (_I, [_I]),
+    "nystrom_debug_stall_pinv": (_I, [_I]),
     "nystrom_profile_read": (_I, [_I, ctypes.c_char_p, _I, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -200,6 +201,12 @@ def nystrom_attention(q, k, v, conv_w, m: int, iters: int, out=None, stream=None
     nystrom_attn_fwd(q, k, v, conv_w if ks > 0 else None, out, B, H, n, d, m, iters, ks, dtype,
                      stream)
     return out
+
+
+def nystrom_debug_stall_pinv(on: bool) -> int:
+    """Timeout-path test switch (see include/nystrom.h)."""
+    return _check(load_library().nystrom_debug_stall_pinv(1 if on else 0),
+                  "nystrom_debug_stall_pinv")
 
 
 def nystrom_launch_count() -> int:

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -15,11 +16,14 @@ namespace nys {
 namespace {
 
 constexpr int kMaxDevices = 64;
+std::atomic<uint32_t> g_stall_ns{0};
 thread_local std::string g_last_error;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
+
+uint32_t debug_stall_ns() { return g_stall_ns.load(); }
 
 int set_cuda_error(cudaError_t e) {
   g_last_error = cudaGetErrorString(e);
@@ -446,5 +450,11 @@ const char* nystrom_strerror(int code) {
 }
 
 const char* nystrom_last_error_string(void) { return g_last_error.c_str(); }
+
+int nystrom_debug_stall_pinv(int on) {
+  if (on != 0 && on != 1) return NYS_ERR_ARG;
+  g_stall_ns.store(on ? 1000000u : 0u);  // 1 ms
+  return NYS_OK;
+}
 
 }  // extern "C"

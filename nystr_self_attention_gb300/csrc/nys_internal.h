@@ -71,6 +71,11 @@ class KernelScope {
   cudaEvent_t begin_ = nullptr;
 };
 
+// Timeout test switch (nystrom_debug_stall_pinv): > 0 makes the tensor-core
+// pseudo-inverse kernel (m <= 128) wait that many ns on a phase nothing
+// completes before its first product. 0 (the default): off.
+uint32_t debug_stall_ns();
+
 // Host helpers of the C ABI (nys_api.cu).
 int set_cuda_error(cudaError_t e);  // remembers the message, returns NYS_ERR_CUDA
 // rc unchanged; a CUDA error's message gets the failing step's name in front.
@@ -147,6 +152,14 @@ int launch_conv_mask(const Shape& s, const void* v, const float* conv_w, void* o
 // elements of G), for the plan that computes Z beside the landmark rows.
 int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,
                    cudaStream_t stream);
+
+// Most pseudo-inverse updates the tensor-core kernels run: their products
+// take tf32 operands, whose rounding the iteration amplifies by cond(A_S) as
+// it inverts more of A_S's small singular values. Up to 8 updates (the
+// page's "about 6"; 8 in the long-context workload) this stays well inside
+// the bf16 parity bar; with more (12 can give 6e-2, 24-64 can diverge) the
+// bf16 path runs the pseudo-inverse in fp32 on the CUDA cores instead.
+constexpr int kTf32MaxIters = 8;
 
 // Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
 // Z -> z [B*H][m][m] fp32 when z is set. With gpart == nullptr, Z only: no

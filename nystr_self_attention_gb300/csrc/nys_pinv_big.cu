@@ -581,7 +581,7 @@ constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
 
 bool pinv_big_supported(const Shape& s) {
   return s.dtype == NYS_BF16 && s.m > 128 && s.m <= 256 && s.m % 4 == 0 && s.d % 32 == 0 &&
-         s.d <= 128;
+         s.d <= 128 && s.iters <= kTf32MaxIters;
 }
 
 int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const float* gpart,

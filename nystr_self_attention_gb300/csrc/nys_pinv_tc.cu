@@ -54,6 +54,7 @@ struct PinvParams {
   int* status;
   int BH, m, d, dpad, m64, splits, iters;
   int z_only;     // Z only: no merge of the partials, no W
+  uint32_t stall_ns;  // > 0: wait this long on a phase nothing completes (timeout test)
   int hp;         // heads per CTA
   float scale;    // 1/sqrt(d)
   float c;        // scale * log2(e)
@@ -129,8 +130,11 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   const bool live = head_ok && li < m;
   const bool in_np = row < NP;
 
+  __shared__ uint64_t bar_fin, bar_never;
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_never, 1);  // nothing ever arrives on it
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -138,6 +142,16 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // The timeout path on demand: before any copy or product is in flight, a
+  // bounded wait on a phase that nothing completes runs out, and the CTA
+  // winds down as after any timeout (status word set, no further work).
+  if (p.stall_ns > 0) {
+    if (tid == 0 && !mbar_wait(&bar_never, 0, nullptr, p.stall_ns)) {
+      *abort_flag = 1;
+      atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
+    }
+    __syncthreads();
+  }
   const uint32_t tmem = tmem_base_sh;
   const uint32_t lo = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t COL_Z = 0, COL_X = MP, COL_D = 2 * MP;  // main loop
@@ -232,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   tmem_st_wait();
   tc_fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0 && !*abort_flag) {
     tc_fence_after_sync();
     issue(COL_S, COL_QH, nullptr, khi, NP, d, false);
     issue(COL_S, COL_QH, nullptr, klo, NP, d, true);
@@ -553,6 +567,12 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
           for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + lj] = __float2bfloat16_rn(0.f);
     }
   }
+  // no product of this CTA may still be in flight when its TMEM is freed
+  // (after a timeout the last products were not waited for)
+  if (tid == 0) {
+    mma_commit(&bar_fin);
+    mbar_wait(&bar_fin, 0, nullptr, kWaitNs);
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
@@ -702,7 +722,9 @@ int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 
 }  // namespace
 
-bool pinv_tc_supported(const Shape& s) { return s.dtype == NYS_BF16 && s.m <= 128; }
+bool pinv_tc_supported(const Shape& s) {
+  return s.dtype == NYS_BF16 && s.m <= 128 && s.iters <= kTf32MaxIters;
+}
 
 int pinv_tc_ctas(const Shape& s) {
   const int hp = std::min(128 / mpad_of(s.m), 256 / s.d);
@@ -716,6 +738,7 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   PinvParams p{};
   p.z = z;
   p.z_only = gpart == nullptr ? 1 : 0;
+  p.stall_ns = debug_stall_ns();
   p.qt = qt;
   p.kt = kt;
   p.gpart = gpart;

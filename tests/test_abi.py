@@ -144,3 +144,9 @@ def test_fwd_ex_rejects_bad_variant_arguments(N):
     assert ex(lengths=[a["n"] + 1, a["n"]]) == N.NYS_ERR_SHAPE   # longer than n
     assert ex(ws=256 + 16) == N.NYS_ERR_ALIGN                    # workspace not 256-aligned
     assert ex(ws=256, ws_bytes=8) == N.NYS_ERR_NOMEM              # workspace too small
+
+
+def test_stall_switch_rejects_other_values(N):
+    lib = N.load_library()
+    assert lib.nystrom_debug_stall_pinv(2) == N.NYS_ERR_ARG
+    assert lib.nystrom_debug_stall_pinv(0) == N.NYS_OK

@@ -95,3 +95,11 @@ def test_errors_and_truncation(N):
     assert lib.nystrom_plan_describe(1, 1, 512, 64, 64, 6, 5, 1, buf, 10) == full > 9
     assert buf.raw[:10] == N.nystrom_plan_describe(1, 1, 512, 64, 64, 6, 5, 1)[:9].encode() + b"\0"
     assert buf.raw[10:16] == b"#" * 6  # nothing written past len
+
+
+def test_many_updates_leave_the_tensor_core_pseudo_inverse(N):
+    """Past 8 updates the bf16 path's pseudo-inverse runs in fp32 (CUDA cores)."""
+    assert plan(N, 1, 2, 512, 64, 64, N.NYS_BF16, iters=8)["pinv"].startswith("pinv_tc")
+    assert plan(N, 1, 2, 512, 64, 64, N.NYS_BF16, iters=9)["pinv"] == "pinv_simt"
+    assert plan(N, 1, 2, 512, 128, 256, N.NYS_BF16, iters=8)["pinv"].startswith("pinv_big")
+    assert plan(N, 1, 2, 512, 128, 256, N.NYS_BF16, iters=12)["pinv"] == "pinv_simt"
