@@ -176,6 +176,33 @@ int nystrom_attn_fwd_ex(const void* q, const void* k, const void* v,
                         void* workspace, size_t ws_bytes, nys_stream_t stream);
 
 /*
+ * nystrom_mha_fwd - the multi-head attention module around the op (the
+ * page's model uses Nyström self-attention in place of softmax attention,
+ * abstract and Proposed method bullet 6): with D = H*d,
+ *   [Q | K | V] = x w_qkv + b_qkv,  Q, K, V split into H heads of d columns
+ *   (head h = columns [h*d, (h+1)*d) of each), O_h = the forward pass of the
+ *   top of this file on head h (m landmarks, iters updates, conv_w [H][conv_ks]),
+ *   y = [O_1 | ... | O_H] w_o + b_o.
+ * x, y: [B][n][D], w_qkv: [D][3D] (columns: the Q block, then K, then V),
+ * w_o: [D][D], all row-major in `dtype` (device); b_qkv [3D] and b_o [D]
+ * float32 device arrays, or NULL for no bias. Pointers 16-byte aligned.
+ * The projections run in cuBLAS (fp32 accumulation into the workspace); the
+ * head split and merge, the biases and the attention in this library's
+ * kernels. No residual connection, normalisation or dropout: those belong to
+ * the layer around the module.
+ * workspace: device, 256-byte aligned, ws_bytes >= nystrom_mha_workspace_bytes,
+ * or NULL to use a buffer the library allocates and caches per device.
+ * Returns NYS_OK or a negative nys_status_t (shape rules as the top of this
+ * file, with n, H, d, m of the attention).
+ */
+size_t nystrom_mha_workspace_bytes(int B, int n, int H, int d, int m, int dtype);
+int nystrom_mha_fwd(const void* x, const void* w_qkv, const float* b_qkv,
+                    const void* w_o, const float* b_o, const float* conv_w,
+                    void* y, int B, int n, int H, int d, int m, int iters,
+                    int conv_ks, int dtype, void* workspace, size_t ws_bytes,
+                    nys_stream_t stream);
+
+/*
  * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
  * copies q, k, v, conv_w to the device, runs the forward pass on `stream`,
  * copies out back and waits for the stream. The batch is processed in up

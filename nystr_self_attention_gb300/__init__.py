@@ -9,6 +9,6 @@ from ._binding import (  # noqa: F401
     NYS_STAGE_K_TILDE, NYS_STAGE_Q_TILDE, NYS_STAGE_W, NYS_STAGE_Z, NystromError, load_library,
     nystrom_attention, nystrom_attn_fwd, nystrom_debug_stall_pinv, nystrom_attn_fwd_ex, nystrom_attn_fwd_host, nystrom_attn_fwd_noalloc, nystrom_attn_fwd_ws,
     nystrom_attn_stage_offset, nystrom_attn_workspace_bytes, nystrom_get_status,
-    nystrom_last_error_string, nystrom_launch_count, nystrom_plan_describe, nystrom_profile_enable,
+    nystrom_last_error_string, nystrom_launch_count, nystrom_mha_fwd, nystrom_mha_workspace_bytes, nystrom_plan_describe, nystrom_profile_enable,
     nystrom_profile_read, nystrom_strerror,
 )

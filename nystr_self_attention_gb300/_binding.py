@@ -35,6 +35,9 @@ _SIG = {
     "nystrom_launch_count": (ctypes.c_ulonglong, []),
     "nystrom_profile_enable": (_I, [_I]),
     "nystrom_debug_stall_pinv": (_I, [_I]),
+    "nystrom_mha_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "nystrom_mha_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P,
+                             ctypes.c_size_t, _P]),
     "nystrom_profile_read": (_I, [_I, ctypes.c_char_p, _I, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -201,6 +204,20 @@ def nystrom_attention(q, k, v, conv_w, m: int, iters: int, out=None, stream=None
     nystrom_attn_fwd(q, k, v, conv_w if ks > 0 else None, out, B, H, n, d, m, iters, ks, dtype,
                      stream)
     return out
+
+
+def nystrom_mha_workspace_bytes(B, n, H, d, m, dtype) -> int:
+    return load_library().nystrom_mha_workspace_bytes(B, n, H, d, m, dtype)
+
+
+def nystrom_mha_fwd(x, w_qkv, b_qkv, w_o, b_o, conv_w, y, B, n, H, d, m, iters, conv_ks, dtype,
+                    workspace=None, ws_bytes=0, stream=None):
+    """The attention module around the op (see include/nystrom.h)."""
+    lib = load_library()
+    return _check(lib.nystrom_mha_fwd(_ptr(x), _ptr(w_qkv), _ptr(b_qkv), _ptr(w_o), _ptr(b_o),
+                                      _ptr(conv_w), _ptr(y), B, n, H, d, m, iters, conv_ks, dtype,
+                                      _ptr(workspace), ws_bytes, _stream(stream)),
+                  "nystrom_mha_fwd")
 
 
 def nystrom_debug_stall_pinv(on: bool) -> int:

@@ -58,7 +58,11 @@ def build(verbose: bool = False, force: bool = False, extra: list[str] | None = 
         for obj, log in ex.map(lambda j: _compile(j[0], j[1], extra), jobs):
             if verbose and log.strip():
                 print(log)
-    cmd = [nvcc(), *ARCH_FLAGS, "-shared", "-o", LIB + ".tmp", *objs]
+    # cuBLAS for the module's two projection GEMMs, found through an rpath to
+    # the toolkit that compiled the library
+    cuda_lib = os.path.realpath(os.path.join(os.path.dirname(nvcc()), "..", "lib64"))
+    cmd = [nvcc(), *ARCH_FLAGS, "-shared", "-o", LIB + ".tmp", *objs, "-L", cuda_lib, "-lcublas",
+           "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

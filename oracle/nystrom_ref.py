@@ -52,7 +52,7 @@ __all__ = [
     "pinv_step", "pinv_iterative", "landmark_rows", "token_rows",
     "depthwise_conv_seq", "nystrom_head", "nystrom_attention",
     "softmax_attention", "svd_pinv", "depthwise_conv_seq_channels", "conv_of",
-    "masked_softmax_rows", "nystrom_head_padded",
+    "masked_softmax_rows", "nystrom_head_padded", "split_heads", "merge_heads", "mha_forward",
 ]
 
 
@@ -299,3 +299,49 @@ def softmax_attention(q, k, v):
 def svd_pinv(a):
     """Moore-Penrose inverse by the SVD (what bullet 5's iteration avoids)."""
     return np.linalg.pinv(_f64(a))
+
+
+# -------------------------------------------------------------- the module
+# The multi-head attention module the page's model wraps around the op
+# (abstract; Proposed method, bullet 6: Nyström self-attention replaces
+# softmax attention in the Transformer): projections in, heads, projection
+# out. Random weights only; no residual, normalisation or dropout (those
+# belong to the layer).
+
+def split_heads(x, H):
+    """[B, n, H*d] -> [B, H, n, d]: head h takes columns [h*d, (h+1)*d)."""
+    x = _f64(x)
+    B, n, D = x.shape
+    d = D // H
+    out = np.empty((B, H, n, d))
+    for h in range(H):
+        out[:, h] = x[:, :, h * d:(h + 1) * d]
+    return out
+
+
+def merge_heads(o):
+    """[B, H, n, d] -> [B, n, H*d]: the inverse of ``split_heads``."""
+    o = _f64(o)
+    B, H, n, d = o.shape
+    out = np.empty((B, n, H * d))
+    for h in range(H):
+        out[:, :, h * d:(h + 1) * d] = o[:, h]
+    return out
+
+
+def mha_forward(x, w_qkv, b_qkv, w_o, b_o, conv_w, H, m, iters):
+    """y = merge(Nystrom(Q, K, V)) w_o + b_o with [Q | K | V] = x w_qkv +
+    b_qkv split into H heads. x [B, n, D], w_qkv [D, 3D] (the Q block, then K,
+    then V), b_qkv [3D] or None, w_o [D, D], b_o [D] or None, conv_w [H, ks]."""
+    x = _f64(x)
+    D = x.shape[2]
+    qkv = x @ _f64(w_qkv)
+    if b_qkv is not None:
+        qkv = qkv + _f64(b_qkv)
+    q = split_heads(qkv[..., :D], H)
+    k = split_heads(qkv[..., D:2 * D], H)
+    v = split_heads(qkv[..., 2 * D:], H)
+    y = merge_heads(nystrom_attention(q, k, v, conv_w, m, iters)) @ _f64(w_o)
+    if b_o is not None:
+        y = y + _f64(b_o)
+    return y

@@ -150,3 +150,20 @@ def test_stall_switch_rejects_other_values(N):
     lib = N.load_library()
     assert lib.nystrom_debug_stall_pinv(2) == N.NYS_ERR_ARG
     assert lib.nystrom_debug_stall_pinv(0) == N.NYS_OK
+
+
+def test_module_rejects_bad_arguments(N):
+    lib = N.load_library()
+
+    def mha(x=256, w=256, wo=256, y=256, b=None, ws=None, nbytes=0, **kw):
+        a = dict(dict(B=2, n=64, H=2, d=64, m=8, iters=6, ks=0, dtype=1), **kw)
+        return lib.nystrom_mha_fwd(x, w, b, wo, b, None, y, a["B"], a["n"], a["H"], a["d"], a["m"],
+                                   a["iters"], a["ks"], a["dtype"], ws, nbytes, None)
+    assert mha(x=None) == N.NYS_ERR_ARG
+    assert mha(ks=5) == N.NYS_ERR_ARG            # a conv width without weights
+    assert mha(d=48) == N.NYS_ERR_SHAPE          # bf16 head width outside {32, 64, 128}
+    assert mha(x=264) == N.NYS_ERR_ALIGN
+    assert mha(ws=256 + 64) == N.NYS_ERR_ALIGN
+    assert mha(ws=256, nbytes=16) == N.NYS_ERR_NOMEM
+    assert N.nystrom_mha_workspace_bytes(2, 64, 2, 64, 8, 1) > 0
+    assert N.nystrom_mha_workspace_bytes(2, 64, 2, 48, 8, 1) == 0

@@ -167,3 +167,44 @@ def lengths_for(B: int, n: int, m: int, seed: int) -> np.ndarray:
     if B > 1:
         out[1] = m
     return out
+
+
+@dataclasses.dataclass
+class ModuleInputs:
+    """Inputs of the attention module around the op: x ``[B, n, H*d]``,
+    w_qkv ``[D, 3D]``, b_qkv ``[3D]``, w_o ``[D, D]``, b_o ``[D]`` (fp32
+    arrays holding the values both sides use; ``*_bits`` the bf16 patterns
+    of x, w_qkv, w_o for bf16 workloads) and the per-head conv weights."""
+    wl: Workload
+    x: np.ndarray
+    w_qkv: np.ndarray
+    b_qkv: np.ndarray
+    w_o: np.ndarray
+    b_o: np.ndarray
+    conv_w: np.ndarray
+    bits: dict | None = None
+
+
+def module_inputs(wl: Workload, seed: int) -> ModuleInputs:
+    """Random weights for the module (no trained model exists here): x
+    standard normal, weights normal with variance 1/D (so Q, K, V have about
+    unit variance), biases normal with standard deviation 0.1, conv weights as
+    in ``make_inputs``. Draw order: x, w_qkv, b_qkv, w_o, b_o, conv_w."""
+    rng = np.random.default_rng(seed)
+    D = wl.H * wl.d
+    x = rng.standard_normal((wl.B, wl.n, D), dtype=np.float32)
+    w_qkv = (rng.standard_normal((D, 3 * D), dtype=np.float32) / np.float32(np.sqrt(D))).astype(np.float32)
+    b_qkv = (rng.standard_normal(3 * D, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    w_o = (rng.standard_normal((D, D), dtype=np.float32) / np.float32(np.sqrt(D))).astype(np.float32)
+    b_o = (rng.standard_normal(D, dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    ks = wl.ks
+    conv_w = ((rng.standard_normal((wl.H, ks), dtype=np.float32) * np.float32(1.0 / np.sqrt(ks))).astype(np.float32)
+              if ks > 0 else np.zeros((wl.H, 0), dtype=np.float32))
+    out = ModuleInputs(wl, x, w_qkv, b_qkv, w_o, b_o, conv_w)
+    if wl.dtype == "bf16":
+        out.bits = {}
+        for name in ("x", "w_qkv", "w_o"):
+            vals, bits = round_to_bf16(getattr(out, name))
+            setattr(out, name, vals)
+            out.bits[name] = bits
+    return out
