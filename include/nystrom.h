@@ -203,6 +203,47 @@ int nystrom_mha_fwd(const void* x, const void* w_qkv, const float* b_qkv,
                     nys_stream_t stream);
 
 /*
+ * Clustered attention, centroid path ("Fast Transformers with Clustered
+ * Attention" review page, Proposed method, bullets 1, 2 and 4): per head
+ * (b, h) the queries Q [n, d] are grouped into C clusters by K-means and
+ * attention is computed once per centroid:
+ *   mu      = segment means of Q over C contiguous segments (as Q~ above)
+ *   iters x:  a(i) = argmin_c |q_i - mu_c|^2 (ties: the lowest c), then
+ *             mu_c = mean of the queries with a(i) = c (none: unchanged)
+ *   out[i]  = softmax(mu_{a(i)} K^T / sqrt(d)) V
+ * K-means runs in fp32 on the CUDA cores (the update sums a cluster's
+ * queries in index order: reproducible); the centroid rows run in the
+ * landmark-row kernels of the forward pass (bf16 tensor cores for NYS_BF16,
+ * with the centroids rounded to bf16; fp32 CUDA cores for NYS_FP32).
+ * q, k, v, out: [B][H][n][d] in `dtype`, device, 16-byte aligned; shape rules
+ * as the top of this file with C in place of m; 1 <= iters <= 64.
+ * workspace: device, 256-byte aligned, ws_bytes >=
+ * nystrom_clustered_workspace_bytes(...), or NULL for the library's cached
+ * workspace. Asynchronous on `stream`; nystrom_get_status reports bounded
+ * waits that ran out.
+ * nystrom_clustered_stage_offset: byte offset in the workspace, after a
+ * call with these sizes has finished, of NYS_CSTAGE_ASSIGN (int32
+ * [B*H][n], the last assignment), NYS_CSTAGE_CENTROIDS_PREV (float32
+ * [B*H][C][d], the centroids that assignment used), NYS_CSTAGE_CENTROIDS
+ * (float32 [B*H][C][d], after the last update), NYS_CSTAGE_G (float32
+ * [B*H][C][d], the centroid rows); -1 for invalid sizes or stage.
+ */
+typedef enum {
+  NYS_CSTAGE_ASSIGN = 0,
+  NYS_CSTAGE_CENTROIDS_PREV = 1,
+  NYS_CSTAGE_CENTROIDS = 2,
+  NYS_CSTAGE_G = 3
+} nys_cstage_t;
+size_t nystrom_clustered_workspace_bytes(int B, int H, int n, int d, int C,
+                                         int dtype);
+long long nystrom_clustered_stage_offset(int B, int H, int n, int d, int C,
+                                         int iters, int dtype, int stage);
+int nystrom_clustered_attn_fwd(const void* q, const void* k, const void* v,
+                               void* out, int B, int H, int n, int d, int C,
+                               int iters, int dtype, void* workspace,
+                               size_t ws_bytes, nys_stream_t stream);
+
+/*
  * nystrom_attn_fwd_host - the whole forward pass from and to HOST memory:
  * copies q, k, v, conv_w to the device, runs the forward pass on `stream`,
  * copies out back and waits for the stream. The batch is processed in up

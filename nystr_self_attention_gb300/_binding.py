@@ -12,6 +12,7 @@ NYS_OK, NYS_ERR_ARG, NYS_ERR_SHAPE, NYS_ERR_ALIGN = 0, -1, -2, -3
 NYS_ERR_UNSUPPORTED, NYS_ERR_NOMEM, NYS_ERR_CUDA, NYS_ERR_TIMEOUT = -4, -5, -6, -7
 NYS_STAGE_Q_TILDE, NYS_STAGE_K_TILDE, NYS_STAGE_G, NYS_STAGE_A_S, NYS_STAGE_W, NYS_STAGE_Z = range(6)
 NYS_CONV_PER_HEAD, NYS_CONV_PER_CHANNEL = 0, 1
+NYS_CSTAGE_ASSIGN, NYS_CSTAGE_CENTROIDS_PREV, NYS_CSTAGE_CENTROIDS, NYS_CSTAGE_G = range(4)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnystrom.so")
 _lib = None
@@ -36,6 +37,10 @@ _SIG = {
     "nystrom_profile_enable": (_I, [_I]),
     "nystrom_debug_stall_pinv": (_I, [_I]),
     "nystrom_mha_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "nystrom_clustered_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "nystrom_clustered_stage_offset": (ctypes.c_longlong, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "nystrom_clustered_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                                        ctypes.c_size_t, _P]),
     "nystrom_mha_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P,
                              ctypes.c_size_t, _P]),
     "nystrom_profile_read": (_I, [_I, ctypes.c_char_p, _I, ctypes.POINTER(ctypes.c_double),
@@ -218,6 +223,24 @@ def nystrom_mha_fwd(x, w_qkv, b_qkv, w_o, b_o, conv_w, y, B, n, H, d, m, iters, 
                                       _ptr(conv_w), _ptr(y), B, n, H, d, m, iters, conv_ks, dtype,
                                       _ptr(workspace), ws_bytes, _stream(stream)),
                   "nystrom_mha_fwd")
+
+
+def nystrom_clustered_workspace_bytes(B, H, n, d, C, dtype) -> int:
+    return load_library().nystrom_clustered_workspace_bytes(B, H, n, d, C, dtype)
+
+
+def nystrom_clustered_stage_offset(B, H, n, d, C, iters, dtype, stage) -> int:
+    return load_library().nystrom_clustered_stage_offset(B, H, n, d, C, iters, dtype, stage)
+
+
+def nystrom_clustered_attn_fwd(q, k, v, out, B, H, n, d, C, iters, dtype, workspace=None,
+                               ws_bytes=0, stream=None):
+    """Clustered attention, centroid path (see include/nystrom.h)."""
+    lib = load_library()
+    return _check(lib.nystrom_clustered_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, n, d,
+                                                 C, iters, dtype, _ptr(workspace), ws_bytes,
+                                                 _stream(stream)),
+                  "nystrom_clustered_attn_fwd")
 
 
 def nystrom_debug_stall_pinv(on: bool) -> int:

@@ -155,9 +155,7 @@ int ensure_buffer(void** ptr, size_t* have, size_t need, cudaStream_t stream) {
 
 }  // namespace
 
-int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
-        void* out, char* ws, cudaStream_t stream, int dev, bool clear_status) {
-  const Layout L = make_layout(s);
+int begin_call(char* ws, const Layout& L, cudaStream_t stream, int dev, bool clear_status) {
   {
     std::lock_guard<std::mutex> lk(g_dev[dev].mu);
     g_dev[dev].last_ws = ws;
@@ -167,8 +165,21 @@ int run(const Shape& s, const void* q, const void* k, const void* v, const float
     cudaError_t e = cudaMemsetAsync(ws + L.status, 0, sizeof(int), stream);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  const int rc = launch_forward(s, q, k, v, conv_w, out, ws, L, stream, dev);
-  return rc;
+  return NYS_OK;
+}
+
+void* cached_workspace(int dev, size_t bytes, cudaStream_t stream, int* rc) {
+  std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+  *rc = ensure_buffer(&g_dev[dev].ws, &g_dev[dev].ws_bytes, bytes, stream);
+  return *rc == NYS_OK ? g_dev[dev].ws : nullptr;
+}
+
+int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,
+        void* out, char* ws, cudaStream_t stream, int dev, bool clear_status) {
+  const Layout L = make_layout(s);
+  const int rc = begin_call(ws, L, stream, dev, clear_status);
+  if (rc != NYS_OK) return rc;
+  return launch_forward(s, q, k, v, conv_w, out, ws, L, stream, dev);
 }
 
 int scratch_mats(const Shape& s) { return pinv_big_supported(s) ? 5 : 3; }

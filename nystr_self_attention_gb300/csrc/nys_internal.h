@@ -91,6 +91,12 @@ int check_shape(int B, int H, int n, int d, int m, int iters, int ks, int dtype)
 int check_args(const void* q, const void* k, const void* v, const float* conv_w, const void* out,
                int B, int H, int n, int d, int m, int iters, int ks, int dtype);
 int check_device(int* dev_out);  // current device, must be compute capability 10.3
+// Makes `ws` the workspace nystrom_get_status reads for this device and
+// clears its status word on `stream` (unless told not to).
+int begin_call(char* ws, const Layout& L, cudaStream_t stream, int dev, bool clear_status = true);
+// The library's cached workspace of this device, grown to `bytes` (NULL and
+// *rc < 0 on failure).
+void* cached_workspace(int dev, size_t bytes, cudaStream_t stream, int* rc);
 // Clears the status word (unless told not to) and enqueues the forward
 // pass with workspace `ws`.
 int run(const Shape& s, const void* q, const void* k, const void* v, const float* conv_w,

@@ -167,3 +167,22 @@ def test_module_rejects_bad_arguments(N):
     assert mha(ws=256, nbytes=16) == N.NYS_ERR_NOMEM
     assert N.nystrom_mha_workspace_bytes(2, 64, 2, 64, 8, 1) > 0
     assert N.nystrom_mha_workspace_bytes(2, 64, 2, 48, 8, 1) == 0
+
+
+def test_clustered_rejects_bad_arguments(N):
+    lib = N.load_library()
+
+    def cl(q=256, iters=3, C=8, d=64, ws=None, nbytes=0):
+        return lib.nystrom_clustered_attn_fwd(q, 256, 256, 256, 2, 2, 64, d, C, iters, 1, ws, nbytes,
+                                              None)
+    assert cl(q=None) == N.NYS_ERR_ARG
+    assert cl(iters=0) == N.NYS_ERR_SHAPE
+    assert cl(iters=65) == N.NYS_ERR_SHAPE
+    assert cl(C=65) == N.NYS_ERR_SHAPE     # more clusters than queries
+    assert cl(q=264) == N.NYS_ERR_ALIGN
+    assert cl(ws=256, nbytes=8) == N.NYS_ERR_NOMEM
+    for it in (1, 2, 3):
+        last = N.nystrom_clustered_stage_offset(2, 2, 64, 64, 8, it, 1, N.NYS_CSTAGE_CENTROIDS)
+        prev = N.nystrom_clustered_stage_offset(2, 2, 64, 64, 8, it, 1, N.NYS_CSTAGE_CENTROIDS_PREV)
+        assert last >= 0 and prev >= 0 and last != prev
+    assert N.nystrom_clustered_stage_offset(2, 2, 64, 64, 8, 1, 1, 9) == -1
