@@ -53,6 +53,8 @@ def parse_args():
                         "reported under other_workloads ('' for none)")
     p.add_argument("--no-scan", action="store_true",
                    help="skip the sequence-length scan reported under linear_scan")
+    p.add_argument("--no-next", action="store_true",
+                   help="skip the module / variants / clustered timings reported under next_rows")
     p.add_argument("--min-region-s", type=float, default=1.0,
                    help="repeat the K-step timed region until this much wall time has passed "
                         "(so the clock sampler sees the timed work)")
@@ -461,6 +463,95 @@ def time_brief(N, wl, sets, w, stream, steps=20, seconds=0.3):
     return ms, spread([r / steps for r in region_ms])
 
 
+def time_fn(N, step, stream, steps=20, seconds=0.3):
+    """Median per-step milliseconds of an arbitrary step over ~`seconds` of
+    K-step regions (CUDA events on the launch stream), after 5 warm-up steps."""
+    import torch
+
+    def barrier():
+        torch.cuda.synchronize()
+
+    for i in range(5):
+        step(i)
+    first, _ = time_regions(N, step, steps, stream, barrier, 1)
+    regions = max(3, int(np.ceil(seconds / max(first[0] / 1e3, 1e-6))))
+    region_ms, launches = time_regions(N, step, steps, stream, barrier, regions)
+    assert N.nystrom_get_status(stream) == N.NYS_OK
+    return statistics.median(region_ms) / steps, launches / (regions * steps)
+
+
+def next_rows(N, dev, stream):
+    """The rows past the core path, timed briefly on seeded device draws:
+    the attention module around the op at BERT-base size, the two variants
+    (padded sequences with per-channel filters) on the clustered and
+    long-context shapes, and clustered attention on the clustered shape."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    bf = torch.bfloat16
+    out = {}
+
+    def randn(*shape, scale=1.0, dtype=bf):
+        return (torch.randn(shape, generator=gen, device=dev) * scale).to(dtype)
+
+    # module: B32 n512 H12 d64 (D = 768), projections + attention
+    B, n, H, d, m = 32, 512, 12, 64, 64
+    D = H * d
+    x, wqkv, wo = randn(B, n, D), randn(D, 3 * D, scale=D ** -0.5), randn(D, D, scale=D ** -0.5)
+    bqkv, bo = randn(3 * D, scale=0.1, dtype=torch.float32), randn(D, scale=0.1, dtype=torch.float32)
+    cw = randn(H, 33, scale=33 ** -0.5, dtype=torch.float32)
+    y = torch.empty_like(x)
+    nb = N.nystrom_mha_workspace_bytes(B, n, H, d, m, N.NYS_BF16)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    ms, lps = time_fn(N, lambda i: N.nystrom_mha_fwd(x, wqkv, bqkv, wo, bo, cw, y, B, n, H, d, m, 6,
+                                                     33, N.NYS_BF16, ws, nb, stream), stream)
+    proj_flops = 2.0 * B * n * D * (3 * D + D)
+    out["module"] = {"workload": f"B={B} n={n} H={H} d={d} (D={D}) m={m} iters=6 ks=33 bf16, "
+                                 "QKV and output projections (cuBLAS) + the op",
+                     "ms_per_step": ms, "tokens_per_s": B * n / (ms / 1e3),
+                     "projection_tflops_if_all_time": proj_flops / (ms / 1e3) / 1e12,
+                     "library_launches_per_step": lps}
+    del x, wqkv, wo, y, ws
+    # variants: padded sequences + per-channel filters (c4 and c5 shapes)
+    for name, (B, H, n, d, m, it, ks) in {"c4": (8, 8, 8192, 64, 128, 6, 33),
+                                          "c5": (2, 16, 32768, 128, 256, 8, 65)}.items():
+        q, k, v = randn(B, H, n, d), randn(B, H, n, d), randn(B, H, n, d)
+        o = torch.empty_like(q)
+        cwc = randn(H, d, ks, scale=ks ** -0.5, dtype=torch.float32)
+        lengths = workloads.lengths_for(B, n, m, seed=99).tolist()
+        ms, _ = time_fn(N, lambda i: N.nystrom_attn_fwd_ex(q, k, v, cwc, o, B, H, n, d, m, it, ks,
+                                                           N.NYS_BF16, N.NYS_CONV_PER_CHANNEL,
+                                                           lengths, None, 0, stream), stream)
+        out[f"variants_{name}"] = {
+            "workload": f"{name} shape B={B} H={H} n={n} d={d} m={m} iters={it} ks={ks} bf16, "
+                        f"per-channel filters, lengths {lengths}",
+            "ms_per_step": ms, "tokens_per_s": B * H * n / (ms / 1e3),
+            "real_tokens_per_s": H * sum(lengths) / (ms / 1e3)}
+        del q, k, v, o
+        torch.cuda.empty_cache()
+    # clustered attention: c4 shape, C = 128, 10 K-means rounds
+    B, H, n, d, C, it = 8, 8, 8192, 64, 128, 10
+    q, k, v = randn(B, H, n, d), randn(B, H, n, d), randn(B, H, n, d)
+    o = torch.empty_like(q)
+    nb = N.nystrom_clustered_workspace_bytes(B, H, n, d, C, N.NYS_BF16)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    ms, _ = time_fn(N, lambda i: N.nystrom_clustered_attn_fwd(q, k, v, o, B, H, n, d, C, it,
+                                                              N.NYS_BF16, ws, nb, stream), stream)
+    out["clustered_c4"] = {"workload": f"B={B} H={H} n={n} d={d} C={C} K-means rounds={it} bf16",
+                           "ms_per_step": ms, "tokens_per_s": B * H * n / (ms / 1e3)}
+    N.nystrom_profile_read()
+    N.nystrom_profile_enable(True)
+    for _ in range(5):
+        N.nystrom_clustered_attn_fwd(q, k, v, o, B, H, n, d, C, it, N.NYS_BF16, ws, nb, stream)
+    torch.cuda.synchronize()
+    N.nystrom_profile_enable(False)
+    prof = N.nystrom_profile_read()
+    out["clustered_c4"]["kernels_us_per_step"] = {kname: ms_ / 5 * 1e3 for kname, (ms_, _) in prof.items()}
+    del q, k, v, o, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def linear_scan(N, wl, dev, stream, peaks, peak_src, ns):
     """Time of one pass against the sequence length with every other size of
     the workload fixed (linear time shows as a constant time per token), and
@@ -661,6 +752,7 @@ def run_ours(args, wl):
     # the other workloads and the sequence-length scan ride along (one GPU)
     others = None
     scan = None
+    nxt = None
     if world == 1:
         del sets, q0, k0, v0
         torch.cuda.empty_cache()
@@ -682,6 +774,8 @@ def run_ours(args, wl):
         if not args.no_scan and wl.dtype == "bf16":
             ns = sorted({max(wl.m, wl.n >> 3), max(wl.m, wl.n >> 2), max(wl.m, wl.n >> 1), wl.n})
             scan = linear_scan(N, wl, dev, stream, peaks, peak_src, ns)
+        if not args.no_next:
+            nxt = next_rows(N, dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -709,7 +803,7 @@ def run_ours(args, wl):
         "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": launches // max(1, len(region_ms)),
         "gpu_launches_all_regions": launches,
-        "other_workloads": others, "linear_scan": scan,
+        "other_workloads": others, "linear_scan": scan, "next_rows": nxt,
     }
     print(json.dumps(line), flush=True)
 

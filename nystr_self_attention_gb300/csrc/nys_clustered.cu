@@ -28,14 +28,16 @@ constexpr int kAssignThreads = 128;
 constexpr int kTileC = 32;  // centroids per shared-memory tile
 
 // grid (ceil(n / 128), B*H), block 128: thread = query. The query row sits
-// in registers (DM >= d columns, zero past d); tiles of 32 centroids are
-// staged in shared memory; the squared distance is summed directly (no
-// norm-expansion cancellation).
+// in registers (DM >= d columns, zero past d); tiles of 32 centroids and
+// their squared norms are staged in shared memory. The nearest centroid
+// minimises |mu_c|^2 - 2 q . mu_c (|q|^2 is common to all c): one FMA per
+// element.
 template <typename T, int DM>
 __global__ void __launch_bounds__(kAssignThreads)
 kmeans_assign(const T* __restrict__ q, const float* __restrict__ mu, int* __restrict__ assign,
               int n, int d, int C) {
-  __shared__ float smu[kTileC * DM];
+  __shared__ __align__(16) float smu[kTileC * DM];
+  __shared__ float snorm[kTileC];
   const long long bh = blockIdx.y;
   const int t = blockIdx.x * kAssignThreads + threadIdx.x;
   const bool ok = t < n;
@@ -54,16 +56,26 @@ kmeans_assign(const T* __restrict__ q, const float* __restrict__ mu, int* __rest
       smu[e] = (c < nc && j < d) ? mh[(size_t)(c0 + c) * d + j] : 0.f;
     }
     __syncthreads();
+    if (threadIdx.x < kTileC) {
+      float nrm = 0.f;
+      for (int j = 0; j < DM; ++j) nrm = fmaf(smu[threadIdx.x * DM + j], smu[threadIdx.x * DM + j], nrm);
+      snorm[threadIdx.x] = nrm;
+    }
+    __syncthreads();
     for (int c = 0; c < nc; ++c) {
-      const float* m = smu + c * DM;
-      float acc = 0.f;
+      const float4* m = reinterpret_cast<const float4*>(smu + c * DM);
+      float dot0 = 0.f, dot1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < DM; ++j) {
-        const float df = qr[j] - m[j];
-        acc = fmaf(df, df, acc);
+      for (int j = 0; j < DM / 4; ++j) {
+        const float4 mv = m[j];
+        dot0 = fmaf(qr[4 * j], mv.x, dot0);
+        dot1 = fmaf(qr[4 * j + 1], mv.y, dot1);
+        dot0 = fmaf(qr[4 * j + 2], mv.z, dot0);
+        dot1 = fmaf(qr[4 * j + 3], mv.w, dot1);
       }
-      if (acc < best) {  // strict: a tie keeps the lower index
-        best = acc;
+      const float score = fmaf(-2.f, dot0 + dot1, snorm[c]);
+      if (score < best) {  // strict: a tie keeps the lower index
+        best = score;
         best_c = c0 + c;
       }
     }
@@ -72,32 +84,39 @@ kmeans_assign(const T* __restrict__ q, const float* __restrict__ mu, int* __rest
 }
 
 constexpr int kUpdThreads = 128;
-constexpr int kUpdChunk = 512;  // assignments staged per step
 
-// grid (C, B*H), block 128: CTA = one cluster of one head. Thread j sums
-// column j (j < d) of the cluster's queries in index order; the new centroid
-// is the mean, or the old centroid for an empty cluster.
+// grid (C, B*H), block 128: CTA = one cluster of one head. 128 assignments
+// at a time: each warp ballots which of its 32 queries belong to the
+// cluster; then thread j (j < d) adds column j of the members in index order
+// (reproducible). The new centroid is the mean, or the old centroid for an
+// empty cluster.
 template <typename T>
 __global__ void __launch_bounds__(kUpdThreads)
 kmeans_update(const T* __restrict__ q, const int* __restrict__ assign,
               const float* __restrict__ mu_old, float* __restrict__ mu_new, int n, int d, int C) {
-  __shared__ int sa[kUpdChunk];
+  __shared__ uint32_t masks[kUpdThreads / 32];
   const int c = blockIdx.x;
   const long long bh = blockIdx.y;
-  const int j = threadIdx.x;
+  const int j = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int* ah = assign + (size_t)bh * n;
   const T* qh = q + (size_t)bh * n * d;
   float s = 0.f;
   int cnt = 0;
-  for (int i0 = 0; i0 < n; i0 += kUpdChunk) {
-    const int ni = min(kUpdChunk, n - i0);
+  for (int i0 = 0; i0 < n; i0 += kUpdThreads) {
+    const int i = i0 + threadIdx.x;
+    const bool member = i < n && __ldg(ah + i) == c;
+    const uint32_t mk = __ballot_sync(0xffffffffu, member);
+    __syncthreads();  // the previous chunk's masks have been read
+    if (lane == 0) masks[warp] = mk;
     __syncthreads();
-    for (int e = threadIdx.x; e < ni; e += kUpdThreads) sa[e] = __ldg(ah + i0 + e);
-    __syncthreads();
-    for (int e = 0; e < ni; ++e) {
-      if (sa[e] == c) {
-        ++cnt;
-        if (j < d) s += ldf(qh + (size_t)(i0 + e) * d + j);
+#pragma unroll
+    for (int w = 0; w < kUpdThreads / 32; ++w) {
+      uint32_t b = masks[w];
+      cnt += __popc(b);
+      while (b) {
+        const int bit = __ffs(b) - 1;
+        b &= b - 1;
+        if (j < d) s += ldf(qh + (size_t)(i0 + 32 * w + bit) * d + j);
       }
     }
   }

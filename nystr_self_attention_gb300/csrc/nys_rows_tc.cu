@@ -448,6 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc(const __grid_constant__ R
             exp_chunk(32, r1);
             exp_chunk(64, r2);
             exp_chunk(96, r3);
+          } else if (key0 >= nk) {
+            // a tile wholly past the head's keys (padding): P = 0
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 32) tmem_st16(scol + (c0 >> 1), pk);
           } else {
             // padding rows and keys past the end give P = 0
 #pragma unroll 1

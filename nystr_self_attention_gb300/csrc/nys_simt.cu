@@ -667,60 +667,89 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 // ks = 0 it only zeroes the padding rows.
 //   out[t][c] = t < L ? out[t][c] + sum_j w[j] V[t + j - (ks-1)/2][c] : 0,
 //   V rows outside [0, L) read as zero, L = the entry's length (n if none).
-// grid (ceil(n / CV_ROWS), B*H), block (d / CV_COLS... ) = CV_THREADS: a CTA
-// takes CV_ROWS output rows of one head; their V rows with the halo are
-// staged in shared memory (fp32), each thread computes whole columns of
-// outputs for a strip of rows.
-constexpr int CV_ROWS = 64, CV_THREADS = 256;
+// grid (ceil(n / CV_ROWS), B*H), block CV_THREADS: a CTA takes CV_ROWS
+// output rows of one head; their V rows with the halo and the head's taps
+// (tap-major, so that consecutive channels read consecutive words) are
+// staged in shared memory. A work item is CV_RUN consecutive rows of one
+// column: per tap one weight and one new V value feed CV_RUN FMAs (the V
+// window slides in registers).
+constexpr int CV_ROWS = 64, CV_THREADS = 256, CV_RUN = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(CV_THREADS)
 conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
           int d, int ks, int per_channel, const int* __restrict__ lengths) {
-  extern __shared__ float sv[];  // [CV_ROWS + ks - 1][d]
+  extern __shared__ float sm[];
   const long long bh = blockIdx.y;
   const int h = (int)(bh % H);
   const int len = lengths ? lengths[bh / H] : n;
   const int t0 = blockIdx.x * CV_ROWS;
   const int rad = ks > 0 ? (ks - 1) / 2 : 0;
   const int vrows = CV_ROWS + 2 * rad;
+  float* sv = sm;                       // [vrows][d]
+  float* sw = sm + (size_t)vrows * d;   // per channel: [ks][d]; per head: [ks]
   const T* vb = v + (size_t)bh * n * d;
   T* ob = out + (size_t)bh * n * d;
-  if (ks > 0 && t0 < len) {
+  const bool work = ks > 0 && t0 < len;
+  if (work) {
     for (int e = threadIdx.x; e < vrows * d; e += CV_THREADS) {
       const int u = t0 - rad + e / d, c = e % d;
       sv[e] = (u >= 0 && u < len) ? ld(vb + (size_t)u * d + c) : 0.f;
     }
+    if (per_channel) {
+      // coalesced reads of the head's [d][ks] taps, stored tap-major
+      const float* wh = w + (size_t)h * d * ks;
+      for (int e = threadIdx.x; e < ks * d; e += CV_THREADS) {
+        const int c = e / ks, j = e % ks;
+        sw[(size_t)j * d + c] = wh[e];
+      }
+    } else {
+      for (int j = threadIdx.x; j < ks; j += CV_THREADS) sw[j] = w[(size_t)h * ks + j];
+    }
   }
   __syncthreads();
-  // thread -> column c and a strip of rows: d columns x (CV_THREADS / d) strips
-  const int strips = CV_THREADS / d;
-  const int c = threadIdx.x % d, strip = threadIdx.x / d;
-  if (strip >= strips) return;
-  const float* wc = w ? (per_channel ? w + ((size_t)h * d + c) * ks : w + (size_t)h * ks) : nullptr;
-  for (int r = strip; r < CV_ROWS; r += strips) {
-    const int t = t0 + r;
-    if (t >= n) break;
-    T* o = ob + (size_t)t * d + c;
-    if (t >= len) {
-      st(o, 0.f);
-      continue;
+  const int wstride = per_channel ? d : 0;  // word step between taps in sw
+  for (int item = threadIdx.x; item < (CV_ROWS / CV_RUN) * d; item += CV_THREADS) {
+    const int c = item % d, r0 = (item / d) * CV_RUN;
+    if (t0 + r0 >= n) continue;
+    float acc[CV_RUN];
+#pragma unroll
+    for (int r = 0; r < CV_RUN; ++r) acc[r] = 0.f;
+    if (work) {
+      // window: V rows (r0 + j + r), r < CV_RUN, relative to the staged block
+      const float* x = sv + (size_t)r0 * d + c;
+      const float* wc = sw + (per_channel ? c : 0);
+      float xw[CV_RUN];
+#pragma unroll
+      for (int r = 0; r < CV_RUN; ++r) xw[r] = x[(size_t)r * d];
+#pragma unroll 4
+      for (int j = 0; j < ks; ++j) {
+        const float wj = wc[(size_t)j * wstride + (per_channel ? 0 : j)];
+#pragma unroll
+        for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[r], acc[r]);
+#pragma unroll
+        for (int r = 0; r + 1 < CV_RUN; ++r) xw[r] = xw[r + 1];
+        // row r0 + j + CV_RUN: within the staged rows for every j < ks - 1
+        xw[CV_RUN - 1] = j + 1 < ks ? x[(size_t)(j + CV_RUN) * d] : 0.f;
+      }
     }
-    float acc = ld(o);
-    if (ks > 0) {
-      float cv = 0.f;
-      const float* x = sv + (size_t)r * d + c;
-      for (int j = 0; j < ks; ++j) cv = fmaf(wc[j], x[(size_t)j * d], cv);
-      acc += cv;
+#pragma unroll
+    for (int r = 0; r < CV_RUN; ++r) {
+      const int t = t0 + r0 + r;
+      if (t >= n) break;
+      T* o = ob + (size_t)t * d + c;
+      st(o, t < len ? ld(o) + acc[r] : 0.f);
     }
-    st(o, acc);
   }
 }
 
 template <typename T>
 int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, cudaStream_t stream) {
   const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
-  const size_t smem = s.ks > 0 ? sizeof(float) * (size_t)(CV_ROWS + 2 * rad) * s.d : 0;
+  const bool per_channel = s.conv_layout == NYS_CONV_PER_CHANNEL;
+  const size_t smem = s.ks > 0 ? sizeof(float) * ((size_t)(CV_ROWS + 2 * rad) * s.d +
+                                                  (size_t)s.ks * (per_channel ? s.d : 1))
+                               : 0;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(conv_mask<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
@@ -728,7 +757,7 @@ int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, c
   KernelScope ks_("conv_mask", stream);
   conv_mask<T><<<dim3((s.n + CV_ROWS - 1) / CV_ROWS, (unsigned)s.bh()), CV_THREADS, smem, stream>>>(
       static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d,
-      s.ks, s.conv_layout == NYS_CONV_PER_CHANNEL ? 1 : 0, s.lengths);
+      s.ks, per_channel ? 1 : 0, s.lengths);
   return launch_status();
 }
 
