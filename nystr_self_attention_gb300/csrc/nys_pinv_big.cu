@@ -1,21 +1,32 @@
 // Landmark kernel, iterative pseudo-inverse and W = Z G on the tensor cores
 // for 128 < m <= 256 landmarks ("Nyströmformer" review page, Proposed method,
-// bullets 2, 3 and 5). Same arithmetic as the m <= 128 kernel:
+// bullets 2, 3 and 5):
 //   A_S = softmax(Q~ K~^T s)    scores in 3xTF32 (hi*hi + hi*lo + lo*hi)
 //   Z_0 = A_S^T / (||A_S||_1 ||A_S||_inf)
-//   iters x:  X = A_S Z;  Y1 = X (7I - X);  Y2 = X (15I - Y1);
-//             Z <- 1/4 Z (13I - Y2)              tcgen05 kind::tf32
-//   W   = Z G
+//   iters x:  Z <- 1/4 Z (13I - 15X + 7X^2 - X^3),  X = A_S Z
+//   W   = Z G                                      tcgen05 kind::tf32
+// Each update is evaluated in three dependent levels of products instead of
+// the four of the nested (Horner) form, since its cost is the latency of the
+// chain, not the MMAs:
+//   level 0:  X = A_S Z
+//   level 1:  X X and Z X (one right factor, two left factors, side by side)
+//   level 2:  Z' = 1/4 (13 Z - 15 Z X + Z X (7X - X^2))
+// The update is the same polynomial in A_S and Z (X is recomputed from A_S
+// and Z every update); only the grouping of its terms differs.
 // An m x m fp32 matrix (256 KB at m = 256) does not fit one SM, so a
 // cluster of four CTAs works on one head: CTA (r, c) owns rows
 // [128 r, 128 r + 128) and columns [128 c, 128 c + 128) of every product
-// (a 128 x 128 accumulator in TMEM). Operands live in global memory (L2
-// resident: a head's matrices total about 1.5 MB) as row-major copies of the
-// left factors and of the TRANSPOSED right factors; TMA streams 32-column
-// K-chunks of both into a six-stage shared-memory ring. Each epilogue writes
-// the next product's operands (row-major and/or transposed, with the 7I /
-// 15I / 13I terms applied exactly as the m <= 128 kernel does), then the
-// cluster synchronises before the next product reads them.
+// (128 x 128 accumulators in TMEM; its block of Z stays in TMEM across the
+// updates, and level 2 accumulates onto 13 Z - 15 Z X written there by the
+// level-1 epilogue). Product operands live in global memory (L2 resident: a
+// head's matrices total about 1.5 MB) as row-major copies of the left factors
+// and TRANSPOSED copies of the right factors; TMA streams 32-column K-chunks
+// into a two-stage shared-memory ring. Streaming these operands is what a
+// product's K-loop waits on, so a left factor's K-block that this CTA
+// computed itself is read from TMEM instead (every left factor but A_S), and
+// level 1's two products share one stream of their right factor. Each
+// epilogue writes the next level's operands, then the cluster synchronises
+// before they are read.
 //
 // Warps 0-3: epilogue / softmax (thread = row, TMEM lane = row); warp 4:
 // TMA producer; warp 5: TMEM owner and tcgen05 issuer. Every mbarrier wait
@@ -24,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "nys_internal.h"
 #include "nys_sm100.h"
@@ -34,10 +46,11 @@ namespace {
 
 using namespace sm100;
 
-enum MapIdx { MAP_A = 0, MAP_Z0 = 1, MAP_Z1 = 2, MAP_ZT = 3, MAP_TA = 4, MAP_TB = 5, MAP_GT = 6 };
+enum MapIdx { MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_T1 = 4, MAP_T2 = 5, MAP_GT = 6 };
 
 struct BigPinvMaps {
-  CUtensorMap m[7];  // fp32 [B*H][rows][m]: A_S, Z (two), Z^T, two transposed temporaries, G^T
+  CUtensorMap m[7];   // fp32 [B*H][rows][m]: A_S, Z, X, Z X, two transposed right factors, G^T
+  CUtensorMap st[7];  // the same matrices with 32 x 32 boxes, for the epilogues' stores
 };
 
 struct BigPinvParams {
@@ -47,11 +60,11 @@ struct BigPinvParams {
   const float* gml;    // [B*H][splits][m][2]
   float* g;            // [B*H][m][d]
   float* a_s;          // [B*H][m][m]
-  float* z0;           // [B*H][m][m]  Z (even steps)
-  float* z1;           // [B*H][m][m]  Z (odd steps) / X
-  float* zt;           // [B*H][m][m]  Z^T
-  float* ta;           // [B*H][m][m]  transposed right factors
-  float* tb;           // [B*H][m][m]
+  float* z;            // [B*H][m][m]  Z (row-major; the last update's Z on exit)
+  float* xr;           // [B*H][m][m]  X = A_S Z (row-major)
+  float* zx;           // [B*H][m][m]  Z X (row-major)
+  float* t1;           // [B*H][m][m]  transposed right factors: Z^T, X^T and (7X - X^2)^T,
+  float* t2;           // [B*H][m][m]  alternating between the two buffers
   float* gt;           // [B*H][d][m]  G^T
   float* w;            // [B*H][m][d]
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
@@ -62,9 +75,19 @@ struct BigPinvParams {
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 192;
-constexpr int kStages = 6;
-constexpr uint32_t kStageBytes = 32768;  // A chunk 16 KB + B chunk <= 16 KB
-constexpr uint32_t kTmemCols = 128;
+// The operand ring: two stages of two K-chunks each. A stage holds, per
+// chunk, a 128 x 32 fp32 box of up to two left factors and one <= 128 x 32
+// box of the right factor, behind one mbarrier: an mbarrier round trip costs
+// about as much as streaming 16 KB, so stages are made large, not many.
+constexpr int kStages = 2;
+constexpr uint32_t kStageBytes = 98304;
+constexpr uint32_t kOffA2 = 32768, kOffB = 65536;  // A1 chunks at 0 and 16 KB
+constexpr uint32_t kTmemCols = 512;
+// TMEM column bases of the four 128-column accumulators
+constexpr uint32_t kR0 = 0;    // scores / A_S, then this CTA's block of Z
+constexpr uint32_t kR1 = 128;  // X (level 0), W
+constexpr uint32_t kR2 = 256;  // X X
+constexpr uint32_t kR3 = 384;  // Z X
 constexpr int kCsPitch = 129;  // floats per row of the column-sum staging block
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -376,16 +399,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block)
-  // and Z_0^T = alpha A_S (row store)
+  // and Z_0^T = alpha A_S (row store, the first update's right factor)
   if (worker && !*abort_flag) {
     const float n1 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     const float ninf = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
     const float alpha = 1.f / (n1 * ninf);
-    float* z0 = p.z0 + bh * mm;
-    float* zt = p.zt + bh * mm;
+    float* z = p.z + bh * mm;
+    float* zt = p.t1 + bh * mm;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
-      tmem_ld32(tmem + lo + j0, v);
+      tmem_ld32(tmem + lo + kR0 + j0, v);
       tmem_ld_wait();
       if (rv) {
 #pragma unroll
@@ -399,10 +422,31 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int gj = 128 * c + j0 + e;
-          if (gj < m) z0[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
+          if (gj < m) z[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
         }
       }
     }
+  }
+  cluster_sync_all();
+  // this CTA's block of Z_0 into TMEM (zero beyond m), where it stays across
+  // the updates
+  if (worker && !*abort_flag) {
+    const float* zrow = p.z + bh * mm + (size_t)(rv ? gi : 0) * m;
+    for (int j0 = 0; j0 < 128; j0 += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const int gj = 128 * c + j0 + e;
+        const float4 q = (rv && gj < m) ? *reinterpret_cast<const float4*>(zrow + gj)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[e] = __float_as_uint(q.x);
+        v[e + 1] = __float_as_uint(q.y);
+        v[e + 2] = __float_as_uint(q.z);
+        v[e + 3] = __float_as_uint(q.w);
+      }
+      tmem_st32(tmem + lo + kR0 + j0, v);
+    }
+    tmem_st_wait();
   }
   tc_fence_before_sync();
   fence_proxy_async_all();
@@ -410,55 +454,72 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   fence_proxy_async_all();
   tc_fence_after_sync();
 
-  // ---- 4) the products: 4 per step, then W = Z G
-  const int nprod = 4 * p.iters + 1;
+  // ---- 4) the products: three levels per update, then W = Z G. Per
+  // update, the transposed right factors alternate between t1 and t2: Z^T
+  // is in `tc` (t1 on even updates), X^T goes to the other one (`to`),
+  // (7X - X^2)^T back to `tc`, and Z'^T to `to`, the next update's `tc`.
+  const int nprod = 3 * p.iters + 1;
   const int hw = d >> 1;
   uint32_t kg_prod = 0, kg_mma = 0;   // ring positions of the producer / issuer
   uint32_t n_full[kStages] = {};      // loads issued per stage (producer)
+  int it = 0, lv = 0;                 // update and level of product pi
   for (int pi = 0; pi < nprod; ++pi) {
-    const int it = pi >> 2, st = pi & 3;
     const bool is_w = pi == nprod - 1;
-    const int zc = it & 1;  // Z of this step in z0 (even) / z1 (odd); X and Z' in the other
-    int amap, bmap, b_row0, n_cols;
-    if (is_w) {
-      amap = (p.iters & 1) ? MAP_Z1 : MAP_Z0;
-      bmap = MAP_GT;
-      b_row0 = c * hw;
-      n_cols = hw;
-    } else {
-      amap = st == 0 ? MAP_A : (st == 3 ? (zc ? MAP_Z1 : MAP_Z0) : (zc ? MAP_Z0 : MAP_Z1));
-      bmap = st == 0 ? MAP_ZT : (st == 2 ? MAP_TB : MAP_TA);
-      b_row0 = 128 * c;
-      n_cols = 128;
-    }
+    const int tc = (it & 1) ? MAP_T2 : MAP_T1, to = (it & 1) ? MAP_T1 : MAP_T2;
+    // Left factors: level 0 streams A_S; levels 1, 2 and W read the K-block
+    // of the left factor that this CTA computed itself (columns [128 c,
+    // 128 c + 128): X in R1 and Z in R0 for level 1, Z X in R3 for level 2,
+    // Z in R0 for W) from TMEM, and stream only the neighbour's half. Level
+    // 1 runs its two products over one stream of the shared right factor.
+    const int amap1 = is_w ? MAP_Z : (lv == 0 ? MAP_A : (lv == 1 ? MAP_XR : MAP_ZX));
+    const int bmap = is_w ? MAP_GT : (lv == 1 ? to : tc);
+    const bool two = !is_w && lv == 1;
+    const bool own_tmem = is_w || lv != 0;
+    const int b_row0 = is_w ? c * hw : 128 * c;
+    const int n_cols = is_w ? hw : 128;
     const uint32_t b_bytes = (uint32_t)n_cols * 128u;
+    // stage j of a product holds K-chunks 2j and 2j + 1 (a chunk past m is
+    // read as zeros and adds nothing); both lie in K-block j / 2, so a stage
+    // either streams its left factor or takes it from TMEM
+    const int nst = (p.kc + 1) >> 1;
     if (warp == 4) {
       if (lane == 0 && !*abort_flag) {
-        for (int k = 0; k < p.kc; ++k, ++kg_prod) {
-          const int s = (int)(kg_prod % kStages);
+        for (int j = 0; j < nst; ++j, ++kg_prod) {
+          const int st = (int)(kg_prod % kStages);
           if (kg_prod >= (uint32_t)kStages &&
-              !mbar_wait(&empty[s], ((kg_prod / kStages) - 1) & 1, abort_flag, kWaitNs)) {
+              !mbar_wait(&empty[st], ((kg_prod / kStages) - 1) & 1, abort_flag, kWaitNs)) {
             if (!*abort_flag) {
               *abort_flag = 1;
               atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
             }
             break;
           }
-          uint8_t* sa = sm + s * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], 16384u + b_bytes);
-          tma_load_3d(sa, &maps.m[amap], &full[s], 32 * k, 128 * r, bh);
-          tma_load_3d(sa + 16384, &maps.m[bmap], &full[s], 32 * k, b_row0, bh);
-          ++n_full[s];
+          const bool from_tmem = own_tmem && (j >> 1) == c;
+          uint8_t* sa = sm + st * kStageBytes;
+          mbar_arrive_expect_tx(&full[st], 2u * (b_bytes + (from_tmem ? 0u : (two ? 32768u : 16384u))));
+          ++n_full[st];
+          for (int q = 0; q < 2; ++q) {
+            const int kx = 32 * (2 * j + q);
+            if (!from_tmem) {
+              tma_load_3d(sa + q * 16384, &maps.m[amap1], &full[st], kx, 128 * r, bh);
+              if (two) tma_load_3d(sa + kOffA2 + q * 16384, &maps.m[MAP_Z], &full[st], kx, 128 * r, bh);
+            }
+            tma_load_3d(sa + kOffB + q * 16384, &maps.m[bmap], &full[st], kx, b_row0, bh);
+          }
         }
       }
       __syncwarp();
     } else if (warp == 5) {
       if (lane == 0 && !*abort_flag) {
         const uint32_t id = idesc_tf32(128, n_cols);
+        // accumulators: X (level 0) and W in R1; X X in R2 and Z X in R3
+        // (level 1); level 2 accumulates onto 13 Z - 15 Z X in R0
+        const uint32_t d1 = (is_w || lv == 0) ? kR1 : (lv == 1 ? kR2 : kR0);
+        const uint32_t t1 = is_w ? kR0 : (lv == 1 ? kR1 : kR3);  // own K-block of the left factor
         bool ok = true;
-        for (int k = 0; k < p.kc; ++k, ++kg_mma) {
-          const int s = (int)(kg_mma % kStages);
-          if (!mbar_wait(&full[s], (kg_mma / kStages) & 1, abort_flag, kWaitNs)) {
+        for (int j = 0; j < nst; ++j, ++kg_mma) {
+          const int st = (int)(kg_mma % kStages);
+          if (!mbar_wait(&full[st], (kg_mma / kStages) & 1, abort_flag, kWaitNs)) {
             if (!*abort_flag) {
               *abort_flag = 1;
               atomicExch(p.status, (int)NYS_ERR_TIMEOUT);
@@ -467,12 +528,31 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a0 = smem_desc(smem_u32(sm + s * kStageBytes), 16, 1024, SW_128B);
-          const uint64_t b0 = smem_desc(smem_u32(sm + s * kStageBytes + 16384), 16, 1024, SW_128B);
+          const bool from_tmem = own_tmem && (j >> 1) == c;
+          const uint32_t sb = smem_u32(sm + st * kStageBytes);
+          // one accumulator at a time: switching accumulators between
+          // consecutive MMAs halves their throughput
+          for (int pr = 0; pr < (two ? 2 : 1); ++pr) {
+            const uint32_t dacc = pr ? kR3 : d1;
+            const uint32_t tsrc = pr ? kR0 : t1;
+            const uint32_t aoff = pr ? kOffA2 : 0u;
+            const bool fresh = j == 0 && !(lv == 2 && !is_w);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_tf32(tmem, a0 + kk * 2, b0 + kk * 2, id, (k > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
+            for (int q = 0; q < 2; ++q) {
+              const uint32_t ta = tmem + tsrc + (uint32_t)(((2 * j + q) & 3) * 32);
+              const uint64_t a0 = smem_desc(sb + aoff + q * 16384, 16, 1024, SW_128B);
+              const uint64_t b0 = smem_desc(sb + kOffB + q * 16384, 16, 1024, SW_128B);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (fresh && q == 0 && kk == 0) ? 0u : 1u;
+                if (from_tmem)
+                  mma_tf32_tA(tmem + dacc, ta + kk * 8, b0 + kk * 2, id, acc);
+                else
+                  mma_tf32(tmem + dacc, a0 + kk * 2, b0 + kk * 2, id, acc);
+              }
+            }
+          }
+          mma_commit(&empty[st]);
         }
         if (ok) mma_commit(&done);
       }
@@ -485,7 +565,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         __nv_bfloat16* wt = p.wt + (size_t)bh * p.dpad * p.m64;
         for (int j0 = 0; j0 < hw; j0 += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lo + j0, v);
+          tmem_ld16(tmem + lo + kR1 + j0, v);
           tmem_ld_wait();
           if (rv) {
 #pragma unroll
@@ -503,54 +583,79 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (c == 1 && gi < p.m64)
           for (int j = d; j < p.dpad; ++j) wt[(size_t)j * p.m64 + gi] = __float2bfloat16_rn(0.f);
       } else if (!is_w) {
-        // st 0: X -> other Z buffer (row-major), 7I - X -> ta (transposed)
-        // st 1: 15I - Y -> tb (transposed);  st 2: 13I - Y -> ta (transposed)
-        // st 3: Z' = Y / 4 -> other Z buffer (row-major) and zt (transposed)
+        // level 0: X (R1)            -> xr (row-major), X^T -> to
+        // level 1: Z X (R3)          -> zx (row-major), (7X - X^2)^T -> tc,
+        //          R0 <- 13 Z - 15 Z X
+        // level 2: Z' = R0 / 4 -> R0, z (row-major), Z'^T -> to
         // Both blocks are staged in the (now idle) operand ring as four
         // SWIZZLE_128B boxes of [128 rows x 32 columns] and leave by TMA
         // stores; the store clips what lies beyond m.
-        const int rm_map = (st == 0 || st == 3) ? (zc ? MAP_Z0 : MAP_Z1) : -1;
-        const int tr_map = (st == 0 || st == 2) ? MAP_TA : (st == 1 ? MAP_TB : MAP_ZT);
-        const float diag = st == 0 ? 7.f : (st == 1 ? 15.f : (st == 2 ? 13.f : 0.f));
-        const float sign = st == 3 ? 1.f : -1.f;
-        const float sc = st == 3 ? 0.25f : 1.f;
+        const int rm_map = lv == 0 ? MAP_XR : (lv == 1 ? MAP_ZX : MAP_Z);
+        const int tr_map = lv == 1 ? tc : to;
         uint8_t* rm_stage = sm;          // box b: block columns [32 b, 32 b + 32), row = tid
         uint8_t* tr_stage = sm + 65536;  // box b = warp: block rows [32 b, ..) as columns
+        uint8_t* tbox = tr_stage + warp * 16384;
+        const bool store = ok_epi && !*abort_flag;
         for (int j0 = 0; ok_epi && j0 < 128; j0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lo + j0, v);
-          tmem_ld_wait();
-          float x[32];
+          for (int h = 0; h < 32; h += 16) {
+            const int jc = j0 + h;
+            float rmv[16], trv[16];
+            if (lv == 0) {
+              uint32_t v[16];
+              tmem_ld16(tmem + lo + kR1 + jc, v);
+              tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = sc * __uint_as_float(v[e]);
-          if (rm_map >= 0) {
+              for (int e = 0; e < 16; ++e) rmv[e] = trv[e] = __uint_as_float(v[e]);
+            } else if (lv == 1) {
+              uint32_t vx[16], vx2[16], vzx[16], vz[16];
+              tmem_ld16(tmem + lo + kR1 + jc, vx);
+              tmem_ld16(tmem + lo + kR2 + jc, vx2);
+              tmem_ld16(tmem + lo + kR3 + jc, vzx);
+              tmem_ld16(tmem + lo + kR0 + jc, vz);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float zx = __uint_as_float(vzx[e]);
+                rmv[e] = zx;
+                trv[e] = fmaf(7.f, __uint_as_float(vx[e]), -__uint_as_float(vx2[e]));
+                vz[e] = __float_as_uint(fmaf(13.f, __uint_as_float(vz[e]), -15.f * zx));
+              }
+              tmem_st16(tmem + lo + kR0 + jc, vz);
+            } else {
+              uint32_t v[16];
+              tmem_ld16(tmem + lo + kR0 + jc, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                rmv[e] = trv[e] = 0.25f * __uint_as_float(v[e]);
+                v[e] = __float_as_uint(rmv[e]);
+              }
+              tmem_st16(tmem + lo + kR0 + jc, v);
+            }
             uint8_t* box = rm_stage + (j0 >> 5) * 16384;
+            const int q0 = h >> 2;  // first 16-byte unit of the box row
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              *reinterpret_cast<float4*>(box + sw128_offset(tid, q4 * 16)) =
-                  make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(box + sw128_offset(tid, (q0 + q4) * 16)) =
+                  make_float4(rmv[4 * q4], rmv[4 * q4 + 1], rmv[4 * q4 + 2], rmv[4 * q4 + 3]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              *reinterpret_cast<float*>(tbox + sw128_offset(jc + e, lane * 4)) = trv[e];
           }
-          uint8_t* tbox = tr_stage + warp * 16384;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int gj = 128 * c + j0 + e;
-            *reinterpret_cast<float*>(tbox + sw128_offset(j0 + e, lane * 4)) =
-                fmaf(sign, x[e], gj == gi ? diag : 0.f);
+          // this warp's 32 x 32 pieces of both blocks leave at once, while
+          // the next columns are staged
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && store) {
+            tma_store_3d(&maps.st[rm_map], rm_stage + (j0 >> 5) * 16384 + warp * 4096, 128 * c + j0,
+                         128 * r + 32 * warp, bh);
+            tma_store_3d(&maps.st[tr_map], tbox + (j0 >> 5) * 4096, 128 * r + 32 * warp, 128 * c + j0, bh);
+            bulk_commit();
           }
         }
-        fence_async_smem();
-        // the four epilogue warps, all of them whatever their wait gave (a
-        // wait that ran out has set the abort flag: no store then)
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (tid == 0 && !*abort_flag) {
-          if (rm_map >= 0)
-            for (int b = 0; b < 4; ++b)
-              tma_store_3d(&maps.m[rm_map], rm_stage + b * 16384, 128 * c + 32 * b, 128 * r, bh);
-          for (int b = 0; b < 4; ++b)
-            tma_store_3d(&maps.m[tr_map], tr_stage + b * 16384, 128 * r + 32 * b, 128 * c, bh);
-          bulk_commit();
-          bulk_wait0();  // written before the cluster barrier publishes them
-        }
+        if (lv != 0) tmem_st_wait();
+        if (lane == 0 && store) bulk_wait0();  // written before the cluster barrier publishes them
+        __syncwarp();
       }
     }
     tc_fence_before_sync();
@@ -558,6 +663,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     fence_proxy_async_all();
     tc_fence_after_sync();
+    if (++lv == 3) {
+      lv = 0;
+      ++it;
+    }
   }
 
   // ---- teardown: no copy or MMA of this CTA may still be in flight
@@ -596,14 +705,13 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.gml = gml;
   p.g = g;
   p.a_s = a_s;
-  // scratch holds, per head block of the whole batch: the second Z, zt,
-  // ta, tb, gt. Z alternates between z0 (even updates) and z1; the buffers
-  // are assigned so that the last Z lands in `z` (stage export).
-  p.z0 = (s.iters & 1) ? scratch : z;
-  p.z1 = (s.iters & 1) ? z : scratch;
-  p.zt = scratch + BH * mm;
-  p.ta = scratch + 2 * BH * mm;
-  p.tb = scratch + 3 * BH * mm;
+  // scratch holds, per head block of the whole batch: X, Z X, the two
+  // transposed right factors and G^T. Z itself lives in `z` (stage export).
+  p.z = z;
+  p.xr = scratch;
+  p.zx = scratch + BH * mm;
+  p.t1 = scratch + 2 * BH * mm;
+  p.t2 = scratch + 3 * BH * mm;
   p.gt = scratch + 4 * BH * mm;
   p.w = w;
   p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
@@ -618,13 +726,17 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.scale = 1.0f / sqrtf((float)s.d);
 
   BigPinvMaps maps;
-  const float* bufs[6] = {p.a_s, p.z0, p.z1, p.zt, p.ta, p.tb};
+  memset(&maps, 0, sizeof(maps));
+  const float* bufs[6] = {p.a_s, p.z, p.xr, p.zx, p.t1, p.t2};
   for (int i = 0; i < 6; ++i) {
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
     const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)mm * 4};
     const uint32_t box[3] = {32, 128, 1};
+    const uint32_t sbox[3] = {32, 32, 1};
     if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
-                         box, CU_TENSOR_MAP_SWIZZLE_128B))
+                         box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&maps.st[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
+                         sbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return tensor_map_error(__FILE__, __LINE__);
   }
   {
