@@ -4,6 +4,7 @@
 //   A_S = softmax(Q~ K~^T s)    scores in 3xTF32 (hi*hi + hi*lo + lo*hi)
 //   Z_0 = A_S^T / (||A_S||_1 ||A_S||_inf)
 //   iters x:  Z <- 1/4 Z (13I - 15X + 7X^2 - X^3),  X = A_S Z
+//                                                  tcgen05 kind::f16 (fp16 operands)
 //   W   = Z G                                      tcgen05 kind::tf32
 // Each update is evaluated in three dependent levels of products instead of
 // the four of the nested (Horner) form, since its cost is the latency of the
@@ -18,21 +19,30 @@
 // [128 r, 128 r + 128) and columns [128 c, 128 c + 128) of every product
 // (128 x 128 accumulators in TMEM; its block of Z stays in TMEM across the
 // updates, and level 2 accumulates onto 13 Z - 15 Z X written there by the
-// level-1 epilogue). Product operands live in global memory (L2 resident: a
-// head's matrices total about 1.5 MB) as row-major copies of the left factors
-// and TRANSPOSED copies of the right factors; TMA streams 32-column K-chunks
-// into a two-stage shared-memory ring. Streaming these operands is what a
-// product's K-loop waits on, so a left factor's K-block that this CTA
-// computed itself is read from TMEM instead (every left factor but A_S), and
-// level 1's two products share one stream of their right factor. Each
-// epilogue writes the next level's operands, then the cluster synchronises
-// before they are read.
+// level-1 epilogue). Product operands live in global memory (L2 resident) as
+// fp16 row-major copies of the left factors and fp16 TRANSPOSED copies of the
+// right factors; TMA streams 64-column K-chunks into a two-stage shared-memory
+// ring, and level 1's two products share one stream of their right factor.
+// Each epilogue writes the next level's operands, then the cluster
+// synchronises before they are read.
+// Why fp16 operands: the chain's time goes to moving operands (an SM writes
+// to L2 at about 32 bytes per clock, and a tf32 product reads shared memory
+// as fast as TMA fills it), and fp16 halves those bytes. Its 11-bit
+// significand (rounded to nearest) is finer than tf32's truncated one, and
+// its range holds the iterates: Z_k = A_S^T q(A_S A_S^T) shares A_S's
+// singular vectors, and with x = sigma z per singular value sigma the update
+// maps x in [0, 1] into [0, 1] and grows it at most 13/4-fold, so
+// z_k <= min(1/sigma, (13/4)^k alpha sigma) <= (13/4)^(k/2) (alpha <= 1):
+// ||Z||_2 < 112 after at most 8 updates, far below fp16's 65504. Entries
+// below fp16's normal range carry absolute errors near 6e-8. Accumulation stays fp32 (TMEM), Z itself stays fp32 in
+// TMEM across the updates, and W = Z G runs in tf32 from the fp32 Z.
 //
 // Warps 0-3: epilogue / softmax (thread = row, TMEM lane = row); warp 4:
 // TMA producer; warp 5: TMEM owner and tcgen05 issuer. Every mbarrier wait
 // is bounded; after a timeout the CTA skips its remaining work but still
 // takes part in every cluster barrier, so its peers never wait on it.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <cstring>
@@ -46,11 +56,14 @@ namespace {
 
 using namespace sm100;
 
-enum MapIdx { MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_T1 = 4, MAP_T2 = 5, MAP_GT = 6 };
+// fp16 operand matrices [B*H][m][mp] (A_S, Z, X, Z X, two transposed right
+// factors), then the fp32 maps of W = Z G: G^T [B*H][d][m] and Z [B*H][m][m]
+enum MapIdx { MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_T1 = 4, MAP_T2 = 5, MAP_GT = 6, MAP_Z32 = 7 };
 
 struct BigPinvMaps {
-  CUtensorMap m[7];   // fp32 [B*H][rows][m]: A_S, Z, X, Z X, two transposed right factors, G^T
-  CUtensorMap st[7];  // the same matrices with 32 x 32 boxes, for the epilogues' stores
+  CUtensorMap m[8];   // loads: fp16 boxes of 128 rows x 64 columns; fp32 boxes of <= 128 rows x 32
+  CUtensorMap st[6];  // stores of the fp16 matrices: row-major 32 x 64 boxes (SWIZZLE_128B),
+                      // transposed 32 x 32 boxes (SWIZZLE_64B)
 };
 
 struct BigPinvParams {
@@ -59,17 +72,19 @@ struct BigPinvParams {
   const float* gpart;  // [B*H][splits][m][d]
   const float* gml;    // [B*H][splits][m][2]
   float* g;            // [B*H][m][d]
-  float* a_s;          // [B*H][m][m]
-  float* z;            // [B*H][m][m]  Z (row-major; the last update's Z on exit)
-  float* xr;           // [B*H][m][m]  X = A_S Z (row-major)
-  float* zx;           // [B*H][m][m]  Z X (row-major)
-  float* t1;           // [B*H][m][m]  transposed right factors: Z^T, X^T and (7X - X^2)^T,
-  float* t2;           // [B*H][m][m]  alternating between the two buffers
-  float* gt;           // [B*H][d][m]  G^T
+  float* a_s;          // [B*H][m][m]   A_S (fp32)
+  float* z;            // [B*H][m][m]   Z_0, then the last update's Z (fp32)
+  __half* a16;         // [B*H][m][mp]  A_S                       (fp16 operands,
+  __half* z16;         // [B*H][m][mp]  Z (row-major)              row pitch mp)
+  __half* xr16;        // [B*H][m][mp]  X = A_S Z (row-major)
+  __half* zx16;        // [B*H][m][mp]  Z X (row-major)
+  __half* t1_16;       // [B*H][m][mp]  transposed right factors: Z^T, X^T and (7X - X^2)^T,
+  __half* t2_16;       // [B*H][m][mp]  alternating between the two buffers
+  float* gt;           // [B*H][d][m]   G^T
   float* w;            // [B*H][m][d]
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
   int* status;
-  int m, d, dpad, m64, splits, iters, kc;  // kc: 32-column K-chunks of an m x m matrix
+  int m, mp, d, dpad, m64, splits, iters;
   float scale;
 };
 
@@ -339,6 +354,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const float sum = c == 0 ? own + peer : peer + own;  // same order in both CTAs
     const float inv = rv ? 1.f / sum : 0.f;
     float* arow = p.a_s + bh * mm + (size_t)(rv ? gi : 0) * m;
+    __half* arow16 = p.a16 + ((size_t)bh * m + (rv ? gi : 0)) * p.mp;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lo + j0, v);
@@ -355,10 +371,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int gj = 128 * c + j0 + e;
-          if (gj < m)
+          if (gj < m) {
             *reinterpret_cast<float4*>(arow + gj) =
                 make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            const __half2 h0 = __floats2half2_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            const __half2 h1 = __floats2half2_rn(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            *reinterpret_cast<uint2*>(arow16 + gj) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+          }
         }
       }
     }
@@ -398,14 +419,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block)
-  // and Z_0^T = alpha A_S (row store, the first update's right factor)
+  // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block,
+  // fp32 and fp16) and Z_0^T = alpha A_S (fp16 row store, the first update's
+  // right factor)
   if (worker && !*abort_flag) {
     const float n1 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     const float ninf = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
     const float alpha = 1.f / (n1 * ninf);
     float* z = p.z + bh * mm;
-    float* zt = p.t1 + bh * mm;
+    __half* z16 = p.z16 + (size_t)bh * m * p.mp;
+    __half* zt16 = p.t1_16 + (size_t)bh * m * p.mp;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lo + kR0 + j0, v);
@@ -414,15 +437,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int gj = 128 * c + j0 + e;
-          if (gj < m)
-            *reinterpret_cast<float4*>(zt + (size_t)gi * m + gj) =
-                make_float4(alpha * __uint_as_float(v[e]), alpha * __uint_as_float(v[e + 1]),
-                            alpha * __uint_as_float(v[e + 2]), alpha * __uint_as_float(v[e + 3]));
+          if (gj < m) {
+            const __half2 h0 = __floats2half2_rn(alpha * __uint_as_float(v[e]), alpha * __uint_as_float(v[e + 1]));
+            const __half2 h1 = __floats2half2_rn(alpha * __uint_as_float(v[e + 2]), alpha * __uint_as_float(v[e + 3]));
+            *reinterpret_cast<uint2*>(zt16 + (size_t)gi * p.mp + gj) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+          }
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int gj = 128 * c + j0 + e;
-          if (gj < m) z[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
+          if (gj < m) {
+            const float zv = alpha * __uint_as_float(v[e]);
+            z[(size_t)gj * m + gi] = zv;
+            z16[(size_t)gj * p.mp + gi] = __float2half_rn(zv);
+          }
         }
       }
     }
@@ -466,22 +495,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   for (int pi = 0; pi < nprod; ++pi) {
     const bool is_w = pi == nprod - 1;
     const int tc = (it & 1) ? MAP_T2 : MAP_T1, to = (it & 1) ? MAP_T1 : MAP_T2;
-    // Left factors: level 0 streams A_S; levels 1, 2 and W read the K-block
-    // of the left factor that this CTA computed itself (columns [128 c,
-    // 128 c + 128): X in R1 and Z in R0 for level 1, Z X in R3 for level 2,
-    // Z in R0 for W) from TMEM, and stream only the neighbour's half. Level
-    // 1 runs its two products over one stream of the shared right factor.
-    const int amap1 = is_w ? MAP_Z : (lv == 0 ? MAP_A : (lv == 1 ? MAP_XR : MAP_ZX));
+    // Update products (fp16): K-chunks of 64 columns, every operand streamed;
+    // level 1 runs its two products over one stream of the shared right
+    // factor. W (tf32): K-chunks of 32 columns; its left factor Z is read
+    // from TMEM (R0) for the K-block this CTA holds and streamed for the
+    // other.
+    const int amap1 = is_w ? MAP_Z32 : (lv == 0 ? MAP_A : (lv == 1 ? MAP_XR : MAP_ZX));
     const int bmap = is_w ? MAP_GT : (lv == 1 ? to : tc);
     const bool two = !is_w && lv == 1;
-    const bool own_tmem = is_w || lv != 0;
+    const int kw = is_w ? 32 : 64;  // K-chunk width (elements)
     const int b_row0 = is_w ? c * hw : 128 * c;
     const int n_cols = is_w ? hw : 128;
     const uint32_t b_bytes = (uint32_t)n_cols * 128u;
     // stage j of a product holds K-chunks 2j and 2j + 1 (a chunk past m is
-    // read as zeros and adds nothing); both lie in K-block j / 2, so a stage
-    // either streams its left factor or takes it from TMEM
-    const int nst = (p.kc + 1) >> 1;
+    // read as zeros and adds nothing)
+    const int nst = ((m + kw - 1) / kw + 1) >> 1;
     if (warp == 4) {
       if (lane == 0 && !*abort_flag) {
         for (int j = 0; j < nst; ++j, ++kg_prod) {
@@ -494,12 +522,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             }
             break;
           }
-          const bool from_tmem = own_tmem && (j >> 1) == c;
+          // W: the 32-column chunks 2j, 2j + 1 lie in K-block (2j) / 4
+          const bool from_tmem = is_w && ((2 * j) >> 2) == c;
           uint8_t* sa = sm + st * kStageBytes;
           mbar_arrive_expect_tx(&full[st], 2u * (b_bytes + (from_tmem ? 0u : (two ? 32768u : 16384u))));
           ++n_full[st];
           for (int q = 0; q < 2; ++q) {
-            const int kx = 32 * (2 * j + q);
+            const int kx = kw * (2 * j + q);
             if (!from_tmem) {
               tma_load_3d(sa + q * 16384, &maps.m[amap1], &full[st], kx, 128 * r, bh);
               if (two) tma_load_3d(sa + kOffA2 + q * 16384, &maps.m[MAP_Z], &full[st], kx, 128 * r, bh);
@@ -511,11 +540,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == 5) {
       if (lane == 0 && !*abort_flag) {
-        const uint32_t id = idesc_tf32(128, n_cols);
+        const uint32_t id = is_w ? idesc_tf32(128, n_cols) : idesc_f16(128, n_cols);
         // accumulators: X (level 0) and W in R1; X X in R2 and Z X in R3
         // (level 1); level 2 accumulates onto 13 Z - 15 Z X in R0
         const uint32_t d1 = (is_w || lv == 0) ? kR1 : (lv == 1 ? kR2 : kR0);
-        const uint32_t t1 = is_w ? kR0 : (lv == 1 ? kR1 : kR3);  // own K-block of the left factor
         bool ok = true;
         for (int j = 0; j < nst; ++j, ++kg_mma) {
           const int st = (int)(kg_mma % kStages);
@@ -528,24 +556,25 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const bool from_tmem = own_tmem && (j >> 1) == c;
+          const bool from_tmem = is_w && ((2 * j) >> 2) == c;
           const uint32_t sb = smem_u32(sm + st * kStageBytes);
           // one accumulator at a time: switching accumulators between
           // consecutive MMAs halves their throughput
           for (int pr = 0; pr < (two ? 2 : 1); ++pr) {
             const uint32_t dacc = pr ? kR3 : d1;
-            const uint32_t tsrc = pr ? kR0 : t1;
             const uint32_t aoff = pr ? kOffA2 : 0u;
             const bool fresh = j == 0 && !(lv == 2 && !is_w);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-              const uint32_t ta = tmem + tsrc + (uint32_t)(((2 * j + q) & 3) * 32);
+              const uint32_t ta = tmem + kR0 + (uint32_t)(((2 * j + q) & 3) * 32);
               const uint64_t a0 = smem_desc(sb + aoff + q * 16384, 16, 1024, SW_128B);
               const uint64_t b0 = smem_desc(sb + kOffB + q * 16384, 16, 1024, SW_128B);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (fresh && q == 0 && kk == 0) ? 0u : 1u;
-                if (from_tmem)
+                if (!is_w)
+                  mma_bf16(tmem + dacc, a0 + kk * 2, b0 + kk * 2, id, acc);  // kind::f16, fp16 by idesc
+                else if (from_tmem)
                   mma_tf32_tA(tmem + dacc, ta + kk * 8, b0 + kk * 2, id, acc);
                 else
                   mma_tf32(tmem + dacc, a0 + kk * 2, b0 + kk * 2, id, acc);
@@ -586,17 +615,22 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         // level 0: X (R1)            -> xr (row-major), X^T -> to
         // level 1: Z X (R3)          -> zx (row-major), (7X - X^2)^T -> tc,
         //          R0 <- 13 Z - 15 Z X
-        // level 2: Z' = R0 / 4 -> R0, z (row-major), Z'^T -> to
-        // Both blocks are staged in the (now idle) operand ring as four
-        // SWIZZLE_128B boxes of [128 rows x 32 columns] and leave by TMA
-        // stores; the store clips what lies beyond m.
+        // level 2: Z' = R0 / 4 -> R0, z (row-major), Z'^T -> to; after the
+        //          last update also the fp32 Z (for W and the stage export)
+        // Both blocks are rounded to fp16 and staged in the (now idle)
+        // operand ring: row-major as two SWIZZLE_128B boxes of [128 rows x
+        // 64 columns], transposed as [32 block columns x 32 rows] SWIZZLE_64B
+        // tiles per warp. Each warp stores its pieces as soon as they are
+        // staged; the stores clip what lies beyond m.
         const int rm_map = lv == 0 ? MAP_XR : (lv == 1 ? MAP_ZX : MAP_Z);
         const int tr_map = lv == 1 ? tc : to;
-        uint8_t* rm_stage = sm;          // box b: block columns [32 b, 32 b + 32), row = tid
-        uint8_t* tr_stage = sm + 65536;  // box b = warp: block rows [32 b, ..) as columns
-        uint8_t* tbox = tr_stage + warp * 16384;
+        const bool last_z = lv == 2 && it == p.iters - 1;
+        uint8_t* rm_stage = sm;                         // box b: block columns [64 b, 64 b + 64)
+        uint8_t* tr_stage = sm + 32768 + warp * 8192;  // tile j0 / 32 of this warp's rows
+        float* z32 = p.z + ((size_t)bh * m + (rv ? gi : 0)) * m + 128 * c;
         const bool store = ok_epi && !*abort_flag;
         for (int j0 = 0; ok_epi && j0 < 128; j0 += 32) {
+          uint8_t* tbox = tr_stage + (j0 >> 5) * 2048;
           for (int h = 0; h < 32; h += 16) {
             const int jc = j0 + h;
             float rmv[16], trv[16];
@@ -631,25 +665,36 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 v[e] = __float_as_uint(rmv[e]);
               }
               tmem_st16(tmem + lo + kR0 + jc, v);
-            }
-            uint8_t* box = rm_stage + (j0 >> 5) * 16384;
-            const int q0 = h >> 2;  // first 16-byte unit of the box row
+              if (last_z && rv) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              *reinterpret_cast<float4*>(box + sw128_offset(tid, (q0 + q4) * 16)) =
-                  make_float4(rmv[4 * q4], rmv[4 * q4 + 1], rmv[4 * q4 + 2], rmv[4 * q4 + 3]);
+                for (int e = 0; e < 16; e += 4)
+                  if (128 * c + jc + e < m)
+                    *reinterpret_cast<float4*>(z32 + jc + e) = make_float4(rmv[e], rmv[e + 1], rmv[e + 2], rmv[e + 3]);
+              }
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const __half2 h2 = __floats2half2_rn(rmv[2 * e], rmv[2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint8_t* box = rm_stage + (jc >> 6) * 16384;
+            const uint32_t byte0 = (uint32_t)(jc & 63) * 2u;
+            *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              *reinterpret_cast<float*>(tbox + sw128_offset(jc + e, lane * 4)) = trv[e];
+              *reinterpret_cast<__half*>(tbox + sw64_offset(h + e, lane * 2)) = __float2half_rn(trv[e]);
           }
-          // this warp's 32 x 32 pieces of both blocks leave at once, while
-          // the next columns are staged
+          // this warp's transposed tile, and every 64 columns its rows of the
+          // row-major box, leave while the next columns are staged
           fence_async_smem();
           __syncwarp();
           if (lane == 0 && store) {
-            tma_store_3d(&maps.st[rm_map], rm_stage + (j0 >> 5) * 16384 + warp * 4096, 128 * c + j0,
-                         128 * r + 32 * warp, bh);
-            tma_store_3d(&maps.st[tr_map], tbox + (j0 >> 5) * 4096, 128 * r + 32 * warp, 128 * c + j0, bh);
+            tma_store_3d(&maps.st[tr_map], tbox, 128 * r + 32 * warp, 128 * c + j0, bh);
+            if ((j0 & 63) == 32)
+              tma_store_3d(&maps.st[rm_map], rm_stage + (j0 >> 6) * 16384 + warp * 4096, 128 * c + (j0 & ~63),
+                           128 * r + 32 * warp, bh);
             bulk_commit();
           }
         }
@@ -705,38 +750,46 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.gml = gml;
   p.g = g;
   p.a_s = a_s;
-  // scratch holds, per head block of the whole batch: X, Z X, the two
-  // transposed right factors and G^T. Z itself lives in `z` (stage export).
+  // scratch holds, for the whole batch, the six fp16 operand matrices
+  // [B*H][m][mp] (A_S, Z, X, Z X and the two transposed right factors; mp =
+  // m rounded up to 8, so that every row starts on a 16-byte boundary) in
+  // its first 4 m^2 floats, then G^T. Z (fp32) lives in `z` (stage export).
+  const int mp = (s.m + 7) & ~7;
+  const size_t hm = BH * (size_t)s.m * mp;  // halves per fp16 matrix
+  __half* h16 = reinterpret_cast<__half*>(scratch);
   p.z = z;
-  p.xr = scratch;
-  p.zx = scratch + BH * mm;
-  p.t1 = scratch + 2 * BH * mm;
-  p.t2 = scratch + 3 * BH * mm;
+  p.a16 = h16;
+  p.z16 = h16 + hm;
+  p.xr16 = h16 + 2 * hm;
+  p.zx16 = h16 + 3 * hm;
+  p.t1_16 = h16 + 4 * hm;
+  p.t2_16 = h16 + 5 * hm;
   p.gt = scratch + 4 * BH * mm;
   p.w = w;
   p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
   p.status = status;
   p.m = s.m;
+  p.mp = mp;
   p.d = s.d;
   p.dpad = s.dpad();
   p.m64 = s.m64();
   p.splits = splits;
   p.iters = s.iters;
-  p.kc = (s.m + 31) / 32;
   p.scale = 1.0f / sqrtf((float)s.d);
 
   BigPinvMaps maps;
   memset(&maps, 0, sizeof(maps));
-  const float* bufs[6] = {p.a_s, p.z, p.xr, p.zx, p.t1, p.t2};
+  const __half* bufs[6] = {p.a16, p.z16, p.xr16, p.zx16, p.t1_16, p.t2_16};
   for (int i = 0; i < 6; ++i) {
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
-    const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)mm * 4};
-    const uint32_t box[3] = {32, 128, 1};
-    const uint32_t sbox[3] = {32, 32, 1};
-    if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
-                         box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&maps.st[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, bufs[i], dims, strides,
-                         sbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t strides[2] = {(uint64_t)mp * 2, (uint64_t)s.m * mp * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    const bool transposed = i == MAP_T1 || i == MAP_T2;
+    const uint32_t sbox[3] = {transposed ? 32u : 64u, 32, 1};
+    if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs[i], dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&maps.st[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs[i], dims, strides, sbox,
+                         transposed ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return tensor_map_error(__FILE__, __LINE__);
   }
   {
@@ -745,6 +798,14 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
     const uint32_t box[3] = {32, (uint32_t)(s.d / 2), 1};
     if (!make_tensor_map(&maps.m[MAP_GT], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.gt, dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return tensor_map_error(__FILE__, __LINE__);
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
+    const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)mm * 4};
+    const uint32_t box[3] = {32, 128, 1};
+    if (!make_tensor_map(&maps.m[MAP_Z32], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.z, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
       return tensor_map_error(__FILE__, __LINE__);
   }
   if (cudaFuncSetAttribute(pinv_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=

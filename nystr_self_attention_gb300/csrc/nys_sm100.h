@@ -325,6 +325,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with fp16 A/B (both K-major) and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::tf32 with fp32 D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
@@ -337,6 +342,14 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row) {
   const uint32_t chunk = (byte_in_row >> 4) ^ (row & 7u);
   return row * 128u + (chunk << 4) + (byte_in_row & 15u);
+}
+
+// Byte offset of element (row, byte-in-row) inside a SWIZZLE_64B tile whose
+// rows are 64 bytes: 16-byte chunk c of row r sits at chunk c ^ ((r / 2) % 4).
+// The tile base must be 512-byte aligned.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t byte_in_row) {
+  const uint32_t chunk = (byte_in_row >> 4) ^ ((row >> 1) & 3u);
+  return row * 64u + (chunk << 4) + (byte_in_row & 15u);
 }
 
 // 2^x on the SFU (ex2.approx, flush-to-zero).
