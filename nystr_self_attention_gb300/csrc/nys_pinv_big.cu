@@ -60,10 +60,14 @@ using namespace sm100;
 // factors), then the fp32 maps of W = Z G: G^T [B*H][d][m] and Z [B*H][m][m]
 enum MapIdx { MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_T1 = 4, MAP_T2 = 5, MAP_GT = 6, MAP_Z32 = 7 };
 
+// store-only maps beside the six fp16 matrices' store maps
+enum StoreIdx { ST_AS32 = 6, ST_Z16T = 7 };
+
 struct BigPinvMaps {
   CUtensorMap m[8];   // loads: fp16 boxes of 128 rows x 64 columns; fp32 boxes of <= 128 rows x 32
-  CUtensorMap st[6];  // stores of the fp16 matrices: row-major 32 x 64 boxes (SWIZZLE_128B),
-                      // transposed 32 x 32 boxes (SWIZZLE_64B)
+  CUtensorMap st[8];  // stores of the fp16 matrices: row-major 32 x 64 boxes (SWIZZLE_128B),
+                      // transposed ones 32 x 32 (SWIZZLE_64B); then A_S fp32 in 32 x 32 boxes
+                      // (SWIZZLE_128B) and Z fp16 in 32 x 32 boxes (SWIZZLE_64B)
 };
 
 struct BigPinvParams {
@@ -103,7 +107,6 @@ constexpr uint32_t kR0 = 0;    // scores / A_S, then this CTA's block of Z
 constexpr uint32_t kR1 = 128;  // X (level 0), W
 constexpr uint32_t kR2 = 256;  // X X
 constexpr uint32_t kR3 = 384;  // Z X
-constexpr int kCsPitch = 129;  // floats per row of the column-sum staging block
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
@@ -184,31 +187,37 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- 1) G = merge of the key-split partials: rows of this row block,
   // columns [c d/2, (c+1) d/2). G -> g (row-major), G^T -> gt. One pass
-  // over the splits per 16-column chunk, four splits at a time with all
+  // over the splits per 8-column chunk, four splits at a time with all
   // their loads in flight; a running (max, denominator) rescales the
   // accumulated row as in an online softmax, and an empty partial (max =
-  // -inf, rows never written) contributes nothing.
-  if (rv) {
-    const int hw = d >> 1, c0 = c * hw;
+  // -inf, rows never written) contributes nothing. Only W = Z G reads G, so
+  // the chunks are merged one per update level, while the workers would
+  // otherwise wait for the level's products.
+  constexpr int kMw = 8;              // columns per merge chunk
+  const int n_merge = (d >> 1) / kMw;  // chunks of this CTA's columns of G
+  auto merge_chunk = [&](int chunk) {
+    if (!rv) return;
+    const int hw = d >> 1;
     float* grow = p.g + ((size_t)bh * m + gi) * d;
     float* gtb = p.gt + (size_t)bh * d * m;
     const float2* ml_base = reinterpret_cast<const float2*>(p.gml) + (size_t)bh * p.splits * m + gi;
     const float* gp_base = p.gpart + ((size_t)bh * p.splits * m + gi) * d;
-    for (int j0 = c0; j0 < c0 + hw; j0 += 16) {
-      float acc[16];
+    {
+      const int j0 = c * hw + kMw * chunk;
+      float acc[kMw];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+      for (int e = 0; e < kMw; ++e) acc[e] = 0.f;
       float gm = -INFINITY, den = 0.f;
       for (int sp = 0; sp < p.splits; sp += 4) {
         float2 ml[4];
-        float4 v[4][4];
+        float4 v[4][kMw / 4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int spk = sp + k < p.splits ? sp + k : sp;
           ml[k] = __ldg(ml_base + (size_t)spk * m);
           const float4* src = reinterpret_cast<const float4*>(gp_base + (size_t)spk * m * d + j0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[k][e] = __ldg(src + e);
+          for (int e = 0; e < kMw / 4; ++e) v[k][e] = __ldg(src + e);
         }
         bool ok[4];
         float cm = gm;
@@ -228,12 +237,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
         gm = cm;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] *= r;
+        for (int e = 0; e < kMw; ++e) acc[e] *= r;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           if (ok[k]) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < kMw / 4; ++e) {
               acc[4 * e] = fmaf(v[k][e].x, f[k], acc[4 * e]);
               acc[4 * e + 1] = fmaf(v[k][e].y, f[k], acc[4 * e + 1]);
               acc[4 * e + 2] = fmaf(v[k][e].z, f[k], acc[4 * e + 2]);
@@ -243,14 +252,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const float inv = 1.f / den;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] *= inv;
+      for (int e = 0; e < kMw; ++e) acc[e] *= inv;
       float4* go = reinterpret_cast<float4*>(grow + j0);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+      for (int e = 0; e < kMw / 4; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) gtb[(size_t)(j0 + e) * m + gi] = acc[e];
+      for (int e = 0; e < kMw; ++e) gtb[(size_t)(j0 + e) * m + gi] = acc[e];
     }
-  }
+  };
+  if (p.iters == 0)
+    for (int k = 0; k < n_merge; ++k) merge_chunk(k);
 
   // ---- 2) scores S = Q~ K~^T (rows of block r, columns of block c) in
   // 3xTF32. Per pass, up to two 32-column chunks of d; chunk slot layout:
@@ -348,13 +359,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (worker) rsum_sh[tid] = part;
   cluster_sync_all();
-  float* cs_stage = reinterpret_cast<float*>(sm);  // [128][kCsPitch]
+  // The normalised block is staged in shared memory, in fp32 as four
+  // SWIZZLE_128B boxes [128 rows x 32 columns] (also read back for the
+  // column sums) and in fp16 as two [128 rows x 64 columns] boxes; each warp
+  // stores its 32 rows of both by TMA (clipped at m).
+  uint8_t* as_stage = sm;
+  uint8_t* a16_stage = sm + 65536;
   if (worker && !*abort_flag) {
     const float own = rsum_sh[tid], peer = ld_peer(&rsum_sh[tid], rank ^ 1u);
     const float sum = c == 0 ? own + peer : peer + own;  // same order in both CTAs
     const float inv = rv ? 1.f / sum : 0.f;
-    float* arow = p.a_s + bh * mm + (size_t)(rv ? gi : 0) * m;
-    __half* arow16 = p.a16 + ((size_t)bh * m + (rv ? gi : 0)) * p.mp;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lo + j0, v);
@@ -364,36 +378,48 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const float x = __uint_as_float(v[e]) * inv;
         v[e] = __float_as_uint(x);
         a_row_sum += fabsf(x);
-        cs_stage[tid * kCsPitch + j0 + e] = x;
       }
       tmem_st32(tmem + lo + j0, v);
-      if (rv) {
+      uint8_t* box = as_stage + (j0 >> 5) * 16384;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int gj = 128 * c + j0 + e;
-          if (gj < m) {
-            *reinterpret_cast<float4*>(arow + gj) =
-                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                            __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-            const __half2 h0 = __floats2half2_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-            const __half2 h1 = __floats2half2_rn(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-            *reinterpret_cast<uint2*>(arow16 + gj) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-          }
-        }
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(box + sw128_offset(tid, q * 16)) =
+            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
       }
+      uint8_t* hbox = a16_stage + (j0 >> 6) * 16384;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(hbox + sw128_offset(tid, (j0 & 63) * 2 + q * 16)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
     tmem_st_wait();
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      for (int b = 0; b < 4; ++b)
+        tma_store_3d(&maps.st[ST_AS32], as_stage + b * 16384 + warp * 4096, 128 * c + 32 * b, 128 * r + 32 * warp, bh);
+      for (int b = 0; b < 2; ++b)
+        tma_store_3d(&maps.st[MAP_A], a16_stage + b * 16384 + warp * 4096, 128 * c + 64 * b, 128 * r + 32 * warp, bh);
+      bulk_commit();
+    }
   }
   __syncthreads();
   if (worker) {
     // this CTA's part of column tid's abs-sum (four independent partials)
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (!*abort_flag)
+    if (!*abort_flag) {
+      const uint8_t* cbox = as_stage + (tid >> 5) * 16384;
       for (int i = 0; i < 128; i += 4) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) s4[t] += fabsf(cs_stage[(i + t) * kCsPitch + tid]);
+        for (int t = 0; t < 4; ++t)
+          s4[t] += fabsf(*reinterpret_cast<const float*>(cbox + sw128_offset(i + t, (tid & 31) * 4)));
       }
+    }
     cs_sh[tid] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     rs_sh[tid] = a_row_sum;
   }
@@ -420,42 +446,58 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block,
-  // fp32 and fp16) and Z_0^T = alpha A_S (fp16 row store, the first update's
-  // right factor)
+  // fp32 by plain coalesced stores and fp16 by TMA) and Z_0^T = alpha A_S
+  // (fp16 by TMA, the first update's right factor)
   if (worker && !*abort_flag) {
     const float n1 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     const float ninf = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
     const float alpha = 1.f / (n1 * ninf);
     float* z = p.z + bh * mm;
-    __half* z16 = p.z16 + (size_t)bh * m * p.mp;
-    __half* zt16 = p.t1_16 + (size_t)bh * m * p.mp;
+    // fp16 staging, SWIZZLE_64B tiles of 32 x 32: alpha A_S (this warp's
+    // rows, 32 columns per tile) and its transpose (32 block columns per tile)
+    uint8_t* zt_stage = sm + 98304 + warp * 8192;
+    uint8_t* z16_stage = sm + 131072 + warp * 8192;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
       tmem_ld32(tmem + lo + kR0 + j0, v);
       tmem_ld_wait();
       if (rv) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int gj = 128 * c + j0 + e;
-          if (gj < m) {
-            const __half2 h0 = __floats2half2_rn(alpha * __uint_as_float(v[e]), alpha * __uint_as_float(v[e + 1]));
-            const __half2 h1 = __floats2half2_rn(alpha * __uint_as_float(v[e + 2]), alpha * __uint_as_float(v[e + 3]));
-            *reinterpret_cast<uint2*>(zt16 + (size_t)gi * p.mp + gj) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
-          }
-        }
-#pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int gj = 128 * c + j0 + e;
-          if (gj < m) {
-            const float zv = alpha * __uint_as_float(v[e]);
-            z[(size_t)gj * m + gi] = zv;
-            z16[(size_t)gj * p.mp + gi] = __float2half_rn(zv);
-          }
+          if (gj < m) z[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
         }
       }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const __half2 h2 = __floats2half2_rn(alpha * __uint_as_float(v[2 * e]), alpha * __uint_as_float(v[2 * e + 1]));
+        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      uint8_t* rt = zt_stage + (j0 >> 5) * 2048;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(rt + sw64_offset(lane, q * 16)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      uint8_t* tt = z16_stage + (j0 >> 5) * 2048;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        *reinterpret_cast<__half*>(tt + sw64_offset(e, lane * 2)) = __float2half_rn(alpha * __uint_as_float(v[e]));
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      for (int k = 0; k < 4; ++k) {
+        tma_store_3d(&maps.st[MAP_T1], zt_stage + k * 2048, 128 * c + 32 * k, 128 * r + 32 * warp, bh);
+        tma_store_3d(&maps.st[ST_Z16T], z16_stage + k * 2048, 128 * r + 32 * warp, 128 * c + 32 * k, bh);
+      }
+      bulk_commit();
     }
   }
+  // every store of the prologue has landed (and read its staging) before
+  // the products start
+  if (worker && lane == 0) bulk_wait0();
+  __syncwarp();
   cluster_sync_all();
   // this CTA's block of Z_0 into TMEM (zero beyond m), where it stays across
   // the updates
@@ -587,7 +629,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else {
-      // epilogue: thread = row gi of the product block
+      // epilogue: thread = row gi of the product block. Before an update
+      // level's products are done, merge the next chunk of G (the last
+      // update level merges whatever is left).
+      if (!is_w && !*abort_flag) {
+        if (pi < nprod - 2) {
+          if (pi < n_merge) merge_chunk(pi);
+        } else if (pi == nprod - 2) {
+          for (int k = pi; k < n_merge; ++k) merge_chunk(k);
+        }
+      }
       const bool ok_epi = __all_sync(0xffffffffu, wait_done());  // warp-uniform: TMEM loads are warp-wide
       if (is_w && ok_epi) {
         float* wrow = p.w + ((size_t)bh * m + (rv ? gi : 0)) * d + c * hw;
@@ -803,9 +854,15 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   {
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
     const uint64_t strides[2] = {(uint64_t)s.m * 4, (uint64_t)mm * 4};
-    const uint32_t box[3] = {32, 128, 1};
+    const uint32_t box[3] = {32, 128, 1}, sbox[3] = {32, 32, 1};
     if (!make_tensor_map(&maps.m[MAP_Z32], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.z, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&maps.st[ST_AS32], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.a_s, dims, strides, sbox,
                          CU_TENSOR_MAP_SWIZZLE_128B))
+      return tensor_map_error(__FILE__, __LINE__);
+    const uint64_t hstrides[2] = {(uint64_t)mp * 2, (uint64_t)s.m * mp * 2};
+    if (!make_tensor_map(&maps.st[ST_Z16T], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p.z16, dims, hstrides, sbox,
+                         CU_TENSOR_MAP_SWIZZLE_64B))
       return tensor_map_error(__FILE__, __LINE__);
   }
   if (cudaFuncSetAttribute(pinv_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
