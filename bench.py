@@ -278,6 +278,18 @@ def pinv_flops(wl, with_w=True):
     return wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + (2.0 * m * m * d if with_w else 0.0))
 
 
+def pinv_peak_time(wl, bf16_tflops, with_w=True):
+    """Seconds the pseudo-inverse kernel's flops take at the tensor peaks of
+    the types they run in: the scores and W = Z G in tf32; the update
+    products in tf32 for m <= 128 and with fp16 operands (the bf16/fp16 rate)
+    for m > 128."""
+    m, d = wl.m, wl.d
+    tf32 = bf16_tflops * TF32_OVER_BF16 * 1e12
+    upd = wl.heads * 8.0 * wl.iters * m ** 3
+    rest = pinv_flops(wl, with_w) - upd
+    return rest / tf32 + upd / (bf16_tflops * 1e12 if m > 128 else tf32)
+
+
 def kernel_source_hash(kernel):
     import hashlib
     src = os.path.join(ROOT, "nystr_self_attention_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
@@ -333,11 +345,14 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src, w_separate
         flops = pinv_flops(wl, with_w=not w_separate) / per_step
     achieved = flops / t_launch / 1e12
     if kernel in ("pinv_tc", "pinv_big"):
-        peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+        # the peak of this mix of tf32 and fp16 products: its flops over the
+        # time they take at each type's peak
+        peak = flops / (pinv_peak_time(wl, peaks["bf16_tflops"], with_w=not w_separate) / per_step) / 1e12
         return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_flops": flops,
-                "peak_source": f"bf16_tflops burst ({peak_src}) x 1.1/2.25 (tf32/bf16 nominal)"}
+                "peak_source": f"bf16_tflops burst ({peak_src}); tf32 products at x 1.1/2.25 (tf32/bf16 "
+                               f"nominal), fp16 update products (m > 128) at the bf16 rate"}
     peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
     return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -356,14 +371,13 @@ def pass_roofline(wl, ms_per_step, peaks, peak_src):
     n_tok = wl.B * wl.H * wl.n
     mm_flops = n_tok * (2.0 * wl.m * wl.d * 2 + 2.0 * wl.m * wl.d * 2 + 2.0 * wl.ks * wl.d)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    t_mma = mm_flops / (peaks["bf16_tflops"] * 1e12) + pinv_flops(wl) / (
-        peaks["bf16_tflops"] * TF32_OVER_BF16 * 1e12)
+    t_mma = mm_flops / (peaks["bf16_tflops"] * 1e12) + pinv_peak_time(wl, peaks["bf16_tflops"])
     t_roof = max(t_hbm, t_mma)
     return {"bytes": nbytes, "flops": mm_flops + pinv_flops(wl), "t_hbm_us": t_hbm * 1e6,
             "t_tensor_us": t_mma * 1e6, "bound": "hbm" if t_hbm >= t_mma else "tensor",
             "t_roofline_us": t_roof * 1e6, "t_measured_us": ms_per_step * 1e3,
             "frac": t_roof / (ms_per_step / 1e3),
-            "peak_source": f"hbm_gbs, bf16_tflops ({peak_src}); tf32 = bf16 x 1.1/2.25"}
+            "peak_source": f"hbm_gbs, bf16_tflops ({peak_src}); tf32 = bf16 x 1.1/2.25, fp16 = bf16"}
 
 
 def resident_inputs(inp, dev):

@@ -30,14 +30,29 @@ def test_head_groups_split_the_bytes_of_a_launch():
 
 def test_pseudo_inverse_roofline_is_tf32_of_the_burst_peak():
     """Per-kernel times are short event-timed launches: the burst bf16 peak,
-    scaled to tf32 by the nominal ratio."""
-    wl = workloads.WORKLOADS["c5"]
-    r = bench.roofline_for("pinv_big", 1.0, 4, 1, wl, PEAKS, "measured")
+    scaled to tf32 by the nominal ratio (m <= 128: every product is tf32)."""
+    wl = workloads.WORKLOADS["c4"]
+    r = bench.roofline_for("pinv_tc", 1.0, 4, 1, wl, PEAKS, "measured")
     m, d = wl.m, wl.d
     flops = wl.heads * (2.0 * m * m * d + 8.0 * wl.iters * m ** 3 + 2.0 * m * m * d)
     assert r["bound"] == "tensor" and r["algorithmic_flops"] == flops
     assert r["peak"] == pytest.approx(1800.0 * 1.1 / 2.25)
     assert r["achieved"] == pytest.approx(flops / 250e-6 / 1e12)
+
+
+def test_large_m_pseudo_inverse_peak_mixes_fp16_updates_and_tf32_rest():
+    """m > 128: the update products run with fp16 operands (the bf16 rate),
+    the scores and W = Z G in tf32; the peak is the flops over the time they
+    take at those rates."""
+    wl = workloads.WORKLOADS["c5"]
+    r = bench.roofline_for("pinv_big", 1.0, 4, 1, wl, PEAKS, "measured")
+    m, d = wl.m, wl.d
+    upd = wl.heads * 8.0 * wl.iters * m ** 3
+    rest = wl.heads * 4.0 * m * m * d
+    t = upd / 1800e12 + rest / (1800e12 * 1.1 / 2.25)
+    assert r["algorithmic_flops"] == upd + rest
+    assert r["peak"] == pytest.approx((upd + rest) / t / 1e12)
+    assert 1800.0 * 1.1 / 2.25 < r["peak"] < 1800.0
 
 
 def test_pseudo_inverse_not_credited_with_w_when_w_tc_forms_it():
