@@ -211,10 +211,14 @@ int nystrom_mha_fwd(const void* x, const void* w_qkv, const float* b_qkv,
  *   iters x:  a(i) = argmin_c |q_i - mu_c|^2 (ties: the lowest c), then
  *             mu_c = mean of the queries with a(i) = c (none: unchanged)
  *   out[i]  = softmax(mu_{a(i)} K^T / sqrt(d)) V
- * K-means runs in fp32 on the CUDA cores (the update sums a cluster's
- * queries in index order: reproducible); the centroid rows run in the
- * landmark-row kernels of the forward pass (bf16 tensor cores for NYS_BF16,
- * with the centroids rounded to bf16; fp32 CUDA cores for NYS_FP32).
+ * K-means: for NYS_BF16 with d in {64, 128} and C <= 128 on the tensor
+ * cores (distances to fp32 accuracy: the centroids split into three bf16
+ * terms; the members' sums as a one-hot product with fp32 accumulation,
+ * added across CTAs in a fixed order: deterministic), otherwise in fp32 on
+ * the CUDA cores (the update sums a cluster's queries in index order). The
+ * centroid rows run in the landmark-row kernels of the forward pass (bf16
+ * tensor cores for NYS_BF16, with the centroids rounded to bf16; fp32 CUDA
+ * cores for NYS_FP32).
  * q, k, v, out: [B][H][n][d] in `dtype`, device, 16-byte aligned; shape rules
  * as the top of this file with C in place of m; 1 <= iters <= 64.
  * workspace: device, 256-byte aligned, ws_bytes >=

@@ -9,10 +9,12 @@
 //   out_i = G[a(i)]
 // It shares the Nyström path's kernels for the segment means and for
 // softmax(. K^T s) V (the landmark-row kernels with the centroids in place of
-// the landmarks, then the merge of the key-split partials); the K-means
-// steps and the broadcast are CUDA-core kernels here. The assignment and the
-// update run in fp32 (the update sums a cluster's queries in index order, so
-// it is reproducible bit for bit).
+// the landmarks, then the merge of the key-split partials). K-means runs on
+// the tensor cores for bf16 queries with d in {64, 128} and C <= 128
+// (nys_kmeans_tc.cu: the distances to fp32 accuracy, the members' sums as a
+// one-hot product, deterministic), and otherwise in the CUDA-core kernels
+// below in fp32 (the update sums a cluster's queries in index order). The
+// broadcast is a CUDA-core kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -165,6 +167,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct ClusteredLayout {
   Layout attn;  // the landmark-row partials, G, the status word, scratch
   size_t assign, mu_a, mu_b, total;
+  bool tc;                          // K-means on the tensor cores
+  size_t mu3, norms, part, cnt;     // its workspace (tc only)
 };
 
 ClusteredLayout clustered_layout(const Shape& s) {
@@ -175,6 +179,14 @@ ClusteredLayout clustered_layout(const Shape& s) {
   L.assign = take((size_t)s.bh() * s.n * 4);
   L.mu_a = take((size_t)s.bh() * s.m * s.d * 4);
   L.mu_b = take((size_t)s.bh() * s.m * s.d * 4);
+  L.tc = kmeans_tc_supported(s);
+  if (L.tc) {
+    const KmWorkspace w = kmeans_tc_workspace(s);
+    L.mu3 = take(w.mu3_bytes);
+    L.norms = take(w.norm_bytes);
+    L.part = take(w.part_bytes);
+    L.cnt = take(w.cnt_bytes);
+  }
   L.total = off;
   return L;
 }
@@ -279,21 +291,35 @@ int nystrom_clustered_attn_fwd(const void* q, const void* k, const void* v, void
   rc = launch_landmarks(s, q, k, mu[0], reinterpret_cast<float*>(at(L.attn.k_tilde)), nullptr,
                         nullptr, stream);
   if (rc != NYS_OK) return error_in("initial centroids", rc);
+  int* status = reinterpret_cast<int*>(at(L.attn.status));
   int cur = 0;
-  for (int it = 0; it < iters; ++it) {
-    rc = bf16 ? assign_t<__nv_bfloat16>(s, q, mu[cur], assign, stream)
-              : assign_t<float>(s, q, mu[cur], assign, stream);
-    if (rc != NYS_OK) return error_in("K-means assignment", rc);
-    rc = bf16 ? update_t<__nv_bfloat16>(s, q, assign, mu[cur], mu[cur ^ 1], stream)
-              : update_t<float>(s, q, assign, mu[cur], mu[cur ^ 1], stream);
-    if (rc != NYS_OK) return error_in("K-means update", rc);
-    cur ^= 1;
+  if (L.tc) {
+    void* mu3 = at(L.mu3);
+    float* norms = reinterpret_cast<float*>(at(L.norms));
+    rc = launch_kmeans_prep(s, mu[0], mu3, norms, stream);
+    if (rc != NYS_OK) return error_in("K-means set-up", rc);
+    for (int it = 0; it < iters; ++it) {
+      rc = launch_kmeans_round_tc(s, q, mu3, norms, assign, reinterpret_cast<float*>(at(L.part)),
+                                  reinterpret_cast<int*>(at(L.cnt)), mu[cur], mu[cur ^ 1], norms, mu3,
+                                  status, stream);
+      if (rc != NYS_OK) return error_in("K-means round", rc);
+      cur ^= 1;
+    }
+  } else {
+    for (int it = 0; it < iters; ++it) {
+      rc = bf16 ? assign_t<__nv_bfloat16>(s, q, mu[cur], assign, stream)
+                : assign_t<float>(s, q, mu[cur], assign, stream);
+      if (rc != NYS_OK) return error_in("K-means assignment", rc);
+      rc = bf16 ? update_t<__nv_bfloat16>(s, q, assign, mu[cur], mu[cur ^ 1], stream)
+                : update_t<float>(s, q, assign, mu[cur], mu[cur ^ 1], stream);
+      if (rc != NYS_OK) return error_in("K-means update", rc);
+      cur ^= 1;
+    }
   }
   // G = softmax(mu K^T / sqrt(d)) V with the centroids as the landmark rows
   float* gp = reinterpret_cast<float*>(at(L.attn.g_part));
   float* gml = reinterpret_cast<float*>(at(L.attn.g_ml));
   float* g = reinterpret_cast<float*>(at(L.attn.g));
-  int* status = reinterpret_cast<int*>(at(L.attn.status));
   if (bf16) {
     __nv_bfloat16* mb = reinterpret_cast<__nv_bfloat16*>(at(L.attn.qt_bf16));
     {

@@ -159,6 +159,24 @@ int launch_conv_mask(const Shape& s, const void* v, const float* conv_w, void* o
 int launch_merge_g(const Shape& s, const float* gp, const float* gml, float* g, int splits,
                    cudaStream_t stream);
 
+// K-means rounds of clustered attention on the tensor cores (bf16, d in {64,
+// 128}, C = s.m <= 128). Workspace per call: the bf16 split of the centroids
+// (hi, mid, lo), their squared norms, and the per-CTA members' sums and
+// counts of one round.
+struct KmWorkspace {
+  int S, C_pad;
+  size_t mu3_bytes, norm_bytes, part_bytes, cnt_bytes;
+};
+bool kmeans_tc_supported(const Shape& s);
+KmWorkspace kmeans_tc_workspace(const Shape& s);
+// split and squared norms of the centroids mu (fp32 [B*H][C][d])
+int launch_kmeans_prep(const Shape& s, const float* mu, void* mu3, float* norms, cudaStream_t st);
+// one round: assignment with mu3 / norms (the split of mu_old), members'
+// sums, then mu_new and, in place in mu3 / norms, the split of mu_new
+int launch_kmeans_round_tc(const Shape& s, const void* q, const void* mu3, const float* norms,
+                           int* assign, float* part, int* cnt, const float* mu_old, float* mu_new,
+                           float* norms_next, void* mu3_next, int* status, cudaStream_t st);
+
 // Most pseudo-inverse updates the tensor-core kernels run: their products
 // take tf32 operands, whose rounding the iteration amplifies by cond(A_S) as
 // it inverts more of A_S's small singular values. Up to 8 updates (the

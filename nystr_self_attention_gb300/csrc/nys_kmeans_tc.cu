@@ -1,0 +1,421 @@
+// K-means rounds of clustered attention on the tensor cores ("Fast
+// Transformers with Clustered Attention" review page, Proposed method,
+// bullets 1 and 2), for bf16 queries with d in {64, 128} and C <= 128
+// clusters. One round per launch of `kmeans_round_tc`, over 128-query tiles:
+//   assignment  S = Q mu^T (128 x C_pad) as three bf16 products: mu is split
+//               into hi + mid + lo (bf16 each, 24 bits of mu together) and Q
+//               is exact in bf16, so S matches fp32 to rounding; then
+//               a(i) = argmin_c |mu_c|^2 - 2 S[i, c] (ties: the lowest c),
+//               the squared norms taken from the fp32 centroids
+//   update      the members' sums onehot(a)^T Q (C_pad x d, one bf16 product
+//               per tile with exact products and fp32 accumulation in TMEM,
+//               reusing the Q tile as the MN-major right factor) and the
+//               member counts, per CTA over its range of tiles of one head
+// and `kmeans_reduce` sums the CTAs' partial sums in a fixed order (so a
+// round is deterministic), divides by the counts (an empty cluster keeps its
+// centroid), and prepares the next round's bf16 split and squared norms.
+//
+// 128 threads: thread = query row of the tile (TMEM lane) in the assignment
+// epilogue, = cluster row in the update epilogue; thread 0 issues the TMA
+// copies and the MMAs. The Q tile is double-buffered: the next tile's copy
+// starts once the update product of the tile before has read its buffer.
+// Every mbarrier wait is bounded; a wait that runs out sets the status word
+// and the CTA winds down (copies and products in flight awaited, TMEM
+// freed).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "nys_internal.h"
+#include "nys_sm100.h"
+#include "nys_tma_host.h"
+
+namespace nys {
+namespace {
+
+using namespace sm100;
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kThreads = 128;
+constexpr uint32_t kColS = 0, kColU = 128;  // TMEM: scores (C_pad columns), members' sums (d columns)
+
+struct KmMaps {
+  CUtensorMap q;    // bf16 [B*H][n][d], box 64 x 128
+  CUtensorMap mu3;  // bf16 [B*H*3][C_pad][d] (hi, mid, lo per head), box 64 x C_pad
+};
+
+struct KmParams {
+  const float* norms;  // [B*H][C_pad]  |mu_c|^2 of the fp32 centroids
+  int* assign;         // [B*H][n]
+  float* part;         // [B*H][S][C_pad][d]  members' sums per CTA
+  int* cnt;            // [B*H][S][C_pad]     member counts per CTA
+  int* status;
+  int n, d, C, C_pad, tiles_per_head, tiles_per_cta, S;
+  uint32_t off_mu, off_q, off_oh;  // shared-memory layout
+};
+
+struct KmBars {
+  uint64_t mu, q[2], asg, upd, fin;
+};
+
+__device__ __forceinline__ bool km_wait(uint64_t* bar, uint32_t parity, int* status,
+                                        volatile int* abort_flag) {
+  if (mbar_wait(bar, parity, abort_flag, kWaitNs)) return true;
+  if (!*abort_flag) {
+    *abort_flag = 1;
+    atomicExch(status, (int)NYS_ERR_TIMEOUT);
+  }
+  return false;
+}
+
+// grid (S, B*H): CTA (s, bh) runs tiles [s tpc, (s + 1) tpc) of head bh.
+// DCH = d / 64 column boxes of Q and mu.
+template <int DCH>
+__global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_constant__ KmMaps maps,
+                                                               const KmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* mus = sm + p.off_mu;  // [3][DCH] boxes of C_pad rows x 128 B
+  uint8_t* qb = sm + p.off_q;    // [2][DCH] boxes of 128 rows x 128 B
+  uint8_t* oh = sm + p.off_oh;   // one-hot^T: [2] boxes of 128 cluster rows x 64 queries (bf16)
+  __shared__ KmBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ float norm_s[128];
+  __shared__ int cnt_s[128];
+  volatile int* abort_flag = &abort_sh;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int s = blockIdx.x;
+  const long long bh = blockIdx.y;
+  const int t0 = s * p.tiles_per_cta;
+  const int ntiles = max(0, min(p.tiles_per_head, t0 + p.tiles_per_cta) - t0);
+  const uint32_t q_bytes = (uint32_t)DCH * 16384u;
+  const uint32_t mu_box = (uint32_t)p.C_pad * 128u;
+
+  if (tid == 0) {
+    mbar_init(&bars.mu, 1);
+    mbar_init(&bars.q[0], 1);
+    mbar_init(&bars.q[1], 1);
+    mbar_init(&bars.asg, 1);
+    mbar_init(&bars.upd, 1);
+    mbar_init(&bars.fin, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  norm_s[tid] = tid < p.C_pad ? p.norms[bh * p.C_pad + tid] : 0.f;
+  cnt_s[tid] = 0;
+  // the one-hot tile starts all zero; each thread later clears only its own 1
+  for (int e = tid; e < 2 * 128 * 128 / 16; e += kThreads)
+    reinterpret_cast<uint4*>(oh)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_async_smem();
+  if (warp == 0) tmem_alloc(&tmem_base_sh, 256);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+
+  uint32_t n_mu = 0, n_q[2] = {0, 0};  // copies issued (thread 0)
+  if (tid == 0 && ntiles > 0) {
+    tma_prefetch(&maps.q);
+    tma_prefetch(&maps.mu3);
+    mbar_arrive_expect_tx(&bars.mu, 3u * DCH * mu_box);
+    for (int k = 0; k < 3; ++k)
+      for (int c = 0; c < DCH; ++c)
+        tma_load_3d(mus + (k * DCH + c) * mu_box, &maps.mu3, &bars.mu, 64 * c, 0, (int)(bh * 3 + k));
+    n_mu = 1;
+    mbar_arrive_expect_tx(&bars.q[0], q_bytes);
+    for (int c = 0; c < DCH; ++c) tma_load_3d(qb + c * 16384, &maps.q, &bars.q[0], 64 * c, t0 * 128, (int)bh);
+    n_q[0] = 1;
+  }
+  const uint32_t id_s = idesc_bf16(128, p.C_pad, false, false);
+  const uint32_t id_u = idesc_bf16(128, 64 * DCH, false, true);
+  int prev_a = -1;  // where this thread's query put its 1 in the one-hot tile
+  for (int j = 0; j < ntiles; ++j) {
+    const int b = j & 1, tile = t0 + j;
+    if (tid == 0 && !*abort_flag) {
+      bool ok = true;
+      // the next tile's Q into the other buffer, once the members' product
+      // of tile j-1 has read that buffer
+      if (j + 1 < ntiles) {
+        if (j >= 1) ok = km_wait(&bars.upd, (j - 1) & 1, p.status, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars.q[b ^ 1], q_bytes);
+          for (int c = 0; c < DCH; ++c)
+            tma_load_3d(qb + ((b ^ 1) * DCH + c) * 16384, &maps.q, &bars.q[b ^ 1], 64 * c, (tile + 1) * 128,
+                        (int)bh);
+          ++n_q[b ^ 1];
+        }
+      }
+      if (ok && j == 0) ok = km_wait(&bars.mu, 0, p.status, abort_flag);
+      if (ok) ok = km_wait(&bars.q[b], (n_q[b] - 1) & 1, p.status, abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        // scores: Q mu^T as Q mu_hi^T + Q mu_mid^T + Q mu_lo^T
+        for (int k = 0; k < 3; ++k)
+          for (int kk = 0; kk < 4 * DCH; ++kk) {
+            const uint64_t a = smem_desc(smem_u32(qb + (b * DCH + (kk >> 2)) * 16384), 16, 1024, SW_128B);
+            const uint64_t bd = smem_desc(smem_u32(mus + (k * DCH + (kk >> 2)) * mu_box), 16, 1024, SW_128B);
+            mma_bf16(tmem + kColS, a + (uint64_t)((kk & 3) * 2), bd + (uint64_t)((kk & 3) * 2), id_s,
+                     (k > 0 || kk > 0) ? 1u : 0u);
+          }
+        mma_commit(&bars.asg);
+      }
+    }
+    // assignment: nearest centroid of this thread's query
+    bool ok = km_wait(&bars.asg, j & 1, p.status, abort_flag);
+    const bool go = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-wide
+    tc_fence_after_sync();
+    float best = INFINITY;
+    int best_c = 0;
+    if (go) {
+      for (int c0 = 0; c0 < p.C_pad; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lo + kColS + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int c = c0 + e;
+          if (c < p.C) {
+            const float score = fmaf(-2.f, __uint_as_float(v[e]), norm_s[c]);
+            if (score < best) {  // strict: a tie keeps the lower index
+              best = score;
+              best_c = c;
+            }
+          }
+        }
+      }
+    }
+    const int i = tile * 128 + tid;
+    const bool valid = go && i < p.n;
+    if (valid) {
+      p.assign[bh * p.n + i] = best_c;
+      atomicAdd(&cnt_s[best_c], 1);
+    }
+    // one-hot^T for the members' product: this thread's column, once the
+    // product of tile j-1 has read the tile
+    if (j >= 1) km_wait(&bars.upd, (j - 1) & 1, p.status, abort_flag);
+    uint8_t* ohb = oh + (tid >> 6) * 16384;
+    if (prev_a >= 0) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(prev_a, (tid & 63) * 2)) = 0;
+    prev_a = valid ? best_c : -1;
+    if (valid) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(best_c, (tid & 63) * 2)) = 0x3F80;  // bf16 1
+    fence_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && !*abort_flag) {
+      tc_fence_after_sync();
+      // members' sums += onehot^T (clusters x 128 queries) Q (128 queries x d)
+      const uint64_t q0 = smem_desc(smem_u32(qb + b * DCH * 16384), 16384, 1024, SW_128B);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t a = smem_desc(smem_u32(oh + (kk >> 2) * 16384), 16, 1024, SW_128B);
+        mma_bf16(tmem + kColU, a + (uint64_t)((kk & 3) * 2), q0 + (uint64_t)(kk * 128), id_u,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bars.upd);
+    }
+  }
+
+  // this CTA's members' sums and counts; thread = cluster row
+  bool ok = true;
+  if (ntiles > 0) ok = km_wait(&bars.upd, (ntiles - 1) & 1, p.status, abort_flag);
+  const bool go = __all_sync(0xffffffffu, ok) && ntiles > 0;
+  tc_fence_after_sync();
+  float* prow = p.part + (((size_t)bh * p.S + s) * p.C_pad + (tid < p.C_pad ? tid : 0)) * p.d;
+  for (int c0 = 0; c0 < p.d; c0 += 32) {
+    uint32_t v[32];
+    if (go) {
+      tmem_ld32(tmem + lo + kColU + c0, v);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = 0u;
+    }
+    if (tid < p.C_pad) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<uint4*>(prow + c0 + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    }
+  }
+  if (tid < p.C_pad) p.cnt[((size_t)bh * p.S + s) * p.C_pad + tid] = cnt_s[tid];
+
+  // wind-down: no copy or product of this CTA may still be in flight
+  if (tid == 0) {
+    if (*abort_flag) {
+      if (n_mu) mbar_wait(&bars.mu, 0, nullptr, kWaitNs);
+      for (int r = 0; r < 2; ++r)
+        if (n_q[r]) mbar_wait(&bars.q[r], (n_q[r] - 1) & 1, nullptr, kWaitNs);
+    }
+    mma_commit(&bars.fin);
+    mbar_wait(&bars.fin, 0, nullptr, kWaitNs);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// grid (C_pad, B*H), block d: thread j of centroid c. With S > 0: the new
+// centroid = the CTAs' members' sums added in CTA order, over the summed
+// counts (an empty cluster keeps mu_old); with S = 0 the centroid is mu_old
+// as it is. Either way it writes the bf16 split (hi, mid, lo) of the
+// centroid and its squared norm for the next assignment; rows c >= C are
+// zero.
+__global__ void kmeans_reduce(const float* __restrict__ part, const int* __restrict__ cnt,
+                              const float* __restrict__ mu_old, float* __restrict__ mu_new,
+                              __nv_bfloat16* __restrict__ mu3, float* __restrict__ norms, int S, int d,
+                              int C, int C_pad) {
+  __shared__ float red[4];
+  const int c = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  const long long bh = blockIdx.y;
+  float x = 0.f;
+  if (c < C) {
+    const size_t o = ((size_t)bh * C + c) * d + j;
+    x = mu_old[o];
+    if (S > 0) {
+      float sum = 0.f;
+      int count = 0;
+      for (int s = 0; s < S; ++s) {
+        const size_t r = ((size_t)bh * S + s) * C_pad + c;
+        sum += part[r * d + j];
+        count += cnt[r];
+      }
+      if (count > 0) x = sum / (float)count;
+      mu_new[o] = x;
+    }
+  }
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  const size_t base = ((size_t)bh * 3 * C_pad + c) * d + j;
+  mu3[base] = hi;
+  mu3[base + (size_t)C_pad * d] = mid;
+  mu3[base + 2 * (size_t)C_pad * d] = lo;
+  float sq = x * x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  if (lane == 0) red[warp] = sq;
+  __syncthreads();
+  if (j == 0) {
+    float t = 0.f;
+    for (int w = 0; w < (d + 31) / 32; ++w) t += red[w];
+    norms[(size_t)bh * C_pad + c] = t;
+  }
+}
+
+struct KmPlan {
+  int C_pad, T_h, tpc, S, dch;
+  uint32_t off_mu, off_q, off_oh;
+  size_t smem;
+};
+
+KmPlan km_plan(const Shape& s) {
+  KmPlan k{};
+  k.dch = s.d / 64;
+  k.C_pad = (s.m + 15) & ~15;
+  k.T_h = (s.n + 127) / 128;
+  // about two CTAs per SM over all heads, whole tiles per CTA
+  const int bh = (int)s.bh();
+  const int want = std::max(1, (2 * plan_sms() + bh - 1) / bh);
+  k.tpc = std::max(1, (k.T_h + want - 1) / want);
+  k.S = (k.T_h + k.tpc - 1) / k.tpc;
+  k.off_mu = 0;
+  k.off_q = k.off_mu + 3u * k.dch * k.C_pad * 128u;
+  k.off_oh = k.off_q + 2u * k.dch * 16384u;
+  // at least 80 KB, so that at most two CTAs (2 x 256 TMEM columns) share an SM
+  k.smem = std::max<size_t>((size_t)k.off_oh + 2 * 16384 + 1024, 80 * 1024);
+  return k;
+}
+
+}  // namespace
+
+bool kmeans_tc_supported(const Shape& s) {
+  if (s.dtype != NYS_BF16 || (s.d != 64 && s.d != 128) || s.m < 1 || s.m > 128) return false;
+  return km_plan(s).smem <= 227 * 1024;
+}
+
+KmWorkspace kmeans_tc_workspace(const Shape& s) {
+  const KmPlan k = km_plan(s);
+  KmWorkspace w{};
+  w.S = k.S;
+  w.C_pad = k.C_pad;
+  w.mu3_bytes = (size_t)s.bh() * 3 * k.C_pad * s.d * 2;
+  w.norm_bytes = (size_t)s.bh() * k.C_pad * 4;
+  w.part_bytes = (size_t)s.bh() * k.S * k.C_pad * s.d * 4;
+  w.cnt_bytes = (size_t)s.bh() * k.S * k.C_pad * 4;
+  return w;
+}
+
+int launch_kmeans_prep(const Shape& s, const float* mu, void* mu3, float* norms, cudaStream_t st) {
+  const KmPlan k = km_plan(s);
+  KernelScope scope("kmeans_reduce", st);
+  kmeans_reduce<<<dim3((unsigned)k.C_pad, (unsigned)s.bh()), s.d, 0, st>>>(
+      nullptr, nullptr, mu, nullptr, static_cast<__nv_bfloat16*>(mu3), norms, 0, s.d, s.m, k.C_pad);
+  return launch_status();
+}
+
+int launch_kmeans_round_tc(const Shape& s, const void* q, const void* mu3, const float* norms,
+                           int* assign, float* part, int* cnt, const float* mu_old, float* mu_new,
+                           float* norms_next, void* mu3_next, int* status, cudaStream_t st) {
+  if (!kmeans_tc_supported(s)) return NYS_ERR_UNSUPPORTED;
+  const KmPlan k = km_plan(s);
+  const uint64_t BH = (uint64_t)s.bh();
+  KmMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  {
+    const uint64_t dims[3] = {(uint64_t)s.d, (uint64_t)s.n, BH};
+    const uint64_t strides[2] = {(uint64_t)s.d * 2, (uint64_t)s.n * s.d * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!make_tensor_map(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+      return tensor_map_error(__FILE__, __LINE__);
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)s.d, (uint64_t)k.C_pad, BH * 3};
+    const uint64_t strides[2] = {(uint64_t)s.d * 2, (uint64_t)k.C_pad * s.d * 2};
+    const uint32_t box[3] = {64, (uint32_t)k.C_pad, 1};
+    if (!make_tensor_map(&maps.mu3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, mu3, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+      return tensor_map_error(__FILE__, __LINE__);
+  }
+  KmParams p{};
+  p.norms = norms;
+  p.assign = assign;
+  p.part = part;
+  p.cnt = cnt;
+  p.status = status;
+  p.n = s.n;
+  p.d = s.d;
+  p.C = s.m;
+  p.C_pad = k.C_pad;
+  p.tiles_per_head = k.T_h;
+  p.tiles_per_cta = k.tpc;
+  p.S = k.S;
+  p.off_mu = k.off_mu;
+  p.off_q = k.off_q;
+  p.off_oh = k.off_oh;
+  const dim3 grid((unsigned)k.S, (unsigned)BH);
+  {
+    KernelScope scope("kmeans_round_tc", st);
+    if (k.dch == 1) {
+      if (cudaFuncSetAttribute(kmeans_round_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)k.smem) != cudaSuccess)
+        return set_cuda_error(cudaGetLastError());
+      kmeans_round_tc<1><<<grid, kThreads, k.smem, st>>>(maps, p);
+    } else {
+      if (cudaFuncSetAttribute(kmeans_round_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)k.smem) != cudaSuccess)
+        return set_cuda_error(cudaGetLastError());
+      kmeans_round_tc<2><<<grid, kThreads, k.smem, st>>>(maps, p);
+    }
+    const int rc = launch_status();
+    if (rc != NYS_OK) return rc;
+  }
+  KernelScope scope("kmeans_reduce", st);
+  kmeans_reduce<<<dim3((unsigned)k.C_pad, (unsigned)BH), s.d, 0, st>>>(
+      part, cnt, mu_old, mu_new, static_cast<__nv_bfloat16*>(mu3_next), norms_next, k.S, s.d, s.m,
+      k.C_pad);
+  return launch_status();
+}
+
+}  // namespace nys

@@ -131,8 +131,10 @@ def test_one_cluster_per_query_is_exact_attention(dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("shape", [(2, 3, 512, 64, 64, 10), (1, 2, 777, 32, 48, 4),
-                                   (1, 1, 1024, 128, 256, 6)],
-                         ids=["n512d64C64", "n777d32C48", "n1024d128C256"])
+                                   (1, 1, 1024, 128, 256, 6), (1, 2, 1000, 128, 100, 4),
+                                   (2, 2, 300, 64, 128, 5)],
+                         ids=["n512d64C64", "n777d32C48", "n1024d128C256", "n1000d128C100",
+                              "n300d64C128"])
 def test_random_inputs_give_a_valid_result(shape, dtype):
     B, H, n, d, C, iters = shape
     wl = workloads.custom(B, H, n, d, C, iters, 0, dtype)
@@ -152,3 +154,17 @@ def test_full_size_clustered_workload():
     inp = workloads.make_inputs(wl)
     out, a, mp, mu, qv, kv, vv = run_clustered(inp.q, inp.k, inp.v, 128, 10, "bf16")
     check_valid(out, a, mp, mu, qv, kv, vv, "bf16")
+
+
+@pytest.mark.parametrize("shape", [(2, 2, 1000, 64, 96, 6), (1, 2, 640, 128, 128, 3)],
+                         ids=["n1000d64C96", "n640d128C128"])
+def test_rounds_are_deterministic(shape):
+    """The members' sums are added across CTAs in a fixed order: two calls
+    give the same assignments, centroids and output, bit for bit."""
+    B, H, n, d, C, iters = shape
+    wl = workloads.custom(B, H, n, d, C, iters, 0, "bf16")
+    inp = workloads.make_inputs(wl, seed=900 + C)
+    first = run_clustered(inp.q, inp.k, inp.v, C, iters, "bf16")
+    second = run_clustered(inp.q, inp.k, inp.v, C, iters, "bf16")
+    for x, y in zip(first[:4], second[:4]):
+        assert np.array_equal(x, y)
