@@ -541,6 +541,15 @@ def next_rows(N, dev, stream):
                         f"per-channel filters, lengths {lengths}",
             "ms_per_step": ms, "tokens_per_s": B * H * n / (ms / 1e3),
             "real_tokens_per_s": H * sum(lengths) / (ms / 1e3)}
+        N.nystrom_profile_read()
+        N.nystrom_profile_enable(True)
+        for _ in range(5):
+            N.nystrom_attn_fwd_ex(q, k, v, cwc, o, B, H, n, d, m, it, ks, N.NYS_BF16,
+                                  N.NYS_CONV_PER_CHANNEL, lengths, None, 0, stream)
+        torch.cuda.synchronize()
+        N.nystrom_profile_enable(False)
+        prof = N.nystrom_profile_read()
+        out[f"variants_{name}"]["kernels_us_per_step"] = {kname: ms_ / 5 * 1e3 for kname, (ms_, _) in prof.items()}
         del q, k, v, o
         torch.cuda.empty_cache()
     # clustered attention: c4 shape, C = 128, 10 K-means rounds

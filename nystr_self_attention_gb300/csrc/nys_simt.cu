@@ -667,78 +667,157 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 // ks = 0 it only zeroes the padding rows.
 //   out[t][c] = t < L ? out[t][c] + sum_j w[j] V[t + j - (ks-1)/2][c] : 0,
 //   V rows outside [0, L) read as zero, L = the entry's length (n if none).
-// grid (ceil(n / CV_ROWS), B*H), block CV_THREADS: a CTA takes CV_ROWS
-// output rows of one head; their V rows with the halo and the head's taps
-// (tap-major, so that consecutive channels read consecutive words) are
-// staged in shared memory. A work item is CV_RUN consecutive rows of one
-// column: per tap one weight and one new V value feed CV_RUN FMAs (the V
-// window slides in registers).
-constexpr int CV_ROWS = 64, CV_THREADS = 256, CV_RUN = 8;
+// grid (ceil(n / (CV_ROWS CV_BLOCKS)), B*H), block CV_THREADS: a CTA takes
+// CV_BLOCKS consecutive blocks of CV_ROWS output rows of one head. The
+// head's taps are staged once (tap-major, so that consecutive channels read
+// consecutive words); per block, its V rows with the halo are staged in
+// shared memory by 16-byte loads, all of a thread's loads in flight before
+// its first store. A work item is CV_RUN consecutive rows of one column: the
+// V window lives in a ring of CV_RUN registers, and with the tap loop
+// unrolled in blocks of CV_RUN the ring's indices are static, so a tap costs
+// one weight, one new V value and CV_RUN FMAs.
+constexpr int CV_ROWS = 64, CV_THREADS = 256, CV_RUN = 16, CV_BLOCKS = 8;
 
-template <typename T>
+__device__ __forceinline__ void ld8(const float* p, float (&x)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+template <typename T, bool PER_CHANNEL>
 __global__ void __launch_bounds__(CV_THREADS)
 conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
-          int d, int ks, int per_channel, const int* __restrict__ lengths) {
+          int d, int ks, const int* __restrict__ lengths) {
+  constexpr bool per_channel = PER_CHANNEL;
   extern __shared__ float sm[];
   const long long bh = blockIdx.y;
   const int h = (int)(bh % H);
   const int len = lengths ? lengths[bh / H] : n;
-  const int t0 = blockIdx.x * CV_ROWS;
   const int rad = ks > 0 ? (ks - 1) / 2 : 0;
   const int vrows = CV_ROWS + 2 * rad;
   float* sv = sm;                       // [vrows][d]
   float* sw = sm + (size_t)vrows * d;   // per channel: [ks][d]; per head: [ks]
   const T* vb = v + (size_t)bh * n * d;
   T* ob = out + (size_t)bh * n * d;
-  const bool work = ks > 0 && t0 < len;
-  if (work) {
-    for (int e = threadIdx.x; e < vrows * d; e += CV_THREADS) {
-      const int u = t0 - rad + e / d, c = e % d;
-      sv[e] = (u >= 0 && u < len) ? ld(vb + (size_t)u * d + c) : 0.f;
-    }
+  const int tb0 = blockIdx.x * CV_BLOCKS * CV_ROWS;
+  if (ks > 0 && tb0 < len) {
     if (per_channel) {
-      // coalesced reads of the head's [d][ks] taps, stored tap-major
+      // the head's [d][ks] taps, read in order, stored tap-major; eight
+      // loads in flight per thread
       const float* wh = w + (size_t)h * d * ks;
-      for (int e = threadIdx.x; e < ks * d; e += CV_THREADS) {
-        const int c = e / ks, j = e % ks;
-        sw[(size_t)j * d + c] = wh[e];
+      const int total = ks * d;
+      for (int e0 = threadIdx.x; e0 < total; e0 += 8 * CV_THREADS) {
+        float t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int e = e0 + k * CV_THREADS;
+          t[k] = e < total ? __ldg(wh + e) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int e = e0 + k * CV_THREADS;
+          if (e < total) sw[(size_t)(e % ks) * d + e / ks] = t[k];
+        }
       }
     } else {
       for (int j = threadIdx.x; j < ks; j += CV_THREADS) sw[j] = w[(size_t)h * ks + j];
     }
   }
-  __syncthreads();
-  const int wstride = per_channel ? d : 0;  // word step between taps in sw
-  for (int item = threadIdx.x; item < (CV_ROWS / CV_RUN) * d; item += CV_THREADS) {
-    const int c = item % d, r0 = (item / d) * CV_RUN;
-    if (t0 + r0 >= n) continue;
-    float acc[CV_RUN];
-#pragma unroll
-    for (int r = 0; r < CV_RUN; ++r) acc[r] = 0.f;
+  const int wstride = per_channel ? d : 1;  // word step between taps in sw
+  const int d8 = d / 8;                     // d is a multiple of 8
+  const int ks_full = ks - ks % CV_RUN;     // taps in whole blocks of CV_RUN
+  for (int blk = 0; blk < CV_BLOCKS; ++blk) {
+    const int t0 = tb0 + blk * CV_ROWS;
+    if (t0 >= n) break;  // uniform across the CTA
+    const bool work = ks > 0 && t0 < len;
+    __syncthreads();  // the previous block's readers of sv are done (and the taps are staged)
     if (work) {
-      // window: V rows (r0 + j + r), r < CV_RUN, relative to the staged block
-      const float* x = sv + (size_t)r0 * d + c;
-      const float* wc = sw + (per_channel ? c : 0);
-      float xw[CV_RUN];
+      constexpr int kPer = 8;  // 16-byte loads in flight per thread
+      for (int e0 = threadIdx.x; e0 < vrows * d8; e0 += kPer * CV_THREADS) {
+        float x[kPer][8];
 #pragma unroll
-      for (int r = 0; r < CV_RUN; ++r) xw[r] = x[(size_t)r * d];
-#pragma unroll 4
-      for (int j = 0; j < ks; ++j) {
-        const float wj = wc[(size_t)j * wstride + (per_channel ? 0 : j)];
+        for (int k = 0; k < kPer; ++k) {
+          const int e = e0 + k * CV_THREADS;
+          const int u = t0 - rad + e / d8, c = (e % d8) * 8;
+          if (e < vrows * d8 && u >= 0 && u < len) {
+            ld8(vb + (size_t)u * d + c, x[k]);
+          } else {
 #pragma unroll
-        for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[r], acc[r]);
+            for (int q = 0; q < 8; ++q) x[k][q] = 0.f;
+          }
+        }
 #pragma unroll
-        for (int r = 0; r + 1 < CV_RUN; ++r) xw[r] = xw[r + 1];
-        // row r0 + j + CV_RUN: within the staged rows for every j < ks - 1
-        xw[CV_RUN - 1] = j + 1 < ks ? x[(size_t)(j + CV_RUN) * d] : 0.f;
+        for (int k = 0; k < kPer; ++k) {
+          const int e = e0 + k * CV_THREADS;
+          if (e < vrows * d8) {
+            float* dst = sv + (size_t)(e / d8) * d + (e % d8) * 8;
+            *reinterpret_cast<float4*>(dst) = make_float4(x[k][0], x[k][1], x[k][2], x[k][3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(x[k][4], x[k][5], x[k][6], x[k][7]);
+          }
+        }
       }
     }
+    __syncthreads();
+    for (int item = threadIdx.x; item < (CV_ROWS / CV_RUN) * d; item += CV_THREADS) {
+      const int c = item % d, r0 = (item / d) * CV_RUN;
+      if (t0 + r0 >= n) continue;
+      // the attention term already in out: all of the run's loads issued
+      // before the taps, so their latency hides behind the FMAs (stored
+      // rows could alias later loads, so loads after a store would wait)
+      float acc[CV_RUN];
 #pragma unroll
-    for (int r = 0; r < CV_RUN; ++r) {
-      const int t = t0 + r0 + r;
-      if (t >= n) break;
-      T* o = ob + (size_t)t * d + c;
-      st(o, t < len ? ld(o) + acc[r] : 0.f);
+      for (int r = 0; r < CV_RUN; ++r) {
+        const int t = t0 + r0 + r;
+        acc[r] = (t < n && t < len) ? ld(ob + (size_t)t * d + c) : 0.f;
+      }
+      if (work) {
+        // ring: before tap j, V row (r0 + j + r) of the staged block sits in
+        // xw[(j + r) % CV_RUN]; after it, the slot of row r0 + j takes row
+        // r0 + j + CV_RUN (staged for every j < ks - 1)
+        const float* x = sv + (size_t)r0 * d + c;
+        const float* wp = sw + (per_channel ? c : 0);  // tap j of this channel: wp[j * wstride]
+        const float* xp = x + (size_t)CV_RUN * d;      // row r0 + j + CV_RUN: xp[j * d]
+        float xw[CV_RUN];
+#pragma unroll
+        for (int r = 0; r < CV_RUN; ++r) xw[r] = x[(size_t)r * d];
+        // whole blocks: no tap past ks, and (ks odd, CV_RUN even) never the
+        // last tap, so every next row is inside the staged block
+        for (int jb = 0; jb < ks_full; jb += CV_RUN) {
+#pragma unroll
+          for (int jj = 0; jj < CV_RUN; ++jj) {
+            const float wj = wp[jj * wstride];
+#pragma unroll
+            for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[(jj + r) % CV_RUN], acc[r]);
+            xw[jj] = xp[jj * d];
+          }
+          wp += CV_RUN * wstride;
+          xp += CV_RUN * d;
+        }
+        // the last ks % CV_RUN taps
+#pragma unroll
+        for (int jj = 0; jj < CV_RUN; ++jj) {
+          const int j = ks_full + jj;
+          if (j >= ks) break;
+          const float wj = wp[jj * wstride];
+#pragma unroll
+          for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[(jj + r) % CV_RUN], acc[r]);
+          if (j + 1 < ks) xw[jj] = xp[jj * d];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < CV_RUN; ++r) {
+        const int t = t0 + r0 + r;
+        if (t >= n) break;
+        st(ob + (size_t)t * d + c, t < len ? acc[r] : 0.f);
+      }
     }
   }
 }
@@ -751,13 +830,21 @@ int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, c
                                                   (size_t)s.ks * (per_channel ? s.d : 1))
                                : 0;
   if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(conv_mask<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
+      (cudaFuncSetAttribute(conv_mask<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+           cudaSuccess ||
+       cudaFuncSetAttribute(conv_mask<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+           cudaSuccess))
     return set_cuda_error(cudaGetLastError());
   KernelScope ks_("conv_mask", stream);
-  conv_mask<T><<<dim3((s.n + CV_ROWS - 1) / CV_ROWS, (unsigned)s.bh()), CV_THREADS, smem, stream>>>(
-      static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d,
-      s.ks, per_channel ? 1 : 0, s.lengths);
+  const dim3 grid((s.n + CV_ROWS * CV_BLOCKS - 1) / (CV_ROWS * CV_BLOCKS), (unsigned)s.bh());
+  if (per_channel)
+    conv_mask<T, true><<<grid, CV_THREADS, smem, stream>>>(
+        static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
+        s.lengths);
+  else
+    conv_mask<T, false><<<grid, CV_THREADS, smem, stream>>>(
+        static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
+        s.lengths);
   return launch_status();
 }
 
