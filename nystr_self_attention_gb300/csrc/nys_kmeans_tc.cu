@@ -15,10 +15,13 @@
 // round is deterministic), divides by the counts (an empty cluster keeps its
 // centroid), and prepares the next round's bf16 split and squared norms.
 //
-// 128 threads: thread = query row of the tile (TMEM lane) in the assignment
-// epilogue, = cluster row in the update epilogue; thread 0 issues the TMA
-// copies and the MMAs. The Q tile is double-buffered: the next tile's copy
-// starts once the update product of the tile before has read its buffer.
+// Four worker warps (thread = query row of the tile, a TMEM lane, in the
+// assignment; = cluster row for the members' sums) and an issuer warp whose
+// lane 0 issues the TMA copies and the MMAs, driven by the workers' mbarrier
+// arrivals. One CTA per SM. The Q tiles go through a ring of three buffers,
+// and the next tile's scores are issued as soon as every worker has read
+// this tile's, so the tensor cores work while the workers take the argmin
+// and build the one-hot tile.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word
 // and the CTA winds down (copies and products in flight awaited, TMEM
 // freed).
@@ -37,8 +40,9 @@ namespace {
 using namespace sm100;
 
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr int kThreads = 128;
+constexpr int kThreads = 160;  // four worker warps and the issuer warp
 constexpr uint32_t kColS = 0, kColU = 128;  // TMEM: scores (C_pad columns), members' sums (d columns)
+constexpr int kNQ = 3;                      // Q tile buffers
 
 struct KmMaps {
   CUtensorMap q;    // bf16 [B*H][n][d], box 64 x 128
@@ -56,7 +60,8 @@ struct KmParams {
 };
 
 struct KmBars {
-  uint64_t mu, q[2], asg, upd, fin;
+  uint64_t mu, q[kNQ], asg, upd, fin;
+  uint64_t rd, ready;  // workers: a tile's scores read; its one-hot tile written
 };
 
 __device__ __forceinline__ bool km_wait(uint64_t* bar, uint32_t parity, int* status,
@@ -77,15 +82,16 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* mus = sm + p.off_mu;  // [3][DCH] boxes of C_pad rows x 128 B
-  uint8_t* qb = sm + p.off_q;    // [2][DCH] boxes of 128 rows x 128 B
+  uint8_t* qb = sm + p.off_q;    // [kNQ][DCH] boxes of 128 rows x 128 B
   uint8_t* oh = sm + p.off_oh;   // one-hot^T: [2] boxes of 128 cluster rows x 64 queries (bf16)
   __shared__ KmBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float norm_s[128];
+  __shared__ __align__(16) float norm_s[128];  // |mu_c|^2; +inf for c >= C (never the argmin)
   __shared__ int cnt_s[128];
   volatile int* abort_flag = &abort_sh;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool worker = warp < 4;
   const int s = blockIdx.x;
   const long long bh = blockIdx.y;
   const int t0 = s * p.tiles_per_cta;
@@ -95,17 +101,20 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
 
   if (tid == 0) {
     mbar_init(&bars.mu, 1);
-    mbar_init(&bars.q[0], 1);
-    mbar_init(&bars.q[1], 1);
+    for (int r = 0; r < kNQ; ++r) mbar_init(&bars.q[r], 1);
     mbar_init(&bars.asg, 1);
     mbar_init(&bars.upd, 1);
+    mbar_init(&bars.rd, 128);
+    mbar_init(&bars.ready, 128);
     mbar_init(&bars.fin, 1);
     abort_sh = 0;
     fence_barrier_init();
   }
-  norm_s[tid] = tid < p.C_pad ? p.norms[bh * p.C_pad + tid] : 0.f;
-  cnt_s[tid] = 0;
-  // the one-hot tile starts all zero; each thread later clears only its own 1
+  if (worker) {
+    norm_s[tid] = tid < p.C ? p.norms[bh * p.C_pad + tid] : INFINITY;
+    cnt_s[tid] = 0;
+  }
+  // the one-hot tile starts all zero; each worker later clears only its own 1
   for (int e = tid; e < 2 * 128 * 128 / 16; e += kThreads)
     reinterpret_cast<uint4*>(oh)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_async_smem();
@@ -114,138 +123,171 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
 
-  uint32_t n_mu = 0, n_q[2] = {0, 0};  // copies issued (thread 0)
-  if (tid == 0 && ntiles > 0) {
-    tma_prefetch(&maps.q);
-    tma_prefetch(&maps.mu3);
-    mbar_arrive_expect_tx(&bars.mu, 3u * DCH * mu_box);
-    for (int k = 0; k < 3; ++k)
-      for (int c = 0; c < DCH; ++c)
-        tma_load_3d(mus + (k * DCH + c) * mu_box, &maps.mu3, &bars.mu, 64 * c, 0, (int)(bh * 3 + k));
-    n_mu = 1;
-    mbar_arrive_expect_tx(&bars.q[0], q_bytes);
-    for (int c = 0; c < DCH; ++c) tma_load_3d(qb + c * 16384, &maps.q, &bars.q[0], 64 * c, t0 * 128, (int)bh);
-    n_q[0] = 1;
-  }
-  const uint32_t id_s = idesc_bf16(128, p.C_pad, false, false);
-  const uint32_t id_u = idesc_bf16(128, 64 * DCH, false, true);
-  int prev_a = -1;  // where this thread's query put its 1 in the one-hot tile
-  for (int j = 0; j < ntiles; ++j) {
-    const int b = j & 1, tile = t0 + j;
-    if (tid == 0 && !*abort_flag) {
-      bool ok = true;
-      // the next tile's Q into the other buffer, once the members' product
-      // of tile j-1 has read that buffer
-      if (j + 1 < ntiles) {
-        if (j >= 1) ok = km_wait(&bars.upd, (j - 1) & 1, p.status, abort_flag);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars.q[b ^ 1], q_bytes);
-          for (int c = 0; c < DCH; ++c)
-            tma_load_3d(qb + ((b ^ 1) * DCH + c) * 16384, &maps.q, &bars.q[b ^ 1], 64 * c, (tile + 1) * 128,
-                        (int)bh);
-          ++n_q[b ^ 1];
-        }
-      }
-      if (ok && j == 0) ok = km_wait(&bars.mu, 0, p.status, abort_flag);
-      if (ok) ok = km_wait(&bars.q[b], (n_q[b] - 1) & 1, p.status, abort_flag);
-      if (ok) {
+  if (warp == 4) {
+    // ---------------------------------------------- issuer: copies, products
+    if (lane == 0 && ntiles > 0) {
+      uint32_t n_mu = 0, n_q[kNQ] = {};  // copies issued per buffer
+      const uint32_t id_s = idesc_bf16(128, p.C_pad, false, false);
+      const uint32_t id_u = idesc_bf16(128, 64 * DCH, false, true);
+      auto load_q = [&](int jt) {  // tile t0 + jt into buffer jt % kNQ
+        const int r = jt % kNQ;
+        mbar_arrive_expect_tx(&bars.q[r], q_bytes);
+        for (int c = 0; c < DCH; ++c)
+          tma_load_3d(qb + (r * DCH + c) * 16384, &maps.q, &bars.q[r], 64 * c, (t0 + jt) * 128, (int)bh);
+        ++n_q[r];
+      };
+      // scores of tile jt: Q mu^T as Q mu_hi^T + Q mu_mid^T + Q mu_lo^T
+      auto scores = [&](int jt) -> bool {
+        const int r = jt % kNQ;
+        if (!km_wait(&bars.q[r], (n_q[r] - 1) & 1, p.status, abort_flag)) return false;
         tc_fence_after_sync();
-        // scores: Q mu^T as Q mu_hi^T + Q mu_mid^T + Q mu_lo^T
         for (int k = 0; k < 3; ++k)
           for (int kk = 0; kk < 4 * DCH; ++kk) {
-            const uint64_t a = smem_desc(smem_u32(qb + (b * DCH + (kk >> 2)) * 16384), 16, 1024, SW_128B);
+            const uint64_t a = smem_desc(smem_u32(qb + (r * DCH + (kk >> 2)) * 16384), 16, 1024, SW_128B);
             const uint64_t bd = smem_desc(smem_u32(mus + (k * DCH + (kk >> 2)) * mu_box), 16, 1024, SW_128B);
             mma_bf16(tmem + kColS, a + (uint64_t)((kk & 3) * 2), bd + (uint64_t)((kk & 3) * 2), id_s,
                      (k > 0 || kk > 0) ? 1u : 0u);
           }
         mma_commit(&bars.asg);
+        return true;
+      };
+      tma_prefetch(&maps.q);
+      tma_prefetch(&maps.mu3);
+      mbar_arrive_expect_tx(&bars.mu, 3u * DCH * mu_box);
+      for (int k = 0; k < 3; ++k)
+        for (int c = 0; c < DCH; ++c)
+          tma_load_3d(mus + (k * DCH + c) * mu_box, &maps.mu3, &bars.mu, 64 * c, 0, (int)(bh * 3 + k));
+      n_mu = 1;
+      for (int jt = 0; jt < kNQ - 1 && jt < ntiles; ++jt) load_q(jt);
+      bool ok = km_wait(&bars.mu, 0, p.status, abort_flag) && scores(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        // tile j + 1's scores once every worker has read tile j's
+        ok = km_wait(&bars.rd, j & 1, p.status, abort_flag);
+        if (ok && j + 1 < ntiles) ok = scores(j + 1);
+        // tile j's members' product once its one-hot tile is written (the
+        // workers waited for tile j - 1's product before writing it)
+        if (ok) ok = km_wait(&bars.ready, j & 1, p.status, abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int r = j % kNQ;
+        const uint64_t q0 = smem_desc(smem_u32(qb + r * DCH * 16384), 16384, 1024, SW_128B);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc(smem_u32(oh + (kk >> 2) * 16384), 16, 1024, SW_128B);
+          mma_bf16(tmem + kColU, a + (uint64_t)((kk & 3) * 2), q0 + (uint64_t)(kk * 128), id_u,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars.upd);
+        // tile j + 2 into the buffer of tile j - 1, whose product is done
+        if (j + kNQ - 1 < ntiles) load_q(j + kNQ - 1);
+      }
+      if (*abort_flag) {
+        // no copy of this CTA may still be in flight
+        if (n_mu) mbar_wait(&bars.mu, 0, nullptr, kWaitNs);
+        for (int r = 0; r < kNQ; ++r)
+          if (n_q[r]) mbar_wait(&bars.q[r], (n_q[r] - 1) & 1, nullptr, kWaitNs);
       }
     }
-    // assignment: nearest centroid of this thread's query
-    bool ok = km_wait(&bars.asg, j & 1, p.status, abort_flag);
-    const bool go = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-wide
-    tc_fence_after_sync();
-    float best = INFINITY;
-    int best_c = 0;
-    if (go) {
-      for (int c0 = 0; c0 < p.C_pad; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lo + kColS + c0, v);
-        tmem_ld_wait();
+    __syncwarp();
+  } else {
+    // ----------------------------------------- workers: thread = query row
+    const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+    int prev_a = -1;  // where this thread's query put its 1 in the one-hot tile
+    for (int j = 0; j < ntiles; ++j) {
+      const int tile = t0 + j;
+      // assignment: nearest centroid of this thread's query
+      const bool ok = km_wait(&bars.asg, j & 1, p.status, abort_flag);
+      const bool go = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-wide
+      tc_fence_after_sync();
+      // four independent running minima (column c in chain c % 4) over the
+      // 128 score columns, loaded at once (columns C_pad and up are inside
+      // the score region, and the +inf norms past C keep them out);
+      // strict < keeps a chain's lowest index among equal scores, and the
+      // chains combine by (score, index)
+      float bv[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+      int bc[4] = {0, 0, 0, 0};
+      if (go) {
+        uint32_t v[4][32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = c0 + e;
-          if (c < p.C) {
-            const float score = fmaf(-2.f, __uint_as_float(v[e]), norm_s[c]);
-            if (score < best) {  // strict: a tie keeps the lower index
-              best = score;
-              best_c = c;
+        for (int h = 0; h < 4; ++h) tmem_ld32(tmem + lo + kColS + 32 * h, v[h]);
+        tmem_ld_wait();
+        const float4* n4 = reinterpret_cast<const float4*>(norm_s);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 nr = n4[(32 * h + e) >> 2];
+            const float nn[4] = {nr.x, nr.y, nr.z, nr.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float score = fmaf(-2.f, __uint_as_float(v[h][e + k]), nn[k]);
+              if (score < bv[k]) {
+                bv[k] = score;
+                bc[k] = 32 * h + e + k;
+              }
             }
           }
         }
       }
-    }
-    const int i = tile * 128 + tid;
-    const bool valid = go && i < p.n;
-    if (valid) {
-      p.assign[bh * p.n + i] = best_c;
-      atomicAdd(&cnt_s[best_c], 1);
-    }
-    // one-hot^T for the members' product: this thread's column, once the
-    // product of tile j-1 has read the tile
-    if (j >= 1) km_wait(&bars.upd, (j - 1) & 1, p.status, abort_flag);
-    uint8_t* ohb = oh + (tid >> 6) * 16384;
-    if (prev_a >= 0) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(prev_a, (tid & 63) * 2)) = 0;
-    prev_a = valid ? best_c : -1;
-    if (valid) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(best_c, (tid & 63) * 2)) = 0x3F80;  // bf16 1
-    fence_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0 && !*abort_flag) {
-      tc_fence_after_sync();
-      // members' sums += onehot^T (clusters x 128 queries) Q (128 queries x d)
-      const uint64_t q0 = smem_desc(smem_u32(qb + b * DCH * 16384), 16384, 1024, SW_128B);
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t a = smem_desc(smem_u32(oh + (kk >> 2) * 16384), 16, 1024, SW_128B);
-        mma_bf16(tmem + kColU, a + (uint64_t)((kk & 3) * 2), q0 + (uint64_t)(kk * 128), id_u,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+      float best = bv[0];
+      int best_c = bc[0];
+#pragma unroll
+      for (int k = 1; k < 4; ++k)
+        if (bv[k] < best || (bv[k] == best && bc[k] < best_c)) {
+          best = bv[k];
+          best_c = bc[k];
+        }
+      tc_fence_before_sync();
+      mbar_arrive(&bars.rd);  // the scores of tile j are read
+      const int i = tile * 128 + tid;
+      const bool valid = go && i < p.n;
+      if (valid) {
+        p.assign[bh * p.n + i] = best_c;
+        atomicAdd(&cnt_s[best_c], 1);
       }
-      mma_commit(&bars.upd);
+      // one-hot^T for the members' product: this thread's column, once the
+      // product of tile j-1 has read the tile
+      if (j >= 1) km_wait(&bars.upd, (j - 1) & 1, p.status, abort_flag);
+      uint8_t* ohb = oh + (tid >> 6) * 16384;
+      if (prev_a >= 0) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(prev_a, (tid & 63) * 2)) = 0;
+      prev_a = valid ? best_c : -1;
+      if (valid) *reinterpret_cast<uint16_t*>(ohb + sw128_offset(best_c, (tid & 63) * 2)) = 0x3F80;  // bf16 1
+      fence_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(&bars.ready);
     }
+    // the last members' product done
+    if (ntiles > 0) km_wait(&bars.upd, (ntiles - 1) & 1, p.status, abort_flag);
   }
+  tc_fence_before_sync();
+  __syncthreads();  // counts complete; the members' sums in TMEM
+  tc_fence_after_sync();
 
   // this CTA's members' sums and counts; thread = cluster row
-  bool ok = true;
-  if (ntiles > 0) ok = km_wait(&bars.upd, (ntiles - 1) & 1, p.status, abort_flag);
-  const bool go = __all_sync(0xffffffffu, ok) && ntiles > 0;
-  tc_fence_after_sync();
-  float* prow = p.part + (((size_t)bh * p.S + s) * p.C_pad + (tid < p.C_pad ? tid : 0)) * p.d;
-  for (int c0 = 0; c0 < p.d; c0 += 32) {
-    uint32_t v[32];
-    if (go) {
-      tmem_ld32(tmem + lo + kColU + c0, v);
-      tmem_ld_wait();
-    } else {
+  if (worker) {
+    const uint32_t lo = static_cast<uint32_t>(warp * 32) << 16;
+    const bool go = __all_sync(0xffffffffu, !*abort_flag) && ntiles > 0;
+    float* prow = p.part + (((size_t)bh * p.S + s) * p.C_pad + (tid < p.C_pad ? tid : 0)) * p.d;
+    for (int c0 = 0; c0 < p.d; c0 += 32) {
+      uint32_t v[32];
+      if (go) {
+        tmem_ld32(tmem + lo + kColU + c0, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = 0u;
-    }
-    if (tid < p.C_pad) {
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      if (tid < p.C_pad) {
 #pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<uint4*>(prow + c0 + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<uint4*>(prow + c0 + e) = make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
     }
+    if (tid < p.C_pad) p.cnt[((size_t)bh * p.S + s) * p.C_pad + tid] = cnt_s[tid];
   }
-  if (tid < p.C_pad) p.cnt[((size_t)bh * p.S + s) * p.C_pad + tid] = cnt_s[tid];
 
-  // wind-down: no copy or product of this CTA may still be in flight
-  if (tid == 0) {
-    if (*abort_flag) {
-      if (n_mu) mbar_wait(&bars.mu, 0, nullptr, kWaitNs);
-      for (int r = 0; r < 2; ++r)
-        if (n_q[r]) mbar_wait(&bars.q[r], (n_q[r] - 1) & 1, nullptr, kWaitNs);
-    }
+  // wind-down: no product of this CTA may still be in flight
+  if (warp == 4 && lane == 0) {
     mma_commit(&bars.fin);
     mbar_wait(&bars.fin, 0, nullptr, kWaitNs);
   }
@@ -314,16 +356,17 @@ KmPlan km_plan(const Shape& s) {
   k.dch = s.d / 64;
   k.C_pad = (s.m + 15) & ~15;
   k.T_h = (s.n + 127) / 128;
-  // about two CTAs per SM over all heads, whole tiles per CTA
-  const int bh = (int)s.bh();
-  const int want = std::max(1, (2 * plan_sms() + bh - 1) / bh);
+  // one CTA per SM (the shared-memory request below keeps it so), at most
+  // one wave: floor(SMs / heads) CTAs per head, whole tiles each
+  const int bh = (int)std::min<long long>(s.bh(), 1 << 30);
+  const int want = std::max(1, plan_sms() / bh);
   k.tpc = std::max(1, (k.T_h + want - 1) / want);
   k.S = (k.T_h + k.tpc - 1) / k.tpc;
   k.off_mu = 0;
   k.off_q = k.off_mu + 3u * k.dch * k.C_pad * 128u;
-  k.off_oh = k.off_q + 2u * k.dch * 16384u;
-  // at least 80 KB, so that at most two CTAs (2 x 256 TMEM columns) share an SM
-  k.smem = std::max<size_t>((size_t)k.off_oh + 2 * 16384 + 1024, 80 * 1024);
+  k.off_oh = k.off_q + (uint32_t)kNQ * k.dch * 16384u;
+  // more than half an SM's shared memory, so that one CTA (256 TMEM columns) holds an SM
+  k.smem = std::max<size_t>((size_t)k.off_oh + 2 * 16384 + 1024, 116 * 1024);
   return k;
 }
 
@@ -331,7 +374,8 @@ KmPlan km_plan(const Shape& s) {
 
 bool kmeans_tc_supported(const Shape& s) {
   if (s.dtype != NYS_BF16 || (s.d != 64 && s.d != 128) || s.m < 1 || s.m > 128) return false;
-  return km_plan(s).smem <= 227 * 1024;
+  // dynamic shared memory, leaving room for the kernel's static part
+  return km_plan(s).smem <= 225 * 1024;
 }
 
 KmWorkspace kmeans_tc_workspace(const Shape& s) {
