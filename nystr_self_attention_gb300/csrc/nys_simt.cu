@@ -443,9 +443,51 @@ __device__ void block_gemm(const float* A, int lda, const float* Bm, int ldb, bo
   __syncthreads();
 }
 
+// C = diag * I + alpha * A B for m x m matrices (m <= 64) held in shared
+// memory with row pitch kResPitch, zero past m (and C kept so: the diagonal
+// term only inside m). 256 threads, a 4 x 4 block of C each; the products
+// run from shared memory without a barrier per step. C must not alias A or B.
+constexpr int kResPitch = 68, kResM = 64;
+constexpr int kCoefMax = 4096;  // split weights kept in shared memory: splits * m at most
+
+__device__ void smem_gemm64(const float* A, const float* B, float* C, int m, float alpha, float diag) {
+  const int tid = threadIdx.x, tr = tid >> 4, tc = tid & 15;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k = 0; k < m; ++k) {
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = A[(4 * tr + i) * kResPitch + k];
+    const float4 b = *reinterpret_cast<const float4*>(B + k * kResPitch + 4 * tc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[i][0] = fmaf(a[i], b.x, acc[i][0]);
+      acc[i][1] = fmaf(a[i], b.y, acc[i][1]);
+      acc[i][2] = fmaf(a[i], b.z, acc[i][2]);
+      acc[i][3] = fmaf(a[i], b.w, acc[i][3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * tr + i;
+    float4 o;
+    o.x = alpha * acc[i][0] + (r == 4 * tc && r < m ? diag : 0.f);
+    o.y = alpha * acc[i][1] + (r == 4 * tc + 1 && r < m ? diag : 0.f);
+    o.z = alpha * acc[i][2] + (r == 4 * tc + 2 && r < m ? diag : 0.f);
+    o.w = alpha * acc[i][3] + (r == 4 * tc + 3 && r < m ? diag : 0.f);
+    *reinterpret_cast<float4*>(C + r * kResPitch + 4 * tc) = o;
+  }
+  __syncthreads();
+}
+
 // grid (B*H), block 256. Everything for one head: merge the key-split
-// partials into G, form A_S, run the iteration, write W = Z G.
-__global__ void __launch_bounds__(256)
+// partials into G, form A_S, run the iteration, write W = Z G. For m <= 64
+// the iteration runs on matrices resident in shared memory (dynamic, five
+// 64 x 64 blocks); larger m streams them through the head's workspace.
+__global__ void __launch_bounds__(256, 1)
 pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
           const float* __restrict__ gpart, const float* __restrict__ gml, float* __restrict__ g_all,
           float* __restrict__ a_all, float* __restrict__ z_all, float* __restrict__ w_all,
@@ -453,6 +495,7 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
           int splits, int iters, float scale, int m64, int dpad) {
   __shared__ float smem[2 * GK * GP];
   __shared__ float red[2][8];
+  extern __shared__ float dsm[];  // m <= 64: A_S, Z, X, U, T resident
   const long long bh = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t md = (size_t)m * d, mm = (size_t)m * m;
@@ -467,6 +510,38 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
   float* V = U + mm;
 
   // 1) G = merge over splits of (O_s, max_s, sum_s)
+  if (m <= kResM && splits * m <= kCoefMax) {  // uniform
+    // each row's split weights f_s / den once, in shared memory after the
+    // resident matrices; then every element is a weighted sum (an empty
+    // partial, max -inf, has weight 0 and its rows are never read)
+    float* coef = dsm + 5 * kResM * kResPitch;  // [splits][m]
+    for (int i = tid; i < m; i += 256) {
+      const float2* ml = reinterpret_cast<const float2*>(gml) + (size_t)bh * splits * m + i;
+      float mx = -INFINITY;
+      for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ml[(size_t)s * m].x);
+      float den = 0.f;
+      for (int s = 0; s < splits; ++s) {
+        const float2 v = ml[(size_t)s * m];
+        const float f = v.x == -INFINITY ? 0.f : expf(v.x - mx);
+        den += v.y * f;
+        coef[s * m + i] = f;
+      }
+      const float inv = 1.f / den;
+      for (int s = 0; s < splits; ++s) coef[s * m + i] *= inv;
+    }
+    __syncthreads();
+    for (size_t e = tid; e < md; e += 256) {
+      const int i = (int)(e / d), c = (int)(e % d);
+      const float* gp = gpart + ((size_t)bh * splits * m + i) * d + c;
+      float num = 0.f;
+#pragma unroll 4
+      for (int s = 0; s < splits; ++s) {
+        const float w = coef[s * m + i];
+        if (w != 0.f) num = fmaf(w, gp[(size_t)s * m * d], num);
+      }
+      g[e] = num;
+    }
+  } else
   for (size_t e = tid; e < md; e += 256) {
     const int i = (int)(e / d);
     float mx = -INFINITY;
@@ -499,6 +574,59 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
   }
   __syncthreads();
   // 3) Z_0 = A^T / (max column abs-sum * max row abs-sum)
+  if (m <= kResM) {
+    // A_S resident in shared memory from here on; the norms and Z_0 from it
+    float* sA = dsm;
+    float* zc = sA + kResM * kResPitch;      // Z
+    float* zt = sA + 4 * kResM * kResPitch;  // T, then the next Z
+    float* sX = sA + 2 * kResM * kResPitch;
+    float* sU = sA + 3 * kResM * kResPitch;
+    for (int e = tid; e < kResM * kResM; e += 256) {
+      const int i = e / kResM, j = e % kResM;
+      sA[i * kResPitch + j] = (i < m && j < m) ? A[(size_t)i * m + j] : 0.f;
+    }
+    __syncthreads();
+    // thread j < m: column j's and row j's abs-sums, in index order
+    float cs = 0.f, rs = 0.f;
+    if (tid < m)
+      for (int i = 0; i < m; ++i) {
+        cs += fabsf(sA[i * kResPitch + tid]);
+        rs += fabsf(sA[tid * kResPitch + i]);
+      }
+    float cm = warp_max(cs), rm = warp_max(rs);
+    if (lane == 0) { red[0][warp] = cm; red[1][warp] = rm; }
+    __syncthreads();
+    if (tid == 0) {
+      float c = 0.f, r = 0.f;
+      for (int w = 0; w < 8; ++w) { c = fmaxf(c, red[0][w]); r = fmaxf(r, red[1][w]); }
+      red[0][0] = 1.f / (c * r);
+    }
+    __syncthreads();
+    const float alpha = red[0][0];
+    for (int e = tid; e < kResM * kResM; e += 256) {
+      const int i = e / kResM, j = e % kResM;
+      zc[i * kResPitch + j] = sA[j * kResPitch + i] * alpha;
+    }
+    __syncthreads();
+    // 4) Z <- 1/4 Z (13I - X (15I - X (7I - X))), X = A Z, in shared memory
+    for (int it = 0; it < iters; ++it) {
+      smem_gemm64(sA, zc, sX, m, 1.f, 0.f);  // X = A Z
+      for (int e = tid; e < kResM * kResM; e += 256) {  // U = 7I - X
+        const int i = e / kResM, j = e % kResM;
+        sU[i * kResPitch + j] = (i == j && i < m ? 7.f : 0.f) - sX[i * kResPitch + j];
+      }
+      __syncthreads();
+      smem_gemm64(sX, sU, zt, m, -1.f, 15.f);      // T = 15I - X U
+      smem_gemm64(sX, zt, sU, m, -1.f, 13.f);      // U = 13I - X T
+      smem_gemm64(zc, sU, zt, m, 0.25f, 0.f);      // Z' = Z U / 4
+      float* t = zc;
+      zc = zt;
+      zt = t;
+    }
+    for (int e = tid; e < m * m; e += 256) Z[e] = zc[(e / m) * kResPitch + (e % m)];
+    __syncthreads();
+  }
+  if (m > kResM) {  // uniform
   float cmax = 0.f, rmax = 0.f;
   for (int j = tid; j < m; j += 256) {
     float cs = 0.f, rs = 0.f;
@@ -525,10 +653,11 @@ pinv_simt(const float* __restrict__ qt_all, const float* __restrict__ kt_all,
     Z[e] = A[(size_t)j * m + i] * alpha0;
   }
   __syncthreads();
-  // 4) Z <- 1/4 Z (13I - X (15I - X (7I - X))), X = A Z
+  }
+  // 4) (m > 64) Z <- 1/4 Z (13I - X (15I - X (7I - X))), X = A Z, through the workspace
   float* zc = Z;
   float* zn = V;
-  for (int it = 0; it < iters; ++it) {
+  for (int it = 0; m > kResM && it < iters; ++it) {
     block_gemm(A, m, zc, m, false, X, m, m, m, m, 1.f, 0.f, smem);            // X = A Z
     for (size_t e = tid; e < mm; e += 256)                                       // U = 7I - X
       U[e] = ((e / m) == (e % m) ? 7.f : 0.f) - X[e];
@@ -932,8 +1061,12 @@ int launch_rows_simt(const Shape& s, const float* qt, const void* k, const void*
 int launch_pinv_simt(const Shape& s, const float* qt, const float* kt, const float* gp,
                      const float* gml, float* g, float* a, float* z, float* w, float* scratch,
                      __nv_bfloat16* wt_b, int splits, cudaStream_t stream) {
+  const size_t dsmem = s.m <= kResM ? sizeof(float) * (5 * kResM * kResPitch + kCoefMax) : 0;
+  if (dsmem > 48 * 1024 &&
+      cudaFuncSetAttribute(pinv_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsmem) != cudaSuccess)
+    return set_cuda_error(cudaGetLastError());
   KernelScope ks_("pinv_simt", stream);
-  pinv_simt<<<(unsigned)s.bh(), 256, 0, stream>>>(qt, kt, gp, gml, g, a, z, w, scratch, wt_b, s.d,
+  pinv_simt<<<(unsigned)s.bh(), 256, dsmem, stream>>>(qt, kt, gp, gml, g, a, z, w, scratch, wt_b, s.d,
                                                   s.m, splits, s.iters,
                                                   1.0f / sqrtf((float)s.d), s.m64(), s.dpad());
   return launch_status();
