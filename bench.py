@@ -258,8 +258,10 @@ def run_reference(args, wl):
 # (T = B*H*n*d elements, e = element bytes), or algorithmic flops.
 KERNEL_BYTES = {
     "landmarks_vec": 2.0, "landmarks_small": 2.0, "landmarks_simt": 2.0,  # read Q, K
-    "rows_tc": 2.0, "rows_simt": 2.0,             # read K, V
+    "rows_tc": 2.0, "rows_simt": 2.0, "rows_x3": 2.0,  # read K, V
     "tokens_tc": 3.0, "tokens_simt": 3.0, "tokens_big": 3.0,  # read Q, V; write out
+    "tokens_x3": 2.0,                             # read Q; write out (attention term)
+    "conv_mask": 3.0,                             # read V, out; write out
 }
 KERNEL_SOURCES = {
     "landmarks_vec": "nys_simt.cu", "landmarks_small": "nys_simt.cu",
@@ -267,6 +269,7 @@ KERNEL_SOURCES = {
     "pinv_simt": "nys_simt.cu", "tokens_simt": "nys_simt.cu", "rows_tc": "nys_rows_tc.cu",
     "pinv_tc": "nys_pinv_tc.cu", "tokens_tc": "nys_tokens_tc.cu", "pinv_big": "nys_pinv_big.cu",
     "tokens_big": "nys_tokens_big.cu", "w_tc": "nys_pinv_tc.cu", "merge_g": "nys_simt.cu",
+    "rows_x3": "nys_x3.cu", "tokens_x3": "nys_x3.cu", "conv_mask": "nys_simt.cu",
 }
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates
 
@@ -282,9 +285,12 @@ def pinv_peak_time(wl, bf16_tflops, with_w=True):
     """Seconds the pseudo-inverse kernel's flops take at the tensor peaks of
     the types they run in: the scores and W = Z G in tf32; the update
     products in tf32 for m <= 128 and with fp16 operands (the bf16/fp16 rate)
-    for m > 128."""
+    for m > 128. fp32 inputs: three tf32 products per product (a third of
+    the tf32 rate)."""
     m, d = wl.m, wl.d
     tf32 = bf16_tflops * TF32_OVER_BF16 * 1e12
+    if wl.dtype == "f32":  # fp32 inputs: every product is three tf32 products
+        return pinv_flops(wl, with_w) / (tf32 / 3.0)
     upd = wl.heads * 8.0 * wl.iters * m ** 3
     rest = pinv_flops(wl, with_w) - upd
     return rest / tf32 + upd / (bf16_tflops * 1e12 if m > 128 else tf32)
@@ -352,7 +358,8 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src, w_separate
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_flops": flops,
                 "peak_source": f"bf16_tflops burst ({peak_src}); tf32 products at x 1.1/2.25 (tf32/bf16 "
-                               f"nominal), fp16 update products (m > 128) at the bf16 rate"}
+                               f"nominal), fp16 update products (m > 128) at the bf16 rate; fp32 "
+                               f"inputs: three tf32 products per product (tf32 rate / 3)"}
     peak = 152 * 128 * 2 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
     return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -371,7 +378,9 @@ def pass_roofline(wl, ms_per_step, peaks, peak_src):
     n_tok = wl.B * wl.H * wl.n
     mm_flops = n_tok * (2.0 * wl.m * wl.d * 2 + 2.0 * wl.m * wl.d * 2 + 2.0 * wl.ks * wl.d)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    t_mma = mm_flops / (peaks["bf16_tflops"] * 1e12) + pinv_peak_time(wl, peaks["bf16_tflops"])
+    # bf16 operands at the bf16 rate; fp32 as three tf32 products
+    mma_rate = peaks["bf16_tflops"] * 1e12 * (TF32_OVER_BF16 / 3.0 if wl.dtype == "f32" else 1.0)
+    t_mma = mm_flops / mma_rate + pinv_peak_time(wl, peaks["bf16_tflops"])
     t_roof = max(t_hbm, t_mma)
     return {"bytes": nbytes, "flops": mm_flops + pinv_flops(wl), "t_hbm_us": t_hbm * 1e6,
             "t_tensor_us": t_mma * 1e6, "bound": "hbm" if t_hbm >= t_mma else "tensor",

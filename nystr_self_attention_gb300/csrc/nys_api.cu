@@ -193,6 +193,8 @@ Layout make_layout(const Shape& s) {
   L.tiles_per_split = 0;
   if (s.dtype == NYS_BF16) {
     rows_tc_split(s, rows_tc_ctas(s), &L.splits, &L.tiles_per_split);
+  } else if (x3_supported(s)) {
+    x3_rows_split(s, &L.splits, &L.tiles_per_split);
   } else {
     const long long rb = (s.m + 7) / 8;
     const long long sms = plan_sms();

@@ -114,6 +114,7 @@ int run_group(const Shape& full, const Shape& sg_in, long long bh0, const void* 
   const bool tc_tokens = tokens_tc_smem(full) > 0;
   const bool big_tokens = !tc_tokens && tokens_big_supported(full);
   const bool bf16_ops = tc_tokens || big_tokens;  // token step reads K~, W^T as bf16
+  const bool x3 = x3_supported(full);  // fp32 on the tensor cores
   __nv_bfloat16* qt_b = bf16 ? at<__nv_bfloat16>(ws, L.qt_bf16) + bh0 * pad : nullptr;
   __nv_bfloat16* kt_b = (bf16 && bf16_ops) ? at<__nv_bfloat16>(ws, L.kt_bf16) + bh0 * pad : nullptr;
   __nv_bfloat16* wt_b = bf16 ? at<__nv_bfloat16>(ws, L.wt_bf16) + bh0 * pad : nullptr;
@@ -138,6 +139,7 @@ int run_group(const Shape& full, const Shape& sg_in, long long bh0, const void* 
     rc = error_in("W = Z G", launch_w_tc(sg, z, g, w, wt_b, status, st));
   } else {
   rc = bf16 ? launch_rows_tc(sg, qt_b, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st)
+       : x3 ? launch_rows_x3(sg, qt, kg, vg, gp, gml, L.splits, L.tiles_per_split, status, st)
             : launch_rows_simt(sg, qt, kg, vg, gp, gml, L.splits, st);
   if (rc != NYS_OK) return error_in("landmark rows", rc);
   rc = pinv_tc_supported(full)
@@ -150,15 +152,17 @@ int run_group(const Shape& full, const Shape& sg_in, long long bh0, const void* 
   }
   if (rc != NYS_OK) return rc;
   Shape stok = sg;  // the token pass: with the variants, the attention term alone
-  if (full.separate_conv()) stok.ks = 0;
+  if (full.separate_conv() || x3) stok.ks = 0;
   if (tc_tokens)
     rc = launch_tokens_tc(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else if (big_tokens)
     rc = launch_tokens_big(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
+  else if (x3)
+    rc = launch_tokens_x3(stok, qg, kt, w, og, status, st);
   else
     rc = launch_tokens_simt(stok, qg, vg, kt, w, stok.ks > 0 ? conv_w : nullptr, og, st);
   rc = error_in("token rows", rc);
-  if (rc == NYS_OK && full.separate_conv())
+  if (rc == NYS_OK && (full.separate_conv() || (x3 && full.ks > 0)))
     rc = error_in("convolution", launch_conv_mask(sg, vg, conv_w, og, st));
   return rc;
 }
@@ -220,6 +224,9 @@ std::string describe_plan(const Shape& s) {
     const long long ctas = (total + L.tiles_per_split - 1) / L.tiles_per_split;
     out += " rows=rows_tc[ctas=" + std::to_string(ctas) + ",parts=" + std::to_string(L.splits) +
            ",tiles_per_cta=" + std::to_string(L.tiles_per_split) + "]";
+  } else if (x3_supported(s)) {
+    out += " rows=rows_x3[splits=" + std::to_string(L.splits) +
+           ",tiles_per_split=" + std::to_string(L.tiles_per_split) + "]";
   } else {
     out += " rows=rows_simt[splits=" + std::to_string(L.splits) + "]";
   }
@@ -234,8 +241,11 @@ std::string describe_plan(const Shape& s) {
   } else {
     out += " pinv=pinv_simt";
   }
-  out += tc_tokens ? " tokens=tokens_tc" : big_tokens ? " tokens=tokens_big" : " tokens=tokens_simt";
-  if (s.separate_conv()) out += " conv=conv_mask";
+  out += tc_tokens    ? " tokens=tokens_tc"
+         : big_tokens ? " tokens=tokens_big"
+         : x3_supported(s) ? " tokens=tokens_x3"
+                           : " tokens=tokens_simt";
+  if (s.separate_conv() || (x3_supported(s) && s.ks > 0)) out += " conv=conv_mask";
   return out;
 }
 

@@ -121,6 +121,18 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
                       const void* wt_bf16, const float* conv_w, void* out, int* status,
                       int num_sms, cudaStream_t stream);
 
+// fp32 landmark-row and token-row passes on the tensor cores in three tf32
+// products (nys_x3.cu): fp32, d <= 64 with d % 4 == 0, m <= 128. The
+// landmark-row pass splits each head's 128-key tiles into `splits` ranges
+// of `tiles_per_split` (x3_rows_split); the token pass writes the attention
+// term only (the convolution is added by conv_mask).
+bool x3_supported(const Shape& s);
+void x3_rows_split(const Shape& s, int* splits, int* tiles_per_split);
+int launch_rows_x3(const Shape& s, const float* qt, const void* k, const void* v, float* gpart,
+                   float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream);
+int launch_tokens_x3(const Shape& s, const void* q, const float* kt, const float* w, void* out,
+                     int* status, cudaStream_t stream);
+
 // Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs. `s` may be
 // a group of heads of the full problem: splits / tiles_per_split come from
 // the full problem's layout.
@@ -184,8 +196,13 @@ int launch_kmeans_round_tc(const Shape& s, const void* q, const void* mu3, const
 // the bf16 parity bar; with more (12 can give 6e-2, 24-64 can diverge) the
 // bf16 path runs the pseudo-inverse in fp32 on the CUDA cores instead.
 constexpr int kTf32MaxIters = 8;
+// fp32 inputs: the tensor-core pseudo-inverse (three tf32 products per
+// product, close to fp32 rounding) up to this many updates; the CUDA-core
+// kernel beyond.
+constexpr int kX3MaxIters = 12;
 
-// Tensor-core pseudo-inverse (nys_pinv_tc.cu), bf16 path, m <= 128.
+// Tensor-core pseudo-inverse (nys_pinv_tc.cu): bf16 path, m <= 128; fp32
+// path (three tf32 products per product), m <= 64, d 32 or 64.
 // Z -> z [B*H][m][m] fp32 when z is set. With gpart == nullptr, Z only: no
 // merge of the partials, no W (gml, g, w and wt_bf16 unused; z required).
 bool pinv_tc_supported(const Shape& s);

@@ -60,6 +60,7 @@ struct PinvParams {
   float c;        // scale * log2(e)
   uint32_t tmem_cols;
   uint32_t abuf_off, bbuf_off, klo_off;  // smem offsets (G^T at 0)
+  uint32_t abuf_lo_off, bbuf_lo_off, gbuf_lo_off;  // three-product mode: lo halves
 };
 
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -101,8 +102,19 @@ __device__ __forceinline__ float tf32_hi(float x) {
 // (half h = w / 4 takes the chunks with index % 2 == h).
 constexpr int kThreads = 256;
 
-template <int MP>
-__global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
+// tf32 hi / lo split: hi keeps the leading 11 significand bits (exact in
+// tf32), lo = x - hi (exact in fp32)
+__device__ __forceinline__ void split_tf32(float x, float& h, float& l) {
+  h = tf32_hi(x);
+  l = x - h;
+}
+
+// X3: every product as three tf32 products of its operands' hi / lo halves
+// (A_hi B_hi + A_lo B_hi + A_hi B_lo), for fp32 inputs (MP <= 64): the lo
+// halves of A_S, of the B operand and of G^T sit in shared memory beside
+// the hi halves, those of Z and X in TMEM beside theirs.
+template <int MP, bool X3>
+__global__ void __launch_bounds__(kThreads, (MP == 128 || X3) ? 1 : 2)
     pinv_tc(const __grid_constant__ PinvParams p) {
   constexpr int NCH = MP / 32;  // 32-column chunks of a head's m x m block
   extern __shared__ uint8_t smem_raw[];
@@ -114,6 +126,9 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   uint8_t* bbuf = sm + p.bbuf_off;    // B operand:            [NP rows x MP]
   uint8_t* khi = abuf;                // K~ hi / lo, stacked:  [NP rows x d]
   uint8_t* klo = sm + p.klo_off;      //   (score step only, over abuf / bbuf)
+  uint8_t* abuf_lo = sm + p.abuf_lo_off;  // X3 only
+  uint8_t* bbuf_lo = sm + p.bbuf_lo_off;
+  uint8_t* gbuf_lo = sm + p.gbuf_lo_off;
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -155,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   const uint32_t tmem = tmem_base_sh;
   const uint32_t lo = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t COL_Z = 0, COL_X = MP, COL_D = 2 * MP;  // main loop
+  // X3: lo halves of Z and X after the product region
+  const uint32_t COL_ZL = COL_D + (uint32_t)max(NP, NW), COL_XL = COL_ZL + MP;
   const uint32_t COL_QH = 0, COL_QL = d, COL_S = 2 * d;  // score step
   const uint32_t dblk = (uint32_t)(hs * MP);  // this head's block of a stacked result
 
@@ -162,8 +179,8 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   // tf32 product D (+)= A x B, M = 128, N = b_rows, K = k_dim. A from TMEM
   // columns a_col.. or, if a_smem is set, from shared memory (K-major,
   // 128 rows); B from shared memory (K-major, b_rows rows).
-  auto issue = [&](uint32_t d_col, uint32_t a_col, const uint8_t* a_smem, const uint8_t* b,
-                   int b_rows, int k_dim, bool acc_first) {
+  auto issue1 = [&](uint32_t d_col, uint32_t a_col, const uint8_t* a_smem, const uint8_t* b,
+                    int b_rows, int k_dim, bool acc_first) {
     const uint64_t b0 = smem_desc(smem_u32(b), 16, 1024, SW_128B);
     const uint32_t id = idesc_tf32(128, b_rows);
     const uint32_t bchunk = (uint32_t)b_rows * 8u;  // (b_rows * 128 B) >> 4
@@ -182,6 +199,17 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
         const uint64_t bd = b0 + (uint64_t)((uint32_t)(kk >> 2) * bchunk + (uint32_t)(kk & 3) * 2u);
         mma_tf32_tA(tmem + d_col, tmem + a_col + kk * 8, bd, id, (kk > 0 || acc_first) ? 1u : 0u);
       }
+    }
+  };
+  // one product; X3: A_hi B_hi + A_lo B_hi + A_hi B_lo, the lo halves at
+  // a_col_lo / a_smem_lo and b_lo
+  auto issue = [&](uint32_t d_col, uint32_t a_col, uint32_t a_col_lo, const uint8_t* a_smem,
+                   const uint8_t* a_smem_lo, const uint8_t* b, const uint8_t* b_lo, int b_rows,
+                   int k_dim) {
+    issue1(d_col, a_col, a_smem, b, b_rows, k_dim, false);
+    if constexpr (X3) {
+      issue1(d_col, a_col_lo, a_smem ? a_smem_lo : nullptr, b, b_rows, k_dim, true);
+      issue1(d_col, a_col, a_smem, b_lo, b_rows, k_dim, true);
     }
   };
   auto wait_mma = [&]() {
@@ -248,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   __syncthreads();
   if (tid == 0 && !*abort_flag) {
     tc_fence_after_sync();
-    issue(COL_S, COL_QH, nullptr, khi, NP, d, false);
-    issue(COL_S, COL_QH, nullptr, klo, NP, d, true);
-    issue(COL_S, COL_QL, nullptr, khi, NP, d, true);
+    issue1(COL_S, COL_QH, nullptr, khi, NP, d, false);
+    issue1(COL_S, COL_QH, nullptr, klo, NP, d, true);
+    issue1(COL_S, COL_QL, nullptr, khi, NP, d, true);
     mma_commit(&bar_mma);
   }
   wait_mma();
@@ -348,11 +376,17 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   // Z_0 = alpha A_S^T -> TMEM: row i of Z_0 is alpha * column i of A_S
   if (head_ok) {
     for (int c = half; c < NCH; c += 2) {
-      uint32_t r[32];
+      uint32_t r[32], rl[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        r[e] = __float_as_uint(alpha * ld_elem(abuf, 128, hs * MP + c * 32 + e, li));
+      for (int e = 0; e < 32; ++e) {
+        const float x = alpha * ld_elem(abuf, 128, hs * MP + c * 32 + e, li);
+        float h = x, l = 0.f;
+        if constexpr (X3) split_tf32(x, h, l);
+        r[e] = __float_as_uint(h);
+        rl[e] = __float_as_uint(l);
+      }
       tmem_st32(tmem + lo + COL_Z + c * 32, r);
+      if constexpr (X3) tmem_st32(tmem + lo + COL_ZL + c * 32, rl);
     }
   }
   // B operand of X = A_S Z_0: row hs MP + j holds column j of Z_0, i.e.
@@ -363,12 +397,41 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
       for (int e = 0; e < 32; e += 4) {
         float4 v = *reinterpret_cast<const float4*>(abuf + kmaj_off(row, c * 32 + e, 128));
         v.x *= alpha; v.y *= alpha; v.z *= alpha; v.w *= alpha;
-        store_row4(bbuf, NP, row, c * 32 + e, v);
+        if constexpr (X3) {
+          float4 h, l;
+          split_tf32(v.x, h.x, l.x);
+          split_tf32(v.y, h.y, l.y);
+          split_tf32(v.z, h.z, l.z);
+          split_tf32(v.w, h.w, l.w);
+          store_row4(bbuf, NP, row, c * 32 + e, h);
+          store_row4(bbuf_lo, NP, row, c * 32 + e, l);
+        } else {
+          store_row4(bbuf, NP, row, c * 32 + e, v);
+        }
       }
   fence_async_smem();
   tmem_st_wait();
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (X3) {
+    // A_S -> hi in place and lo beside it (the norms and Z_0 have read it;
+    // the stage export reads hi + lo, which is A_S exactly)
+    for (int c = half; c < NCH; c += 2)
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const uint32_t off = kmaj_off(row, c * 32 + e, 128);
+        const float4 v = *reinterpret_cast<const float4*>(abuf + off);
+        float4 h, l;
+        split_tf32(v.x, h.x, l.x);
+        split_tf32(v.y, h.y, l.y);
+        split_tf32(v.z, h.z, l.z);
+        split_tf32(v.w, h.w, l.w);
+        *reinterpret_cast<float4*>(abuf + off) = h;
+        *reinterpret_cast<float4*>(abuf_lo + off) = l;
+      }
+    fence_async_smem();
+    __syncthreads();
+  }
 
   // ---- 4) the iteration
   // Stage export of A_S (abuf is constant from here on): seven rows per
@@ -385,12 +448,14 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     const int bh2 = (int)blockIdx.x * hp + h2;
     if (bh2 >= p.BH) return;
     float* a_out = p.a_s + ((size_t)bh2 * m + i) * m;
-    for (int j = lane; j < m; j += 32) a_out[j] = ld_elem(abuf, 128, h2 * MP + i, j);
+    for (int j = lane; j < m; j += 32)
+      a_out[j] = X3 ? ld_elem(abuf, 128, h2 * MP + i, j) + ld_elem(abuf_lo, 128, h2 * MP + i, j)
+                    : ld_elem(abuf, 128, h2 * MP + i, j);
   };
   auto gemm = [&](uint32_t a_col, const uint8_t* a_smem) {
     if (tid == 0) {
       tc_fence_after_sync();
-      issue(COL_D, a_col, a_smem, bbuf, NP, MP, false);
+      issue(COL_D, a_col, a_col == COL_Z ? COL_ZL : COL_XL, a_smem, abuf_lo, bbuf, bbuf_lo, NP, MP);
       mma_commit(&bar_mma);
     }
     if (exp_row < hp * m) export_rows();
@@ -408,6 +473,20 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
       const float x = scale_ * __uint_as_float(r[e]);
       r[e] = __float_as_uint(x);
       v[e] = fmaf(sign, x, (j0 + e == li) ? diag : 0.f);
+    }
+    if constexpr (X3) {
+      float vl[32];
+      uint32_t rl[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        split_tf32(v[e], v[e], vl[e]);
+        float h, l;
+        split_tf32(__uint_as_float(r[e]), h, l);
+        r[e] = __float_as_uint(h);
+        rl[e] = __float_as_uint(l);
+      }
+      store_col32(bbuf_lo, NP, li, hs * MP + j0, vl);
+      if (to_col >= 0) tmem_st32(tmem + lo + (to_col == (int)COL_X ? COL_XL : COL_ZL) + j0, rl);
     }
     store_col32(bbuf, NP, li, hs * MP + j0, v);
     if (to_col >= 0) tmem_st32(tmem + lo + (uint32_t)to_col + j0, r);
@@ -503,7 +582,15 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
 #pragma unroll
         for (int e = 0; e < 8; ++e) go[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
       }
-      if (hs < hp) store_col32(gbuf, NW, li, hs * d + c0, acc);
+      if (hs < hp) {
+        if constexpr (X3) {
+          float al[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) split_tf32(acc[e], acc[e], al[e]);
+          store_col32(gbuf_lo, NW, li, hs * d + c0, al);
+        }
+        store_col32(gbuf, NW, li, hs * d + c0, acc);
+      }
     }
   }
 
@@ -516,6 +603,13 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
     for (int c0 = half * 32; c0 < m; c0 += 64) {
       uint32_t r[32];
       tmem_ld32(tmem + lo + COL_Z + c0, r);
+      if constexpr (X3) {
+        uint32_t rl[32];
+        tmem_ld32(tmem + lo + COL_ZL + c0, rl);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(rl[e]));
+      }
       tmem_ld_wait();
       if (!live) continue;
       if (c0 + 32 <= m && (m & 3) == 0) {
@@ -535,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
   if (!z_only && !*abort_flag) {
     if (tid == 0) {
       tc_fence_after_sync();
-      issue(COL_D, COL_Z, nullptr, gbuf, NW, MP, false);
+      issue(COL_D, COL_Z, COL_ZL, nullptr, nullptr, gbuf, gbuf_lo, NW, MP);
       mma_commit(&bar_mma);
     }
     wait_mma();
@@ -554,15 +648,15 @@ __global__ void __launch_bounds__(kThreads, MP == 128 ? 1 : 2)
                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
         }
         // W^T (bf16, zero padded to m64 columns): column li, and li + MP
-        // where MP < m64
-        for (int lj = li; lj < p.m64; lj += MP) {
+        // where MP < m64 (the bf16 token kernels' operand; fp32: none)
+        for (int lj = li; p.wt && lj < p.m64; lj += MP) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             wt[(size_t)(c0 + e) * p.m64 + lj] =
                 __float2bfloat16_rn(lj == li && live ? __uint_as_float(r[e]) : 0.f);
         }
       }
-      if (half == 0)
+      if (half == 0 && p.wt)
         for (int lj = li; lj < p.m64; lj += MP)
           for (int c = d; c < p.dpad; ++c) wt[(size_t)c * p.m64 + lj] = __float2bfloat16_rn(0.f);
     }
@@ -723,6 +817,8 @@ int mpad_of(int m) { return m <= 32 ? 32 : (m <= 64 ? 64 : 128); }
 }  // namespace
 
 bool pinv_tc_supported(const Shape& s) {
+  if (s.dtype == NYS_FP32)  // three tf32 products per product
+    return s.m <= 64 && s.d % 32 == 0 && s.d <= 64 && s.iters <= kX3MaxIters;
   return s.dtype == NYS_BF16 && s.m <= 128 && s.iters <= kTf32MaxIters;
 }
 
@@ -758,9 +854,10 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.scale = 1.0f / sqrtf((float)s.d);
   p.c = p.scale * 1.4426950408889634f;
   const int MP = mpad_of(s.m);
+  const bool x3 = s.dtype == NYS_FP32;
   p.hp = std::min(128 / MP, 256 / s.d);
   const int NP = p.hp * MP, NW = p.hp * s.d;
-  const uint32_t need = std::max<uint32_t>(2 * s.d + NP, 2 * MP + std::max(NP, NW));
+  const uint32_t need = std::max<uint32_t>(2 * s.d + NP, (x3 ? 4 : 2) * MP + std::max(NP, NW));
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
   p.tmem_cols = cols;
@@ -771,8 +868,13 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.abuf_off = (uint32_t)gbytes;
   p.bbuf_off = (uint32_t)(gbytes + abytes);
   p.klo_off = (uint32_t)(gbytes + kbytes);
-  const size_t smem = gbytes + std::max(abytes + bbytes, 2 * kbytes) + 1024;
-  auto kern = MP == 32 ? pinv_tc<32> : (MP == 64 ? pinv_tc<64> : pinv_tc<128>);
+  const size_t base = gbytes + std::max(abytes + bbytes, 2 * kbytes);
+  p.abuf_lo_off = (uint32_t)base;
+  p.bbuf_lo_off = (uint32_t)(base + abytes);
+  p.gbuf_lo_off = (uint32_t)(base + abytes + bbytes);
+  const size_t smem = (x3 ? base + abytes + bbytes + gbytes : base) + 1024;
+  auto kern = x3 ? (MP == 32 ? pinv_tc<32, true> : pinv_tc<64, true>)
+                 : (MP == 32 ? pinv_tc<32, false> : (MP == 64 ? pinv_tc<64, false> : pinv_tc<128, false>));
   // (two CTAs per SM for MP <= 64: the largest shared-memory carveout)
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
@@ -786,7 +888,7 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
 
 int launch_w_tc(const Shape& s, const float* z, const float* g, float* w, void* wt_bf16,
                 int* status, cudaStream_t stream) {
-  if (!pinv_tc_supported(s) || s.d % 16 != 0) return NYS_ERR_UNSUPPORTED;
+  if (s.dtype != NYS_BF16 || !pinv_tc_supported(s) || s.d % 16 != 0) return NYS_ERR_UNSUPPORTED;
   WParams p{};
   p.z = z;
   p.g = g;

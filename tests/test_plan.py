@@ -26,11 +26,25 @@ def workload_plan(N, name):
                 w.iters, w.ks)
 
 
-def test_fp32_runs_the_cuda_core_kernels(N):
+def test_fp32_runs_three_tf32_products_on_the_tensor_cores(N):
+    # c1: one head, n 512 -> four 128-key tiles, one landmark-row CTA each
     p = workload_plan(N, "c1")
     assert p["plan"] == "serial"
-    assert (p["rows"].split("[")[0], p["pinv"], p["tokens"]) == ("rows_simt", "pinv_simt",
-                                                               "tokens_simt")
+    assert p["rows"] == "rows_x3[splits=4,tiles_per_split=1]"
+    assert p["pinv"].startswith("pinv_tc[") and p["tokens"] == "tokens_x3"
+    assert p["conv"] == "conv_mask"  # the convolution in its own pass
+
+
+@pytest.mark.parametrize("d,m,iters,rows,pinv,tokens", [
+    (64, 128, 6, "rows_x3", "pinv_simt", "tokens_x3"),     # pseudo-inverse: m <= 64 only
+    (64, 64, 13, "rows_x3", "pinv_simt", "tokens_x3"),     # past the three-product update limit
+    (128, 64, 6, "rows_simt", "pinv_simt", "tokens_simt"),  # d > 64
+    (40, 64, 6, "rows_x3", "pinv_simt", "tokens_x3"),      # d not a multiple of 32
+    (8, 16, 6, "rows_x3", "pinv_simt", "tokens_x3"),
+])
+def test_fp32_kernel_choice(N, d, m, iters, rows, pinv, tokens):
+    p = plan(N, 1, 2, 512, d, m, N.NYS_FP32, iters=iters)
+    assert (p["rows"].split("[")[0], p["pinv"].split("[")[0], p["tokens"]) == (rows, pinv, tokens)
 
 
 @pytest.mark.parametrize("name,pinv,rows_ctas", [
