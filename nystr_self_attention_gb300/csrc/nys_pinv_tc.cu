@@ -822,8 +822,14 @@ bool pinv_tc_supported(const Shape& s) {
   return s.dtype == NYS_BF16 && s.m <= 128 && s.iters <= kTf32MaxIters;
 }
 
+// heads stacked per CTA: as many as the 128 TMEM lanes and a 256-column W
+// product take, no more than there are
+int heads_per_cta(const Shape& s) {
+  return (int)std::min<long long>(std::min(128 / mpad_of(s.m), 256 / s.d), s.bh());
+}
+
 int pinv_tc_ctas(const Shape& s) {
-  const int hp = std::min(128 / mpad_of(s.m), 256 / s.d);
+  const int hp = heads_per_cta(s);
   return (int)((s.bh() + hp - 1) / hp);
 }
 
@@ -855,7 +861,7 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.c = p.scale * 1.4426950408889634f;
   const int MP = mpad_of(s.m);
   const bool x3 = s.dtype == NYS_FP32;
-  p.hp = std::min(128 / MP, 256 / s.d);
+  p.hp = heads_per_cta(s);
   const int NP = p.hp * MP, NW = p.hp * s.d;
   const uint32_t need = std::max<uint32_t>(2 * s.d + NP, (x3 ? 4 : 2) * MP + std::max(NP, NW));
   uint32_t cols = 32;

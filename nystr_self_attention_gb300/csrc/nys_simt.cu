@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "nys_internal.h"
@@ -796,8 +797,8 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 // ks = 0 it only zeroes the padding rows.
 //   out[t][c] = t < L ? out[t][c] + sum_j w[j] V[t + j - (ks-1)/2][c] : 0,
 //   V rows outside [0, L) read as zero, L = the entry's length (n if none).
-// grid (ceil(n / (CV_ROWS CV_BLOCKS)), B*H), block CV_THREADS: a CTA takes
-// CV_BLOCKS consecutive blocks of CV_ROWS output rows of one head. The
+// grid (ceil(n / (CV_ROWS nblk)), B*H), block CV_THREADS: a CTA takes nblk
+// (at most CV_BLOCKS) consecutive blocks of CV_ROWS output rows of one head. The
 // head's taps are staged once (tap-major, so that consecutive channels read
 // consecutive words); per block, its V rows with the halo are staged in
 // shared memory by 16-byte loads, all of a thread's loads in flight before
@@ -824,7 +825,7 @@ __device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&x)[8]) {
 template <typename T, bool PER_CHANNEL>
 __global__ void __launch_bounds__(CV_THREADS)
 conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
-          int d, int ks, const int* __restrict__ lengths) {
+          int d, int ks, const int* __restrict__ lengths, int nblk) {
   constexpr bool per_channel = PER_CHANNEL;
   extern __shared__ float sm[];
   const long long bh = blockIdx.y;
@@ -836,7 +837,7 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
   float* sw = sm + (size_t)vrows * d;   // per channel: [ks][d]; per head: [ks]
   const T* vb = v + (size_t)bh * n * d;
   T* ob = out + (size_t)bh * n * d;
-  const int tb0 = blockIdx.x * CV_BLOCKS * CV_ROWS;
+  const int tb0 = blockIdx.x * nblk * CV_ROWS;
   if (ks > 0 && tb0 < len) {
     if (per_channel) {
       // the head's [d][ks] taps, read in order, stored tap-major; eight
@@ -863,7 +864,7 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
   const int wstride = per_channel ? d : 1;  // word step between taps in sw
   const int d8 = d / 8;                     // d is a multiple of 8
   const int ks_full = ks - ks % CV_RUN;     // taps in whole blocks of CV_RUN
-  for (int blk = 0; blk < CV_BLOCKS; ++blk) {
+  for (int blk = 0; blk < nblk; ++blk) {
     const int t0 = tb0 + blk * CV_ROWS;
     if (t0 >= n) break;  // uniform across the CTA
     const bool work = ks > 0 && t0 < len;
@@ -965,15 +966,20 @@ int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, c
            cudaSuccess))
     return set_cuda_error(cudaGetLastError());
   KernelScope ks_("conv_mask", stream);
-  const dim3 grid((s.n + CV_ROWS * CV_BLOCKS - 1) / (CV_ROWS * CV_BLOCKS), (unsigned)s.bh());
+  // blocks per CTA: up to CV_BLOCKS (the taps staged once for all of them),
+  // fewer where that would leave SMs idle
+  const long long blocks = (long long)((s.n + CV_ROWS - 1) / CV_ROWS) * s.bh();
+  const long long ctas_min = 2ll * plan_sms();
+  const int nblk = (int)std::max(1ll, std::min<long long>(CV_BLOCKS, blocks / ctas_min));
+  const dim3 grid((s.n + CV_ROWS * nblk - 1) / (CV_ROWS * nblk), (unsigned)s.bh());
   if (per_channel)
     conv_mask<T, true><<<grid, CV_THREADS, smem, stream>>>(
         static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
-        s.lengths);
+        s.lengths, nblk);
   else
     conv_mask<T, false><<<grid, CV_THREADS, smem, stream>>>(
         static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
-        s.lengths);
+        s.lengths, nblk);
   return launch_status();
 }
 
