@@ -4,8 +4,11 @@
 //   out[t] = softmax(Q[t] K~^T / sqrt(d)) W + sum_j w[h][j] V[t + j - (ks-1)/2]
 // ("Nyströmformer" review page, Proposed method, bullets 3 and 6).
 //
-// Shared memory holds K~ (m x d), W^T (d x m) and the conv's Toeplitz block
-// per head, plus ONE buffer shared by the Q tile and the V halo. TMEM: F/P
+// Shared memory holds K~ (m x d), W^T (d x m) and the conv's Toeplitz
+// operand per head (as its distinct 64 x 64 blocks: a block depends only on
+// its block diagonal), ONE buffer shared by the Q tile and the V halo, and
+// two 2 KB boxes per worker warp in which output rows are staged for TMA
+// stores. TMEM: F/P
 // (m columns), PW and CV accumulators (d columns each). One CTA per SM
 // walks a contiguous range of 128-token tiles with five warps:
 //   warp 4, one thread: TMA copies and tcgen05 products, in program order
@@ -32,6 +35,7 @@ using namespace sm100;
 
 struct BigMaps {
   CUtensorMap q, v, kt, wt;
+  CUtensorMap out;  // stores: boxes of 32 tokens x 32 columns (SWIZZLE_64B)
 };
 
 struct BigParams {
@@ -41,7 +45,8 @@ struct BigParams {
   int H, n, d, m, m_pad, ks, kc;
   int tiles_per_head, total_tiles, tiles_per_cta;
   float c;  // softmax scale * log2(e)
-  uint32_t off_kt, off_wt, off_t, off_qv;
+  uint32_t off_kt, off_wt, off_t, off_qv, off_stage;
+  int nbox;  // 64-column boxes of the conv's K (the V halo's rows)
   uint32_t kt_bytes, wt_bytes, q_bytes, v_bytes;
 };
 
@@ -49,6 +54,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int DP = 128, DC = 2;  // head width 128: two 64-column chunks
 constexpr size_t kSmemBudget = 227 * 1024 - 1024;
 constexpr int kThreads = 160;
+constexpr uint32_t kStageBytes = 4 * 4096;  // output staging, two 2 KB boxes per worker warp
 
 struct BigBars {
   uint64_t kw, q, v;           // TMA: K~ / W^T, Q tile, V halo
@@ -75,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant_
   uint8_t* wts = sm + p.off_wt;
   uint8_t* tbs = sm + p.off_t;
   uint8_t* qv = sm + p.off_qv;
+  uint8_t* stage = sm + p.off_stage;  // output staging: two 32 x 32 bf16 boxes per worker warp
   __shared__ BigBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -168,10 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant_
           if (ok && j > 0) ok = wait_or_fail(&bars.epi, (j - 1) & 1, p.status, abort_flag);
           if (!ok) break;
           tc_fence_after_sync();
+          // K-box c of the Toeplitz operand is the 128-row window [B_c; B_c-1]
+          // of the compact block list, which starts at block nbox - 1 - c
           const uint64_t a0 = smem_desc(smem_u32(tbs), 16, 1024, SW_128B);
           const uint64_t v0 = smem_desc(smem_u32(qv), p.kc * 128, 1024, SW_128B);
           for (int kk = 0; kk < p.kc / 16; ++kk)
-            mma_bf16(tmem + COL_CV, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+            mma_bf16(tmem + COL_CV, a0 + (uint64_t)((p.nbox - 1 - (kk >> 2)) * 512 + (kk & 3) * 2),
                      v0 + (uint64_t)(kk * 128), idc, kk > 0);
           mma_commit(&bars.cv);
           // the next Q tile into the buffer CV(j) frees
@@ -217,25 +226,32 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant_
     const uint32_t fcol = tmem + lo + COL_F;
     const bool full_m = p.m == p.m_pad && (p.m_pad & 63) == 0;
     int bh = g0 / tph, t = g0 - (g0 / tph) * tph, cur_h = -1;
-    const int kc64 = (p.kc + 63) & ~63;
     for (int j = 0; j < ntiles; ++j) {
       const int h = bh % p.H;
       if (p.kc > 0 && h != cur_h) {
-        // Toeplitz block of head h: row tid, column u holds w[u - tid]. Its
-        // previous reader, CV(j-1), completed before PW(j-1), which the
-        // epilogue of tile j-1 waited for.
+        // Toeplitz operand of head h: element (t, u) is w[u - t] (t the
+        // tile's token, u the halo row), so its 64 x 64 block (r, c) depends
+        // on c - r only: B_k[t'][u'] = w[64 k + u' - t']. Stored once each,
+        // as the list B_(nbox-1), ..., B_0, B_-1 (= 0) of 8 KB blocks; thread
+        // tid writes row tid % 64 of every other block. Its previous reader,
+        // CV(j-1), completed before PW(j-1), which the epilogue of tile j-1
+        // waited for.
         const float* wh = p.conv_w + (size_t)h * p.ks;
-        for (int u0 = 0; u0 < kc64; u0 += 8) {
-          uint32_t wv[4];
+        const int tr = tid & 63;
+        for (int blk = tid >> 6; blk <= p.nbox; blk += 2) {
+          const int k = p.nbox - 1 - blk;
+          for (int u0 = 0; u0 < 64; u0 += 8) {
+            uint32_t wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ua = u0 + 2 * e - tid, ub = ua + 1;
-            const float fa = (ua >= 0 && ua < p.ks && u0 + 2 * e < p.kc) ? __ldg(wh + ua) : 0.f;
-            const float fb = (ub >= 0 && ub < p.ks && u0 + 2 * e + 1 < p.kc) ? __ldg(wh + ub) : 0.f;
-            wv[e] = pack_bf16x2(fa, fb);
+            for (int e = 0; e < 4; ++e) {
+              const int ua = 64 * k + u0 + 2 * e - tr, ub = ua + 1;
+              const float fa = (ua >= 0 && ua < p.ks) ? __ldg(wh + ua) : 0.f;
+              const float fb = (ub >= 0 && ub < p.ks) ? __ldg(wh + ub) : 0.f;
+              wv[e] = pack_bf16x2(fa, fb);
+            }
+            *reinterpret_cast<uint4*>(tbs + blk * 8192 + sw128_offset(tr, u0 * 2)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
-          *reinterpret_cast<uint4*>(tbs + (u0 >> 6) * 16384 + sw128_offset(tid, (u0 & 63) * 2)) =
-              make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
         fence_async_smem();
         mbar_arrive(&bars.t);
@@ -286,29 +302,40 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant_
       // epilogue: out = PW / l + CV once PW(j) (and CV(j) before it) is done
       if (!__all_sync(0xffffffffu, wait_or_fail(&bars.pw, j & 1, p.status, abort_flag))) break;
       tc_fence_after_sync();
-      const int tok = t * 128 + tid;
+      // out rows, 32 columns at a time, staged in one of this warp's two
+      // swizzled boxes (alternating) and written by a TMA store (rows past n
+      // are clipped by the store); a box is rewritten once the store issued
+      // from it two rounds earlier has read it
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = p.out + ((size_t)bh * p.n + tok) * p.d;
+      const bool in_seq = t * 128 + warp * 32 < p.n;  // no box that starts past the sequence
 #pragma unroll
       for (int c0 = 0; c0 < DP; c0 += 32) {
+        uint8_t* box = stage + warp * 4096 + ((c0 >> 5) & 1) * 2048;
         uint32_t a[32], b[32];
         tmem_ld32(tmem + lo + COL_PW + c0, a);
         if (p.kc > 0) tmem_ld32(tmem + lo + COL_CV + c0, b);
         tmem_ld_wait();
-        if (tok < p.n) {
-          uint32_t o[16];
+        uint32_t o[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
-            if (p.kc > 0) {
-              x0 += __uint_as_float(b[2 * e]);
-              x1 += __uint_as_float(b[2 * e + 1]);
-            }
-            o[e] = pack_bf16x2(x0, x1);
+        for (int e = 0; e < 16; ++e) {
+          float x0 = __uint_as_float(a[2 * e]) * inv_l, x1 = __uint_as_float(a[2 * e + 1]) * inv_l;
+          if (p.kc > 0) {
+            x0 += __uint_as_float(b[2 * e]);
+            x1 += __uint_as_float(b[2 * e + 1]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+          o[e] = pack_bf16x2(x0, x1);
+        }
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint4*>(box + sw64_offset(lane, 16 * e)) =
+              make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0 && in_seq) {
+          tma_store_3d(&maps.out, box, c0, t * 128 + warp * 32, (int)bh);
+          bulk_commit();
         }
       }
       tc_fence_before_sync();
@@ -319,13 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_big(const __grid_constant_
       }
     }
   }
+  if (warp < 4 && lane == 0) bulk_wait0();  // this warp's output stores are done
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 struct BigPlan {
-  int m_pad, kc;
+  int m_pad, kc, nbox;
   uint32_t kt_bytes, wt_bytes, t_bytes, q_bytes, v_bytes, qv_bytes;
   size_t smem;
 };
@@ -337,11 +365,12 @@ bool plan_big(const Shape& s, BigPlan* pl) {
   if (pl->m_pad > 256 || pl->kc > 256) return false;
   pl->kt_bytes = (uint32_t)pl->m_pad * DP * 2;
   pl->wt_bytes = (uint32_t)((pl->m_pad + 63) / 64) * DP * 128;
-  pl->t_bytes = pl->kc > 0 ? (uint32_t)((pl->kc + 63) / 64) * 16384 : 0;
+  pl->nbox = (pl->kc + 63) / 64;
+  pl->t_bytes = pl->kc > 0 ? (uint32_t)(pl->nbox + 1) * 8192 : 0;  // compact Toeplitz blocks
   pl->q_bytes = 128 * DP * 2;
   pl->v_bytes = (uint32_t)pl->kc * DP * 2;
   pl->qv_bytes = std::max(pl->q_bytes, pl->v_bytes);
-  pl->smem = (size_t)pl->kt_bytes + pl->wt_bytes + pl->t_bytes + pl->qv_bytes + 1024;
+  pl->smem = (size_t)pl->kt_bytes + pl->wt_bytes + pl->t_bytes + pl->qv_bytes + kStageBytes + 1024;
   return pl->smem <= kSmemBudget;
 }
 
@@ -365,8 +394,11 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
     const uint64_t strides[2] = {(uint64_t)s.d * 2, (uint64_t)s.n * s.d * 2};
     const uint32_t boxq[3] = {64, 128, 1};
     const uint32_t boxv[3] = {64, (uint32_t)(pl.kc > 0 ? pl.kc : 16), 1};
+    const uint32_t boxo[3] = {32, 32, 1};
     if (!make_tensor_map(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, boxq,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&maps.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, boxo,
+                         CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_tensor_map(&maps.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, boxv,
                          CU_TENSOR_MAP_SWIZZLE_128B))
       return tensor_map_error(__FILE__, __LINE__);
@@ -412,6 +444,8 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
   p.off_wt = pl.kt_bytes;
   p.off_t = p.off_wt + pl.wt_bytes;
   p.off_qv = p.off_t + pl.t_bytes;
+  p.off_stage = p.off_qv + pl.qv_bytes;
+  p.nbox = pl.nbox;
   if (cudaFuncSetAttribute(tokens_big, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
       cudaSuccess)
     return set_cuda_error(cudaGetLastError());
