@@ -117,6 +117,28 @@ def test_small_shapes_f32_head_sizes(shape):
     test_small_shapes(shape, "f32")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d,m", [(128, 256), (64, 128), (64, 64)])
+def test_scores_rising_along_the_landmarks(d, m, dtype):
+    """Keys whose segments grow steadily in norm (the last ~16x the first),
+    so that a token's scores rise from one block of landmarks to the next by
+    far more than the softmax's exponent range: the row maximum must come
+    from the last blocks, not the first (most rows here have a block maximum
+    2^8 above every earlier block's, several times over)."""
+    n = 8 * m
+    wl = workloads.custom(1, 2, n, d, m, 6, 0, dtype)
+    inp = workloads.make_inputs(wl, seed=77 + m)
+    seg = np.arange(n) // (n // m)
+    k = inp.k * (1.0 + 15.0 * seg / (m - 1)).astype(np.float32)[None, None, :, None]
+    if dtype == "bf16":
+        inp.k, inp.k_bits = workloads.round_to_bf16(k)
+    else:
+        inp.k = k.astype(np.float32)
+    ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, m, wl.iters)
+    got, _ = run_gpu(inp)
+    assert rel_err(got, ref) <= TOL[dtype]
+
+
 # ------------------------------------------------------------------ stages ----
 
 # few heads: the pseudo-inverse runs beside the landmark-row pass and W = Z G
