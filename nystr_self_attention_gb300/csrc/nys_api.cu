@@ -110,7 +110,7 @@ int check_device(int* dev_out) {
 }
 
 namespace {
-constexpr int kHostChunks = 4;  // batch chunks of the pipelined host entry
+constexpr int kHostChunks = 8;  // chunks (head ranges) of the pipelined host entry
 
 struct DeviceCache {
   std::mutex mu;
@@ -377,15 +377,29 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_
     }
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  // Pipeline over chunks of whole batch entries: chunk c's inputs go up on
-  // the h2d stream while chunk c - 1 is computed on `stream` and chunk c - 2's
-  // output comes back on the d2h stream (the two copy directions overlap;
-  // uploading q, k and v on separate streams was slower).
-  int chunks = B < kHostChunks ? B : kHostChunks;
-  while (B % chunks != 0) --chunks;
-  const int bc = B / chunks;
-  const size_t cbytes = (size_t)bc * H * n * d * esz;
-  const Shape sc{bc, H, n, d, m, iters, conv_ks, dtype};
+  // Pipeline over chunks: chunk c's inputs go up on the h2d stream while
+  // chunk c - 1 is computed on `stream` and chunk c - 2's output comes back
+  // on the d2h stream (the two copy directions overlap; uploading q, k and v
+  // on separate streams was slower). A chunk is a range of heads that are
+  // contiguous in [B][H] (whole batch entries when B is large, else an
+  // equal split of each entry's heads), so that the last chunk's compute
+  // and download, which nothing overlaps, are short.
+  int per_b = 1;  // chunks per batch entry (a divisor of H)
+  if (B < kHostChunks) {
+    per_b = (kHostChunks + B - 1) / B;
+    while (per_b > 1 && H % per_b != 0) --per_b;
+  }
+  int bc = 1;  // batch entries per chunk (when per_b == 1)
+  if (per_b == 1) {
+    int chunks_b = B < kHostChunks ? B : kHostChunks;
+    while (B % chunks_b != 0) --chunks_b;
+    bc = B / chunks_b;
+  }
+  const int hc = H / per_b;  // heads per chunk (per_b > 1)
+  const int chunks = per_b > 1 ? B * per_b : B / bc;
+  const size_t cbytes = (per_b > 1 ? (size_t)hc : (size_t)bc * H) * n * d * esz;
+  const Shape sc = per_b > 1 ? Shape{1, hc, n, d, m, iters, conv_ks, dtype}
+                             : Shape{bc, H, n, d, m, iters, conv_ks, dtype};
   char* ws = nullptr;
   {
     std::lock_guard<std::mutex> lk(dc.mu);
@@ -413,8 +427,10 @@ int nystrom_attn_fwd_host(const void* q_host, const void* k_host, const void* v_
       return set_cuda_error(e);
     // the chunks share the library workspace (in stream order) and its
     // status word, which only the first clears
-    rc = run(sc, dq + off, dk + off, dv + off, conv_ks > 0 ? dw : nullptr, dout + off, ws, stream,
-             dev, c == 0);
+    // a head-range chunk's conv filters: rows h0 .. of [H][ks]
+    const int h0 = per_b > 1 ? (c % per_b) * hc : 0;
+    rc = run(sc, dq + off, dk + off, dv + off, conv_ks > 0 ? dw + (size_t)h0 * conv_ks : nullptr,
+             dout + off, ws, stream, dev, c == 0);
     if (rc != NYS_OK) return rc;
     if ((e = cudaEventRecord(dc.ev_comp[c], stream)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(dc.d2h, dc.ev_comp[c], 0)) != cudaSuccess ||
