@@ -808,22 +808,37 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 // one weight, one new V value and CV_RUN FMAs.
 constexpr int CV_ROWS = 64, CV_THREADS = 256, CV_RUN = 16, CV_BLOCKS = 8;
 
-__device__ __forceinline__ void ld8(const float* p, float (&x)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+// A block's V rows are staged in the input type. NARROW (bf16, or d <= 64):
+// the staged rows and taps leave room for three CTAs per SM, so registers
+// are capped to allow them (fewer staging loads in flight, the attention
+// term added after the taps so its loads overlap them); fp32 with d = 128
+// is bound by shared memory to two CTAs and keeps every register.
+template <typename T> struct Row8;  // eight consecutive elements of a row
+template <> struct Row8<float> { float4 a, b; };
+template <> struct Row8<__nv_bfloat16> { uint4 a; };
+__device__ __forceinline__ void ld_row8(const float* p, Row8<float>& r) {
+  r.a = *reinterpret_cast<const float4*>(p);
+  r.b = *reinterpret_cast<const float4*>(p + 4);
 }
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = __uint_as_float(w[e] << 16);
-    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-  }
+__device__ __forceinline__ void ld_row8(const __nv_bfloat16* p, Row8<__nv_bfloat16>& r) {
+  r.a = *reinterpret_cast<const uint4*>(p);
 }
+__device__ __forceinline__ void zero_row8(Row8<float>& r) {
+  r.a = r.b = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ void zero_row8(Row8<__nv_bfloat16>& r) { r.a = make_uint4(0u, 0u, 0u, 0u); }
+__device__ __forceinline__ void st_row8(float* p, const Row8<float>& r) {
+  *reinterpret_cast<float4*>(p) = r.a;
+  *reinterpret_cast<float4*>(p + 4) = r.b;
+}
+__device__ __forceinline__ void st_row8(__nv_bfloat16* p, const Row8<__nv_bfloat16>& r) {
+  *reinterpret_cast<uint4*>(p) = r.a;
+}
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-template <typename T, bool PER_CHANNEL>
-__global__ void __launch_bounds__(CV_THREADS)
+template <typename T, bool PER_CHANNEL, bool NARROW>
+__global__ void __launch_bounds__(CV_THREADS, NARROW ? 3 : 1)
 conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
           int d, int ks, const int* __restrict__ lengths, int nblk) {
   constexpr bool per_channel = PER_CHANNEL;
@@ -833,8 +848,8 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
   const int len = lengths ? lengths[bh / H] : n;
   const int rad = ks > 0 ? (ks - 1) / 2 : 0;
   const int vrows = CV_ROWS + 2 * rad;
-  float* sv = sm;                       // [vrows][d]
-  float* sw = sm + (size_t)vrows * d;   // per channel: [ks][d]; per head: [ks]
+  T* sv = reinterpret_cast<T*>(sm);                           // [vrows][d], input type
+  float* sw = reinterpret_cast<float*>(sv + (size_t)vrows * d);  // per channel: [ks][d]; per head: [ks]
   const T* vb = v + (size_t)bh * n * d;
   T* ob = out + (size_t)bh * n * d;
   const int tb0 = blockIdx.x * nblk * CV_ROWS;
@@ -870,28 +885,22 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
     const bool work = ks > 0 && t0 < len;
     __syncthreads();  // the previous block's readers of sv are done (and the taps are staged)
     if (work) {
-      constexpr int kPer = 8;  // 16-byte loads in flight per thread
+      constexpr int kPer = NARROW ? 4 : 8;  // row pieces in flight per thread
       for (int e0 = threadIdx.x; e0 < vrows * d8; e0 += kPer * CV_THREADS) {
-        float x[kPer][8];
+        Row8<T> x[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int e = e0 + k * CV_THREADS;
           const int u = t0 - rad + e / d8, c = (e % d8) * 8;
-          if (e < vrows * d8 && u >= 0 && u < len) {
-            ld8(vb + (size_t)u * d + c, x[k]);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) x[k][q] = 0.f;
-          }
+          if (e < vrows * d8 && u >= 0 && u < len)
+            ld_row8(vb + (size_t)u * d + c, x[k]);
+          else
+            zero_row8(x[k]);
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int e = e0 + k * CV_THREADS;
-          if (e < vrows * d8) {
-            float* dst = sv + (size_t)(e / d8) * d + (e % d8) * 8;
-            *reinterpret_cast<float4*>(dst) = make_float4(x[k][0], x[k][1], x[k][2], x[k][3]);
-            *reinterpret_cast<float4*>(dst + 4) = make_float4(x[k][4], x[k][5], x[k][6], x[k][7]);
-          }
+          if (e < vrows * d8) st_row8(sv + (size_t)(e / d8) * d + (e % d8) * 8, x[k]);
         }
       }
     }
@@ -900,24 +909,27 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
       const int c = item % d, r0 = (item / d) * CV_RUN;
       if (t0 + r0 >= n) continue;
       // the attention term already in out: all of the run's loads issued
-      // before the taps, so their latency hides behind the FMAs (stored
-      // rows could alias later loads, so loads after a store would wait)
-      float acc[CV_RUN];
+      // before the taps (stored rows could alias later loads, so loads
+      // after a store would wait); NARROW adds them after the taps, so that
+      // their latency hides behind the FMAs
+      float att[CV_RUN], acc[CV_RUN];
 #pragma unroll
       for (int r = 0; r < CV_RUN; ++r) {
         const int t = t0 + r0 + r;
-        acc[r] = (t < n && t < len) ? ld(ob + (size_t)t * d + c) : 0.f;
+        const float a = (t < n && t < len) ? ld(ob + (size_t)t * d + c) : 0.f;
+        att[r] = NARROW ? a : 0.f;
+        acc[r] = NARROW ? 0.f : a;
       }
       if (work) {
         // ring: before tap j, V row (r0 + j + r) of the staged block sits in
         // xw[(j + r) % CV_RUN]; after it, the slot of row r0 + j takes row
         // r0 + j + CV_RUN (staged for every j < ks - 1)
-        const float* x = sv + (size_t)r0 * d + c;
+        const T* x = sv + (size_t)r0 * d + c;
         const float* wp = sw + (per_channel ? c : 0);  // tap j of this channel: wp[j * wstride]
-        const float* xp = x + (size_t)CV_RUN * d;      // row r0 + j + CV_RUN: xp[j * d]
+        const T* xp = x + (size_t)CV_RUN * d;          // row r0 + j + CV_RUN: xp[j * d]
         float xw[CV_RUN];
 #pragma unroll
-        for (int r = 0; r < CV_RUN; ++r) xw[r] = x[(size_t)r * d];
+        for (int r = 0; r < CV_RUN; ++r) xw[r] = to_f(x[(size_t)r * d]);
         // whole blocks: no tap past ks, and (ks odd, CV_RUN even) never the
         // last tap, so every next row is inside the staged block
         for (int jb = 0; jb < ks_full; jb += CV_RUN) {
@@ -926,7 +938,7 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
             const float wj = wp[jj * wstride];
 #pragma unroll
             for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[(jj + r) % CV_RUN], acc[r]);
-            xw[jj] = xp[jj * d];
+            xw[jj] = to_f(xp[jj * d]);
           }
           wp += CV_RUN * wstride;
           xp += CV_RUN * d;
@@ -939,14 +951,14 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
           const float wj = wp[jj * wstride];
 #pragma unroll
           for (int r = 0; r < CV_RUN; ++r) acc[r] = fmaf(wj, xw[(jj + r) % CV_RUN], acc[r]);
-          if (j + 1 < ks) xw[jj] = xp[jj * d];
+          if (j + 1 < ks) xw[jj] = to_f(xp[jj * d]);
         }
       }
 #pragma unroll
       for (int r = 0; r < CV_RUN; ++r) {
         const int t = t0 + r0 + r;
         if (t >= n) break;
-        st(ob + (size_t)t * d + c, t < len ? acc[r] : 0.f);
+        st(ob + (size_t)t * d + c, t < len ? att[r] + acc[r] : 0.f);
       }
     }
   }
@@ -956,14 +968,14 @@ template <typename T>
 int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, cudaStream_t stream) {
   const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
   const bool per_channel = s.conv_layout == NYS_CONV_PER_CHANNEL;
-  const size_t smem = s.ks > 0 ? sizeof(float) * ((size_t)(CV_ROWS + 2 * rad) * s.d +
-                                                  (size_t)s.ks * (per_channel ? s.d : 1))
+  const size_t smem = s.ks > 0 ? sizeof(T) * (size_t)(CV_ROWS + 2 * rad) * s.d +
+                                    sizeof(float) * (size_t)s.ks * (per_channel ? s.d : 1)
                                : 0;
+  const bool narrow = sizeof(T) == 2 || s.d <= 64;
+  auto kern = per_channel ? (narrow ? conv_mask<T, true, true> : conv_mask<T, true, false>)
+                          : (narrow ? conv_mask<T, false, true> : conv_mask<T, false, false>);
   if (smem > 48 * 1024 &&
-      (cudaFuncSetAttribute(conv_mask<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-           cudaSuccess ||
-       cudaFuncSetAttribute(conv_mask<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-           cudaSuccess))
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return set_cuda_error(cudaGetLastError());
   KernelScope ks_("conv_mask", stream);
   // blocks per CTA: up to CV_BLOCKS (the taps staged once for all of them),
@@ -972,14 +984,8 @@ int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, c
   const long long ctas_min = 2ll * plan_sms();
   const int nblk = (int)std::max(1ll, std::min<long long>(CV_BLOCKS, blocks / ctas_min));
   const dim3 grid((s.n + CV_ROWS * nblk - 1) / (CV_ROWS * nblk), (unsigned)s.bh());
-  if (per_channel)
-    conv_mask<T, true><<<grid, CV_THREADS, smem, stream>>>(
-        static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
-        s.lengths, nblk);
-  else
-    conv_mask<T, false><<<grid, CV_THREADS, smem, stream>>>(
-        static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr, static_cast<T*>(out), s.H, s.n, s.d, s.ks,
-        s.lengths, nblk);
+  kern<<<grid, CV_THREADS, smem, stream>>>(static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr,
+                                          static_cast<T*>(out), s.H, s.n, s.d, s.ks, s.lengths, nblk);
   return launch_status();
 }
 
