@@ -3,7 +3,7 @@ oracle over m in {16, 32, 64, 128, 192, 256} and 0, 2, 6, 8, 12 updates of the
 pseudo-inverse ("about 6 iterations", Nyströmformer review page, Proposed
 method, bullet 5), plus the largest count the ABI accepts (64).
 
-Bars: the benchmark spec tolerances (2e-2 bf16 inputs, 1e-4 float32) everywhere
+Bars: the parity tolerances (2e-2 bf16 inputs, 1e-4 float32) everywhere
 except the float32 path at 64 updates. On the bf16 path the library runs the
 pseudo-inverse's products on the tensor cores (tf32 operands) for up to 8
 updates, the page's range, and in fp32 on the CUDA cores beyond: the
@@ -12,7 +12,9 @@ the rounding of the products is amplified by cond(A_S) (tf32 products gave
 6e-2 at 12 updates and non-finite output at 64 on these inputs). In fp32 a
 numpy model of the arithmetic gives up to 2.7e-5 at 12 updates and up to
 5.5e-3 at 64 on these inputs, so the float32 path keeps 1e-4 through 12
-updates and is held to 1e-2 at 64. At 64 updates the bf16 path is held to
+updates and is held to 1e-2 at 64. (float32 inputs run the pseudo-inverse
+for m <= 64 up to 12 updates as three tf32 products per product, close to
+fp32 rounding, and on the CUDA cores in fp32 beyond.) At 64 updates the bf16 path is held to
 5e-2: Z, and with it W = Z G, grows with the update count, and W enters the
 token pass as a bf16 tensor-core operand (2^-9 relative rounding) whose
 products cancel; measured 2.4e-2 on these inputs.
