@@ -228,6 +228,27 @@ def test_host_entry_matches_device_entry():
     assert np.array_equal(host_out, dev_out)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_host_entry_in_head_range_chunks(dtype):
+    """One batch entry of 16 heads: the host-buffer entry pipelines it in
+    eight chunks of two heads (each with its own rows of the conv filters)."""
+    import nystr_self_attention_gb300 as N
+    wl = workloads.custom(1, 16, 640, 64, 64, 6, 9, dtype)
+    inp = workloads.make_inputs(wl, seed=23)
+    ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, wl.m, wl.iters)
+    if dtype == "bf16":
+        out_bits = np.zeros(inp.q_bits.shape, np.uint16)
+        N.nystrom_attn_fwd_host(inp.q_bits, inp.k_bits, inp.v_bits, inp.conv_w, out_bits, wl.B, wl.H,
+                                wl.n, wl.d, wl.m, wl.iters, wl.ks, N.NYS_BF16)
+        got = (out_bits.astype(np.uint32) << 16).view(np.float32)
+    else:
+        got = np.zeros(inp.q.shape, np.float32)
+        N.nystrom_attn_fwd_host(inp.q, inp.k, inp.v, inp.conv_w, got, wl.B, wl.H, wl.n, wl.d, wl.m,
+                                wl.iters, wl.ks, N.NYS_FP32)
+    for h in range(wl.H):
+        assert rel_err(got[0, h], ref[0, h]) <= TOL[dtype], h
+
+
 def test_repeatable_and_workspace_entry_agrees():
     wl = workloads.custom(1, 4, 1024, 64, 64, 6, 33, "bf16")
     inp = workloads.make_inputs(wl, seed=12)
