@@ -296,53 +296,73 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// grid (C_pad, B*H), block d: thread j of centroid c. With S > 0: the new
+// grid (ceil(C_pad / cpb), B*H), block 256: thread (centroid c, columns
+// [j, j + 4)), d / 4 threads per centroid and cpb = 256 / (d / 4) centroids
+// per CTA (d = 64 or 128), every load in flight at once. With S > 0: the new
 // centroid = the CTAs' members' sums added in CTA order, over the summed
 // counts (an empty cluster keeps mu_old); with S = 0 the centroid is mu_old
 // as it is. Either way it writes the bf16 split (hi, mid, lo) of the
-// centroid and its squared norm for the next assignment; rows c >= C are
-// zero.
-__global__ void kmeans_reduce(const float* __restrict__ part, const int* __restrict__ cnt,
-                              const float* __restrict__ mu_old, float* __restrict__ mu_new,
-                              __nv_bfloat16* __restrict__ mu3, float* __restrict__ norms, int S, int d,
-                              int C, int C_pad) {
-  __shared__ float red[4];
-  const int c = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
+// centroid and its squared norm (reduced over the centroid's lanes) for the
+// next assignment; rows c >= C are zero.
+constexpr int kRedThreads = 256;
+
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+  return make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
+}
+
+__global__ void __launch_bounds__(kRedThreads) kmeans_reduce(const float* __restrict__ part,
+                                                             const int* __restrict__ cnt,
+                                                             const float* __restrict__ mu_old,
+                                                             float* __restrict__ mu_new,
+                                                             __nv_bfloat16* __restrict__ mu3,
+                                                             float* __restrict__ norms, int S, int d,
+                                                             int C, int C_pad) {
+  const int tpc = d >> 2, cpb = kRedThreads / tpc;
+  const int c = blockIdx.x * cpb + (int)threadIdx.x / tpc, j = ((int)threadIdx.x % tpc) * 4;
   const long long bh = blockIdx.y;
-  float x = 0.f;
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
   if (c < C) {
     const size_t o = ((size_t)bh * C + c) * d + j;
-    x = mu_old[o];
+    x = *reinterpret_cast<const float4*>(mu_old + o);
     if (S > 0) {
-      float sum = 0.f;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
       int count = 0;
       for (int s = 0; s < S; ++s) {
         const size_t r = ((size_t)bh * S + s) * C_pad + c;
-        sum += part[r * d + j];
+        const float4 v = *reinterpret_cast<const float4*>(part + r * d + j);
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
         count += cnt[r];
       }
-      if (count > 0) x = sum / (float)count;
-      mu_new[o] = x;
+      if (count > 0) {
+        const float f = (float)count;
+        x = make_float4(sum.x / f, sum.y / f, sum.z / f, sum.w / f);
+      }
+      *reinterpret_cast<float4*>(mu_new + o) = x;
     }
   }
-  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-  const float r1 = x - __bfloat162float(hi);
-  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-  const size_t base = ((size_t)bh * 3 * C_pad + c) * d + j;
-  mu3[base] = hi;
-  mu3[base + (size_t)C_pad * d] = mid;
-  mu3[base + 2 * (size_t)C_pad * d] = lo;
-  float sq = x * x;
+  if (c < C_pad) {
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    float hi[4], mid[4], lo[4];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-  if (lane == 0) red[warp] = sq;
-  __syncthreads();
-  if (j == 0) {
-    float t = 0.f;
-    for (int w = 0; w < (d + 31) / 32; ++w) t += red[w];
-    norms[(size_t)bh * C_pad + c] = t;
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(xs[e]);
+      const float r1 = xs[e] - __bfloat162float(h);
+      const __nv_bfloat16 m2 = __float2bfloat16_rn(r1);
+      hi[e] = __bfloat162float(h);
+      mid[e] = __bfloat162float(m2);
+      lo[e] = r1 - mid[e];
+    }
+    const size_t base = ((size_t)bh * 3 * C_pad + c) * d + j;
+    *reinterpret_cast<uint2*>(mu3 + base) = pack_bf16x4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint2*>(mu3 + base + (size_t)C_pad * d) = pack_bf16x4(mid[0], mid[1], mid[2], mid[3]);
+    *reinterpret_cast<uint2*>(mu3 + base + 2 * (size_t)C_pad * d) = pack_bf16x4(lo[0], lo[1], lo[2], lo[3]);
   }
+  float sq = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+  for (int off = tpc >> 1; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  if (c < C_pad && j == 0) norms[(size_t)bh * C_pad + c] = sq;
 }
 
 struct KmPlan {
@@ -393,7 +413,8 @@ KmWorkspace kmeans_tc_workspace(const Shape& s) {
 int launch_kmeans_prep(const Shape& s, const float* mu, void* mu3, float* norms, cudaStream_t st) {
   const KmPlan k = km_plan(s);
   KernelScope scope("kmeans_reduce", st);
-  kmeans_reduce<<<dim3((unsigned)k.C_pad, (unsigned)s.bh()), s.d, 0, st>>>(
+  const int cpb = kRedThreads / (s.d / 4);
+  kmeans_reduce<<<dim3((unsigned)((k.C_pad + cpb - 1) / cpb), (unsigned)s.bh()), kRedThreads, 0, st>>>(
       nullptr, nullptr, mu, nullptr, static_cast<__nv_bfloat16*>(mu3), norms, 0, s.d, s.m, k.C_pad);
   return launch_status();
 }
@@ -456,7 +477,8 @@ int launch_kmeans_round_tc(const Shape& s, const void* q, const void* mu3, const
     if (rc != NYS_OK) return rc;
   }
   KernelScope scope("kmeans_reduce", st);
-  kmeans_reduce<<<dim3((unsigned)k.C_pad, (unsigned)BH), s.d, 0, st>>>(
+  const int cpb = kRedThreads / (s.d / 4);
+  kmeans_reduce<<<dim3((unsigned)((k.C_pad + cpb - 1) / cpb), (unsigned)BH), kRedThreads, 0, st>>>(
       part, cnt, mu_old, mu_new, static_cast<__nv_bfloat16*>(mu3_next), norms_next, k.S, s.d, s.m,
       k.C_pad);
   return launch_status();
