@@ -18,10 +18,13 @@
 // Four worker warps (thread = query row of the tile, a TMEM lane, in the
 // assignment; = cluster row for the members' sums) and an issuer warp whose
 // lane 0 issues the TMA copies and the MMAs, driven by the workers' mbarrier
-// arrivals. One CTA per SM. The Q tiles go through a ring of three buffers,
-// and the next tile's scores are issued as soon as every worker has read
-// this tile's, so the tensor cores work while the workers take the argmin
-// and build the one-hot tile.
+// arrivals. One CTA per SM. At d = 64 the Q tiles go through a ring of
+// four buffers and the scores through two TMEM buffers, two tiles ahead of
+// the members' product: tile j + 2's scores are issued right after tile j's
+// product, into the buffer the workers read tile j's from. At d = 128 (three
+// Q buffers, one score buffer) the next tile's scores are issued as soon as
+// every worker has read this tile's. Either way the tensor cores work while
+// the workers take the argmin and build the one-hot tile.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word
 // and the CTA winds down (copies and products in flight awaited, TMEM
 // freed).
@@ -41,8 +44,16 @@ using namespace sm100;
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 160;  // four worker warps and the issuer warp
-constexpr uint32_t kColS = 0, kColU = 128;  // TMEM: scores (C_pad columns), members' sums (d columns)
-constexpr int kNQ = 3;                      // Q tile buffers
+// TMEM: scores (C_pad columns; two buffers when the scores run two tiles
+// ahead), members' sums (d columns)
+constexpr uint32_t kColS = 0, kColU = 128, kColS2 = 256;
+constexpr int kNQMax = 4;
+// Q tile buffers, and how many tiles the scores run ahead of the members'
+// product: d = 64 keeps four tiles of Q and two score buffers, so that a
+// tile's scores never wait for the workers to read the previous tile's; at
+// d = 128 shared memory holds three tiles and one score buffer.
+__host__ __device__ constexpr int km_nq(int dch) { return dch == 1 ? 4 : 3; }
+__host__ __device__ constexpr int km_ahead(int dch) { return dch == 1 ? 2 : 1; }
 
 struct KmMaps {
   CUtensorMap q;    // bf16 [B*H][n][d], box 64 x 128
@@ -60,7 +71,7 @@ struct KmParams {
 };
 
 struct KmBars {
-  uint64_t mu, q[kNQ], asg, upd, fin;
+  uint64_t mu, q[kNQMax], asg[2], upd, fin;
   uint64_t rd, ready;  // workers: a tile's scores read; its one-hot tile written
 };
 
@@ -82,6 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* mus = sm + p.off_mu;  // [3][DCH] boxes of C_pad rows x 128 B
+  constexpr int kNQ = km_nq(DCH), kAhead = km_ahead(DCH);
+  constexpr uint32_t kCols = kAhead == 2 ? 512 : 256;
   uint8_t* qb = sm + p.off_q;    // [kNQ][DCH] boxes of 128 rows x 128 B
   uint8_t* oh = sm + p.off_oh;   // one-hot^T: [2] boxes of 128 cluster rows x 64 queries (bf16)
   __shared__ KmBars bars;
@@ -102,7 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   if (tid == 0) {
     mbar_init(&bars.mu, 1);
     for (int r = 0; r < kNQ; ++r) mbar_init(&bars.q[r], 1);
-    mbar_init(&bars.asg, 1);
+    mbar_init(&bars.asg[0], 1);
+    mbar_init(&bars.asg[1], 1);
     mbar_init(&bars.upd, 1);
     mbar_init(&bars.rd, 128);
     mbar_init(&bars.ready, 128);
@@ -118,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   for (int e = tid; e < 2 * 128 * 128 / 16; e += kThreads)
     reinterpret_cast<uint4*>(oh)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_async_smem();
-  if (warp == 0) tmem_alloc(&tmem_base_sh, 256);
+  if (warp == 0) tmem_alloc(&tmem_base_sh, kCols);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -137,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
           tma_load_3d(qb + (r * DCH + c) * 16384, &maps.q, &bars.q[r], 64 * c, (t0 + jt) * 128, (int)bh);
         ++n_q[r];
       };
-      // scores of tile jt: Q mu^T as Q mu_hi^T + Q mu_mid^T + Q mu_lo^T
+      // scores of tile jt: Q mu^T as Q mu_hi^T + Q mu_mid^T + Q mu_lo^T, into
+      // score buffer jt % 2 (with two buffers), completing on asg[jt % 2]
       auto scores = [&](int jt) -> bool {
         const int r = jt % kNQ;
         if (!km_wait(&bars.q[r], (n_q[r] - 1) & 1, p.status, abort_flag)) return false;
@@ -146,10 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
           for (int kk = 0; kk < 4 * DCH; ++kk) {
             const uint64_t a = smem_desc(smem_u32(qb + (r * DCH + (kk >> 2)) * 16384), 16, 1024, SW_128B);
             const uint64_t bd = smem_desc(smem_u32(mus + (k * DCH + (kk >> 2)) * mu_box), 16, 1024, SW_128B);
-            mma_bf16(tmem + kColS, a + (uint64_t)((kk & 3) * 2), bd + (uint64_t)((kk & 3) * 2), id_s,
-                     (k > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tmem + ((kAhead == 2 && (jt & 1)) ? kColS2 : kColS), a + (uint64_t)((kk & 3) * 2),
+                     bd + (uint64_t)((kk & 3) * 2), id_s, (k > 0 || kk > 0) ? 1u : 0u);
           }
-        mma_commit(&bars.asg);
+        mma_commit(&bars.asg[jt & 1]);
         return true;
       };
       tma_prefetch(&maps.q);
@@ -160,13 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
           tma_load_3d(mus + (k * DCH + c) * mu_box, &maps.mu3, &bars.mu, 64 * c, 0, (int)(bh * 3 + k));
       n_mu = 1;
       for (int jt = 0; jt < kNQ - 1 && jt < ntiles; ++jt) load_q(jt);
-      bool ok = km_wait(&bars.mu, 0, p.status, abort_flag) && scores(0);
+      bool ok = km_wait(&bars.mu, 0, p.status, abort_flag);
+      for (int jt = 0; ok && jt < kAhead && jt < ntiles; ++jt) ok = scores(jt);
       for (int j = 0; ok && j < ntiles; ++j) {
-        // tile j + 1's scores once every worker has read tile j's
-        ok = km_wait(&bars.rd, j & 1, p.status, abort_flag);
-        if (ok && j + 1 < ntiles) ok = scores(j + 1);
+        // one score buffer: tile j + 1's scores once every worker has read tile j's
+        if (kAhead == 1) {
+          ok = km_wait(&bars.rd, j & 1, p.status, abort_flag);
+          if (ok && j + 1 < ntiles) ok = scores(j + 1);
+        }
         // tile j's members' product once its one-hot tile is written (the
-        // workers waited for tile j - 1's product before writing it)
+        // workers waited for tile j - 1's product before writing it, and
+        // had read tile j's scores)
         if (ok) ok = km_wait(&bars.ready, j & 1, p.status, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
@@ -178,7 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
                    (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars.upd);
-        // tile j + 2 into the buffer of tile j - 1, whose product is done
+        // two score buffers: tile j + 2's scores into the buffer tile j's
+        // scores were read from (its Q tile landed one tile earlier)
+        if (kAhead == 2 && j + 2 < ntiles && !scores(j + 2)) break;
+        // tile j + kNQ - 1 into the buffer of tile j - 1, whose product is
+        // done (the workers waited for it before this tile's one-hot tile)
         if (j + kNQ - 1 < ntiles) load_q(j + kNQ - 1);
       }
       if (*abort_flag) {
@@ -196,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
     for (int j = 0; j < ntiles; ++j) {
       const int tile = t0 + j;
       // assignment: nearest centroid of this thread's query
-      const bool ok = km_wait(&bars.asg, j & 1, p.status, abort_flag);
+      const bool ok = km_wait(&bars.asg[j & 1], (j >> 1) & 1, p.status, abort_flag);
       const bool go = __all_sync(0xffffffffu, ok);  // warp-uniform: TMEM loads are warp-wide
       tc_fence_after_sync();
       // four independent running minima (column c in chain c % 4) over the
@@ -208,8 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
       int bc[4] = {0, 0, 0, 0};
       if (go) {
         uint32_t v[4][32];
+        const uint32_t scol = (kAhead == 2 && (j & 1)) ? kColS2 : kColS;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) tmem_ld32(tmem + lo + kColS + 32 * h, v[h]);
+        for (int h = 0; h < 4; ++h) tmem_ld32(tmem + lo + scol + 32 * h, v[h]);
         tmem_ld_wait();
         const float4* n4 = reinterpret_cast<const float4*>(norm_s);
 #pragma unroll
@@ -293,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) kmeans_round_tc(const __grid_cons
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
 // grid (ceil(C_pad / cpb), B*H), block 256: thread (centroid c, columns
@@ -384,8 +408,8 @@ KmPlan km_plan(const Shape& s) {
   k.S = (k.T_h + k.tpc - 1) / k.tpc;
   k.off_mu = 0;
   k.off_q = k.off_mu + 3u * k.dch * k.C_pad * 128u;
-  k.off_oh = k.off_q + (uint32_t)kNQ * k.dch * 16384u;
-  // more than half an SM's shared memory, so that one CTA (256 TMEM columns) holds an SM
+  k.off_oh = k.off_q + (uint32_t)km_nq(k.dch) * k.dch * 16384u;
+  // more than half an SM's shared memory, so that one CTA (256 or 512 TMEM columns) holds an SM
   k.smem = std::max<size_t>((size_t)k.off_oh + 2 * 16384 + 1024, 116 * 1024);
   return k;
 }
