@@ -368,13 +368,15 @@ def roofline_for(kernel, ms, launches, per_step, wl, peaks, peak_src, w_separate
 
 
 def pass_roofline(wl, ms_per_step, peaks, peak_src):
-    """Whole forward pass against its own roofline: two streaming passes over
-    Q, K and V plus the output write (7 T e bytes) at the measured HBM rate,
-    and the dense contractions (landmark rows S and P V, token F and P W, the
-    conv as a banded product, the pseudo-inverse) at the tensor rate; the
-    slower of the two is the roofline time."""
+    """Whole forward pass against its own roofline: the method's minimum
+    traffic (6 T e bytes: Q and V read twice, K once, the output written once)
+    at the measured HBM rate, and the dense contractions (landmark rows S and
+    P V, token F and P W, the conv as a banded product, the pseudo-inverse) at
+    the tensor rate; the slower of the two is the roofline time. `frac_7te`
+    counts this implementation's schedule instead, which reads K twice (the
+    landmark pass and the landmark rows): 7 T e bytes."""
     te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
-    nbytes = 7.0 * te
+    nbytes = 6.0 * te
     n_tok = wl.B * wl.H * wl.n
     mm_flops = n_tok * (2.0 * wl.m * wl.d * 2 + 2.0 * wl.m * wl.d * 2 + 2.0 * wl.ks * wl.d)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
@@ -382,10 +384,12 @@ def pass_roofline(wl, ms_per_step, peaks, peak_src):
     mma_rate = peaks["bf16_tflops"] * 1e12 * (TF32_OVER_BF16 / 3.0 if wl.dtype == "f32" else 1.0)
     t_mma = mm_flops / mma_rate + pinv_peak_time(wl, peaks["bf16_tflops"])
     t_roof = max(t_hbm, t_mma)
+    t_roof7 = max(7.0 / 6.0 * t_hbm, t_mma)
     return {"bytes": nbytes, "flops": mm_flops + pinv_flops(wl), "t_hbm_us": t_hbm * 1e6,
             "t_tensor_us": t_mma * 1e6, "bound": "hbm" if t_hbm >= t_mma else "tensor",
             "t_roofline_us": t_roof * 1e6, "t_measured_us": ms_per_step * 1e3,
-            "frac": t_roof / (ms_per_step / 1e3),
+            "frac": t_roof / (ms_per_step / 1e3), "bytes_7te": 7.0 * te,
+            "frac_7te": t_roof7 / (ms_per_step / 1e3),
             "peak_source": f"hbm_gbs, bf16_tflops ({peak_src}); tf32 = bf16 x 1.1/2.25, fp16 = bf16"}
 
 
@@ -720,6 +724,16 @@ def run_ours(args, wl):
     value = job_throughput(tokens_step, world, steps, elapsed_ms)
     ms_per_step = elapsed_ms / steps
 
+    # the same steps on one input set (warm L2 where the inputs fit in it)
+    def step_warm(i):
+        q, k, v, out = sets[0]
+        N.nystrom_attn_fwd(q, k, v, w, out, B, H, n, d, m, wl.iters, wl.ks, dt_code, stream)
+
+    warm_ms, _ = time_fn(N, step_warm, stream)
+    warm_l2 = {"ms_per_step": warm_ms, "tokens_per_s": tokens_step * world / (warm_ms / 1e3),
+               "inputs": "one input set reused every step (in L2 when its 4 T e bytes fit there); "
+                         "the headline value rotates sets past L2"}
+
     # per-kernel times (CUDA events on the launch stream) over a second pass of
     # the same steps (capped), for the roofline of the dominant kernel
     prof_steps = min(steps, 500)
@@ -832,6 +846,7 @@ def run_ours(args, wl):
                                     "value and ms_per_step from the median region",
                    "parallelism": f"replicas x{world} (independent heads, no collective)"},
         "roofline": roofline, "pass_roofline": pass_roofline(wl, ms_per_step, peaks, peak_src),
+        "warm_l2": warm_l2,
         "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks, "gpu_launches": launches // max(1, len(region_ms)),
         "gpu_launches_all_regions": launches,

@@ -80,10 +80,14 @@ def test_pass_roofline_is_the_slower_of_bytes_and_flops():
     wl = workloads.WORKLOADS["c3"]
     te = wl.B * wl.H * wl.n * wl.d * wl.elem_bytes
     r = bench.pass_roofline(wl, 0.1, PEAKS, "measured")
-    assert r["bytes"] == 7 * te
-    assert r["t_hbm_us"] == pytest.approx(7 * te / 6000e9 * 1e6)
+    # the method's minimum traffic: Q and V twice, K once, the output once
+    assert r["bytes"] == 6 * te
+    assert r["t_hbm_us"] == pytest.approx(6 * te / 6000e9 * 1e6)
     assert r["t_roofline_us"] == pytest.approx(max(r["t_hbm_us"], r["t_tensor_us"]))
     assert r["frac"] == pytest.approx(r["t_roofline_us"] / 100.0)
+    # this schedule's traffic (K read twice) alongside
+    assert r["bytes_7te"] == 7 * te
+    assert r["frac_7te"] == pytest.approx(max(7 * te / 6000e9 * 1e6, r["t_tensor_us"]) / 100.0)
 
 
 def test_traffic_is_used_only_while_the_kernel_source_is_unchanged(tmp_path, monkeypatch):
