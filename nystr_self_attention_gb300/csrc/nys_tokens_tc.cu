@@ -123,20 +123,24 @@ struct Ring {
   }
 };
 
-// One 16-byte chunk (8 taps) of row t of the Toeplitz block: column u holds
-// w[u - t] for 0 <= u - t < ks and u < kc, else 0.
-__device__ __forceinline__ void toeplitz_chunk(uint8_t* tbuf, const float* wh, int ks, int kc,
-                                               int t, int u0) {
+// The Toeplitz operand of the conv: element (t, u) is w[u - t] (t the tile's
+// token, u the halo row), so its 64 x 64 block (r, c) depends on c - r only:
+// B_k[t'][u'] = w[64 k + u' - t']. It is kept as the list B_(nbox-1), ...,
+// B_0, B_-1 (= 0) of 8 KB blocks; K-box c of the operand (128 rows) is then
+// the window [B_c; B_c-1], which starts at block nbox - 1 - c. One 16-byte
+// chunk (8 taps, columns u0 ..) of row t' of list block blk:
+__device__ __forceinline__ void toeplitz_chunk(uint8_t* tbuf, const float* wh, int ks, int nbox,
+                                               int blk, int t, int u0) {
+  const int base = 64 * (nbox - 1 - blk) + u0 - t;  // tap index of column u0
   uint32_t wv[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int ua = u0 + 2 * e - t, ub = ua + 1;
-    const float fa = (ua >= 0 && ua < ks && u0 + 2 * e < kc) ? __ldg(wh + ua) : 0.f;
-    const float fb = (ub >= 0 && ub < ks && u0 + 2 * e + 1 < kc) ? __ldg(wh + ub) : 0.f;
+    const int ua = base + 2 * e, ub = ua + 1;
+    const float fa = (ua >= 0 && ua < ks) ? __ldg(wh + ua) : 0.f;
+    const float fb = (ub >= 0 && ub < ks) ? __ldg(wh + ub) : 0.f;
     wv[e] = pack_bf16x2(fa, fb);
   }
-  *reinterpret_cast<uint4*>(tbuf + (u0 >> 6) * 16384 + sw128_offset(t, (u0 & 63) * 2)) =
-      make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  *reinterpret_cast<uint4*>(tbuf + blk * 8192 + sw128_offset(t, u0 * 2)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
 template <int DP>
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
   const int g1 = min(p.total_tiles, g0 + p.tiles_per_cta);
   const int ntiles = g1 - g0;
   const int rad = p.ks > 0 ? (p.ks - 1) / 2 : 0;
-  const int kc64 = (p.kc + 63) & ~63;
+  const int nbox = (p.kc + 63) >> 6;  // 64-column boxes of the conv's K
   auto head_of = [&](int g) { return g / p.tiles_per_head; };
 
   if (tid == 0) {
@@ -185,9 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
   // the first head's Toeplitz block, by the whole CTA
   if (p.kc > 0 && ntiles > 0) {
     const float* wh = p.conv_w + (size_t)(head_of(g0) % p.H) * p.ks;
-    const int nch = kc64 >> 3;
-    for (int task = tid; task < 128 * nch; task += kThreads)
-      toeplitz_chunk(sm + p.off_t, wh, p.ks, p.kc, task / nch, (task % nch) * 8);
+    for (int task = tid; task < (nbox + 1) * 64 * 8; task += kThreads)
+      toeplitz_chunk(sm + p.off_t, wh, p.ks, nbox, task >> 9, (task >> 3) & 63, (task & 7) * 8);
     fence_async_smem();
   }
   tc_fence_before_sync();
@@ -349,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
             const uint64_t a0 = smem_desc(smem_u32(sm + p.off_t + tcur * p.t_bytes), 16, 1024, SW_128B);
             const uint64_t v0 = smem_desc(smem_u32(sm + p.off_v + rvc.i * p.v_stage), p.kc * 128, 1024, SW_128B);
             for (int kk = 0; kk < p.kc / 16; ++kk)
-              mma_bf16(acc + DP, a0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2), v0 + (uint64_t)(kk * 128), idc, kk > 0);
+              mma_bf16(acc + DP, a0 + (uint64_t)((nbox - 1 - (kk >> 2)) * 512 + (kk & 3) * 2),
+                       v0 + (uint64_t)(kk * 128), idc, kk > 0);
             mma_commit(&bars.vempty[rvc.i]);
             mma_commit(&bars.acc_full[jc & 1]);
             if (wc.last(tph, ntiles)) mma_commit(&bars.t_empty[tcur]);
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
   } else if (warp < 4) {
     // ------------------------------------------------- Toeplitz builders
     if (p.kc > 0 && ntiles > 0) {
-      const int lt = tid - 64;  // rows lt and lt + 64
+      const int lt = tid - 64;  // row lt of every block
       int hi = 0, cur_bh = head_of(g0);
       for (int j = 1; j < ntiles; ++j) {
         const int bh = head_of(g0 + j);
@@ -432,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) tokens_tc(const __grid_constant__
         if (hi >= p.nt && !wait_or_fail(&bars.t_empty[tb], ((hi / p.nt) - 1) & 1, p.status, abort_flag)) break;
         const float* wh = p.conv_w + (size_t)(bh % p.H) * p.ks;
         uint8_t* tbuf = sm + p.off_t + tb * p.t_bytes;
-        for (int rr = 0; rr < 2; ++rr)
-          for (int u0 = 0; u0 < kc64; u0 += 8) toeplitz_chunk(tbuf, wh, p.ks, p.kc, lt + rr * 64, u0);
+        for (int blk = 0; blk <= nbox; ++blk)
+          for (int u0 = 0; u0 < 64; u0 += 8) toeplitz_chunk(tbuf, wh, p.ks, nbox, blk, lt, u0);
         fence_async_smem();
         mbar_arrive(&bars.t_ready[tb]);
       }
@@ -579,7 +583,7 @@ bool plan_tokens(const Shape& s, TokPlan* pl) {
   pl->v_stage = (uint32_t)pl->kc * pl->DP * 2;
   pl->kt_bytes = (uint32_t)pl->m_pad * pl->DP * 2;
   pl->wt_bytes = (uint32_t)((pl->m_pad + 63) / 64) * pl->DP * 128;
-  pl->t_bytes = pl->kc > 0 ? (uint32_t)((pl->kc + 63) / 64) * 16384 : 0;
+  pl->t_bytes = pl->kc > 0 ? (uint32_t)((pl->kc + 63) / 64 + 1) * 8192 : 0;  // compact blocks
   const uint32_t need = 2 * pl->m_pad + 4 * pl->DP;
   if (need > 512) return false;
   uint32_t cols = 32;
