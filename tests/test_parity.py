@@ -139,6 +139,27 @@ def test_scores_rising_along_the_landmarks(d, m, dtype):
     assert rel_err(got, ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("rising", [False, True])
+def test_f32_landmark_rows_over_several_key_tiles(rising):
+    """160 heads (more than there are SMs): the fp32 landmark-row pass then
+    runs each head's key tiles in one CTA, one tile after another (the next
+    tile's loads during P V, the online softmax rescaling O), with a ragged
+    last tile; with keys rising along the sequence the running maximum grows
+    from tile to tile."""
+    import nystr_self_attention_gb300 as N
+    B, H, n, d, m = 1, 160, 1000, 64, 40
+    plan = N.nystrom_plan_describe(B, H, n, d, m, 6, 9, N.NYS_FP32)
+    assert "rows=rows_x3[splits=1,tiles_per_split=8]" in plan, plan
+    wl = workloads.custom(B, H, n, d, m, 6, 9, "f32")
+    inp = workloads.make_inputs(wl, seed=31 + rising)
+    if rising:
+        inp.k = (inp.k * (1.0 + 3.0 * np.arange(n) / n).astype(np.float32)[None, None, :, None]).astype(np.float32)
+    got, _ = run_gpu(inp)
+    ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, m, wl.iters)
+    for h in range(H):
+        assert rel_err(got[0, h], ref[0, h]) <= TOL["f32"], h
+
+
 # ------------------------------------------------------------------ stages ----
 
 # few heads: the pseudo-inverse runs beside the landmark-row pass and W = Z G
