@@ -160,6 +160,30 @@ def test_f32_landmark_rows_over_several_key_tiles(rising):
         assert rel_err(got[0, h], ref[0, h]) <= TOL["f32"], h
 
 
+@pytest.mark.parametrize("shape", [
+    (2, 4, 384, 64, 32),   # four heads stacked per CTA (m_pad 32)
+    (2, 4, 384, 32, 32),   # four heads, d = 32
+    (1, 6, 256, 32, 64),   # two heads per CTA, d = 32, three CTAs
+    (1, 3, 200, 64, 24),   # three heads in one CTA (N = 96 products)
+    (1, 5, 200, 64, 24),   # four heads, then one in the last CTA
+], ids=lambda s: "B%dH%dn%dd%dm%d" % s)
+def test_f32_pseudo_inverse_with_stacked_heads(shape):
+    """The fp32 pseudo-inverse on the tensor cores (three tf32 products per
+    product) with several heads stacked along the TMEM lanes of one CTA."""
+    import nystr_self_attention_gb300 as N
+    B, H, n, d, m = shape
+    assert "pinv=pinv_tc[" in N.nystrom_plan_describe(B, H, n, d, m, 6, 5, N.NYS_FP32)
+    wl = workloads.custom(B, H, n, d, m, 6, 5, "f32")
+    inp = workloads.make_inputs(wl, seed=41 + m)
+    got, ws = run_gpu(inp, workspace=True)
+    ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, m, wl.iters)
+    assert rel_err(got, ref) <= TOL["f32"]
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    st = stage(ws, wl, N.NYS_STAGE_Z, m, m)
+    for (b, h), r in oracle_heads(inp, heads).items():
+        assert rel_err(st[b * H + h], r["z"]) <= 1e-4, (b, h)
+
+
 # ------------------------------------------------------------------ stages ----
 
 # few heads: the pseudo-inverse runs beside the landmark-row pass and W = Z G
