@@ -22,18 +22,19 @@ def library():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 256, 64, 32), (16, 8, 512, 64, 128)],
-                         ids=["z-beside-rows", "serial"])
-def test_timeout_is_reported_and_the_next_call_is_correct(shape):
+@pytest.mark.parametrize("shape,dtype", [((1, 2, 256, 64, 32), "bf16"), ((16, 8, 512, 64, 128), "bf16"),
+                                         ((1, 2, 256, 64, 32), "f32")],
+                         ids=["z-beside-rows", "serial", "fp32-three-products"])
+def test_timeout_is_reported_and_the_next_call_is_correct(shape, dtype):
     import torch
     import nystr_self_attention_gb300 as N
     B, H, n, d, m = shape
-    wl = workloads.custom(B, H, n, d, m, 6, 9, "bf16")
-    assert "pinv_tc" in N.nystrom_plan_describe(B, H, n, d, m, 6, 9, N.NYS_BF16)
+    wl = workloads.custom(B, H, n, d, m, 6, 9, dtype)
+    assert "pinv_tc" in N.nystrom_plan_describe(B, H, n, d, m, 6, 9, dtype_code(dtype))
     inp = workloads.make_inputs(wl, seed=77)
     q, k, v, w = to_device(inp)
     out = torch.empty_like(q)
-    args = (B, H, n, d, m, wl.iters, wl.ks, dtype_code("bf16"))
+    args = (B, H, n, d, m, wl.iters, wl.ks, dtype_code(dtype))
     try:
         N.nystrom_debug_stall_pinv(True)
         N.nystrom_attn_fwd(q, k, v, w, out, *args)
@@ -48,7 +49,7 @@ def test_timeout_is_reported_and_the_next_call_is_correct(shape):
     ref = R.nystrom_attention(inp.q, inp.k, inp.v, inp.conv_w, m, wl.iters, heads=[(0, 0), (B - 1, H - 1)])
     got = out.float().cpu().numpy()
     for b, h in [(0, 0), (B - 1, H - 1)]:
-        assert rel_err(got[b, h], ref[b, h]) <= TOL["bf16"]
+        assert rel_err(got[b, h], ref[b, h]) <= TOL[dtype]
 
 
 def test_switch_rejects_other_values():
