@@ -260,7 +260,7 @@ KERNEL_BYTES = {
     "landmarks_vec": 2.0, "landmarks_small": 2.0, "landmarks_simt": 2.0,  # read Q, K
     "rows_tc": 2.0, "rows_simt": 2.0, "rows_x3": 2.0,  # read K, V
     "tokens_tc": 3.0, "tokens_simt": 3.0, "tokens_big": 3.0,  # read Q, V; write out
-    "tokens_x3": 2.0,                             # read Q; write out (attention term)
+    "tokens_x3": 3.0,                             # read Q, V; write out (the conv fused)
     "conv_mask": 3.0,                             # read V, out; write out
 }
 KERNEL_SOURCES = {

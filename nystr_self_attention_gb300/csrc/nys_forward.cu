@@ -152,17 +152,17 @@ int run_group(const Shape& full, const Shape& sg_in, long long bh0, const void* 
   }
   if (rc != NYS_OK) return rc;
   Shape stok = sg;  // the token pass: with the variants, the attention term alone
-  if (full.separate_conv() || x3) stok.ks = 0;
+  if (full.separate_conv()) stok.ks = 0;
   if (tc_tokens)
     rc = launch_tokens_tc(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else if (big_tokens)
     rc = launch_tokens_big(stok, qg, vg, kt_b, wt_b, conv_w, og, status, plan_sms(), st);
   else if (x3)
-    rc = launch_tokens_x3(stok, qg, kt, w, og, status, st);
+    rc = launch_tokens_x3(stok, qg, vg, kt, w, stok.ks > 0 ? conv_w : nullptr, og, status, st);
   else
     rc = launch_tokens_simt(stok, qg, vg, kt, w, stok.ks > 0 ? conv_w : nullptr, og, st);
   rc = error_in("token rows", rc);
-  if (rc == NYS_OK && (full.separate_conv() || (x3 && full.ks > 0)))
+  if (rc == NYS_OK && full.separate_conv())
     rc = error_in("convolution", launch_conv_mask(sg, vg, conv_w, og, st));
   return rc;
 }
@@ -245,7 +245,7 @@ std::string describe_plan(const Shape& s) {
          : big_tokens ? " tokens=tokens_big"
          : x3_supported(s) ? " tokens=tokens_x3"
                            : " tokens=tokens_simt";
-  if (s.separate_conv() || (x3_supported(s) && s.ks > 0)) out += " conv=conv_mask";
+  if (s.separate_conv()) out += " conv=conv_mask";
   return out;
 }
 

@@ -124,14 +124,15 @@ int launch_tokens_big(const Shape& s, const void* q, const void* v, const void* 
 // fp32 landmark-row and token-row passes on the tensor cores in three tf32
 // products (nys_x3.cu): fp32, d <= 64 with d % 4 == 0, m <= 128. The
 // landmark-row pass splits each head's 128-key tiles into `splits` ranges
-// of `tiles_per_split` (x3_rows_split); the token pass writes the attention
-// term only (the convolution is added by conv_mask).
+// of `tiles_per_split` (x3_rows_split); the token pass adds the
+// convolution of V (per-head taps) when s.ks > 0, else writes the attention
+// term alone.
 bool x3_supported(const Shape& s);
 void x3_rows_split(const Shape& s, int* splits, int* tiles_per_split);
 int launch_rows_x3(const Shape& s, const float* qt, const void* k, const void* v, float* gpart,
                    float* gml, int splits, int tiles_per_split, int* status, cudaStream_t stream);
-int launch_tokens_x3(const Shape& s, const void* q, const float* kt, const float* w, void* out,
-                     int* status, cudaStream_t stream);
+int launch_tokens_x3(const Shape& s, const void* q, const void* v, const float* kt, const float* w,
+                     const float* conv_w, void* out, int* status, cudaStream_t stream);
 
 // Tensor-core landmark-row kernel (nys_rows_tc.cu), bf16 inputs. `s` may be
 // a group of heads of the full problem: splits / tiles_per_split come from

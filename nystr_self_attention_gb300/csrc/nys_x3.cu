@@ -38,16 +38,20 @@ struct X3Params {
   float* o;             // landmark rows: partial O [BH][splits][m][d]; token rows: out [BH][n][d]
   float* ml;            // landmark rows: [BH][splits][m][2] (max of the scaled scores, sum)
   const int* lengths;   // landmark rows: keys at or past lengths[b] take no part (null: none)
+  const float* vseq;    // token rows with the conv: V [BH][n][d]
+  const float* conv_w;  // token rows with the conv: [H][ks] taps (null: no conv)
   int* status;
   int H, n, d, m;
   int splits, tiles_per_split;  // landmark rows
   int tiles_per_head;           // token rows
+  int ks;                       // token rows: conv taps (0: the attention term alone)
   float c;                      // scale * log2(e)
   float scale;                  // 1 / sqrt(d)
 };
 
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kConvRun = 16;  // conv outputs per item: consecutive rows of one column
 constexpr uint32_t COL_S = 0, COL_PL = 128, COL_O = 256, kTmemCols = 512;
 
 __device__ __forceinline__ float tf32_hi(float x) {
@@ -389,6 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_x3(const X3Params p) {
     for (int e = 0; e < HC; ++e) o[e] = 0.f;
   }
   const int c0 = half * HC;
+  const bool fuse_conv = !ROWS && p.ks > 0;  // uniform
+  float* att_s = reinterpret_cast<float*>(sm);  // with the conv: the tile's attention term [128][DP]
   if (alive && row < q_rows) {
     float* dst;
     if constexpr (ROWS) {
@@ -401,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_x3(const X3Params p) {
       }
     } else {
       const int t = (int)(blockIdx.x - bh * p.tiles_per_head);
-      dst = p.o + ((size_t)bh * p.n + (size_t)t * 128 + row) * d;
+      // the operand buffers are free (the last P V is done): with the conv,
+      // the attention term waits there for it
+      dst = fuse_conv ? att_s + (size_t)row * DP : p.o + ((size_t)bh * p.n + (size_t)t * 128 + row) * d;
       const float inv = 1.f / lrun;
 #pragma unroll
       for (int e = 0; e < HC; ++e) o[e] *= inv;
@@ -409,6 +417,72 @@ __global__ void __launch_bounds__(kThreads, 1) attn_x3(const X3Params p) {
 #pragma unroll
     for (int e = 0; e < HC; e += 4)
       if (c0 + e < d) *reinterpret_cast<float4*>(dst + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+  }
+  if constexpr (!ROWS) {
+    if (fuse_conv && alive) {  // uniform
+      // out[t][c] = att[t][c] + sum_j w[h][j] V[t + j - (ks - 1)/2][c], V
+      // rows outside [0, n) zero, in fp32 FMAs: the tile's V rows with the
+      // halo and the head's taps staged in the free operand buffers; an
+      // item is kConvRun consecutive rows of one column, the V window in a
+      // ring of registers whose indices the tap loop (unrolled in blocks of
+      // kConvRun) keeps static: a tap costs one weight, one new V value and
+      // kConvRun FMAs
+      const int rad = (p.ks - 1) / 2, vrows = 128 + 2 * rad;
+      float* v_s = att_s + 128 * DP;            // [vrows][DP]: V rows tok0 - rad ..
+      float* w_s = v_s + (size_t)vrows * DP;    // [ks]
+      const int tok0 = (int)(blockIdx.x - bh * p.tiles_per_head) * 128;
+      const float* vb = p.vseq + (size_t)bh * p.n * d;
+      const int d4 = d >> 2;
+      for (int e = tid; e < vrows * d4; e += kThreads) {
+        const int r = e / d4, c4 = (e - r * d4) * 4, u = tok0 - rad + r;
+        const float4 x = (u >= 0 && u < p.n) ? __ldg(reinterpret_cast<const float4*>(vb + (size_t)u * d + c4))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(v_s + (size_t)r * DP + c4) = x;
+      }
+      const float* wh = p.conv_w + (size_t)(bh % p.H) * p.ks;
+      for (int j = tid; j < p.ks; j += kThreads) w_s[j] = wh[j];
+      __syncthreads();
+      const int ks_full = p.ks - p.ks % kConvRun;  // taps in whole blocks
+      for (int item = tid; item < (128 / kConvRun) * d; item += kThreads) {
+        const int c = item % d, r0 = (item / d) * kConvRun;
+        if (tok0 + r0 >= p.n) continue;
+        float acc[kConvRun], xw[kConvRun];
+        const float* x = v_s + (size_t)r0 * DP + c;
+#pragma unroll
+        for (int r = 0; r < kConvRun; ++r) {
+          acc[r] = 0.f;
+          xw[r] = x[r * DP];  // before tap j, row r0 + j + r sits in xw[(j + r) % kConvRun]
+        }
+        const float* xp = x + kConvRun * DP;  // row r0 + j + kConvRun: xp[j * DP]
+        const float* wp = w_s;
+        // whole blocks: ks is odd, so a block never holds the last tap and
+        // every next row lies inside the staged rows
+        for (int jb = 0; jb < ks_full; jb += kConvRun) {
+#pragma unroll
+          for (int jj = 0; jj < kConvRun; ++jj) {
+            const float wj = wp[jj];
+#pragma unroll
+            for (int r = 0; r < kConvRun; ++r) acc[r] = fmaf(wj, xw[(jj + r) % kConvRun], acc[r]);
+            xw[jj] = xp[jj * DP];
+          }
+          wp += kConvRun;
+          xp += kConvRun * DP;
+        }
+#pragma unroll
+        for (int jj = 0; jj < kConvRun; ++jj) {
+          const int j = ks_full + jj;
+          if (j >= p.ks) break;
+          const float wj = wp[jj];
+#pragma unroll
+          for (int r = 0; r < kConvRun; ++r) acc[r] = fmaf(wj, xw[(jj + r) % kConvRun], acc[r]);
+          if (j + 1 < p.ks) xw[jj] = xp[jj * DP];
+        }
+        float* dst = p.o + ((size_t)bh * p.n + tok0 + r0) * d + c;
+#pragma unroll
+        for (int r = 0; r < kConvRun; ++r)
+          if (tok0 + r0 + r < p.n) dst[(size_t)r * d] = att_s[(size_t)(r0 + r) * DP + c] + acc[r];
+      }
+    }
   }
 
   // wind-down: no product of this CTA may still be in flight
@@ -483,13 +557,17 @@ int launch_rows_x3(const Shape& s, const float* qt, const void* k, const void* v
                    : launch_x3<64, true>(p, items, "rows_x3", stream);
 }
 
-int launch_tokens_x3(const Shape& s, const void* q, const float* kt, const float* w, void* out,
-                     int* status, cudaStream_t stream) {
+int launch_tokens_x3(const Shape& s, const void* q, const void* v, const float* kt, const float* w,
+                     const float* conv_w, void* out, int* status, cudaStream_t stream) {
   if (!x3_supported(s)) return NYS_ERR_UNSUPPORTED;
+  if (s.ks > 0 && (!conv_w || s.ks % 2 == 0)) return NYS_ERR_ARG;
   X3Params p = base_params(s, status);
   p.q = static_cast<const float*>(q);
   p.k = kt;
   p.v = w;
+  p.vseq = static_cast<const float*>(v);
+  p.conv_w = s.ks > 0 ? conv_w : nullptr;
+  p.ks = s.ks;
   p.o = static_cast<float*>(out);
   p.tiles_per_head = (s.n + 127) / 128;
   const long long items = s.bh() * p.tiles_per_head;
