@@ -84,6 +84,17 @@ __device__ __forceinline__ void store_col32(uint8_t* buf, int rows, int col, int
     *reinterpret_cast<float*>(base + e * 128 + ((L ^ (uint32_t)(e & 7)) << 4)) = v[e];
 }
 
+// v[e] -> element (j0 + e, col) for e < 16 (j0 % 8 == 0), as store_col32
+__device__ __forceinline__ void store_col16(uint8_t* buf, int rows, int col, int j0,
+                                            const float (&v)[16]) {
+  uint8_t* base = buf + (uint32_t)(col >> 5) * (uint32_t)(rows * 128) + (uint32_t)j0 * 128u +
+                  (uint32_t)(col & 3) * 4u;
+  const uint32_t L = (uint32_t)(col & 31) >> 2;
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    *reinterpret_cast<float*>(base + e * 128 + ((L ^ (uint32_t)(e & 7)) << 4)) = v[e];
+}
+
 // four consecutive elements (row, c .. c+3), c % 4 == 0, as one 16-byte store
 __device__ __forceinline__ void store_row4(uint8_t* buf, int rows, int row, int c, float4 v) {
   *reinterpret_cast<float4*>(buf + kmaj_off(row, c, rows)) = v;
@@ -113,8 +124,12 @@ __device__ __forceinline__ void split_tf32(float x, float& h, float& l) {
 // (A_hi B_hi + A_lo B_hi + A_hi B_lo), for fp32 inputs (MP <= 64): the lo
 // halves of A_S, of the B operand and of G^T sit in shared memory beside
 // the hi halves, those of Z and X in TMEM beside theirs.
-template <int MP, bool X3>
-__global__ void __launch_bounds__(kThreads, (MP == 128 || X3) ? 1 : 2)
+// THREE: each update in three dependent levels of products instead of four
+// (X = A_S Z; X X and Z X side by side over one B operand; Z' = 1/4 (13 Z -
+// 15 Z X + Z X (7X - X^2)) accumulated onto 13 Z - 15 Z X), with a second
+// accumulator in TMEM: where one CTA per SM runs anyway.
+template <int MP, bool X3, bool THREE>
+__global__ void __launch_bounds__(kThreads, (MP == 128 || X3 || THREE) ? 1 : 2)
     pinv_tc(const __grid_constant__ PinvParams p) {
   constexpr int NCH = MP / 32;  // 32-column chunks of a head's m x m block
   extern __shared__ uint8_t smem_raw[];
@@ -170,8 +185,10 @@ __global__ void __launch_bounds__(kThreads, (MP == 128 || X3) ? 1 : 2)
   const uint32_t tmem = tmem_base_sh;
   const uint32_t lo = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t COL_Z = 0, COL_X = MP, COL_D = 2 * MP;  // main loop
-  // X3: lo halves of Z and X after the product region
-  const uint32_t COL_ZL = COL_D + (uint32_t)max(NP, NW), COL_XL = COL_ZL + MP;
+  // THREE: the second accumulator (Z X) after the product region; X3: lo
+  // halves of Z and X after those
+  const uint32_t COL_D2 = COL_D + (uint32_t)max(NP, NW);
+  const uint32_t COL_ZL = COL_D2 + (THREE ? (uint32_t)NP : 0u), COL_XL = COL_ZL + MP;
   const uint32_t COL_QH = 0, COL_QL = d, COL_S = 2 * d;  // score step
   const uint32_t dblk = (uint32_t)(hs * MP);  // this head's block of a stacked result
 
@@ -205,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, (MP == 128 || X3) ? 1 : 2)
   // a_col_lo / a_smem_lo and b_lo
   auto issue = [&](uint32_t d_col, uint32_t a_col, uint32_t a_col_lo, const uint8_t* a_smem,
                    const uint8_t* a_smem_lo, const uint8_t* b, const uint8_t* b_lo, int b_rows,
-                   int k_dim) {
-    issue1(d_col, a_col, a_smem, b, b_rows, k_dim, false);
+                   int k_dim, bool acc = false) {
+    issue1(d_col, a_col, a_smem, b, b_rows, k_dim, acc);
     if constexpr (X3) {
       issue1(d_col, a_col_lo, a_smem ? a_smem_lo : nullptr, b, b_rows, k_dim, true);
       issue1(d_col, a_col, a_smem, b_lo, b_rows, k_dim, true);
@@ -514,7 +531,86 @@ __global__ void __launch_bounds__(kThreads, (MP == 128 || X3) ? 1 : 2)
     tc_fence_before_sync();
     __syncthreads();
   };
-  for (int it = 0; it < p.iters && !*abort_flag; ++it) {
+  // three levels: X X -> D and Z X -> D2 over one B operand (X)
+  auto gemm2 = [&]() {
+    if (tid == 0) {
+      tc_fence_after_sync();
+      issue(COL_D, COL_X, COL_XL, nullptr, nullptr, bbuf, bbuf_lo, NP, MP);
+      issue(COL_D2, COL_Z, COL_ZL, nullptr, nullptr, bbuf, bbuf_lo, NP, MP);
+      mma_commit(&bar_mma);
+    }
+    if (exp_row < hp * m) export_rows();
+    wait_mma();
+  };
+  // D (holding 13 Z - 15 Z X) += Z X (7X - X^2): A = Z X (TMEM, in X's columns)
+  auto gemm3 = [&]() {
+    if (tid == 0) {
+      tc_fence_after_sync();
+      issue(COL_D, COL_X, COL_XL, nullptr, nullptr, bbuf, bbuf_lo, NP, MP, true);
+      mma_commit(&bar_mma);
+    }
+    if (exp_row < hp * m) export_rows();
+    wait_mma();
+  };
+  // the level-2 epilogue, 16 columns at a time of this row of the head's
+  // blocks of X X (D), Z X (D2), X and Z: B <- 7X - X^2 (transposed), X's
+  // columns <- Z X (the A operand of the last level), D <- 13 Z - 15 Z X
+  auto epi2 = [&]() {
+    if (head_ok) {
+      for (int c = half; c < MP / 16; c += 2) {
+        const int j0 = c * 16;
+        uint32_t x2[16], zx[16], xv[16], zv[16], xl[16], zl[16];
+        tmem_ld16(tmem + lo + COL_D + dblk + j0, x2);
+        tmem_ld16(tmem + lo + COL_D2 + dblk + j0, zx);
+        tmem_ld16(tmem + lo + COL_X + j0, xv);
+        tmem_ld16(tmem + lo + COL_Z + j0, zv);
+        if constexpr (X3) {
+          tmem_ld16(tmem + lo + COL_XL + j0, xl);
+          tmem_ld16(tmem + lo + COL_ZL + j0, zl);
+        }
+        tmem_ld_wait();
+        float b[16], bl[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x = __uint_as_float(xv[e]) + (X3 ? __uint_as_float(xl[e]) : 0.f);
+          const float z = __uint_as_float(zv[e]) + (X3 ? __uint_as_float(zl[e]) : 0.f);
+          const float zxe = __uint_as_float(zx[e]);
+          b[e] = fmaf(7.f, x, -__uint_as_float(x2[e]));
+          zv[e] = __float_as_uint(fmaf(13.f, z, -15.f * zxe));
+          if constexpr (X3) {
+            split_tf32(b[e], b[e], bl[e]);
+            float h, l;
+            split_tf32(zxe, h, l);
+            zx[e] = __float_as_uint(h);
+            xl[e] = __float_as_uint(l);
+          }
+        }
+        store_col16(bbuf, NP, li, hs * MP + j0, b);
+        if constexpr (X3) {
+          store_col16(bbuf_lo, NP, li, hs * MP + j0, bl);
+          tmem_st16(tmem + lo + COL_XL + j0, xl);
+        }
+        tmem_st16(tmem + lo + COL_X + j0, zx);
+        tmem_st16(tmem + lo + COL_D + dblk + j0, zv);
+      }
+    }
+    fence_async_smem();
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncthreads();
+  };
+  for (int it = 0; THREE && it < p.iters && !*abort_flag; ++it) {
+    gemm(0, abuf);                          // X = A_S Z
+    if (*abort_flag) break;
+    store_bt(0.f, 1.f, 1.f, (int)COL_X);    // B <- X ; X -> TMEM
+    gemm2();                                // X X, Z X
+    if (*abort_flag) break;
+    epi2();                                 // B <- 7X - X^2 ; Z X -> TMEM ; D <- 13Z - 15ZX
+    gemm3();                                // D += Z X (7X - X^2)
+    if (*abort_flag) break;
+    store_bt(0.f, 1.f, 0.25f, (int)COL_Z);  // Z <- D / 4 ; B <- Z by columns
+  }
+  for (int it = 0; !THREE && it < p.iters && !*abort_flag; ++it) {
     gemm(0, abuf);                          // X = A_S Z
     if (*abort_flag) break;
     store_bt(7.f, -1.f, 1.f, (int)COL_X);   // B <- 7I - X ; X -> TMEM
@@ -863,7 +959,12 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   const bool x3 = s.dtype == NYS_FP32;
   p.hp = heads_per_cta(s);
   const int NP = p.hp * MP, NW = p.hp * s.d;
-  const uint32_t need = std::max<uint32_t>(2 * s.d + NP, (x3 ? 4 : 2) * MP + std::max(NP, NW));
+  // three levels per update where the CTAs run one per SM anyway (the
+  // second accumulator takes TMEM that two CTAs per SM would share)
+  const int grid_ctas = (p.BH + p.hp - 1) / p.hp;
+  const uint32_t base_cols = (x3 ? 4 : 2) * MP + std::max(NP, NW);
+  const bool three = (x3 || grid_ctas <= plan_sms()) && base_cols + NP <= 512;
+  const uint32_t need = std::max<uint32_t>(2 * s.d + NP, base_cols + (three ? NP : 0));
   uint32_t cols = 32;
   while (cols < need) cols <<= 1;
   p.tmem_cols = cols;
@@ -879,8 +980,9 @@ int launch_pinv_tc(const Shape& s, const float* qt, const float* kt, const float
   p.bbuf_lo_off = (uint32_t)(base + abytes);
   p.gbuf_lo_off = (uint32_t)(base + abytes + bbytes);
   const size_t smem = (x3 ? base + abytes + bbytes + gbytes : base) + 1024;
-  auto kern = x3 ? (MP == 32 ? pinv_tc<32, true> : pinv_tc<64, true>)
-                 : (MP == 32 ? pinv_tc<32, false> : (MP == 64 ? pinv_tc<64, false> : pinv_tc<128, false>));
+  auto kern = x3 ? (MP == 32 ? pinv_tc<32, true, true> : pinv_tc<64, true, true>)
+           : three ? (MP == 32 ? pinv_tc<32, false, true> : (MP == 64 ? pinv_tc<64, false, true> : pinv_tc<128, false, true>))
+                   : (MP == 32 ? pinv_tc<32, false, false> : (MP == 64 ? pinv_tc<64, false, false> : pinv_tc<128, false, false>));
   // (two CTAs per SM for MP <= 64: the largest shared-memory carveout)
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
