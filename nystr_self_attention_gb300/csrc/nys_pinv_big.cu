@@ -20,11 +20,12 @@
 // (128 x 128 accumulators in TMEM; its block of Z stays in TMEM across the
 // updates, and level 2 accumulates onto 13 Z - 15 Z X written there by the
 // level-1 epilogue). Product operands live in global memory (L2 resident) as
-// fp16 row-major copies of the left factors and fp16 TRANSPOSED copies of the
-// right factors; TMA streams 64-column K-chunks into a two-stage shared-memory
-// ring, and level 1's two products share one stream of their right factor.
-// Each epilogue writes the next level's operands, then the cluster
-// synchronises before they are read.
+// one fp16 row-major copy each (Z, X, Z X, 7X - X^2): a left factor is read
+// K-major from it, a right factor MN-major (64-row K-chunks of the same
+// rows), so each product block is written once. TMA streams 64-wide
+// K-chunks into a two-stage shared-memory ring, and level 1's two products
+// share one stream of their right factor. Each epilogue writes the next
+// level's operands, then the cluster synchronises before they are read.
 // Why fp16 operands: the chain's time goes to moving operands (an SM writes
 // to L2 at about 32 bytes per clock, and a tf32 product reads shared memory
 // as fast as TMA fills it), and fp16 halves those bytes. Its 11-bit
@@ -56,18 +57,23 @@ namespace {
 
 using namespace sm100;
 
-// fp16 operand matrices [B*H][m][mp] (A_S, Z, X, Z X, two transposed right
-// factors), then the fp32 maps of W = Z G: G^T [B*H][d][m] and Z [B*H][m][m]
-enum MapIdx { MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_T1 = 4, MAP_T2 = 5, MAP_GT = 6, MAP_Z32 = 7 };
+// Loads: the fp16 operand matrices [B*H][m][mp] as left factors (A_S, Z, X,
+// Z X: boxes of 128 rows x 64 columns) and as right factors (Z, X, 7X - X^2:
+// boxes of 64 rows x 64 columns, read MN-major), then the fp32 maps of
+// W = Z G: G^T [B*H][d][m] and Z [B*H][m][m]
+enum MapIdx {
+  MAP_A = 0, MAP_Z = 1, MAP_XR = 2, MAP_ZX = 3, MAP_BZ = 4, MAP_BX = 5, MAP_GT = 6, MAP_Z32 = 7,
+  MAP_BY = 8, kLoadMaps = 9
+};
 
-// store-only maps beside the six fp16 matrices' store maps
-enum StoreIdx { ST_AS32 = 6, ST_Z16T = 7 };
+// Stores: row-major 32 x 64 boxes (SWIZZLE_128B) of A_S, Z, X, Z X and
+// 7X - X^2 (fp16); then A_S fp32 in 32 x 32 boxes (SWIZZLE_128B) and Z_0
+// fp16 from its transposed staging, 32 x 32 boxes (SWIZZLE_64B)
+enum StoreIdx { ST_Y = 4, ST_AS32 = 6, ST_Z16T = 7, kStoreMaps = 8 };
 
 struct BigPinvMaps {
-  CUtensorMap m[8];   // loads: fp16 boxes of 128 rows x 64 columns; fp32 boxes of <= 128 rows x 32
-  CUtensorMap st[8];  // stores of the fp16 matrices: row-major 32 x 64 boxes (SWIZZLE_128B),
-                      // transposed ones 32 x 32 (SWIZZLE_64B); then A_S fp32 in 32 x 32 boxes
-                      // (SWIZZLE_128B) and Z fp16 in 32 x 32 boxes (SWIZZLE_64B)
+  CUtensorMap m[kLoadMaps];
+  CUtensorMap st[kStoreMaps];
 };
 
 struct BigPinvParams {
@@ -82,8 +88,7 @@ struct BigPinvParams {
   __half* z16;         // [B*H][m][mp]  Z (row-major)              row pitch mp)
   __half* xr16;        // [B*H][m][mp]  X = A_S Z (row-major)
   __half* zx16;        // [B*H][m][mp]  Z X (row-major)
-  __half* t1_16;       // [B*H][m][mp]  transposed right factors: Z^T, X^T and (7X - X^2)^T,
-  __half* t2_16;       // [B*H][m][mp]  alternating between the two buffers
+  __half* y16;         // [B*H][m][mp]  7X - X^2 (row-major)
   float* gt;           // [B*H][d][m]   G^T
   float* w;            // [B*H][m][d]
   __nv_bfloat16* wt;   // [B*H][dpad][m64] zero padded
@@ -95,8 +100,9 @@ struct BigPinvParams {
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kThreads = 192;
 // The operand ring: two stages of two K-chunks each. A stage holds, per
-// chunk, a 128 x 32 fp32 box of up to two left factors and one <= 128 x 32
-// box of the right factor, behind one mbarrier: an mbarrier round trip costs
+// chunk, the 128 x 64 fp16 boxes of up to two left factors and the right
+// factor's 64 K-rows x 128 columns as two 64 x 64 boxes (W: one <= 128 x 32
+// fp32 box, K-major), behind one mbarrier: an mbarrier round trip costs
 // about as much as streaming 16 KB, so stages are made large, not many.
 constexpr int kStages = 2;
 constexpr uint32_t kStageBytes = 98304;
@@ -445,17 +451,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  // Z_0 = alpha A_S^T: Z_0 row-major (transposed store of the A_S block,
-  // fp32 by plain coalesced stores and fp16 by TMA) and Z_0^T = alpha A_S
-  // (fp16 by TMA, the first update's right factor)
+  // Z_0 = alpha A_S^T row-major: the transposed A_S block, fp32 by plain
+  // coalesced stores and fp16 by TMA
   if (worker && !*abort_flag) {
     const float n1 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     const float ninf = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
     const float alpha = 1.f / (n1 * ninf);
     float* z = p.z + bh * mm;
-    // fp16 staging, SWIZZLE_64B tiles of 32 x 32: alpha A_S (this warp's
-    // rows, 32 columns per tile) and its transpose (32 block columns per tile)
-    uint8_t* zt_stage = sm + 98304 + warp * 8192;
+    // fp16 staging of the transpose, SWIZZLE_64B tiles of 32 x 32 (32 block
+    // columns per tile)
     uint8_t* z16_stage = sm + 131072 + warp * 8192;
     for (int j0 = 0; j0 < 128; j0 += 32) {
       uint32_t v[32];
@@ -468,17 +472,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           if (gj < m) z[(size_t)gj * m + gi] = alpha * __uint_as_float(v[e]);
         }
       }
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const __half2 h2 = __floats2half2_rn(alpha * __uint_as_float(v[2 * e]), alpha * __uint_as_float(v[2 * e + 1]));
-        pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
-      uint8_t* rt = zt_stage + (j0 >> 5) * 2048;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(rt + sw64_offset(lane, q * 16)) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       uint8_t* tt = z16_stage + (j0 >> 5) * 2048;
 #pragma unroll
       for (int e = 0; e < 32; ++e)
@@ -487,10 +480,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      for (int k = 0; k < 4; ++k) {
-        tma_store_3d(&maps.st[MAP_T1], zt_stage + k * 2048, 128 * c + 32 * k, 128 * r + 32 * warp, bh);
+      for (int k = 0; k < 4; ++k)
         tma_store_3d(&maps.st[ST_Z16T], z16_stage + k * 2048, 128 * r + 32 * warp, 128 * c + 32 * k, bh);
-      }
       bulk_commit();
     }
   }
@@ -525,10 +516,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   fence_proxy_async_all();
   tc_fence_after_sync();
 
-  // ---- 4) the products: three levels per update, then W = Z G. Per
-  // update, the transposed right factors alternate between t1 and t2: Z^T
-  // is in `tc` (t1 on even updates), X^T goes to the other one (`to`),
-  // (7X - X^2)^T back to `tc`, and Z'^T to `to`, the next update's `tc`.
+  // ---- 4) the products: three levels per update, then W = Z G. Right
+  // factors: Z (level 0), X (level 1), 7X - X^2 (level 2), G^T (W).
   const int nprod = 3 * p.iters + 1;
   const int hw = d >> 1;
   uint32_t kg_prod = 0, kg_mma = 0;   // ring positions of the producer / issuer
@@ -536,17 +525,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   int it = 0, lv = 0;                 // update and level of product pi
   for (int pi = 0; pi < nprod; ++pi) {
     const bool is_w = pi == nprod - 1;
-    const int tc = (it & 1) ? MAP_T2 : MAP_T1, to = (it & 1) ? MAP_T1 : MAP_T2;
-    // Update products (fp16): K-chunks of 64 columns, every operand streamed;
+    // Update products (fp16): K-chunks of 64, every operand streamed (the
+    // right factor MN-major: 64 of its rows, as two boxes of 64 columns);
     // level 1 runs its two products over one stream of the shared right
     // factor. W (tf32): K-chunks of 32 columns; its left factor Z is read
     // from TMEM (R0) for the K-block this CTA holds and streamed for the
     // other.
     const int amap1 = is_w ? MAP_Z32 : (lv == 0 ? MAP_A : (lv == 1 ? MAP_XR : MAP_ZX));
-    const int bmap = is_w ? MAP_GT : (lv == 1 ? to : tc);
+    const int bmap = is_w ? MAP_GT : (lv == 0 ? MAP_BZ : (lv == 1 ? MAP_BX : MAP_BY));
     const bool two = !is_w && lv == 1;
     const int kw = is_w ? 32 : 64;  // K-chunk width (elements)
-    const int b_row0 = is_w ? c * hw : 128 * c;
+    const int b_row0 = c * hw;  // W: this CTA's rows of G^T
     const int n_cols = is_w ? hw : 128;
     const uint32_t b_bytes = (uint32_t)n_cols * 128u;
     // stage j of a product holds K-chunks 2j and 2j + 1 (a chunk past m is
@@ -575,14 +564,19 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
               tma_load_3d(sa + q * 16384, &maps.m[amap1], &full[st], kx, 128 * r, bh);
               if (two) tma_load_3d(sa + kOffA2 + q * 16384, &maps.m[MAP_Z], &full[st], kx, 128 * r, bh);
             }
-            tma_load_3d(sa + kOffB + q * 16384, &maps.m[bmap], &full[st], kx, b_row0, bh);
+            if (is_w) {
+              tma_load_3d(sa + kOffB + q * 16384, &maps.m[bmap], &full[st], kx, b_row0, bh);
+            } else {
+              tma_load_3d(sa + kOffB + q * 16384, &maps.m[bmap], &full[st], 128 * c, kx, bh);
+              tma_load_3d(sa + kOffB + q * 16384 + 8192, &maps.m[bmap], &full[st], 128 * c + 64, kx, bh);
+            }
           }
         }
       }
       __syncwarp();
     } else if (warp == 5) {
       if (lane == 0 && !*abort_flag) {
-        const uint32_t id = is_w ? idesc_tf32(128, n_cols) : idesc_f16(128, n_cols);
+        const uint32_t id = is_w ? idesc_tf32(128, n_cols) : idesc_f16(128, n_cols, true);
         // accumulators: X (level 0) and W in R1; X X in R2 and Z X in R3
         // (level 1); level 2 accumulates onto 13 Z - 15 Z X in R0
         const uint32_t d1 = (is_w || lv == 0) ? kR1 : (lv == 1 ? kR2 : kR0);
@@ -610,12 +604,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 2; ++q) {
               const uint32_t ta = tmem + kR0 + (uint32_t)(((2 * j + q) & 3) * 32);
               const uint64_t a0 = smem_desc(sb + aoff + q * 16384, 16, 1024, SW_128B);
-              const uint64_t b0 = smem_desc(sb + kOffB + q * 16384, 16, 1024, SW_128B);
+              // W: K-major, K-steps of 8 (32 bytes); else MN-major (column
+              // halves 8 KB apart), K-steps of 16 rows (2 KB)
+              const uint64_t b0 = is_w ? smem_desc(sb + kOffB + q * 16384, 16, 1024, SW_128B)
+                                       : smem_desc(sb + kOffB + q * 16384, 8192, 1024, SW_128B);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (fresh && q == 0 && kk == 0) ? 0u : 1u;
                 if (!is_w)
-                  mma_bf16(tmem + dacc, a0 + kk * 2, b0 + kk * 2, id, acc);  // kind::f16, fp16 by idesc
+                  mma_bf16(tmem + dacc, a0 + kk * 2, b0 + kk * 128, id, acc);  // kind::f16, fp16 by idesc
                 else if (from_tmem)
                   mma_tf32_tA(tmem + dacc, ta + kk * 8, b0 + kk * 2, id, acc);
                 else
@@ -663,34 +660,44 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (c == 1 && gi < p.m64)
           for (int j = d; j < p.dpad; ++j) wt[(size_t)j * p.m64 + gi] = __float2bfloat16_rn(0.f);
       } else if (!is_w) {
-        // level 0: X (R1)            -> xr (row-major), X^T -> to
-        // level 1: Z X (R3)          -> zx (row-major), (7X - X^2)^T -> tc,
+        // level 0: X (R1)            -> xr
+        // level 1: Z X (R3)          -> zx, 7X - X^2 -> y,
         //          R0 <- 13 Z - 15 Z X
-        // level 2: Z' = R0 / 4 -> R0, z (row-major), Z'^T -> to; after the
-        //          last update also the fp32 Z (for W and the stage export)
-        // Both blocks are rounded to fp16 and staged in the (now idle)
-        // operand ring: row-major as two SWIZZLE_128B boxes of [128 rows x
-        // 64 columns], transposed as [32 block columns x 32 rows] SWIZZLE_64B
-        // tiles per warp. Each warp stores its pieces as soon as they are
-        // staged; the stores clip what lies beyond m.
+        // level 2: Z' = R0 / 4 -> R0, z; after the last update also the
+        //          fp32 Z (for W and the stage export)
+        // The blocks are rounded to fp16 and staged, row-major, in the (now
+        // idle) operand ring as two SWIZZLE_128B boxes of [128 rows x 64
+        // columns] each; every 64 columns each warp stores its 32 rows of
+        // the box while the next columns are staged. The stores clip what
+        // lies beyond m.
         const int rm_map = lv == 0 ? MAP_XR : (lv == 1 ? MAP_ZX : MAP_Z);
-        const int tr_map = lv == 1 ? tc : to;
         const bool last_z = lv == 2 && it == p.iters - 1;
-        uint8_t* rm_stage = sm;                         // box b: block columns [64 b, 64 b + 64)
-        uint8_t* tr_stage = sm + 32768 + warp * 8192;  // tile j0 / 32 of this warp's rows
+        uint8_t* rm_stage = sm;          // box b: block columns [64 b, 64 b + 64)
+        uint8_t* y_stage = sm + 32768;   // level 1: 7X - X^2, the same way
         float* z32 = p.z + ((size_t)bh * m + (rv ? gi : 0)) * m + 128 * c;
         const bool store = ok_epi && !*abort_flag;
+        auto stage16 = [&](uint8_t* stage, const float* x, int jc) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __half2 h2 = __floats2half2_rn(x[2 * e], x[2 * e + 1]);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          uint8_t* box = stage + (jc >> 6) * 16384;
+          const uint32_t byte0 = (uint32_t)(jc & 63) * 2u;
+          *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        };
         for (int j0 = 0; ok_epi && j0 < 128; j0 += 32) {
-          uint8_t* tbox = tr_stage + (j0 >> 5) * 2048;
           for (int h = 0; h < 32; h += 16) {
             const int jc = j0 + h;
-            float rmv[16], trv[16];
+            float rmv[16];
             if (lv == 0) {
               uint32_t v[16];
               tmem_ld16(tmem + lo + kR1 + jc, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) rmv[e] = trv[e] = __uint_as_float(v[e]);
+              for (int e = 0; e < 16; ++e) rmv[e] = __uint_as_float(v[e]);
             } else if (lv == 1) {
               uint32_t vx[16], vx2[16], vzx[16], vz[16];
               tmem_ld16(tmem + lo + kR1 + jc, vx);
@@ -698,21 +705,23 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
               tmem_ld16(tmem + lo + kR3 + jc, vzx);
               tmem_ld16(tmem + lo + kR0 + jc, vz);
               tmem_ld_wait();
+              float yv[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const float zx = __uint_as_float(vzx[e]);
                 rmv[e] = zx;
-                trv[e] = fmaf(7.f, __uint_as_float(vx[e]), -__uint_as_float(vx2[e]));
+                yv[e] = fmaf(7.f, __uint_as_float(vx[e]), -__uint_as_float(vx2[e]));
                 vz[e] = __float_as_uint(fmaf(13.f, __uint_as_float(vz[e]), -15.f * zx));
               }
               tmem_st16(tmem + lo + kR0 + jc, vz);
+              stage16(y_stage, yv, jc);
             } else {
               uint32_t v[16];
               tmem_ld16(tmem + lo + kR0 + jc, v);
               tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                rmv[e] = trv[e] = 0.25f * __uint_as_float(v[e]);
+                rmv[e] = 0.25f * __uint_as_float(v[e]);
                 v[e] = __float_as_uint(rmv[e]);
               }
               tmem_st16(tmem + lo + kR0 + jc, v);
@@ -723,30 +732,22 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<float4*>(z32 + jc + e) = make_float4(rmv[e], rmv[e + 1], rmv[e + 2], rmv[e + 3]);
               }
             }
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const __half2 h2 = __floats2half2_rn(rmv[2 * e], rmv[2 * e + 1]);
-              pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            uint8_t* box = rm_stage + (jc >> 6) * 16384;
-            const uint32_t byte0 = (uint32_t)(jc & 63) * 2u;
-            *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(box + sw128_offset(tid, byte0 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              *reinterpret_cast<__half*>(tbox + sw64_offset(h + e, lane * 2)) = __float2half_rn(trv[e]);
+            stage16(rm_stage, rmv, jc);
           }
-          // this warp's transposed tile, and every 64 columns its rows of the
-          // row-major box, leave while the next columns are staged
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0 && store) {
-            tma_store_3d(&maps.st[tr_map], tbox, 128 * r + 32 * warp, 128 * c + j0, bh);
-            if ((j0 & 63) == 32)
-              tma_store_3d(&maps.st[rm_map], rm_stage + (j0 >> 6) * 16384 + warp * 4096, 128 * c + (j0 & ~63),
+          // every 64 columns: this warp's rows of the box leave while the
+          // next columns are staged
+          if ((j0 & 63) == 32) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0 && store) {
+              const int bx = j0 >> 6;
+              tma_store_3d(&maps.st[rm_map], rm_stage + bx * 16384 + warp * 4096, 128 * c + 64 * bx,
                            128 * r + 32 * warp, bh);
-            bulk_commit();
+              if (lv == 1)
+                tma_store_3d(&maps.st[ST_Y], y_stage + bx * 16384 + warp * 4096, 128 * c + 64 * bx,
+                             128 * r + 32 * warp, bh);
+              bulk_commit();
+            }
           }
         }
         if (lv != 0) tmem_st_wait();
@@ -801,10 +802,10 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.gml = gml;
   p.g = g;
   p.a_s = a_s;
-  // scratch holds, for the whole batch, the six fp16 operand matrices
-  // [B*H][m][mp] (A_S, Z, X, Z X and the two transposed right factors; mp =
-  // m rounded up to 8, so that every row starts on a 16-byte boundary) in
-  // its first 4 m^2 floats, then G^T. Z (fp32) lives in `z` (stage export).
+  // scratch holds, for the whole batch, the five fp16 operand matrices
+  // [B*H][m][mp] (A_S, Z, X, Z X, 7X - X^2; mp = m rounded up to 8, so that
+  // every row starts on a 16-byte boundary) in its first 4 m^2 floats, then
+  // G^T. Z (fp32) lives in `z` (stage export).
   const int mp = (s.m + 7) & ~7;
   const size_t hm = BH * (size_t)s.m * mp;  // halves per fp16 matrix
   __half* h16 = reinterpret_cast<__half*>(scratch);
@@ -813,8 +814,7 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
   p.z16 = h16 + hm;
   p.xr16 = h16 + 2 * hm;
   p.zx16 = h16 + 3 * hm;
-  p.t1_16 = h16 + 4 * hm;
-  p.t2_16 = h16 + 5 * hm;
+  p.y16 = h16 + 4 * hm;
   p.gt = scratch + 4 * BH * mm;
   p.w = w;
   p.wt = static_cast<__nv_bfloat16*>(wt_bf16);
@@ -830,18 +830,28 @@ int launch_pinv_big(const Shape& s, const float* qt, const float* kt, const floa
 
   BigPinvMaps maps;
   memset(&maps, 0, sizeof(maps));
-  const __half* bufs[6] = {p.a16, p.z16, p.xr16, p.zx16, p.t1_16, p.t2_16};
-  for (int i = 0; i < 6; ++i) {
+  {
+    // left factors (128 x 64 boxes) and row-major stores (32 x 64) of A_S, Z,
+    // X, Z X and 7X - X^2; right factors (64 x 64 boxes) of Z, X, 7X - X^2
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.m, BH};
     const uint64_t strides[2] = {(uint64_t)mp * 2, (uint64_t)s.m * mp * 2};
-    const uint32_t box[3] = {64, 128, 1};
-    const bool transposed = i == MAP_T1 || i == MAP_T2;
-    const uint32_t sbox[3] = {transposed ? 32u : 64u, 32, 1};
-    if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs[i], dims, strides, box,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&maps.st[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs[i], dims, strides, sbox,
-                         transposed ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
-      return tensor_map_error(__FILE__, __LINE__);
+    const uint32_t box[3] = {64, 128, 1}, bbox[3] = {64, 64, 1}, sbox[3] = {64, 32, 1};
+    const __half* left[4] = {p.a16, p.z16, p.xr16, p.zx16};
+    for (int i = 0; i < 4; ++i)
+      if (!make_tensor_map(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, left[i], dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+        return tensor_map_error(__FILE__, __LINE__);
+    const __half* rows[5] = {p.a16, p.z16, p.xr16, p.zx16, p.y16};  // store index = position
+    for (int i = 0; i < 5; ++i)
+      if (!make_tensor_map(&maps.st[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, rows[i], dims, strides, sbox,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+        return tensor_map_error(__FILE__, __LINE__);
+    const int bidx[3] = {MAP_BZ, MAP_BX, MAP_BY};
+    const __half* right[3] = {p.z16, p.xr16, p.y16};
+    for (int i = 0; i < 3; ++i)
+      if (!make_tensor_map(&maps.m[bidx[i]], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, right[i], dims, strides,
+                           bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return tensor_map_error(__FILE__, __LINE__);
   }
   {
     const uint64_t dims[3] = {(uint64_t)s.m, (uint64_t)s.d, BH};

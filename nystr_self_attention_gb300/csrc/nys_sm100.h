@@ -330,9 +330,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Instruction descriptor, kind::f16 with fp16 A/B (both K-major) and fp32 D.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor, kind::f16 with fp16 A/B and fp32 D; A K-major, B
+// K-major or (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn = false) {
+  return (1u << 4) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::tf32 with fp32 D, both operands K-major.
