@@ -287,9 +287,8 @@ int nystrom_clustered_attn_fwd(const void* q, const void* k, const void* v, void
   auto at = [&](size_t off) { return ws + off; };
   float* mu[2] = {reinterpret_cast<float*>(at(L.mu_a)), reinterpret_cast<float*>(at(L.mu_b))};
   int* assign = reinterpret_cast<int*>(at(L.assign));
-  // initial centroids: segment means of Q (the K means land in scratch)
-  rc = launch_landmarks(s, q, k, mu[0], reinterpret_cast<float*>(at(L.attn.k_tilde)), nullptr,
-                        nullptr, stream);
+  // initial centroids: segment means of Q (K is not read)
+  rc = launch_landmarks(s, q, nullptr, mu[0], nullptr, nullptr, nullptr, stream);
   if (rc != NYS_OK) return error_in("initial centroids", rc);
   int* status = reinterpret_cast<int*>(at(L.attn.status));
   int cur = 0;

@@ -154,6 +154,7 @@ int launch_rows_tc(const Shape& s, const void* qt_bf16, const void* k, const voi
 // per landmark element, head sizes whose 16-byte row vectors do not divide 32).
 enum class LandmarkKernel { Small, Vec, Simt };
 LandmarkKernel landmark_kernel(const Shape& s);
+// k == nullptr: the means of Q alone (kt, kt_b unused)
 int launch_landmarks(const Shape& s, const void* q, const void* k, float* qt, float* kt,
                      __nv_bfloat16* qt_b, __nv_bfloat16* kt_b, cudaStream_t stream);
 int launch_rows_simt(const Shape& s, const float* qt, const void* k, const void* v, float* gp,

@@ -71,11 +71,11 @@ landmarks_simt(const T* __restrict__ q, const T* __restrict__ k, float* __restri
   float sq = 0.f, sk = 0.f;
   for (int t = 0; t < seg; ++t) {
     sq += ld(q + base + (size_t)t * d);
-    sk += ld(k + base + (size_t)t * d);
+    if (k) sk += ld(k + base + (size_t)t * d);
   }
   const float mq = sq / (float)seg, mk = sk / (float)seg;
   qt[((size_t)bh * m + i) * d + c] = mq;
-  kt[((size_t)bh * m + i) * d + c] = mk;
+  if (k) kt[((size_t)bh * m + i) * d + c] = mk;
   if (kt_b) kt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mk);
   if (qt_b) qt_b[(size_t)bh * m64 * dpad + idx] = __float2bfloat16_rn(mq);
 }
@@ -996,15 +996,18 @@ int landmarks_t(const Shape& s, const void* q, const void* k, float* qt, float* 
   const T* kk = static_cast<const T*>(k);
   const int vpr = s.d / (16 / (int)sizeof(T));
   const LandmarkKernel which = landmark_kernel(s);
+  // Q's jobs come first (the job's tensor is its slowest index): without K,
+  // only they are launched
+  const long long tensors = k ? 2 : 1;
   if (which == LandmarkKernel::Small) {
     const int spw = 32 / vpr;
-    const long long jobs = 2ll * s.bh() * ((s.m64() + spw - 1) / spw);
+    const long long jobs = tensors * s.bh() * ((s.m64() + spw - 1) / spw);
     const unsigned grid = (unsigned)((jobs + 7) / 8);
     KernelScope ks_("landmarks_small", stream);
     landmarks_small<T><<<grid, 256, 0, stream>>>(qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad(),
                                                   s.lengths, s.H);
   } else if (which == LandmarkKernel::Vec) {
-    const long long jobs = 2ll * s.bh() * s.m64();
+    const long long jobs = tensors * s.bh() * s.m64();
     KernelScope ks_("landmarks_vec", stream);
     landmarks_vec<T><<<(unsigned)((jobs + 7) / 8), 256, 0, stream>>>(
         qq, kk, qt, kt, qt_b, kt_b, s.bh(), s.n, s.d, s.m, s.m64(), s.dpad(), s.lengths, s.H);

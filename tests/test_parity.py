@@ -73,6 +73,7 @@ SMALL = [
     (1, 1, 384, 64, 128, 6, 127),  # widest conv
     (1, 2, 960, 128, 192, 6, 33),  # d = 128 with m > 128, ragged last tile
     (2, 1, 640, 128, 160, 6, 0),   # d = 128, m = 160, no conv
+    (1, 2, 528, 64, 132, 6, 5),    # m > 128 not a multiple of 8: the fp16 operands' rows padded to 136
     (2, 10, 1152, 128, 192, 6, 33),  # several heads per CTA range
     (20, 1, 1152, 128, 192, 4, 9),   # consecutive heads sharing conv taps
     (4, 32, 256, 64, 128, 6, 9),     # pseudo-inverse after the landmark rows (128 CTAs)
