@@ -138,27 +138,33 @@ __global__ void pack_centroids(const float* __restrict__ mu, __nv_bfloat16* __re
   mb[((size_t)bh * m64 + c) * dpad + j] = __float2bfloat16_rn(x);
 }
 
-// out[i] = G[a(i)]. One thread per 4 elements; grid (ceil(n d / 4 / 256), B*H).
+// out[i] = G[a(i)]. One thread per 8 elements (d % 8 == 0: one 16-byte
+// store in bf16, two in fp32); grid (ceil(n d / 8 / 256), B*H).
 template <typename T>
 __global__ void __launch_bounds__(256)
 broadcast_rows(const float* __restrict__ g, const int* __restrict__ assign, T* __restrict__ out,
                int n, int d, int C) {
   const long long bh = blockIdx.y;
-  const int e = blockIdx.x * 256 + threadIdx.x;  // group of 4 elements of this head
-  const int d4 = d / 4;
-  if (e >= n * d4) return;
-  const int i = e / d4, j = (e - i * d4) * 4;
+  const int e = blockIdx.x * 256 + threadIdx.x;  // group of 8 elements of this head
+  const int d8 = d / 8;
+  if (e >= n * d8) return;
+  const int i = e / d8, j = (e - i * d8) * 8;
   const int a = __ldg(assign + (size_t)bh * n + i);
-  const float4 x = *reinterpret_cast<const float4*>(g + ((size_t)bh * C + a) * d + j);
+  const float4* src = reinterpret_cast<const float4*>(g + ((size_t)bh * C + a) * d + j);
+  const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
   T* o = out + ((size_t)bh * n + i) * d + j;
   if constexpr (sizeof(T) == 4) {
-    *reinterpret_cast<float4*>(o) = x;
+    reinterpret_cast<float4*>(o)[0] = x0;
+    reinterpret_cast<float4*>(o)[1] = x1;
   } else {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(o) = u;
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x0.x, x0.y), h1 = __floats2bfloat162_rn(x0.z, x0.w);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x1.x, x1.y), h3 = __floats2bfloat162_rn(x1.z, x1.w);
+    uint4 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&h0);
+    u.y = *reinterpret_cast<const uint32_t*>(&h1);
+    u.z = *reinterpret_cast<const uint32_t*>(&h2);
+    u.w = *reinterpret_cast<const uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(o) = u;
   }
 }
 
@@ -218,7 +224,7 @@ int update_t(const Shape& s, const void* q, const int* assign, const float* mu_o
 
 template <typename T>
 int broadcast_t(const Shape& s, const float* g, const int* assign, void* out, cudaStream_t st) {
-  const int groups = s.n * (s.d / 4);
+  const int groups = s.n * (s.d / 8);
   KernelScope scope("broadcast_rows", st);
   broadcast_rows<T><<<dim3((groups + 255) / 256, (unsigned)s.bh()), 256, 0, st>>>(
       g, assign, static_cast<T*>(out), s.n, s.d, s.m);
