@@ -801,8 +801,9 @@ tokens_simt(const T* __restrict__ q, const T* __restrict__ v, const float* __res
 // (at most CV_BLOCKS) consecutive blocks of CV_ROWS output rows of one head. The
 // head's taps are staged once (tap-major, so that consecutive channels read
 // consecutive words); per block, its V rows with the halo are staged in
-// shared memory by 16-byte loads, all of a thread's loads in flight before
-// its first store. A work item is CV_RUN consecutive rows of one column: the
+// shared memory by 16-byte asynchronous copies (rows outside [0, len) zero),
+// with two buffers (nbuf = 2) the next block's while this one is computed.
+// A work item is CV_RUN consecutive rows of one column: the
 // V window lives in a ring of CV_RUN registers, and with the tap loop
 // unrolled in blocks of CV_RUN the ring's indices are static, so a tap costs
 // one weight, one new V value and CV_RUN FMAs.
@@ -810,37 +811,29 @@ constexpr int CV_ROWS = 64, CV_THREADS = 256, CV_RUN = 16, CV_BLOCKS = 8;
 
 // A block's V rows are staged in the input type. NARROW (bf16, or d <= 64):
 // the staged rows and taps leave room for three CTAs per SM, so registers
-// are capped to allow them (fewer staging loads in flight, the attention
-// term added after the taps so its loads overlap them); fp32 with d = 128
-// is bound by shared memory to two CTAs and keeps every register.
-template <typename T> struct Row8;  // eight consecutive elements of a row
-template <> struct Row8<float> { float4 a, b; };
-template <> struct Row8<__nv_bfloat16> { uint4 a; };
-__device__ __forceinline__ void ld_row8(const float* p, Row8<float>& r) {
-  r.a = *reinterpret_cast<const float4*>(p);
-  r.b = *reinterpret_cast<const float4*>(p + 4);
-}
-__device__ __forceinline__ void ld_row8(const __nv_bfloat16* p, Row8<__nv_bfloat16>& r) {
-  r.a = *reinterpret_cast<const uint4*>(p);
-}
-__device__ __forceinline__ void zero_row8(Row8<float>& r) {
-  r.a = r.b = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-__device__ __forceinline__ void zero_row8(Row8<__nv_bfloat16>& r) { r.a = make_uint4(0u, 0u, 0u, 0u); }
-__device__ __forceinline__ void st_row8(float* p, const Row8<float>& r) {
-  *reinterpret_cast<float4*>(p) = r.a;
-  *reinterpret_cast<float4*>(p + 4) = r.b;
-}
-__device__ __forceinline__ void st_row8(__nv_bfloat16* p, const Row8<__nv_bfloat16>& r) {
-  *reinterpret_cast<uint4*>(p) = r.a;
-}
+// are capped to allow them (the attention term added after the taps so its
+// loads overlap them); fp32 with d = 128 is bound by shared memory to two
+// CTAs, and registers are capped for two.
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes sixteen
+// zero bytes and reads nothing
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 template <typename T, bool PER_CHANNEL, bool NARROW>
-__global__ void __launch_bounds__(CV_THREADS, NARROW ? 3 : 1)
+__global__ void __launch_bounds__(CV_THREADS, NARROW ? 3 : 2)
 conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ out, int H, int n,
-          int d, int ks, const int* __restrict__ lengths, int nblk) {
+          int d, int ks, const int* __restrict__ lengths, int nblk, int nbuf) {
   constexpr bool per_channel = PER_CHANNEL;
   extern __shared__ float sm[];
   const long long bh = blockIdx.y;
@@ -848,8 +841,8 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
   const int len = lengths ? lengths[bh / H] : n;
   const int rad = ks > 0 ? (ks - 1) / 2 : 0;
   const int vrows = CV_ROWS + 2 * rad;
-  T* sv = reinterpret_cast<T*>(sm);                           // [vrows][d], input type
-  float* sw = reinterpret_cast<float*>(sv + (size_t)vrows * d);  // per channel: [ks][d]; per head: [ks]
+  T* sv = reinterpret_cast<T*>(sm);                                  // [nbuf][vrows][d], input type
+  float* sw = reinterpret_cast<float*>(sv + (size_t)nbuf * vrows * d);  // per channel: [ks][d]; per head: [ks]
   const T* vb = v + (size_t)bh * n * d;
   T* ob = out + (size_t)bh * n * d;
   const int tb0 = blockIdx.x * nblk * CV_ROWS;
@@ -877,34 +870,38 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
     }
   }
   const int wstride = per_channel ? d : 1;  // word step between taps in sw
-  const int d8 = d / 8;                     // d is a multiple of 8
   const int ks_full = ks - ks % CV_RUN;     // taps in whole blocks of CV_RUN
+  // block blk's V rows [t0 - rad, t0 + CV_ROWS + rad) into buffer blk % nbuf,
+  // as one commit group (empty where the block has no conv work)
+  constexpr int kEl = 16 / (int)sizeof(T);  // elements per 16-byte piece
+  const int pr = d / kEl;                   // pieces per row (d is a multiple of 8)
+  auto stage = [&](int blk) {
+    const int t0 = tb0 + blk * CV_ROWS;
+    if (ks > 0 && t0 < n && t0 < len) {
+      T* dst = sv + (size_t)(blk % nbuf) * vrows * d;
+      for (int e = threadIdx.x; e < vrows * pr; e += CV_THREADS) {
+        const int row = e / pr, c = (e - row * pr) * kEl;
+        const int u = t0 - rad + row;
+        const bool in = u >= 0 && u < len;
+        cp_async16(dst + (size_t)row * d + c, in ? vb + (size_t)u * d + c : vb, in ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+  stage(0);
   for (int blk = 0; blk < nblk; ++blk) {
     const int t0 = tb0 + blk * CV_ROWS;
     if (t0 >= n) break;  // uniform across the CTA
     const bool work = ks > 0 && t0 < len;
-    __syncthreads();  // the previous block's readers of sv are done (and the taps are staged)
-    if (work) {
-      constexpr int kPer = NARROW ? 4 : 8;  // row pieces in flight per thread
-      for (int e0 = threadIdx.x; e0 < vrows * d8; e0 += kPer * CV_THREADS) {
-        Row8<T> x[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int e = e0 + k * CV_THREADS;
-          const int u = t0 - rad + e / d8, c = (e % d8) * 8;
-          if (e < vrows * d8 && u >= 0 && u < len)
-            ld_row8(vb + (size_t)u * d + c, x[k]);
-          else
-            zero_row8(x[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int e = e0 + k * CV_THREADS;
-          if (e < vrows * d8) st_row8(sv + (size_t)(e / d8) * d + (e % d8) * 8, x[k]);
-        }
-      }
+    const T* svb = sv + (size_t)(blk % nbuf) * vrows * d;
+    if (nbuf == 1 && blk > 0) stage(blk);
+    if (nbuf == 2 && blk + 1 < nblk && t0 + CV_ROWS < n) {
+      stage(blk + 1);  // into block blk - 1's buffer, released at the end of its iteration
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    __syncthreads();
+    __syncthreads();  // block blk's rows (and the taps) are in shared memory
     for (int item = threadIdx.x; item < (CV_ROWS / CV_RUN) * d; item += CV_THREADS) {
       const int c = item % d, r0 = (item / d) * CV_RUN;
       if (t0 + r0 >= n) continue;
@@ -924,7 +921,7 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
         // ring: before tap j, V row (r0 + j + r) of the staged block sits in
         // xw[(j + r) % CV_RUN]; after it, the slot of row r0 + j takes row
         // r0 + j + CV_RUN (staged for every j < ks - 1)
-        const T* x = sv + (size_t)r0 * d + c;
+        const T* x = svb + (size_t)r0 * d + c;
         const float* wp = sw + (per_channel ? c : 0);  // tap j of this channel: wp[j * wstride]
         const T* xp = x + (size_t)CV_RUN * d;          // row r0 + j + CV_RUN: xp[j * d]
         float xw[CV_RUN];
@@ -961,6 +958,7 @@ conv_mask(const T* __restrict__ v, const float* __restrict__ w, T* __restrict__ 
         st(ob + (size_t)t * d + c, t < len ? att[r] + acc[r] : 0.f);
       }
     }
+    __syncthreads();  // every reader of this block's buffer is done before it is refilled
   }
 }
 
@@ -968,10 +966,17 @@ template <typename T>
 int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, cudaStream_t stream) {
   const int rad = s.ks > 0 ? (s.ks - 1) / 2 : 0;
   const bool per_channel = s.conv_layout == NYS_CONV_PER_CHANNEL;
-  const size_t smem = s.ks > 0 ? sizeof(T) * (size_t)(CV_ROWS + 2 * rad) * s.d +
-                                    sizeof(float) * (size_t)s.ks * (per_channel ? s.d : 1)
-                               : 0;
   const bool narrow = sizeof(T) == 2 || s.d <= 64;
+  // two V buffers (the next block's rows copied during this block's taps)
+  // unless that leaves fewer CTAs per SM than one buffer: measured, a third
+  // resident CTA hides more than the copy overlap does
+  const size_t vbuf = sizeof(T) * (size_t)(CV_ROWS + 2 * rad) * s.d;
+  const size_t taps = sizeof(float) * (size_t)s.ks * (per_channel ? s.d : 1);
+  auto resident = [&](size_t bytes) {  // CTAs per SM: the launch bound, then shared memory
+    return std::min<size_t>(narrow ? 3 : 2, (228 * 1024) / (bytes + 1024));
+  };
+  const int nbuf = 2 * vbuf + taps <= 227 * 1024 && resident(2 * vbuf + taps) >= resident(vbuf + taps) ? 2 : 1;
+  const size_t smem = s.ks > 0 ? nbuf * vbuf + taps : 0;
   auto kern = per_channel ? (narrow ? conv_mask<T, true, true> : conv_mask<T, true, false>)
                           : (narrow ? conv_mask<T, false, true> : conv_mask<T, false, false>);
   if (smem > 48 * 1024 &&
@@ -979,13 +984,16 @@ int conv_mask_t(const Shape& s, const void* v, const float* conv_w, void* out, c
     return set_cuda_error(cudaGetLastError());
   KernelScope ks_("conv_mask", stream);
   // blocks per CTA: up to CV_BLOCKS (the taps staged once for all of them),
-  // fewer where that would leave SMs idle
+  // fewer where that would leave SMs idle. (One wave of longer CTAs, sized
+  // to the resident slots, was slower at B8 H8 n8192 d64: short CTAs let the
+  // block scheduler even out the SMs' work as they finish.)
   const long long blocks = (long long)((s.n + CV_ROWS - 1) / CV_ROWS) * s.bh();
   const long long ctas_min = 2ll * plan_sms();
   const int nblk = (int)std::max(1ll, std::min<long long>(CV_BLOCKS, blocks / ctas_min));
   const dim3 grid((s.n + CV_ROWS * nblk - 1) / (CV_ROWS * nblk), (unsigned)s.bh());
   kern<<<grid, CV_THREADS, smem, stream>>>(static_cast<const T*>(v), s.ks > 0 ? conv_w : nullptr,
-                                          static_cast<T*>(out), s.H, s.n, s.d, s.ks, s.lengths, nblk);
+                                          static_cast<T*>(out), s.H, s.n, s.d, s.ks, s.lengths, nblk,
+                                          s.ks > 0 ? nbuf : 1);
   return launch_status();
 }
 
